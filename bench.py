@@ -1,0 +1,470 @@
+"""Benchmark of the projection GEMM library on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one pass over the decode-projection workload: C = A . B^T for
+M in {1, 8, 32, 128} tokens against three bf16 weight matrices of
+Qwen3-8B-like dimensions (qkv 6144x4096, o 4096x4096, fused gate/up
+24576x4096), twelve GEMMs per step.  Every GEMM has its own weight copy
+(1.14 GB streamed per step, nine times the L2), so weights come from HBM.
+The metric is algorithmic HBM bytes, 2*(M*K + N*K + M*N) per GEMM, divided
+by device time (CUDA events on the launching stream).
+
+The JSON line also carries:
+  roofline      the dominant kernel's algorithmic GB/s (bytes / its own
+                event-timed launch durations) against the measured HBM peak
+  e2e           the same metric through the public call with host buffers:
+                each step copies its activations host->device (pinned) and
+                its outputs device->host; weights stay resident
+  cpu_baseline  the fp64 CPU oracle on this host, on a bounded sample
+  sweeps        prefill (TFLOP/s), down-projection and W4A16 (GB/s) shapes
+  clocks        nvidia-smi samples taken during the timed region
+
+--impl reference times the oracle (the method's plain definition on the
+host cores) on a sample of the same workload.  Multi-GPU runs are replicas:
+each rank runs the whole step on its own GPU; value sums over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s (prefill) & HBM GB/s (decode), % of GB300 roofline"
+DECODE = [(M, N, 4096) for M in (1, 8, 32, 128) for N in (6144, 4096, 24576)]
+DOWN = [(M, 4096, 12288) for M in (1, 16, 64, 128, 512)]
+PREFILL = [(M, N, K) for M in (1024, 4096, 16384)
+           for (N, K) in ((4096, 4096), (6144, 4096), (24576, 4096), (4096, 12288), (8192, 8192))]
+W4 = [(M, N, K) for M in (1, 16, 64, 128)
+      for (N, K) in ((7168, 5120), (5120, 5120), (34816, 5120), (5120, 17408))]
+WORKLOAD = ("decode projections, Qwen3-8B-like dims: bf16 A[M,4096], M in {1,8,32,128}, "
+            "B in {qkv 6144x4096, o 4096x4096, gate/up 24576x4096}, fp32 accumulate, bf16 out")
+
+
+def bytes_bf16(M, N, K):
+    return 2 * (M * K + N * K + M * N)
+
+
+def bytes_w4(M, N, K, g=128):
+    return N * K // 2 + (N * K // g) * 3 + 2 * M * K + 2 * M * N
+
+
+def flops(M, N, K):
+    return 2 * M * N * K
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- our arm
+
+class Arm:
+    """The GEMMs of one step, with device-resident operands."""
+
+    def __init__(self, dev):
+        import torch
+        from dense_bit_weight_gb300 import gemm
+        self.torch, self.g, self.dev = torch, gemm, dev
+        self.stream = torch.cuda.current_stream(dev)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(0)
+        self.items = []
+        for (M, N, K) in DECODE:
+            A = (torch.randn((M, K), generator=gen, device=dev)).to(torch.bfloat16)
+            B = (torch.randn((N, K), generator=gen, device=dev) * K ** -0.5).to(torch.bfloat16)
+            C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            plan = gemm.gemm_bf16_plan(M, N, K)
+            self.items.append(dict(M=M, N=N, K=K, A=A, B=B, C=C, plan=plan,
+                                   name=self.kname(plan), bytes=bytes_bf16(M, N, K)))
+
+    @staticmethod
+    def kname(plan):
+        return f"{plan['variant_name']}[tile {plan['tile_m']}x{plan['tile_n']}, split {plan['split']}]"
+
+    def call(self, it):
+        rc = self.g.gemm_bf16_ptr(it["A"].data_ptr(), it["B"].data_ptr(), it["C"].data_ptr(),
+                                  it["M"], it["N"], it["K"], it["K"], it["K"], it["N"],
+                                  self.stream.cuda_stream)
+        if rc:
+            raise self.g.GemmError(rc, "gemm_bf16")
+
+    def step(self, events=None):
+        for i, it in enumerate(self.items):
+            if events is not None:
+                events[i][0].record(self.stream)
+            self.call(it)
+            if events is not None:
+                events[i][1].record(self.stream)
+
+
+def dist_init(args):
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return ws, rank, local
+
+
+def barrier_max(x, ws):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def timed_sweep(g, torch, shapes, kind, reps=10, warmup=3):
+    """Per-shape device time (ms, median of reps) for the extra sweeps."""
+    dev = torch.device("cuda")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1)
+    out = []
+    for (M, N, K) in shapes:
+        plan = (g.gemm_w4a16_plan(M, N, K, 128) if kind == "w4" else g.gemm_bf16_plan(M, N, K))
+        if plan["variant"] == 1 and M > 64:
+            continue            # no tensor-core plan for this shape
+        # enough weight copies that consecutive launches miss L2
+        wbytes = N * K * 2 if kind != "w4" else N * K // 2
+        copies = max(1, min(8, int(np.ceil(3 * 126e6 / wbytes))))
+        A = torch.randn((M, K), generator=gen, device=dev).to(torch.bfloat16)
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        if kind == "w4":
+            Bs = [(torch.randint(-2 ** 31, 2 ** 31 - 1, (N, K // 8), generator=gen, device=dev, dtype=torch.int32),
+                   (torch.rand((N, K // 128), generator=gen, device=dev) * 0.018 + 0.002).to(torch.bfloat16),
+                   torch.randint(0, 16, (N, K // 128), generator=gen, device=dev, dtype=torch.uint8))
+                  for _ in range(copies)]
+            fn = lambda i: g.gemm_w4a16(A, *Bs[i % copies], 128, C)
+            work = bytes_w4(M, N, K)
+        else:
+            Bs = [(torch.randn((N, K), generator=gen, device=dev) * K ** -0.5).to(torch.bfloat16)
+                  for _ in range(copies)]
+            fn = lambda i: g.gemm_bf16(A, Bs[i % copies], C)
+            work = flops(M, N, K) if kind == "prefill" else bytes_bf16(M, N, K)
+        for i in range(warmup):
+            fn(i)
+        ts = []
+        for i in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn(i)
+            e1.record()
+            ts.append((e0, e1))
+        torch.cuda.synchronize()
+        ms = float(np.median([a.elapsed_time(b) for a, b in ts]))
+        out.append({"M": M, "N": N, "K": K, "ms": ms, "work": work, "variant": plan["variant_name"]})
+        del Bs, A, C
+    return out
+
+
+def cpu_oracle_sample(target_s=12.0):
+    """Time the oracle on a fraction of every decode GEMM's output columns."""
+    import oracle
+    from dense_bit_weight_gb300 import synth
+    cores = oracle.hardware_threads()
+    # calibrate on a small piece, then size the sample for about target_s seconds
+    A = synth.bf16_normal((1, 4096), 1.0, 0, synth.STREAM_A)
+    B = synth.bf16_normal((512, 4096), 4096 ** -0.5, 0, synth.STREAM_B)
+    t = time.perf_counter()
+    oracle.gemm_bf16(A, B)
+    per_mac = (time.perf_counter() - t) / (512 * 4096)
+    total_macs = sum(M * N * K for (M, N, K) in DECODE)
+    frac = min(1.0, target_s / max(per_mac * total_macs, 1e-9))
+    work, secs = 0, 0.0
+    for (M, N, K) in DECODE:
+        n = max(8, int(N * frac))
+        A = synth.bf16_normal((M, K), 1.0, 0, synth.STREAM_A)
+        B = synth.bf16_normal((n, K), K ** -0.5, 0, synth.STREAM_B)
+        t = time.perf_counter()
+        oracle.gemm_bf16(A, B)
+        secs += time.perf_counter() - t
+        work += bytes_bf16(M, n, K)
+    return {"value": work / secs / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"every decode GEMM on the first {frac:.2%} of its weight rows "
+                      f"({work / 1e6:.1f} MB algorithmic, {secs:.1f} s)"}, secs
+
+
+def run_ours(args):
+    import torch
+    ws, rank, local = dist_init(args)
+    torch.cuda.synchronize()
+    arm = Arm(torch.device("cuda", torch.cuda.current_device()))
+    g = arm.g
+    n_items = len(arm.items)
+    for _ in range(args.warmup):
+        arm.step()
+    torch.cuda.synchronize()
+    events = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n_items)] for _ in range(args.steps)]
+    clocks = Clocks(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(arm.stream)
+    for s in range(args.steps):
+        arm.step(events[s])
+    t1.record(arm.stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clk = clocks.stop()
+    ms_total = barrier_max(t0.elapsed_time(t1), ws)
+    step_bytes = sum(it["bytes"] for it in arm.items)
+    value = ws * step_bytes * args.steps / (ms_total * 1e-3) / 1e9
+
+    # per-kernel durations over the timed region
+    per = {}
+    for s in range(args.steps):
+        for i, it in enumerate(arm.items):
+            d = events[s][i][0].elapsed_time(events[s][i][1])
+            e = per.setdefault(it["name"], {"ms": 0.0, "bytes": 0, "launches": 0})
+            e["ms"] += d
+            e["bytes"] += it["bytes"]
+            e["launches"] += it["plan"]["kernels"]
+    dom_name = max(per, key=lambda k: per[k]["ms"])
+    dom = per[dom_name]
+    hbm, tf, tf_sus, src = peaks()
+    achieved = dom["bytes"] / (dom["ms"] * 1e-3) / 1e9
+    gpu_launches = sum(it["plan"]["kernels"] for it in arm.items) * args.steps
+
+    # end to end through the public call, host buffers, copies inside the timing
+    hostA = [torch.empty(it["A"].shape, dtype=torch.bfloat16, pin_memory=True).copy_(it["A"])
+             for it in arm.items]
+    hostC = [torch.empty(it["C"].shape, dtype=torch.bfloat16, pin_memory=True) for it in arm.items]
+    e2e_steps = max(1, min(args.steps, 10))
+
+    def e2e_step():
+        for it, ha, hc in zip(arm.items, hostA, hostC):
+            it["A"].copy_(ha, non_blocking=True)
+            g.gemm_bf16(it["A"], it["B"], it["C"])
+            hc.copy_(it["C"], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = barrier_max(e0.elapsed_time(e1), ws)
+    h2d = sum(it["M"] * it["K"] * 2 for it in arm.items)
+    d2h = sum(it["M"] * it["N"] * 2 for it in arm.items)
+    e2e = {"value": ws * step_bytes * e2e_steps / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    sweeps = None
+    if rank == 0 and not args.no_sweeps:
+        sweeps = {}
+        pre = timed_sweep(g, torch, PREFILL, "prefill") if not args.quick else []
+        if pre:
+            tot_f = sum(r["work"] for r in pre)
+            tot_ms = sum(r["ms"] for r in pre)
+            sweeps["prefill"] = {"unit": "TFLOP/s", "aggregate": tot_f / (tot_ms * 1e-3) / 1e12,
+                                 "frac_of_peak": tot_f / (tot_ms * 1e-3) / 1e12 / tf,
+                                 "shapes": [[r["M"], r["N"], r["K"], round(r["work"] / (r["ms"] * 1e-3) / 1e12, 1),
+                                             r["variant"]] for r in pre]}
+        for key, shapes, kind in (("down", DOWN, "bf16"), ("w4a16", W4, "w4")):
+            rs = timed_sweep(g, torch, shapes, kind)
+            tot_b = sum(r["work"] for r in rs)
+            tot_ms = sum(r["ms"] for r in rs)
+            sweeps[key] = {"unit": "GB/s", "aggregate": tot_b / (tot_ms * 1e-3) / 1e9,
+                           "frac_of_peak": tot_b / (tot_ms * 1e-3) / 1e9 / hbm,
+                           "shapes": [[r["M"], r["N"], r["K"], round(r["work"] / (r["ms"] * 1e-3) / 1e9, 1),
+                                       r["variant"]] for r in rs]}
+        sweeps["decode_per_shape"] = [
+            [it["M"], it["N"], it["K"],
+             round(it["bytes"] * args.steps / (sum(events[s][i][0].elapsed_time(events[s][i][1])
+                                                  for s in range(args.steps)) * 1e-3) / 1e9, 1),
+             it["plan"]["variant_name"]] for i, it in enumerate(arm.items)]
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        cpu, _ = cpu_oracle_sample(args.cpu_seconds)
+
+    err = g.gemm_last_device_error()
+    if err:
+        raise RuntimeError(f"device error word set: {g.gemm_status_string(err)}")
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_total / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "gemms_per_step": n_items,
+                       "l2": "inputs larger than L2: each GEMM has its own weight copy, "
+                             f"{step_bytes / 1e9:.2f} GB streamed per step",
+                       "parallelism": f"replicas x{ws}"},
+            "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1),
+                         "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                         "peak_source": src, "traffic": None},
+            "e2e": {k: (round(v, 2) if isinstance(v, float) else v) for k, v in e2e.items()},
+            "cpu_baseline": cpu,
+            "gpu_launches": gpu_launches,
+            "clocks": clk,
+            "per_kernel": {k: {"launches": v["launches"], "ms": round(v["ms"], 4),
+                               "GB/s": round(v["bytes"] / (v["ms"] * 1e-3) / 1e9, 1)}
+                           for k, v in per.items()},
+            "sweeps": sweeps,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle (fp64 CPU definition) on the host cores, rank 0 only."""
+    rank = int(os.environ.get("RANK", "0"))
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    import oracle
+    from dense_bit_weight_gb300 import synth
+    cores = oracle.hardware_threads()
+    # each step: every decode GEMM on a slice of its weight rows, about 1 s of CPU work
+    A = synth.bf16_normal((1, 4096), 1.0, 0, synth.STREAM_A)
+    Bc = synth.bf16_normal((512, 4096), 4096 ** -0.5, 0, synth.STREAM_B)
+    t = time.perf_counter()
+    oracle.gemm_bf16(A, Bc)
+    per_mac = (time.perf_counter() - t) / (512 * 4096)
+    total = sum(M * N * K for (M, N, K) in DECODE)
+    frac = min(1.0, args.ref_step_seconds / max(per_mac * total, 1e-9))
+    ops = []
+    for (M, N, K) in DECODE:
+        n = max(8, int(N * frac))
+        ops.append((synth.bf16_normal((M, K), 1.0, 0, synth.STREAM_A),
+                    synth.bf16_normal((n, K), K ** -0.5, 0, synth.STREAM_B), bytes_bf16(M, n, K)))
+    step_bytes = sum(o[2] for o in ops)
+
+    def step():
+        for a, b, _ in ops:
+            oracle.gemm_bf16(a, b)
+
+    for _ in range(args.warmup):
+        step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    secs = time.perf_counter() - t
+    value = step_bytes * args.steps / secs / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "gemms_per_step": len(ops),
+                   "l2": "host oracle; no device caches involved",
+                   "parallelism": "host threads"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: every decode GEMM on the first {frac:.2%} of its "
+                                   f"weight rows ({step_bytes / 1e6:.1f} MB algorithmic)"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-sweeps", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--quick", action="store_true", help="skip the prefill sweep")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=1.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,444 @@
+// api.cu -- the C ABI: argument checks, launch planning, per-device state.
+//
+// Every precondition is checked on the host before anything is enqueued; a
+// failed check returns its gemm_status and launches nothing.  There is no
+// fallback path: a shape no kernel supports is an error.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <map>
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+
+namespace dbw {
+int gemv_grid(int64_t N, int sm_count);
+}
+
+namespace {
+
+using namespace dbw;
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+struct StreamWorkspace {
+    float *partials = nullptr;
+    int *counters = nullptr;
+    int64_t floats = 0, n_counters = 0;
+};
+
+struct DeviceState {
+    bool ready = false;
+    int sm_count = 0;
+    int cc_major = 0, cc_minor = 0;
+    int *d_error = nullptr;
+    std::map<cudaStream_t, StreamWorkspace> ws;  // one workspace per stream
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA; }
+
+// Lazily set up the current device.  Allocates the error word (so it must not
+// run inside stream capture).
+int device_state(DeviceState **out, int *dev_out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState &s = g_dev[dev];
+    if (!s.ready) {
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return GEMM_ERR_CUDA;
+        if (!(prop.major == 10 && prop.minor == 3)) return GEMM_ERR_ARCH;
+        s.sm_count = prop.multiProcessorCount;
+        s.cc_major = prop.major;
+        s.cc_minor = prop.minor;
+        if (cudaMalloc(&s.d_error, sizeof(int)) != cudaSuccess) return GEMM_ERR_CUDA;
+        if (cudaMemset(s.d_error, 0, sizeof(int)) != cudaSuccess) return GEMM_ERR_CUDA;
+        s.ready = true;
+    }
+    *out = &s;
+    *dev_out = dev;
+    return GEMM_OK;
+}
+
+// The split-K workspace of (device, stream), grown to at least the request.
+// Growing frees the old buffers after synchronising the device, so the first
+// split call of a given size class should come before any stream capture.
+int stream_workspace(DeviceState &s, cudaStream_t st, int64_t floats, int64_t counters,
+                     StreamWorkspace **out)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    StreamWorkspace &w = s.ws[st];
+    if (w.floats < floats || w.n_counters < counters) {
+        if (w.partials || w.counters) {
+            if (cudaDeviceSynchronize() != cudaSuccess) return GEMM_ERR_CUDA;
+            cudaFree(w.partials);
+            cudaFree(w.counters);
+            w = StreamWorkspace();
+        }
+        // round up so neighbouring shapes reuse the allocation
+        int64_t f = std::max<int64_t>(floats, int64_t(1) << 20);
+        int64_t c = std::max<int64_t>(counters, 4096);
+        if (cudaMalloc(&w.partials, (size_t)f * sizeof(float)) != cudaSuccess) return GEMM_ERR_CUDA;
+        if (cudaMalloc(&w.counters, (size_t)c * sizeof(int)) != cudaSuccess) return GEMM_ERR_CUDA;
+        if (cudaMemset(w.counters, 0, (size_t)c * sizeof(int)) != cudaSuccess) return GEMM_ERR_CUDA;
+        w.floats = f;
+        w.n_counters = c;
+    }
+    *out = &w;
+    return GEMM_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void *a, int64_t abytes, const void *b, int64_t bbytes)
+{
+    uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+    return a0 < b0 + (uintptr_t)bbytes && b0 < a0 + (uintptr_t)abytes;
+}
+
+// Byte extent of a row-major [rows, cols] matrix with leading dimension ld.
+int64_t extent(int64_t rows, int64_t cols, int64_t ld, int64_t elem)
+{
+    return rows == 0 ? 0 : ((rows - 1) * ld + cols) * elem;
+}
+
+int check_sizes(int64_t M, int64_t N, int64_t K)
+{
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_SHAPE;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMM_ERR_SHAPE;
+    if (K % 8) return GEMM_ERR_SHAPE;
+    return GEMM_OK;
+}
+
+int run(const GemmArgs &a, const Plan &p, cudaStream_t st, bool w4)
+{
+    DeviceState *s = nullptr;
+    int dev = 0;
+    int rc = device_state(&s, &dev);
+    if (rc) return rc;
+    LaunchCtx c{};
+    c.stream = st;
+    c.sm_count = s->sm_count;
+    c.d_error = s->d_error;
+    int64_t nf = 0, nc = 0;
+    workspace_need(p, a.M, a.N, &nf, &nc);
+    if (nf > 0 || nc > 0) {
+        StreamWorkspace *w = nullptr;
+        rc = stream_workspace(*s, st, nf, nc, &w);
+        if (rc) return rc;
+        c.workspace = w->partials;
+        c.counters = w->counters;
+        c.ws_floats = w->floats;
+        c.n_counters = w->n_counters;
+    }
+    cudaError_t e = cudaSuccess;
+    switch (p.variant) {
+    case GEMM_VARIANT_ZERO: e = launch_zero_fill(a, c); break;
+    case GEMM_VARIANT_GEMV: e = w4 ? launch_gemv_w4a16(a, p, c) : launch_gemv_bf16(a, p, c); break;
+    case GEMM_VARIANT_SKINNY:
+    case GEMM_VARIANT_PREFILL:
+        if (w4) return GEMM_ERR_VARIANT;
+        e = launch_umma_bf16(a, p, c);
+        break;
+    default: return GEMM_ERR_VARIANT;
+    }
+    return cuda_status(e);
+}
+
+int sm_count_for_plan(int num_sms, int *out)
+{
+    if (num_sms > 0) {
+        *out = num_sms;
+        return GEMM_OK;
+    }
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    *out = n;
+    return GEMM_OK;
+}
+
+void to_public(const Plan &p, gemm_plan *out)
+{
+    out->variant = p.variant;
+    out->kernels = p.kernels;
+    out->grid = p.grid;
+    out->split = p.split;
+    out->tile_m = p.tile_m;
+    out->tile_n = p.tile_n;
+    out->stages = p.stages;
+    out->reserved = p.m_per_pass;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ planning
+
+namespace dbw {
+
+// tcgen05 planning shared by the skinny (swap AB) and prefill layouts.
+// Whole tiles round-robin when they fill the SMs in nearly whole waves,
+// otherwise stream-K over (tile, k-block) units so every SM gets an equal share.
+static void plan_umma(int64_t M, int64_t N, int64_t K, bool swap, int bn, int sm_count, Plan *p)
+{
+    const int64_t R = swap ? N : M, Q = swap ? M : N;
+    const int64_t tiles_r = (R + kUmmaBM - 1) / kUmmaBM;
+    const int64_t tiles_q = (Q + bn - 1) / bn;
+    const int64_t tiles = tiles_r * tiles_q;
+    const int64_t nk = (K + kUmmaBK - 1) / kUmmaBK;
+    const int64_t G = sm_count;
+    p->variant = swap ? GEMM_VARIANT_SKINNY : GEMM_VARIANT_PREFILL;
+    p->bn = bn;
+    p->stages = umma_stages(bn);
+    p->tile_m = swap ? bn : kUmmaBM;
+    p->tile_n = swap ? kUmmaBM : bn;
+    p->group_r = swap ? (int)tiles_r : (int)std::min<int64_t>(tiles_r, 16);
+    p->kernels = 1;
+    const int64_t waves = (tiles + G - 1) / G;
+    const double eff = (double)tiles / (double)(waves * G);
+    if (tiles >= G && eff >= 0.9) {
+        p->mode = 0;
+        p->grid = (int)G;
+        p->split = 1;
+    } else {
+        const int64_t units = tiles * nk;
+        p->mode = 1;
+        p->grid = (int)std::min<int64_t>(G, units);
+        const int64_t per_cta = units / p->grid;   // >= 1
+        p->split = (int)std::min<int64_t>(p->grid, (nk + per_cta - 1) / per_cta + 1);
+        if (p->split < 1) p->split = 1;
+    }
+}
+
+bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan *p)
+{
+    *p = Plan{};
+    if (K == 0) {
+        if (variant != GEMM_VARIANT_AUTO && variant != GEMM_VARIANT_ZERO) return false;
+        p->variant = GEMM_VARIANT_ZERO;
+        p->kernels = 1;
+        p->split = 1;
+        return true;
+    }
+    if (variant == GEMM_VARIANT_AUTO)
+        variant = M <= 4 ? GEMM_VARIANT_GEMV : M <= 128 ? GEMM_VARIANT_SKINNY : GEMM_VARIANT_PREFILL;
+    switch (variant) {
+    case GEMM_VARIANT_GEMV:
+        p->variant = GEMM_VARIANT_GEMV;
+        p->kernels = 1;
+        p->split = 1;
+        p->m_per_pass = (int)std::min<int64_t>(M, 4);
+        p->tile_m = p->m_per_pass;
+        p->tile_n = 8;
+        p->grid = gemv_grid(N, sm_count);
+        return true;
+    case GEMM_VARIANT_SKINNY: {
+        if (M > 128) return false;
+        int bn = 16;
+        while (bn < M) bn *= 2;
+        plan_umma(M, N, K, true, bn, sm_count, p);
+        return true;
+    }
+    case GEMM_VARIANT_PREFILL:
+        plan_umma(M, N, K, false, 256, sm_count, p);
+        return true;
+    default: return false;
+    }
+}
+
+bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int sm_count, Plan *p)
+{
+    (void)group;
+    *p = Plan{};
+    if (variant == GEMM_VARIANT_AUTO) variant = GEMM_VARIANT_GEMV;
+    if (variant != GEMM_VARIANT_GEMV) return false;
+    if (K == 0) return false;
+    p->variant = GEMM_VARIANT_GEMV;
+    p->kernels = 1;
+    p->split = 1;
+    p->m_per_pass = M >= 4 ? 4 : (M >= 2 ? 2 : 1);
+    p->tile_m = p->m_per_pass;
+    p->tile_n = 8;
+    p->grid = gemv_grid(N, sm_count);
+    return true;
+}
+
+void workspace_need(const Plan &p, int64_t M, int64_t N, int64_t *floats, int64_t *counters)
+{
+    (void)M;
+    (void)N;
+    *floats = 0;
+    *counters = 0;
+    if ((p.variant == GEMM_VARIANT_SKINNY || p.variant == GEMM_VARIANT_PREFILL) && p.mode == 1) {
+        *floats = (int64_t)p.grid * 2 * kUmmaBM * p.bn;
+        *counters = ((M + p.tile_m - 1) / p.tile_m) * ((N + p.tile_n - 1) / p.tile_n);
+    }
+}
+
+}  // namespace dbw
+
+// ------------------------------------------------------------------ C ABI
+
+extern "C" {
+
+int gemm_bf16_ex(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
+                 int64_t lda, int64_t ldb, int64_t ldc, void *stream, int variant)
+{
+    int rc = check_sizes(M, N, K);
+    if (rc) return rc;
+    if (M == 0 || N == 0) return GEMM_OK;
+    // K == 0: A and B are empty and never read; only C is checked
+    if (!C || (K > 0 && (!A || !B))) return GEMM_ERR_NULL;
+    if (ldc < N || ldc % 8 || (K > 0 && (lda < K || ldb < K || lda % 8 || ldb % 8))) return GEMM_ERR_LD;
+    if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B)))) return GEMM_ERR_ALIGN;
+    const int64_t cb = extent(M, N, ldc, 2);
+    if (K > 0 && (overlaps(C, cb, A, extent(M, K, lda, 2)) || overlaps(C, cb, B, extent(N, K, ldb, 2))))
+        return GEMM_ERR_ALIAS;
+    DeviceState *s = nullptr;
+    int dev = 0;
+    rc = device_state(&s, &dev);
+    if (rc) return rc;
+    Plan p;
+    if (!plan_bf16(M, N, K, variant, s->sm_count, &p)) return GEMM_ERR_VARIANT;
+    GemmArgs a{A, B, nullptr, nullptr, C, M, N, K, lda, ldb, ldc, 0};
+    return run(a, p, (cudaStream_t)stream, false);
+}
+
+int gemm_bf16(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
+              int64_t lda, int64_t ldb, int64_t ldc, void *stream)
+{
+    return gemm_bf16_ex(A, B, C, M, N, K, lda, ldb, ldc, stream, GEMM_VARIANT_AUTO);
+}
+
+int gemm_w4a16_ex(const void *A, const void *Bq, const void *scales, const void *zeros, void *C,
+                  int64_t M, int64_t N, int64_t K, int64_t group, void *stream, int variant)
+{
+    int rc = check_sizes(M, N, K);
+    if (rc) return rc;
+    if (N % 8) return GEMM_ERR_SHAPE;
+    if (group != 32 && group != 64 && group != 128) return GEMM_ERR_GROUP;
+    if (K % group) return GEMM_ERR_GROUP;
+    if (K == 0) return GEMM_ERR_SHAPE;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (!A || !Bq || !scales || !zeros || !C) return GEMM_ERR_NULL;
+    if (!aligned16(A) || !aligned16(Bq) || !aligned16(C) || ((uintptr_t)scales & 1u))
+        return GEMM_ERR_ALIGN;
+    const int64_t cb = M * N * 2;
+    if (overlaps(C, cb, A, M * K * 2) || overlaps(C, cb, Bq, N * K / 2) ||
+        overlaps(C, cb, scales, N * (K / group) * 2) || overlaps(C, cb, zeros, N * (K / group)))
+        return GEMM_ERR_ALIAS;
+    DeviceState *s = nullptr;
+    int dev = 0;
+    rc = device_state(&s, &dev);
+    if (rc) return rc;
+    Plan p;
+    if (!plan_w4a16(M, N, K, group, variant, s->sm_count, &p)) return GEMM_ERR_VARIANT;
+    GemmArgs a{A, Bq, scales, zeros, C, M, N, K, K, K / 8, N, group};
+    return run(a, p, (cudaStream_t)stream, true);
+}
+
+int gemm_w4a16(const void *A, const void *Bq, const void *scales, const void *zeros, void *C,
+               int64_t M, int64_t N, int64_t K, int64_t group, void *stream)
+{
+    return gemm_w4a16_ex(A, Bq, scales, zeros, C, M, N, K, group, stream, GEMM_VARIANT_AUTO);
+}
+
+int gemm_bf16_plan(int64_t M, int64_t N, int64_t K, int variant, int num_sms, gemm_plan *out)
+{
+    if (!out) return GEMM_ERR_NULL;
+    int rc = check_sizes(M, N, K);
+    if (rc) return rc;
+    int sms = 0;
+    rc = sm_count_for_plan(num_sms, &sms);
+    if (rc) return rc;
+    Plan p;
+    if (!plan_bf16(M, N, K, variant, sms, &p)) return GEMM_ERR_VARIANT;
+    to_public(p, out);
+    return GEMM_OK;
+}
+
+int gemm_w4a16_plan(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int num_sms,
+                    gemm_plan *out)
+{
+    if (!out) return GEMM_ERR_NULL;
+    int rc = check_sizes(M, N, K);
+    if (rc) return rc;
+    if (group != 32 && group != 64 && group != 128) return GEMM_ERR_GROUP;
+    if (K % group) return GEMM_ERR_GROUP;
+    int sms = 0;
+    rc = sm_count_for_plan(num_sms, &sms);
+    if (rc) return rc;
+    Plan p;
+    if (!plan_w4a16(M, N, K, group, variant, sms, &p)) return GEMM_ERR_VARIANT;
+    to_public(p, out);
+    return GEMM_OK;
+}
+
+int gemm_last_device_error(void)
+{
+    DeviceState *s = nullptr;
+    int dev = 0;
+    int rc = device_state(&s, &dev);
+    if (rc) return rc;
+    int v = 0;
+    if (cudaMemcpy(&v, s->d_error, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (v != 0 && cudaMemset(s->d_error, 0, sizeof(int)) != cudaSuccess) return GEMM_ERR_CUDA;
+    return v;
+}
+
+const char *gemm_status_string(int status)
+{
+    switch (status) {
+    case GEMM_OK: return "ok";
+    case GEMM_ERR_NULL: return "a required pointer is NULL";
+    case GEMM_ERR_SHAPE: return "unsupported or invalid shape";
+    case GEMM_ERR_LD: return "invalid leading dimension";
+    case GEMM_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case GEMM_ERR_GROUP: return "invalid W4A16 group size";
+    case GEMM_ERR_CUDA: return "CUDA runtime error";
+    case GEMM_ERR_DEVICE_TIMEOUT: return "device-side bounded wait expired";
+    case GEMM_ERR_ARCH: return "device is not compute capability 10.3";
+    case GEMM_ERR_ALIAS: return "output overlaps an input";
+    case GEMM_ERR_VARIANT: return "variant cannot run this shape";
+    default: return "unknown status";
+    }
+}
+
+int gemm_debug_inject_timeout(int enable)
+{
+    const int prev = dbw::g_debug_stall;
+    dbw::g_debug_stall = enable ? 1 : 0;
+    return prev;
+}
+
+void gemm_shutdown(void)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    int prev = -1;
+    cudaGetDevice(&prev);
+    for (int d = 0; d < kMaxDevices; ++d) {
+        DeviceState &s = g_dev[d];
+        if (!s.ready) continue;
+        cudaSetDevice(d);
+        cudaDeviceSynchronize();
+        for (auto &kv : s.ws) {
+            cudaFree(kv.second.partials);
+            cudaFree(kv.second.counters);
+        }
+        s.ws.clear();
+        cudaFree(s.d_error);
+        s = DeviceState();
+    }
+    if (prev >= 0) cudaSetDevice(prev);
+}
+
+}  // extern "C"

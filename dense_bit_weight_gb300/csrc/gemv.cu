@@ -1,0 +1,197 @@
+// gemv.cu -- CUDA-core weight-streaming kernels for small M (decode).
+//
+// One warp owns one weight row n at a time and walks K in 16-byte chunks
+// (lane l takes chunks l, l+32, ...), so each warp instruction reads 512
+// contiguous bytes of the row; the weights are read with no-L1-allocate
+// loads, the activations through L1 (every row reuses them).  The K sum is
+// finished with a butterfly of warp shuffles and lane 0 writes the output.
+// This is the decode GEMV of the hk-dsl PyPI page ("Results", kernels inside
+// the engines: "decode GEMV, 1-32 tokens"), with the cross-lane reduction of
+// the FlyDSL prebuilt kernels guide §2 (XOR-shuffle warp reduction).
+//
+// For M larger than the per-pass row count the kernel makes one pass over the
+// weight row per group of rows (the tcgen05 kernels serve those shapes).
+#include "common.cuh"
+#include "internal.h"
+
+namespace dbw {
+namespace {
+
+constexpr int kWarps = 8;
+
+template <int MT, int U>
+__global__ void __launch_bounds__(kWarps * 32)
+k_gemv_bf16(const uint16_t *__restrict__ A, const uint16_t *__restrict__ B,
+            uint16_t *__restrict__ C, int M, int N, int K, int64_t lda, int64_t ldb, int64_t ldc)
+{
+    const int lane = threadIdx.x & 31;
+    const int chunks = K >> 3;  // 8 bf16 per 16-byte chunk
+    for (int n = blockIdx.x * kWarps + (threadIdx.x >> 5); n < N; n += gridDim.x * kWarps) {
+        const uint16_t *brow = B + (int64_t)n * ldb;
+        for (int m0 = 0; m0 < M; m0 += MT) {
+            float acc[MT];
+#pragma unroll
+            for (int i = 0; i < MT; ++i) acc[i] = 0.f;
+            for (int c0 = lane; c0 < chunks; c0 += 32 * U) {
+                uint4 bv[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int c = c0 + 32 * u;
+                    bv[u] = c < chunks ? ld_stream_v4(brow + (int64_t)c * 8) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int c = c0 + 32 * u;
+                    if (c >= chunks) break;
+                    const uint32_t bw[4] = {bv[u].x, bv[u].y, bv[u].z, bv[u].w};
+#pragma unroll
+                    for (int i = 0; i < MT; ++i) {
+                        if (m0 + i >= M) break;
+                        const uint4 av = ld_ro_v4(A + (int64_t)(m0 + i) * lda + (int64_t)c * 8);
+                        const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
+                        float s = acc[i];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            s = fmaf(bf16lo(aw[j]), bf16lo(bw[j]), s);
+                            s = fmaf(bf16hi(aw[j]), bf16hi(bw[j]), s);
+                        }
+                        acc[i] = s;
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < MT; ++i) {
+                const float v = warp_sum(acc[i]);
+                if (lane == 0 && m0 + i < M) C[(int64_t)(m0 + i) * ldc + n] = f32_to_bf16_rn(v);
+            }
+        }
+    }
+}
+
+// W4A16: each lane takes 16 bytes of packed weights = 32 consecutive k, which
+// never straddle a quantisation group (group is a multiple of 32).  With
+// w = (q - z) * s for the whole chunk,
+//     sum_k a_k w_k = s * (sum_k a_k q_k - z * sum_k a_k),
+// exact in real arithmetic; here each partial sum is fp32.
+template <int MT>
+__global__ void __launch_bounds__(kWarps * 32)
+k_gemv_w4a16(const uint16_t *__restrict__ A, const uint32_t *__restrict__ Bq,
+             const uint16_t *__restrict__ S, const uint8_t *__restrict__ Z,
+             uint16_t *__restrict__ C, int M, int N, int K, int group)
+{
+    constexpr int U = 4;
+    const int lane = threadIdx.x & 31;
+    const int chunks = K >> 5;      // 32 k (16 bytes of Bq) per chunk
+    const int groups = K / group;
+    for (int n = blockIdx.x * kWarps + (threadIdx.x >> 5); n < N; n += gridDim.x * kWarps) {
+        const uint32_t *qrow = Bq + (int64_t)n * (K >> 3);
+        for (int m0 = 0; m0 < M; m0 += MT) {
+            float acc[MT];
+#pragma unroll
+            for (int i = 0; i < MT; ++i) acc[i] = 0.f;
+            for (int c0 = lane; c0 < chunks; c0 += 32 * U) {
+                uint4 qv[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int c = c0 + 32 * u;
+                    qv[u] = c < chunks ? ld_stream_v4(qrow + (int64_t)c * 4) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int c = c0 + 32 * u;
+                    if (c >= chunks) break;
+                    const int g = (c * 32) / group;
+                    const float s = __uint_as_float((uint32_t)S[(int64_t)n * groups + g] << 16);
+                    const float z = (float)Z[(int64_t)n * groups + g];
+                    const uint32_t qw[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
+#pragma unroll
+                    for (int i = 0; i < MT; ++i) {
+                        if (m0 + i >= M) break;
+                        const uint16_t *arow = A + (int64_t)(m0 + i) * K + (int64_t)c * 32;
+                        float sq = 0.f, sa = 0.f;
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            const uint4 av = ld_ro_v4(arow + w * 8);
+                            const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const float a0 = bf16lo(aw[j]), a1 = bf16hi(aw[j]);
+                                const float q0 = (float)((qw[w] >> (8 * j)) & 0xFu);
+                                const float q1 = (float)((qw[w] >> (8 * j + 4)) & 0xFu);
+                                sq = fmaf(a0, q0, sq);
+                                sq = fmaf(a1, q1, sq);
+                                sa += a0 + a1;
+                            }
+                        }
+                        acc[i] = fmaf(s, fmaf(-z, sa, sq), acc[i]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < MT; ++i) {
+                const float v = warp_sum(acc[i]);
+                if (lane == 0 && m0 + i < M) C[(int64_t)(m0 + i) * N + n] = f32_to_bf16_rn(v);
+            }
+        }
+    }
+}
+
+__global__ void k_zero_fill(uint16_t *C, int M, int N, int64_t ldc)
+{
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < (int64_t)M * N;
+         i += (int64_t)gridDim.x * blockDim.x)
+        C[(i / N) * ldc + (i % N)] = 0;
+}
+
+int rows_grid(int64_t N, int sm_count)
+{
+    int64_t g = (N + kWarps - 1) / kWarps;
+    int64_t cap = (int64_t)sm_count * 16;
+    return (int)(g < cap ? g : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_zero_fill(const GemmArgs &a, const LaunchCtx &c)
+{
+    int64_t total = a.M * a.N;
+    int grid = (int)((total + 255) / 256);
+    if (grid > c.sm_count * 8) grid = c.sm_count * 8;
+    if (grid < 1) grid = 1;
+    k_zero_fill<<<grid, 256, 0, c.stream>>>((uint16_t *)a.C, (int)a.M, (int)a.N, a.ldc);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemv_bf16(const GemmArgs &a, const Plan &p, const LaunchCtx &c)
+{
+    const uint16_t *A = (const uint16_t *)a.A, *B = (const uint16_t *)a.B;
+    uint16_t *C = (uint16_t *)a.C;
+    const int M = (int)a.M, N = (int)a.N, K = (int)a.K;
+    switch (p.m_per_pass) {
+    case 1: k_gemv_bf16<1, 8><<<p.grid, kWarps * 32, 0, c.stream>>>(A, B, C, M, N, K, a.lda, a.ldb, a.ldc); break;
+    case 2: k_gemv_bf16<2, 8><<<p.grid, kWarps * 32, 0, c.stream>>>(A, B, C, M, N, K, a.lda, a.ldb, a.ldc); break;
+    case 3: k_gemv_bf16<3, 4><<<p.grid, kWarps * 32, 0, c.stream>>>(A, B, C, M, N, K, a.lda, a.ldb, a.ldc); break;
+    default: k_gemv_bf16<4, 4><<<p.grid, kWarps * 32, 0, c.stream>>>(A, B, C, M, N, K, a.lda, a.ldb, a.ldc); break;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemv_w4a16(const GemmArgs &a, const Plan &p, const LaunchCtx &c)
+{
+    const uint16_t *A = (const uint16_t *)a.A;
+    const uint32_t *Q = (const uint32_t *)a.B;
+    const uint16_t *S = (const uint16_t *)a.scales;
+    const uint8_t *Z = (const uint8_t *)a.zeros;
+    uint16_t *C = (uint16_t *)a.C;
+    const int M = (int)a.M, N = (int)a.N, K = (int)a.K, g = (int)a.group;
+    switch (p.m_per_pass) {
+    case 1: k_gemv_w4a16<1><<<p.grid, kWarps * 32, 0, c.stream>>>(A, Q, S, Z, C, M, N, K, g); break;
+    case 2: k_gemv_w4a16<2><<<p.grid, kWarps * 32, 0, c.stream>>>(A, Q, S, Z, C, M, N, K, g); break;
+    default: k_gemv_w4a16<4><<<p.grid, kWarps * 32, 0, c.stream>>>(A, Q, S, Z, C, M, N, K, g); break;
+    }
+    return cudaGetLastError();
+}
+
+int gemv_grid(int64_t N, int sm_count) { return rows_grid(N, sm_count); }
+
+}  // namespace dbw

@@ -1,0 +1,62 @@
+// internal.h -- interface between the host API (api.cu) and the kernel
+// translation units.  Not installed; not part of the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dbw_gemm.h"
+
+namespace dbw {
+
+// Per-call launch context built by the host API.
+struct LaunchCtx {
+    cudaStream_t stream;
+    int sm_count;
+    int *d_error;          // device error word (GEMM_ERR_DEVICE_TIMEOUT on a bounded-wait expiry)
+    float *workspace;      // split-K partial tiles (fp32), may be null if the plan has split == 1
+    int *counters;         // per-tile arrival counters, zero between calls
+    int64_t ws_floats;     // capacity of `workspace` in floats
+    int64_t n_counters;    // capacity of `counters`
+};
+
+struct GemmArgs {
+    const void *A, *B;     // bf16 activations / bf16 weights (or packed int4 for W4A16)
+    const void *scales, *zeros;
+    void *C;
+    int64_t M, N, K, lda, ldb, ldc, group;
+};
+
+// Host-side plan (pure function of the sizes and the SM count).
+struct Plan {
+    int variant;
+    int kernels;
+    int grid;
+    int split;
+    int tile_m, tile_n;
+    int stages;
+    int m_per_pass;        // GEMV: rows of A handled per pass over the weights
+    int mode;              // tcgen05: 0 whole tiles round-robin, 1 stream-K ranges
+    int bn;                // tcgen05: MMA N (columns of the Y operand per tile)
+    int group_r;           // tcgen05: tile-rows per raster group
+};
+
+bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan *p);
+bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int sm_count, Plan *p);
+
+// Workspace need (floats, counters) for a plan; 0 when it needs none.
+void workspace_need(const Plan &p, int64_t M, int64_t N, int64_t *floats, int64_t *counters);
+
+// Kernel launchers: return cudaSuccess or the launch error.
+cudaError_t launch_zero_fill(const GemmArgs &a, const LaunchCtx &c);
+cudaError_t launch_gemv_bf16(const GemmArgs &a, const Plan &p, const LaunchCtx &c);
+cudaError_t launch_gemv_w4a16(const GemmArgs &a, const Plan &p, const LaunchCtx &c);
+cudaError_t launch_umma_bf16(const GemmArgs &a, const Plan &p, const LaunchCtx &c);
+
+// tcgen05 kernel geometry (umma.cu)
+constexpr int kUmmaBM = 128;
+constexpr int kUmmaBK = 64;
+int umma_stages(int bn);
+extern int g_debug_stall;   // test hook: producers issue no copies (forces the watchdog)
+
+}  // namespace dbw

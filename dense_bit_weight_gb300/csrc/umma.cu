@@ -1,0 +1,531 @@
+// umma.cu -- tcgen05 tensor-core GEMM for sm_103a.
+//
+// One persistent, warp-specialised kernel computes D = X . Y^T tile by tile,
+// X and Y both K-contiguous bf16 ([rows, K] row-major), D accumulated in fp32
+// in tensor memory (TMEM) and written as bf16:
+//   prefill (X = A, Y = B):  D[i, j] = C[m0 + i, n0 + j]
+//   skinny  (X = B, Y = A):  D[i, j] = C[m0 + j, n0 + i]   (swap AB: the weight
+//            rows fill the 128-row side of the MMA, the few tokens its N side)
+// The contraction is C[M,N] = A[M,K] . B[N,K]^T of the FlyDSL prebuilt
+// kernels guide §3.1 (preshuffle GEMM); the design is the NVIDIA answer the
+// HipKittens notes give for why producer/consumer specialisation pays on
+// Blackwell (§2, the five reasons: TMA, tcgen05 reading shared/tensor memory,
+// large shared memory, register reallocation, mbarriers).
+//
+// Warp roles (192 threads, one CTA per SM):
+//   warp 0      TMA producer: loads a 128 x 64 X tile and a BN x 64 Y tile per
+//               stage into a ring of shared-memory stages (128-byte swizzle),
+//               signalling `full[s]` with the byte count
+//   warp 1      allocates TMEM; one lane issues tcgen05.mma (M=128, N=BN,
+//               K=16, four per stage) into one of two accumulators and
+//               commits `empty[s]` (stage reusable) and `tfull[a]`
+//   warps 2-5   epilogue: TMEM -> registers (tcgen05.ld 32x32b), bf16
+//               round-to-nearest-even, global stores; release `tempty[a]`
+// The two accumulators let the epilogue of one tile overlap the MMAs of the
+// next (the prefetch-t+1-while-computing-t loop of the FlyDSL kernel
+// authoring skill's "runtime loops" section, done by hardware queues here).
+//
+// Scheduling (the pages' split-K over CTAs only when the grid would underfill
+// the device, FlyDSL prebuilt kernels guide §3c):
+//   mode 0  whole tiles, CTA c takes tiles c, c+G, c+2G, ... in a grouped
+//           raster (tile-rows in groups, so concurrently running CTAs share
+//           operand tiles in L2 -- the L2-reuse window of the HipKittens
+//           notes' Algorithm 1)
+//   mode 1  stream-K: the (tile, k-block) units are cut into G contiguous
+//           equal ranges, one per CTA.  A tile split across CTAs is summed by
+//           whichever contributor arrives last: every contributor stores its
+//           fp32 partial in the workspace, bumps the tile's counter, and the
+//           last one adds all partials in increasing-k order (deterministic,
+//           no float atomics) and resets the counter to zero.
+//
+// Every mbarrier wait is bounded (1 s of %globaltimer).  On expiry the
+// waiting thread raises a shared abort flag and the device error word; all
+// roles leave their loops, the producer waits (bounded) for the copies it
+// issued, the MMA lane for its issued MMAs, and TMEM is freed before exit.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dbw {
+namespace {
+
+constexpr int BM = 128;          // MMA M: rows of X per tile
+constexpr int BK = 64;           // k per stage (one 128-byte swizzle row of bf16)
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr uint64_t kTimeoutNs = 1000000000ull;
+
+struct Sched {
+    int mode;                    // 0 whole tiles, 1 stream-K ranges
+    int tiles_r, tiles_q, tiles;
+    int nk;                      // k-blocks per tile
+    int grid;
+    int group_r;                 // raster: tile-rows per group
+    int stall;                   // test hook: producer issues nothing (forces the watchdog)
+    long long units;             // tiles * nk
+};
+
+struct Segment {
+    int tile, kb0, kb1, slot;
+};
+
+__device__ __forceinline__ void tile_coords(const Sched &s, int t, int &tr, int &tq)
+{
+    const int per_group = s.group_r * s.tiles_q;
+    const int g = t / per_group;
+    const int first_r = g * s.group_r;
+    const int rows_in = min(s.group_r, s.tiles_r - first_r);
+    const int local = t - g * per_group;
+    tr = first_r + local % rows_in;
+    tq = local / rows_in;
+}
+
+__device__ __forceinline__ long long range_begin(const Sched &s, int c)
+{
+    return (long long)c * s.units / s.grid;
+}
+
+// CTA whose unit range contains unit u (mode 1).
+__device__ __forceinline__ int cta_of_unit(const Sched &s, long long u)
+{
+    return (int)(((u + 1) * s.grid + s.units - 1) / s.units) - 1;
+}
+
+struct SegIter {
+    long long u, u_end;
+    int next_tile, count;
+    __device__ SegIter(const Sched &s, int cta)
+    {
+        count = 0;
+        next_tile = cta;
+        u = s.mode == 1 ? range_begin(s, cta) : 0;
+        u_end = s.mode == 1 ? range_begin(s, cta + 1) : 0;
+    }
+    __device__ bool next(const Sched &s, Segment &seg)
+    {
+        if (s.mode == 0) {
+            if (next_tile >= s.tiles) return false;
+            seg.tile = next_tile;
+            seg.kb0 = 0;
+            seg.kb1 = s.nk;
+            seg.slot = 0;
+            next_tile += s.grid;
+        } else {
+            if (u >= u_end) return false;
+            seg.tile = (int)(u / s.nk);
+            seg.kb0 = (int)(u % s.nk);
+            const long long left = u_end - u;
+            seg.kb1 = (int)min((long long)s.nk, seg.kb0 + left);
+            seg.slot = count == 0 ? 0 : 1;
+            u += seg.kb1 - seg.kb0;
+        }
+        ++count;
+        return true;
+    }
+};
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                         int *d_error)
+{
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::global_timer_ns();
+    for (uint32_t spins = 1;; ++spins) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((spins & 31u) == 0) {
+            if (*abort_flag) return false;
+            if (ptx::global_timer_ns() - t0 > kTimeoutNs) {
+                *abort_flag = 1u;
+                atomicExch(d_error, (int)GEMM_ERR_DEVICE_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Wait without looking at the abort flag (used when draining before exit).
+__device__ __forceinline__ void wait_bar_drain(uint32_t bar, uint32_t parity)
+{
+    const uint64_t t0 = ptx::global_timer_ns();
+    while (!ptx::mbar_try_wait(bar, parity))
+        if (ptx::global_timer_ns() - t0 > kTimeoutNs) return;
+}
+
+template <bool SWAP>
+__device__ __forceinline__ void store_chunk(uint16_t *__restrict__ C, int64_t ldc, int R, int Q, int r,
+                                            int q0, const float (&f)[16])
+{
+    if (r >= R) return;
+    if (!SWAP) {
+        uint16_t *dst = C + (int64_t)r * ldc + q0;
+        if (q0 + 16 <= Q) {
+            uint4 w0, w1;
+            w0.x = pack_bf16x2_rn(f[0], f[1]);
+            w0.y = pack_bf16x2_rn(f[2], f[3]);
+            w0.z = pack_bf16x2_rn(f[4], f[5]);
+            w0.w = pack_bf16x2_rn(f[6], f[7]);
+            w1.x = pack_bf16x2_rn(f[8], f[9]);
+            w1.y = pack_bf16x2_rn(f[10], f[11]);
+            w1.z = pack_bf16x2_rn(f[12], f[13]);
+            w1.w = pack_bf16x2_rn(f[14], f[15]);
+            reinterpret_cast<uint4 *>(dst)[0] = w0;
+            reinterpret_cast<uint4 *>(dst)[1] = w1;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (q0 + j < Q) dst[j] = f32_to_bf16_rn(f[j]);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            if (q0 + j < Q) C[(int64_t)(q0 + j) * ldc + r] = f32_to_bf16_rn(f[j]);
+    }
+}
+
+constexpr uint32_t tmem_cols_for(int n)
+{
+    return n <= 32 ? 32u : n <= 64 ? 64u : n <= 128 ? 128u : n <= 256 ? 256u : 512u;
+}
+
+template <int BN, int STAGES>
+struct Layout {
+    static constexpr int X_BYTES = BM * BK * 2;
+    static constexpr int Y_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = X_BYTES + Y_BYTES;
+    static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+    static constexpr int NBARS = 2 * STAGES + 5;
+    static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
+    static constexpr int SMEM = MISC_OFF + 16 + 1024;   // + slack to align the base to 1024
+};
+
+template <int BN, int STAGES, bool SWAP>
+__global__ void __launch_bounds__(kThreads, 1)
+k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
+       uint16_t *__restrict__ C, int R, int Q, int64_t ldc, const Sched sched,
+       float *__restrict__ ws, int *__restrict__ counters, int *__restrict__ d_error)
+{
+    using L = Layout<BN, STAGES>;
+    constexpr uint32_t TMEM_COLS = tmem_cols_for(2 * BN);
+    constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF);
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + L::MISC_OFF);  // [0] tmem, [1] abort, [2] last flag
+    const uint32_t sbase = ptx::smem_addr(smem);
+    const uint32_t bar0 = ptx::smem_addr(bars);
+    auto FULL = [&](int s) { return bar0 + 8u * s; };
+    auto EMPTY = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto TFULL = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+    auto TEMPTY = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+    const uint32_t DONE = bar0 + 8u * (2 * STAGES + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    volatile uint32_t *abort_flag = misc + 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(FULL(s), 1);
+            ptx::mbar_init(EMPTY(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(TFULL(a), 1);
+            ptx::mbar_init(TEMPTY(a), kEpiThreads);
+        }
+        ptx::mbar_init(DONE, 1);
+        misc[1] = 0;
+        misc[2] = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_addr(misc), TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&tmX);
+        ptx::prefetch_tmap(&tmY);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = misc[0];
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol_x = SWAP ? ptx::policy_evict_first() : ptx::policy_evict_last();
+            const uint64_t pol_y = ptx::policy_evict_last();
+            int stage = 0;
+            uint32_t phase = 0;
+            long long issued = 0;
+            SegIter it(sched, blockIdx.x);
+            Segment seg;
+            bool ok = true;
+            while (ok && it.next(sched, seg)) {
+                int tr, tq;
+                tile_coords(sched, seg.tile, tr, tq);
+                for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
+                    if (!wait_bar(EMPTY(stage), phase ^ 1u, abort_flag, d_error)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!sched.stall) {
+                        ptx::mbar_arrive_expect_tx(FULL(stage), L::STAGE_BYTES);
+                        const uint32_t xs = sbase + stage * L::STAGE_BYTES;
+                        ptx::tma_load_2d(xs, &tmX, FULL(stage), kb * BK, tr * BM, pol_x);
+                        ptx::tma_load_2d(xs + L::X_BYTES, &tmY, FULL(stage), kb * BK, tq * BN, pol_y);
+                        ++issued;
+                    }
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // drain: every stage's most recent copy must land before exit
+                for (int s = 0; s < STAGES; ++s) {
+                    if (issued <= s) continue;
+                    const long long last = issued - 1 - ((issued - 1 - s) % STAGES);
+                    wait_bar_drain(FULL(s), (uint32_t)((last / STAGES) & 1));
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            SegIter it(sched, blockIdx.x);
+            Segment seg;
+            bool ok = true;
+            while (ok && it.next(sched, seg)) {
+                if (!wait_bar(TEMPTY(acc), acc_phase ^ 1u, abort_flag, d_error)) break;
+                ptx::tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(acc * BN);
+                for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
+                    if (!wait_bar(FULL(stage), phase, abort_flag, d_error)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t xs = sbase + stage * L::STAGE_BYTES;
+                    const uint64_t ad = ptx::sdesc_kmajor_sw128(xs);
+                    const uint64_t bd = ptx::sdesc_kmajor_sw128(xs + L::X_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)   // +32 bytes along K per step
+                        ptx::mma_bf16(d, ad + 2u * k, bd + 2u * k, IDESC, (kb > seg.kb0 || k > 0) ? 1u : 0u);
+                    ptx::mma_commit(EMPTY(stage));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                ptx::mma_commit(TFULL(acc));
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            ptx::mma_commit(DONE);          // every issued MMA retires before TMEM is freed
+            wait_bar_drain(DONE, 0);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q4 = warp & 3;            // TMEM lane quarter this warp may read
+        const int row = q4 * 32 + lane;     // accumulator row
+        const int etid = threadIdx.x - 64;  // 0..127
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        SegIter it(sched, blockIdx.x);
+        Segment seg;
+        while (it.next(sched, seg)) {
+            if (!wait_bar(TFULL(acc), acc_phase, abort_flag, d_error)) break;
+            ptx::tc_fence_after();
+            int tr, tq;
+            tile_coords(sched, seg.tile, tr, tq);
+            const int r = tr * BM + row;
+            const int qb = tq * BN;
+            const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(acc * BN);
+            const bool whole = seg.kb0 == 0 && seg.kb1 == sched.nk;
+            float *part = ws + (int64_t)(blockIdx.x * 2 + seg.slot) * (BM * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 16) {
+                uint32_t v[16];
+                __syncwarp();
+                ptx::tmem_ld16(taddr + (uint32_t)c, v);
+                ptx::tmem_wait_ld();
+                float f[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(v[j]);
+                if (whole) {
+                    store_chunk<SWAP>(C, ldc, R, Q, r, qb + c, f);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) __stcg(part + (c + j) * BM + row, f[j]);
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(TEMPTY(acc));
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+            if (whole) continue;
+
+            // ---- stream-K fixup: the last contributor of this tile sums the partials
+            const int t = seg.tile;
+            const int c_first = cta_of_unit(sched, (long long)t * sched.nk);
+            const int c_last = cta_of_unit(sched, (long long)(t + 1) * sched.nk - 1);
+            __threadfence();
+            ptx::named_bar_sync(1, kEpiThreads);
+            if (etid == 0) {
+                const int old = atomicAdd(counters + t, 1);
+                const bool last = old == c_last - c_first;
+                if (last) counters[t] = 0;
+                misc[2] = last ? 1u : 0u;
+            }
+            ptx::named_bar_sync(1, kEpiThreads);
+            if (!misc[2]) continue;
+            __threadfence();
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 16) {
+                float f[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) f[j] = 0.f;
+#pragma unroll 1
+                for (int cta = c_first; cta <= c_last; ++cta) {
+                    const int first_tile = (int)(range_begin(sched, cta) / sched.nk);
+                    const int slot = first_tile == t ? 0 : 1;
+                    const float *p = ws + (int64_t)(cta * 2 + slot) * (BM * BN) + (int64_t)c * BM + row;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) f[j] += __ldcg(p + j * BM);
+                }
+                store_chunk<SWAP>(C, ldc, R, Q, r, qb + c, f);
+            }
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// [rows, K] bf16 row-major with leading dimension ld (elements); box 64 x box_rows,
+// 128-byte swizzle, out-of-range elements read as zero.
+bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int64_t ld, int box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int BN, int STAGES, bool SWAP>
+cudaError_t launch_t(const CUtensorMap &mx, const CUtensorMap &my, uint16_t *C, int R, int Q, int64_t ldc,
+                     const Sched &s, const LaunchCtx &c)
+{
+    using L = Layout<BN, STAGES>;
+    static std::once_flag once[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaError_t attr = cudaSuccess;
+    std::call_once(once[dev & 63], [&] {
+        attr = cudaFuncSetAttribute(k_umma<BN, STAGES, SWAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    L::SMEM);
+    });
+    if (attr != cudaSuccess) return attr;
+    k_umma<BN, STAGES, SWAP><<<s.grid, kThreads, L::SMEM, c.stream>>>(mx, my, C, R, Q, ldc, s, c.workspace,
+                                                                         c.counters, c.d_error);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int umma_stages(int bn)
+{
+    return bn <= 32 ? 8 : bn <= 128 ? 6 : 4;
+}
+
+int umma_smem_bytes(int bn)
+{
+    switch (bn) {
+    case 16: return Layout<16, 8>::SMEM;
+    case 32: return Layout<32, 8>::SMEM;
+    case 64: return Layout<64, 6>::SMEM;
+    case 128: return Layout<128, 6>::SMEM;
+    default: return Layout<256, 4>::SMEM;
+    }
+}
+
+int g_debug_stall = 0;
+
+cudaError_t launch_umma_bf16(const GemmArgs &a, const Plan &p, const LaunchCtx &c)
+{
+    const bool swap = p.variant == GEMM_VARIANT_SKINNY;
+    const void *X = swap ? a.B : a.A;
+    const void *Y = swap ? a.A : a.B;
+    const int64_t R = swap ? a.N : a.M, Q = swap ? a.M : a.N;
+    const int64_t ldx = swap ? a.ldb : a.lda, ldy = swap ? a.lda : a.ldb;
+    CUtensorMap mx, my;
+    if (!make_map(&mx, X, R, a.K, ldx, BM) || !make_map(&my, Y, Q, a.K, ldy, p.bn))
+        return cudaErrorInvalidValue;
+    Sched s{};
+    s.mode = p.mode;
+    s.tiles_r = (int)((R + BM - 1) / BM);
+    s.tiles_q = (int)((Q + p.bn - 1) / p.bn);
+    s.tiles = s.tiles_r * s.tiles_q;
+    s.nk = (int)((a.K + BK - 1) / BK);
+    s.grid = p.grid;
+    s.group_r = p.group_r > 0 ? p.group_r : s.tiles_r;
+    s.units = (long long)s.tiles * s.nk;
+    s.stall = g_debug_stall;
+    uint16_t *C = (uint16_t *)a.C;
+    const int r = (int)R, q = (int)Q;
+    if (swap) {
+        switch (p.bn) {
+        case 16: return launch_t<16, 8, true>(mx, my, C, r, q, a.ldc, s, c);
+        case 32: return launch_t<32, 8, true>(mx, my, C, r, q, a.ldc, s, c);
+        case 64: return launch_t<64, 6, true>(mx, my, C, r, q, a.ldc, s, c);
+        case 128: return launch_t<128, 6, true>(mx, my, C, r, q, a.ldc, s, c);
+        default: return cudaErrorInvalidValue;
+        }
+    }
+    switch (p.bn) {
+    case 256: return launch_t<256, 4, false>(mx, my, C, r, q, a.ldc, s, c);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace dbw

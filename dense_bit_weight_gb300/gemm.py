@@ -1,0 +1,186 @@
+"""Thin ctypes binding of libdbw_gemm.so (the C ABI in include/dbw_gemm.h).
+
+Argument marshalling only: torch tensors become device pointers, sizes and
+the current CUDA stream handle; every step of the computation runs in the
+library's kernels.  Importing this module loads the library and raises
+ImportError when it has not been built -- there is no other implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libdbw_gemm.so")
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(
+        f"{_LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+lib = ctypes.CDLL(_LIB_PATH)
+
+GEMM_OK = 0
+STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_NULL", 2: "GEMM_ERR_SHAPE", 3: "GEMM_ERR_LD",
+          4: "GEMM_ERR_ALIGN", 5: "GEMM_ERR_GROUP", 6: "GEMM_ERR_CUDA",
+          7: "GEMM_ERR_DEVICE_TIMEOUT", 8: "GEMM_ERR_ARCH", 9: "GEMM_ERR_ALIAS",
+          10: "GEMM_ERR_VARIANT"}
+VARIANT = {"auto": 0, "gemv": 1, "skinny": 2, "prefill": 3, "zero": 4}
+VARIANT_NAME = {v: k for k, v in VARIANT.items()}
+
+EXPORTS = ["gemm_bf16", "gemm_w4a16", "gemm_bf16_ex", "gemm_w4a16_ex", "gemm_bf16_plan",
+           "gemm_w4a16_plan", "gemm_last_device_error", "gemm_status_string", "gemm_shutdown",
+           "gemm_debug_inject_timeout"]
+
+
+class gemm_plan(ctypes.Structure):
+    _fields_ = [("variant", ctypes.c_int), ("kernels", ctypes.c_int), ("grid", ctypes.c_int),
+                ("split", ctypes.c_int), ("tile_m", ctypes.c_int), ("tile_n", ctypes.c_int),
+                ("stages", ctypes.c_int), ("reserved", ctypes.c_int)]
+
+    def as_dict(self):
+        d = {f: getattr(self, f) for f, _ in self._fields_}
+        d["variant_name"] = VARIANT_NAME.get(self.variant, "?")
+        return d
+
+
+_p, _i64, _i = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+lib.gemm_bf16.argtypes = [_p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _p]
+lib.gemm_bf16_ex.argtypes = lib.gemm_bf16.argtypes + [_i]
+lib.gemm_w4a16.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _p]
+lib.gemm_w4a16_ex.argtypes = lib.gemm_w4a16.argtypes + [_i]
+lib.gemm_bf16_plan.argtypes = [_i64, _i64, _i64, _i, _i, ctypes.POINTER(gemm_plan)]
+lib.gemm_w4a16_plan.argtypes = [_i64, _i64, _i64, _i64, _i, _i, ctypes.POINTER(gemm_plan)]
+lib.gemm_last_device_error.argtypes = []
+lib.gemm_status_string.argtypes = [_i]
+lib.gemm_status_string.restype = ctypes.c_char_p
+lib.gemm_debug_inject_timeout.argtypes = [_i]
+lib.gemm_debug_inject_timeout.restype = _i
+lib.gemm_shutdown.argtypes = []
+lib.gemm_shutdown.restype = None
+for _f in ("gemm_bf16", "gemm_bf16_ex", "gemm_w4a16", "gemm_w4a16_ex", "gemm_bf16_plan",
+           "gemm_w4a16_plan", "gemm_last_device_error"):
+    getattr(lib, _f).restype = _i
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({gemm_status_string(status)})")
+
+
+def _check(rc: int, where: str):
+    if rc != GEMM_OK:
+        raise GemmError(rc, where)
+
+
+def gemm_status_string(status: int) -> str:
+    return lib.gemm_status_string(int(status)).decode()
+
+
+def gemm_last_device_error() -> int:
+    return int(lib.gemm_last_device_error())
+
+
+def gemm_debug_inject_timeout(enable: bool) -> bool:
+    """Test hook: make the tcgen05 kernels' bounded waits expire (see the header)."""
+    return bool(lib.gemm_debug_inject_timeout(1 if enable else 0))
+
+
+def gemm_shutdown() -> None:
+    lib.gemm_shutdown()
+
+
+def _variant(v) -> int:
+    return VARIANT[v] if isinstance(v, str) else int(v)
+
+
+def gemm_bf16_plan(M: int, N: int, K: int, variant="auto", num_sms: int = 0) -> dict:
+    out = gemm_plan()
+    _check(lib.gemm_bf16_plan(M, N, K, _variant(variant), num_sms, ctypes.byref(out)), "gemm_bf16_plan")
+    return out.as_dict()
+
+
+def gemm_w4a16_plan(M: int, N: int, K: int, group: int, variant="auto", num_sms: int = 0) -> dict:
+    out = gemm_plan()
+    _check(lib.gemm_w4a16_plan(M, N, K, group, _variant(variant), num_sms, ctypes.byref(out)),
+           "gemm_w4a16_plan")
+    return out.as_dict()
+
+
+# --------------------------------------------------------------- torch layer
+
+def _stream_handle(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _row_major_2d(t, name):
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be a 2-D tensor with unit stride along its last dimension")
+    return t.stride(0)
+
+
+def gemm_bf16(A, B, C=None, stream=None, variant="auto"):
+    """C[M,N] = A[M,K] @ B[N,K]^T on the device (bf16 in, fp32 accumulate, bf16 out).
+
+    A and B are CUDA bf16 tensors with unit stride along K; C (optional) is a
+    CUDA bf16 [M,N] tensor with unit stride along N.  Runs on ``stream`` (the
+    current torch stream by default) without synchronising.  Returns C.
+    """
+    import torch
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
+        raise TypeError("A and B must be bfloat16")
+    if not (A.is_cuda and B.is_cuda):
+        raise ValueError("A and B must be CUDA tensors")
+    M, K = A.shape
+    N, K2 = B.shape
+    if K != K2:
+        raise ValueError(f"K mismatch: {A.shape} vs {B.shape}")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    if C.dtype != torch.bfloat16 or tuple(C.shape) != (M, N):
+        raise ValueError("C must be bfloat16 [M,N]")
+    lda, ldb, ldc = _row_major_2d(A, "A"), _row_major_2d(B, "B"), _row_major_2d(C, "C")
+    rc = lib.gemm_bf16_ex(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, lda, ldb, ldc,
+                          _stream_handle(stream), _variant(variant))
+    _check(rc, "gemm_bf16")
+    return C
+
+
+def gemm_w4a16(A, Bq, scales, zeros, group: int, C=None, stream=None, variant="auto"):
+    """C[M,N] = A[M,K] @ W[N,K]^T with W = (q - z) * s, q packed 8 per int32 along K.
+
+    A bf16 [M,K]; Bq int32 [N,K/8]; scales bf16 [N,K/group]; zeros uint8
+    [N,K/group]; all contiguous CUDA tensors.  Returns C bf16 [M,N].
+    """
+    import torch
+    M, K = A.shape
+    N = Bq.shape[0]
+    for t, name, dt in ((A, "A", torch.bfloat16), (Bq, "Bq", torch.int32),
+                        (scales, "scales", torch.bfloat16), (zeros, "zeros", torch.uint8)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
+    if tuple(Bq.shape) != (N, K // 8) or tuple(scales.shape) != (N, K // group) \
+            or tuple(zeros.shape) != (N, K // group):
+        raise ValueError("W4A16 operand shapes do not match")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    if C.dtype != torch.bfloat16 or tuple(C.shape) != (M, N) or not C.is_contiguous():
+        raise ValueError("C must be a contiguous bfloat16 [M,N] tensor")
+    rc = lib.gemm_w4a16_ex(A.data_ptr(), Bq.data_ptr(), scales.data_ptr(), zeros.data_ptr(),
+                           C.data_ptr(), M, N, K, group, _stream_handle(stream), _variant(variant))
+    _check(rc, "gemm_w4a16")
+    return C
+
+
+# --------------------------------------------------------------- raw pointers
+
+def gemm_bf16_ptr(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
+                  stream: int = 0, variant="auto") -> int:
+    """The C call on raw device addresses; returns the gemm_status."""
+    return int(lib.gemm_bf16_ex(A, B, C, M, N, K, lda, ldb, ldc, ctypes.c_void_p(stream),
+                                _variant(variant)))
+
+
+def gemm_w4a16_ptr(A: int, Bq: int, scales: int, zeros: int, C: int, M: int, N: int, K: int,
+                   group: int, stream: int = 0, variant="auto") -> int:
+    return int(lib.gemm_w4a16_ex(A, Bq, scales, zeros, C, M, N, K, group, ctypes.c_void_p(stream),
+                                 _variant(variant)))

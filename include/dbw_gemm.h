@@ -1,0 +1,170 @@
+/*
+ * dbw_gemm.h -- C ABI of the GB300 projection-GEMM library (libdbw_gemm.so).
+ *
+ * The operation is the transformer projection
+ *
+ *     C[M,N] = A[M,K] . B[N,K]^T
+ *
+ * with A and B stored K-contiguous ("NT"), bf16 inputs, fp32 accumulation and
+ * bf16 output (round to nearest, ties to even).  Sources: FlyDSL prebuilt
+ * kernels guide, §3.1 "Preshuffle GEMM" (C = A @ B^T with B stored [N,K], M a
+ * run-time argument); FlyDSL-in-PyTorch blog (aixai.ru), sections "Dense GEMM"
+ * (bf16 NT shapes) and "MXFP" (unit stride along K for A and B, fp32
+ * accumulation, bf16 output).  The 4-bit-weight variant is the W4A16 (AWQ)
+ * decode GEMM of the hk-dsl PyPI page, section "Results".
+ *
+ * Conventions shared by every entry point
+ *   - All matrix pointers are DEVICE pointers owned by the caller; the library
+ *     never frees or retains them beyond the call's stream work.
+ *   - Sizes and leading dimensions are int64_t and counted in ELEMENTS.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and the call returns without synchronising.  Results are
+ *     visible to later work on the same stream.
+ *   - A precondition failure returns an error code and enqueues nothing.
+ *     There is no fallback of any kind: an unsupported input is an error.
+ *   - The library owns only lazily created per-device internals (the device
+ *     error word and the split-K workspace), created on the first call on each
+ *     device and released by gemm_shutdown().  The first call on a device
+ *     (and the first split-K call on a stream) must not happen inside CUDA
+ *     stream capture, because it allocates.
+ *   - Determinism: identical inputs give bitwise identical outputs; K-split
+ *     partial sums are added in a fixed order, with no floating-point atomics.
+ *   - The device must be compute capability 10.3 (GB300, sm_103a).
+ */
+#ifndef DBW_GEMM_H
+#define DBW_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_NULL = 1,           /* a required pointer is NULL                     */
+    GEMM_ERR_SHAPE = 2,          /* negative size, K % 8 != 0, or size too large   */
+    GEMM_ERR_LD = 3,             /* leading dimension < row length or not % 8      */
+    GEMM_ERR_ALIGN = 4,          /* a base pointer is not 16-byte aligned          */
+    GEMM_ERR_GROUP = 5,          /* W4A16 group not in {32,64,128} or K % group    */
+    GEMM_ERR_CUDA = 6,           /* a CUDA runtime call or launch failed           */
+    GEMM_ERR_DEVICE_TIMEOUT = 7, /* a kernel's bounded wait expired (see below)    */
+    GEMM_ERR_ARCH = 8,           /* current device is not compute capability 10.3  */
+    GEMM_ERR_ALIAS = 9,          /* C overlaps an input                            */
+    GEMM_ERR_VARIANT = 10        /* a forced variant cannot run this shape         */
+} gemm_status;
+
+/* Kernel variants (what gemm_*_plan reports and gemm_*_ex may force). */
+typedef enum {
+    GEMM_VARIANT_AUTO = 0,
+    GEMM_VARIANT_GEMV = 1,       /* CUDA-core weight streaming, small M            */
+    GEMM_VARIANT_SKINNY = 2,     /* tcgen05, weights as the MMA M side (swap AB)   */
+    GEMM_VARIANT_PREFILL = 3,    /* tcgen05, persistent warp-specialised tiles     */
+    GEMM_VARIANT_ZERO = 4        /* K == 0: C is the empty sum, written as zeros   */
+} gemm_variant;
+
+typedef struct {
+    int variant;   /* gemm_variant chosen                                         */
+    int kernels;   /* kernel launches one call makes                              */
+    int grid;      /* CTAs of the main kernel                                     */
+    int split;     /* K splits per output tile (1 = none)                         */
+    int tile_m;    /* output rows (M) per tile                                    */
+    int tile_n;    /* output columns (N) per tile                                 */
+    int stages;    /* shared-memory pipeline stages (0 for CUDA-core kernels)     */
+    int reserved;
+} gemm_plan;
+
+/*
+ * gemm_bf16 -- C = A . B^T, bf16 in / fp32 accumulate / bf16 out.
+ *
+ *   A   [M,K] bf16, row m at A + m*lda            (read only)
+ *   B   [N,K] bf16, row n at B + n*ldb            (read only; the weights)
+ *   C   [M,N] bf16, row m at C + m*ldc            (written; must not overlap A, B)
+ *   M, N, K >= 0, K % 8 == 0, each < 2^31.  M == 0 or N == 0: nothing to do,
+ *   returns GEMM_OK.  K == 0: C is set to zero.
+ *   lda >= K, ldb >= K, ldc >= N, each a multiple of 8.
+ *   A, B, C 16-byte aligned (rows are then 16-byte aligned too).
+ *   stream: cudaStream_t.
+ * Returns gemm_status.
+ */
+int gemm_bf16(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
+              int64_t lda, int64_t ldb, int64_t ldc, void *stream);
+
+/*
+ * gemm_w4a16 -- C = A . W^T with group-quantised 4-bit weights
+ *     W[n,k] = (q[n,k] - z[n, k/group]) * s[n, k/group].
+ *
+ *   A       [M,K] bf16, dense (row m at A + m*K)
+ *   Bq      [N,K/8] int32, dense: q[n,k] = bits 4*(k%8) .. 4*(k%8)+3 of
+ *           Bq[n*(K/8) + k/8] (eight unsigned nibbles per word, low nibble
+ *           first, sequential along K)
+ *   scales  [N,K/group] bf16, dense
+ *   zeros   [N,K/group] uint8, dense, values 0..15 (the 4-bit zero point)
+ *   C       [M,N] bf16, dense (row m at C + m*N); must not overlap any input
+ *   group in {32, 64, 128}; K % group == 0; K % 8 == 0; N % 8 == 0.
+ *   A, Bq, C 16-byte aligned; scales 2-byte aligned.
+ * The dequantised weight may be rounded to bf16 before it is multiplied
+ * (relative error <= 2^-9 per weight); accumulation is fp32.
+ * Returns gemm_status.
+ */
+int gemm_w4a16(const void *A, const void *Bq, const void *scales, const void *zeros, void *C,
+               int64_t M, int64_t N, int64_t K, int64_t group, void *stream);
+
+/*
+ * gemm_bf16_ex / gemm_w4a16_ex -- as above, but `variant` may force a kernel
+ * family (GEMM_VARIANT_AUTO picks as the plain call does).  A forced variant
+ * that cannot run the shape returns GEMM_ERR_VARIANT and enqueues nothing.
+ * Meant for tests and measurements that need a specific kernel.
+ */
+int gemm_bf16_ex(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
+                 int64_t lda, int64_t ldb, int64_t ldc, void *stream, int variant);
+int gemm_w4a16_ex(const void *A, const void *Bq, const void *scales, const void *zeros,
+                  void *C, int64_t M, int64_t N, int64_t K, int64_t group, void *stream,
+                  int variant);
+
+/*
+ * gemm_bf16_plan / gemm_w4a16_plan -- the launch plan a call with these sizes
+ * would use, without launching anything.  num_sms > 0 plans for that many
+ * SMs (host-only, no GPU needed); num_sms == 0 queries the current device.
+ * Returns a gemm_status for the sizes (pointers are not checked).
+ */
+int gemm_bf16_plan(int64_t M, int64_t N, int64_t K, int variant, int num_sms, gemm_plan *out);
+int gemm_w4a16_plan(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int num_sms,
+                    gemm_plan *out);
+
+/*
+ * gemm_last_device_error -- the device error word of the current device.
+ * Every wait inside the tcgen05 kernels is bounded (about a second); on
+ * expiry the kernel records GEMM_ERR_DEVICE_TIMEOUT here, drains its own
+ * copies, frees its tensor memory and returns, so the context stays usable
+ * and C holds unspecified values.  Call after synchronising the stream.
+ * Reading the word clears it.  Returns GEMM_OK when nothing was recorded.
+ * After a timeout, call gemm_shutdown() before further calls so the split-K
+ * workspace is rebuilt from zero.
+ */
+int gemm_last_device_error(void);
+
+/*
+ * gemm_debug_inject_timeout -- TEST HOOK.  While enabled (non-zero), the
+ * tcgen05 kernels' producer issues no tile copies, so the MMA issuer's bounded
+ * wait on the first stage expires after about a second; the kernel records
+ * GEMM_ERR_DEVICE_TIMEOUT in the device error word and exits cleanly (C is
+ * left unspecified).  Lets a test exercise the watchdog without faulting or
+ * hanging the GPU.  Process-wide; returns the previous setting.
+ */
+int gemm_debug_inject_timeout(int enable);
+
+/* A static, human-readable name for a gemm_status value. */
+const char *gemm_status_string(int status);
+
+/*
+ * gemm_shutdown -- synchronise every device the library has used and free
+ * its internals (error words, split-K workspaces).  Later calls recreate them.
+ */
+void gemm_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DBW_GEMM_H */

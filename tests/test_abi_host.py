@@ -1,0 +1,149 @@
+"""Host-side checks of the C ABI: no GPU needed, nothing is launched.
+
+The library must load, export every function declared in include/dbw_gemm.h,
+reject every precondition violation with its status code before touching a
+device, and plan launches as a pure function of the sizes and the SM count.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from dense_bit_weight_gb300 import build as _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dbw_gemm.h")
+
+
+@pytest.fixture(scope="module")
+def g():
+    _build.build()
+    from dense_bit_weight_gb300 import gemm
+    return gemm
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(gemm_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(g):
+    names = declared_functions()
+    assert {"gemm_bf16", "gemm_w4a16", "gemm_last_device_error", "gemm_status_string",
+            "gemm_shutdown"} <= set(names)
+    out = subprocess.run(["nm", "-D", "--defined-only", g._LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s+(\w+)$", out, flags=re.M))
+    for n in names:
+        assert n in exported, n
+        assert hasattr(g.lib, n)
+    assert sorted(names) == sorted(g.EXPORTS)
+
+
+def test_status_strings(g):
+    for code in range(0, 11):
+        s = g.gemm_status_string(code)
+        assert s and s != "unknown status"
+    assert g.gemm_status_string(99) == "unknown status"
+
+
+A16 = 1 << 20   # a fake 16-byte aligned address: never dereferenced, nothing launches
+
+
+def bf16(**kw):
+    a = dict(A=A16, B=A16 * 4, C=A16 * 8, M=4, N=16, K=32, lda=32, ldb=32, ldc=16)
+    a.update(kw)
+    return a
+
+
+def call_bf16(g, **kw):
+    a = bf16(**kw)
+    return g.gemm_bf16_ptr(a["A"], a["B"], a["C"], a["M"], a["N"], a["K"], a["lda"], a["ldb"], a["ldc"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(M=-1), 2), (dict(N=-3), 2), (dict(K=-8), 2), (dict(K=12, lda=16, ldb=16), 2),
+    (dict(K=1 << 31, lda=1 << 31, ldb=1 << 31), 2),
+    (dict(A=0), 1), (dict(B=0), 1), (dict(C=0), 1),
+    (dict(lda=24), 3), (dict(ldb=36), 3), (dict(ldc=8), 3), (dict(ldc=20), 3),
+    (dict(A=A16 + 2), 4), (dict(B=A16 * 4 + 8), 4), (dict(C=A16 * 8 + 4), 4),
+    (dict(C=A16 + 64), 9), (dict(C=A16 * 4), 9),
+])
+def test_bf16_rejects_before_launch(g, kw, code):
+    assert call_bf16(g, **kw) == code
+
+
+def test_bf16_empty_is_ok_without_device(g):
+    # M == 0 or N == 0: nothing to do, no device needed
+    assert call_bf16(g, M=0) == 0
+    assert call_bf16(g, N=0, ldc=8) == 0
+    assert call_bf16(g, M=0, A=0, B=0) == 0
+
+
+def call_w4(g, **kw):
+    a = dict(A=A16, Bq=A16 * 4, S=A16 * 8, Z=A16 * 12, C=A16 * 16, M=1, N=64, K=256, group=128)
+    a.update(kw)
+    return g.gemm_w4a16_ptr(a["A"], a["Bq"], a["S"], a["Z"], a["C"], a["M"], a["N"], a["K"], a["group"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(group=16), 5), (dict(group=96), 5), (dict(K=320, group=128), 5), (dict(group=0), 5),
+    (dict(K=0), 2), (dict(N=12), 2), (dict(M=-1), 2),
+    (dict(A=0), 1), (dict(Bq=0), 1), (dict(S=0), 1), (dict(Z=0), 1), (dict(C=0), 1),
+    (dict(A=A16 + 8), 4), (dict(Bq=A16 * 4 + 4), 4), (dict(C=A16 * 16 + 2), 4), (dict(S=A16 * 8 + 1), 4),
+    (dict(C=A16 * 4 + 32), 9),
+])
+def test_w4a16_rejects_before_launch(g, kw, code):
+    assert call_w4(g, **kw) == code
+
+
+def test_plans_are_host_only_and_cover_the_workloads(g):
+    sms = 152
+    for M in (1, 8, 32, 128):
+        for N, K in ((6144, 4096), (4096, 4096), (24576, 4096)):
+            p = g.gemm_bf16_plan(M, N, K, num_sms=sms)
+            assert p["variant"] in (1, 2, 3) and p["kernels"] >= 1 and p["grid"] >= 1
+    for M in (1024, 4096, 16384):
+        p = g.gemm_bf16_plan(M, 8192, 8192, num_sms=sms)
+        assert p["variant"] in (1, 2, 3)
+    assert g.gemm_bf16_plan(5, 7, 0, num_sms=sms)["variant"] == 4
+    for M in (1, 16, 64, 128):
+        p = g.gemm_w4a16_plan(M, 7168, 5120, 128, num_sms=sms)
+        assert p["variant"] in (1, 2, 3)
+    with pytest.raises(g.GemmError):
+        g.gemm_bf16_plan(4, 4, 4, num_sms=sms)       # K % 8
+    with pytest.raises(g.GemmError):
+        g.gemm_w4a16_plan(4, 64, 256, 48, num_sms=sms)
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    # the binding must raise, not fall back, when the shared library is absent
+    code = (
+        "import sys, os, importlib.util\n"
+        f"sys.path.insert(0, {ROOT!r})\n"
+        "import dense_bit_weight_gb300.gemm as m\n"
+        "src = m.__file__\n"
+        "spec = importlib.util.spec_from_file_location('g2', src)\n"
+        "mod = importlib.util.module_from_spec(spec)\n"
+        "m_path = m._LIB_PATH\n"
+        "import builtins\n"
+        "real = os.path.exists\n"
+        "os.path.exists = lambda p: False if p == m_path else real(p)\n"
+        "try:\n"
+        "    spec.loader.exec_module(mod)\n"
+        "except ImportError as e:\n"
+        "    print('raised', 'missing' in str(e))\n"
+    )
+    out = subprocess.run(["python", "-c", code], capture_output=True, text=True)
+    assert "raised True" in out.stdout, out.stdout + out.stderr
+
+
+def test_k_zero_ignores_empty_inputs(g):
+    # K == 0: A and B are empty and never read, so their pointers and leading
+    # dimensions are not checked (the call still needs a device, so only the
+    # C-side checks are observable here)
+    assert call_bf16(g, K=0, A=0, B=0, lda=1, ldb=3, ldc=5) == 3      # ldc still checked
+    assert call_bf16(g, K=0, A=0, B=0, C=0) == 1

@@ -1,0 +1,38 @@
+"""The tcgen05 kernels' bounded waits: a forced stall must end in a recorded
+GEMM_ERR_DEVICE_TIMEOUT and a clean exit, leaving the context usable.
+
+The stall is a test hook (gemm_debug_inject_timeout): the producer issues no
+copies, so the MMA issuer's wait on the first stage runs out after about a
+second.  Nothing faults or traps; the GPU stays usable, which the test checks
+by running the same GEMM correctly afterwards.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from gpu_helpers import assert_close, bf16_inputs, dev_bf16, host_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("variant,M", [("skinny", 16), ("prefill", 256)])
+def test_forced_timeout_is_reported_and_recoverable(variant, M):
+    import torch
+    from dense_bit_weight_gb300 import gemm as g
+    N, K = 512, 512
+    A, B = bf16_inputs(M, N, K, seed=5)
+    dA, dB = dev_bf16(A), dev_bf16(B)
+    assert g.gemm_last_device_error() == 0
+    g.gemm_debug_inject_timeout(True)
+    try:
+        g.gemm_bf16(dA, dB, variant=variant)
+        torch.cuda.synchronize()
+    finally:
+        g.gemm_debug_inject_timeout(False)
+    assert g.gemm_last_device_error() == 7          # GEMM_ERR_DEVICE_TIMEOUT
+    assert g.gemm_last_device_error() == 0          # reading clears it
+    g.gemm_shutdown()
+    C = g.gemm_bf16(dA, dB, variant=variant)
+    torch.cuda.synchronize()
+    assert_close(host_bits(C), oracle.gemm_bf16(A, B), what=f"after timeout {variant}")
+    assert g.gemm_last_device_error() == 0
