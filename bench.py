@@ -148,17 +148,18 @@ class Arm:
     def call(self, it):
         rc = self.g.gemm_bf16_ptr(it["A"].data_ptr(), it["B"].data_ptr(), it["C"].data_ptr(),
                                   it["M"], it["N"], it["K"], it["K"], it["K"], it["N"],
-                                  self.stream.cuda_stream)
+                                  self.torch.cuda.current_stream().cuda_stream)
         if rc:
             raise self.g.GemmError(rc, "gemm_bf16")
 
     def step(self, events=None):
+        cur = self.torch.cuda.current_stream()
         for i, it in enumerate(self.items):
             if events is not None:
-                events[i][0].record(self.stream)
+                events[i][0].record(cur)
             self.call(it)
             if events is not None:
-                events[i][1].record(self.stream)
+                events[i][1].record(cur)
 
 
 def dist_init(args):
@@ -191,8 +192,33 @@ def barrier(ws):
         dist.barrier()
 
 
-def timed_sweep(g, torch, shapes, kind, reps=10, warmup=3):
-    """Per-shape device time (ms, median of reps) for the extra sweeps."""
+def graph_time_ms(torch, fn, reps):
+    """Device time per call of fn, from one CUDA-graph replay of `reps` calls
+    (captured after eager warm-up on the same stream, so the library's
+    per-stream workspace exists before capture)."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for i in range(3):
+            fn(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(reps):
+            fn(i)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        g.replay()
+        e1.record(s)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def timed_sweep(g, torch, shapes, kind, reps=20):
+    """Per-shape device time (ms per launch) for the extra sweeps."""
     dev = torch.device("cuda")
     gen = torch.Generator(device=dev)
     gen.manual_seed(1)
@@ -218,17 +244,7 @@ def timed_sweep(g, torch, shapes, kind, reps=10, warmup=3):
                   for _ in range(copies)]
             fn = lambda i: g.gemm_bf16(A, Bs[i % copies], C)
             work = flops(M, N, K) if kind == "prefill" else bytes_bf16(M, N, K)
-        for i in range(warmup):
-            fn(i)
-        ts = []
-        for i in range(reps):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            fn(i)
-            e1.record()
-            ts.append((e0, e1))
-        torch.cuda.synchronize()
-        ms = float(np.median([a.elapsed_time(b) for a, b in ts]))
+        ms = graph_time_ms(torch, fn, reps)
         out.append({"M": M, "N": N, "K": K, "ms": ms, "work": work, "variant": plan["variant_name"]})
         del Bs, A, C
     return out
@@ -268,38 +284,92 @@ def run_ours(args):
     arm = Arm(torch.device("cuda", torch.cuda.current_device()))
     g = arm.g
     n_items = len(arm.items)
-    for _ in range(args.warmup):
-        arm.step()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):          # warm-up (also creates the stream's workspace)
+        for _ in range(args.warmup):
+            arm.step()
     torch.cuda.synchronize()
-    events = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(n_items)] for _ in range(args.steps)]
+
+    # One CUDA graph holds S steps with a pair of timing events around every
+    # GEMM; the timed region replays it K/S times (plus a graph of K % S steps),
+    # so exactly K steps run back to back without host launch gaps.
+    S = max(1, min(args.steps, args.graph_steps))
+    try:
+        mk = lambda: torch.cuda.Event(enable_timing=True, external=True)
+        mk()
+    except TypeError:
+        mk = None
+
+    def capture(nsteps):
+        evs = [[(mk(), mk()) for _ in range(n_items)] for _ in range(nsteps)] if mk else None
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            for k in range(nsteps):
+                arm.step(evs[k] if evs else None)
+        return gr, evs
+
+    graph, events = capture(S)
+    rest = args.steps % S
+    graph_rest, _ = capture(rest) if rest else (None, None)
+    with torch.cuda.stream(stream):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    def replay_steps():
+        for _ in range(args.steps // S):
+            graph.replay()
+        if graph_rest is not None:
+            graph_rest.replay()
+
     clocks = Clocks(torch.cuda.current_device())
     clocks.start()
-    time.sleep(0.3)
+    # keep the GPU under the same load around the timed region so the clock
+    # samples (every 200 ms) see the loaded state
+    t_end = time.time() + args.preroll
+    with torch.cuda.stream(stream):
+        while time.time() < t_end:
+            graph.replay()
+            torch.cuda.synchronize()
     barrier(ws)
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(arm.stream)
-    for s in range(args.steps):
-        arm.step(events[s])
-    t1.record(arm.stream)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        replay_steps()
+        t1.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
+    t_end = time.time() + args.preroll
+    with torch.cuda.stream(stream):
+        while time.time() < t_end:
+            graph.replay()
+            torch.cuda.synchronize()
     clk = clocks.stop()
     ms_total = barrier_max(t0.elapsed_time(t1), ws)
     step_bytes = sum(it["bytes"] for it in arm.items)
     value = ws * step_bytes * args.steps / (ms_total * 1e-3) / 1e9
 
-    # per-kernel durations over the timed region
+    # per-kernel durations: the events of the last replay of the S-step graph
+    # (events in a graph are overwritten by each replay)
     per = {}
-    for s in range(args.steps):
+    per_shape_ms = [0.0] * n_items
+    if events is None:
+        # no external events in this torch: time each GEMM alone in a graph of S calls
         for i, it in enumerate(arm.items):
-            d = events[s][i][0].elapsed_time(events[s][i][1])
-            e = per.setdefault(it["name"], {"ms": 0.0, "bytes": 0, "launches": 0})
-            e["ms"] += d
-            e["bytes"] += it["bytes"]
-            e["launches"] += it["plan"]["kernels"]
+            per_shape_ms[i] = graph_time_ms(torch, lambda _k, it=it: arm.call(it), S) * S
+        nsteps = S
+    else:
+        for k in range(S):
+            for i in range(n_items):
+                per_shape_ms[i] += events[k][i][0].elapsed_time(events[k][i][1])
+        nsteps = S
+    for i, it in enumerate(arm.items):
+        e = per.setdefault(it["name"], {"ms": 0.0, "bytes": 0, "launches": 0})
+        e["ms"] += per_shape_ms[i]
+        e["bytes"] += it["bytes"] * nsteps
+        e["launches"] += it["plan"]["kernels"] * nsteps
     dom_name = max(per, key=lambda k: per[k]["ms"])
     dom = per[dom_name]
     hbm, tf, tf_sus, src = peaks()
@@ -315,7 +385,7 @@ def run_ours(args):
     def e2e_step():
         for it, ha, hc in zip(arm.items, hostA, hostC):
             it["A"].copy_(ha, non_blocking=True)
-            g.gemm_bf16(it["A"], it["B"], it["C"])
+            arm.call(it)
             hc.copy_(it["C"], non_blocking=True)
 
     e2e_step()
@@ -354,8 +424,7 @@ def run_ours(args):
                                        r["variant"]] for r in rs]}
         sweeps["decode_per_shape"] = [
             [it["M"], it["N"], it["K"],
-             round(it["bytes"] * args.steps / (sum(events[s][i][0].elapsed_time(events[s][i][1])
-                                                  for s in range(args.steps)) * 1e-3) / 1e9, 1),
+             round(it["bytes"] * nsteps / (per_shape_ms[i] * 1e-3) / 1e9, 1),
              it["plan"]["variant_name"]] for i, it in enumerate(arm.items)]
 
     cpu = None
@@ -372,6 +441,7 @@ def run_ours(args):
             "ms_per_step": round(ms_total / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": WORKLOAD, "gemms_per_step": n_items,
+                       "timing": f"CUDA graph of {S} steps replayed; per-GEMM events inside the graph",
                        "l2": "inputs larger than L2: each GEMM has its own weight copy, "
                              f"{step_bytes / 1e9:.2f} GB streamed per step",
                        "parallelism": f"replicas x{ws}"},
@@ -449,8 +519,12 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--graph-steps", type=int, default=50,
+                    help="steps per captured CUDA graph (the timed region replays it)")
+    ap.add_argument("--preroll", type=float, default=0.6,
+                    help="seconds of untimed load before and after the timed region (clock sampling)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sweeps", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
