@@ -26,7 +26,7 @@ VARIANT_NAME = {v: k for k, v in VARIANT.items()}
 
 EXPORTS = ["gemm_bf16", "gemm_w4a16", "gemm_bf16_ex", "gemm_w4a16_ex", "gemm_bf16_plan",
            "gemm_w4a16_plan", "gemm_last_device_error", "gemm_status_string", "gemm_shutdown",
-           "gemm_debug_inject_timeout"]
+           "gemm_debug_inject_timeout", "gemm_bf16_noalloc"]
 
 
 class gemm_plan(ctypes.Structure):
@@ -43,6 +43,8 @@ class gemm_plan(ctypes.Structure):
 _p, _i64, _i = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
 lib.gemm_bf16.argtypes = [_p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _p]
 lib.gemm_bf16_ex.argtypes = lib.gemm_bf16.argtypes + [_i]
+lib.gemm_bf16_noalloc.argtypes = lib.gemm_bf16.argtypes
+lib.gemm_bf16_noalloc.restype = _i
 lib.gemm_w4a16.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _p]
 lib.gemm_w4a16_ex.argtypes = lib.gemm_w4a16.argtypes + [_i]
 lib.gemm_bf16_plan.argtypes = [_i64, _i64, _i64, _i, _i, ctypes.POINTER(gemm_plan)]
@@ -178,6 +180,12 @@ def gemm_bf16_ptr(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb:
     """The C call on raw device addresses; returns the gemm_status."""
     return int(lib.gemm_bf16_ex(A, B, C, M, N, K, lda, ldb, ldc, ctypes.c_void_p(stream),
                                 _variant(variant)))
+
+
+def gemm_bf16_noalloc_ptr(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int,
+                          ldc: int, stream: int = 0) -> int:
+    """gemm_bf16_noalloc on raw device addresses (allocates nothing); returns the gemm_status."""
+    return int(lib.gemm_bf16_noalloc(A, B, C, M, N, K, lda, ldb, ldc, ctypes.c_void_p(stream)))
 
 
 def gemm_w4a16_ptr(A: int, Bq: int, scales: int, zeros: int, C: int, M: int, N: int, K: int,
