@@ -184,9 +184,13 @@ void to_public(const Plan &p, gemm_plan *out)
 
 namespace dbw {
 
-// tcgen05 planning shared by the skinny (swap AB) and prefill layouts.
-// Whole tiles round-robin when they fill the SMs in nearly whole waves,
-// otherwise stream-K over (tile, k-block) units so every SM gets an equal share.
+// tcgen05 planning.
+// Skinny (decode, swap AB): one 128-row weight tile per CTA, K split over a
+// cluster of S CTAs (mode 2), S the smallest value in 1..8 that gives every SM
+// a CTA; two CTAs fit per SM, so the whole grid is resident at once and the
+// HBM stream is shared evenly without stream-K.
+// Prefill: whole tiles round-robin when they fill the SMs in nearly whole
+// waves (mode 0), otherwise stream-K over (tile, k-block) units (mode 1).
 static void plan_umma(int64_t M, int64_t N, int64_t K, bool swap, int bn, int sm_count, Plan *p)
 {
     const int64_t R = swap ? N : M, Q = swap ? M : N;
@@ -197,11 +201,19 @@ static void plan_umma(int64_t M, int64_t N, int64_t K, bool swap, int bn, int sm
     const int64_t G = sm_count;
     p->variant = swap ? GEMM_VARIANT_SKINNY : GEMM_VARIANT_PREFILL;
     p->bn = bn;
-    p->stages = umma_stages(bn);
+    p->stages = umma_stages(bn, swap);
     p->tile_m = swap ? bn : kUmmaBM;
     p->tile_n = swap ? kUmmaBM : bn;
     p->group_r = swap ? (int)tiles_r : (int)std::min<int64_t>(tiles_r, 16);
     p->kernels = 1;
+    if (swap) {
+        int64_t S = 1;
+        while (S < 8 && S < nk && tiles * S < G) ++S;
+        p->mode = 2;
+        p->split = (int)S;
+        p->grid = (int)(tiles * S);
+        return;
+    }
     const int64_t waves = (tiles + G - 1) / G;
     const double eff = (double)tiles / (double)(waves * G);
     if (tiles >= G && eff >= 0.9) {

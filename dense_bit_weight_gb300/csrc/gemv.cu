@@ -13,6 +13,7 @@
 // weight row per group of rows (the tcgen05 kernels serve those shapes).
 #include "common.cuh"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace dbw {
 namespace {
@@ -24,6 +25,8 @@ __global__ void __launch_bounds__(kWarps * 32)
 k_gemv_bf16(const uint16_t *__restrict__ A, const uint16_t *__restrict__ B,
             uint16_t *__restrict__ C, int M, int N, int K, int64_t lda, int64_t ldb, int64_t ldc)
 {
+    ptx::pdl_wait();
+    ptx::pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int chunks = K >> 3;  // 8 bf16 per 16-byte chunk
     for (int n = blockIdx.x * kWarps + (threadIdx.x >> 5); n < N; n += gridDim.x * kWarps) {
@@ -79,6 +82,8 @@ k_gemv_w4a16(const uint16_t *__restrict__ A, const uint32_t *__restrict__ Bq,
              const uint16_t *__restrict__ S, const uint8_t *__restrict__ Z,
              uint16_t *__restrict__ C, int M, int N, int K, int group)
 {
+    ptx::pdl_wait();
+    ptx::pdl_launch_dependents();
     constexpr int U = 4;
     const int lane = threadIdx.x & 31;
     const int chunks = K >> 5;      // 32 k (16 bytes of Bq) per chunk
@@ -143,6 +148,22 @@ __global__ void k_zero_fill(uint16_t *C, int M, int N, int64_t ldc)
         C[(i / N) * ldc + (i % N)] = 0;
 }
 
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern kern, int grid, cudaStream_t st, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kWarps * 32, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 int rows_grid(int64_t N, int sm_count)
 {
     int64_t g = (N + kWarps - 1) / kWarps;
@@ -168,12 +189,11 @@ cudaError_t launch_gemv_bf16(const GemmArgs &a, const Plan &p, const LaunchCtx &
     uint16_t *C = (uint16_t *)a.C;
     const int M = (int)a.M, N = (int)a.N, K = (int)a.K;
     switch (p.m_per_pass) {
-    case 1: k_gemv_bf16<1, 8><<<p.grid, kWarps * 32, 0, c.stream>>>(A, B, C, M, N, K, a.lda, a.ldb, a.ldc); break;
-    case 2: k_gemv_bf16<2, 8><<<p.grid, kWarps * 32, 0, c.stream>>>(A, B, C, M, N, K, a.lda, a.ldb, a.ldc); break;
-    case 3: k_gemv_bf16<3, 4><<<p.grid, kWarps * 32, 0, c.stream>>>(A, B, C, M, N, K, a.lda, a.ldb, a.ldc); break;
-    default: k_gemv_bf16<4, 4><<<p.grid, kWarps * 32, 0, c.stream>>>(A, B, C, M, N, K, a.lda, a.ldb, a.ldc); break;
+    case 1: return launch_pdl(k_gemv_bf16<1, 8>, p.grid, c.stream, A, B, C, M, N, K, a.lda, a.ldb, a.ldc);
+    case 2: return launch_pdl(k_gemv_bf16<2, 8>, p.grid, c.stream, A, B, C, M, N, K, a.lda, a.ldb, a.ldc);
+    case 3: return launch_pdl(k_gemv_bf16<3, 4>, p.grid, c.stream, A, B, C, M, N, K, a.lda, a.ldb, a.ldc);
+    default: return launch_pdl(k_gemv_bf16<4, 4>, p.grid, c.stream, A, B, C, M, N, K, a.lda, a.ldb, a.ldc);
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_gemv_w4a16(const GemmArgs &a, const Plan &p, const LaunchCtx &c)
@@ -185,11 +205,10 @@ cudaError_t launch_gemv_w4a16(const GemmArgs &a, const Plan &p, const LaunchCtx 
     uint16_t *C = (uint16_t *)a.C;
     const int M = (int)a.M, N = (int)a.N, K = (int)a.K, g = (int)a.group;
     switch (p.m_per_pass) {
-    case 1: k_gemv_w4a16<1><<<p.grid, kWarps * 32, 0, c.stream>>>(A, Q, S, Z, C, M, N, K, g); break;
-    case 2: k_gemv_w4a16<2><<<p.grid, kWarps * 32, 0, c.stream>>>(A, Q, S, Z, C, M, N, K, g); break;
-    default: k_gemv_w4a16<4><<<p.grid, kWarps * 32, 0, c.stream>>>(A, Q, S, Z, C, M, N, K, g); break;
+    case 1: return launch_pdl(k_gemv_w4a16<1>, p.grid, c.stream, A, Q, S, Z, C, M, N, K, g);
+    case 2: return launch_pdl(k_gemv_w4a16<2>, p.grid, c.stream, A, Q, S, Z, C, M, N, K, g);
+    default: return launch_pdl(k_gemv_w4a16<4>, p.grid, c.stream, A, Q, S, Z, C, M, N, K, g);
     }
-    return cudaGetLastError();
 }
 
 int gemv_grid(int64_t N, int sm_count) { return rows_grid(N, sm_count); }

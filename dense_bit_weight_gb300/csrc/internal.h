@@ -36,7 +36,7 @@ struct Plan {
     int tile_m, tile_n;
     int stages;
     int m_per_pass;        // GEMV: rows of A handled per pass over the weights
-    int mode;              // tcgen05: 0 whole tiles round-robin, 1 stream-K ranges
+    int mode;              // tcgen05: 0 whole tiles round-robin, 1 stream-K, 2 cluster split-K
     int bn;                // tcgen05: MMA N (columns of the Y operand per tile)
     int group_r;           // tcgen05: tile-rows per raster group
 };
@@ -56,7 +56,7 @@ cudaError_t launch_umma_bf16(const GemmArgs &a, const Plan &p, const LaunchCtx &
 // tcgen05 kernel geometry (umma.cu)
 constexpr int kUmmaBM = 128;
 constexpr int kUmmaBK = 64;
-int umma_stages(int bn);
+int umma_stages(int bn, bool skinny);
 extern int g_debug_stall;   // test hook: producers issue no copies (forces the watchdog)
 
 }  // namespace dbw

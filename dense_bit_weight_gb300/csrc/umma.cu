@@ -37,6 +37,16 @@
 //           fp32 partial in the workspace, bumps the tile's counter, and the
 //           last one adds all partials in increasing-k order (deterministic,
 //           no float atomics) and resets the counter to zero.
+//   mode 2  cluster split-K (decode): the S CTAs that split one tile's K
+//           form a thread-block cluster; each leaves its fp32 partial in its
+//           own shared memory, and after a cluster barrier each CTA sums a
+//           slice of the tile's rows over distributed shared memory in rank
+//           order (deterministic, no global scratch).  One tile per CTA; the
+//           grid is small enough for every CTA to be resident at once.
+//
+// Launches use programmatic dependent launch: a kernel's prologue (barrier
+// set-up, TMEM allocation, descriptor prefetch) overlaps the tail of the
+// kernel before it, and it waits for that kernel before touching memory.
 //
 // Every mbarrier wait is bounded (1 s of %globaltimer).  On expiry the
 // waiting thread raises a shared abort flag and the device error word; all
@@ -67,6 +77,7 @@ struct Sched {
     int grid;
     int group_r;                 // raster: tile-rows per group
     int stall;                   // test hook: producer issues nothing (forces the watchdog)
+    int split;                   // mode 2: CTAs per tile (cluster size)
     long long units;             // tiles * nk
 };
 
@@ -108,7 +119,15 @@ struct SegIter {
     }
     __device__ bool next(const Sched &s, Segment &seg)
     {
-        if (s.mode == 0) {
+        if (s.mode == 2) {
+            if (count > 0) return false;
+            const int cta = next_tile;
+            const int r = cta % s.split;
+            seg.tile = cta / s.split;
+            seg.kb0 = (int)((long long)r * s.nk / s.split);
+            seg.kb1 = (int)((long long)(r + 1) * s.nk / s.split);
+            seg.slot = 0;
+        } else if (s.mode == 0) {
             if (next_tile >= s.tiles) return false;
             seg.tile = next_tile;
             seg.kb0 = 0;
@@ -202,8 +221,8 @@ struct Layout {
     static constexpr int SMEM = MISC_OFF + 16 + 1024;   // + slack to align the base to 1024
 };
 
-template <int BN, int STAGES, bool SWAP>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BN, int STAGES, bool SWAP, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB)
 k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
        uint16_t *__restrict__ C, int R, int Q, int64_t ldc, const Sched sched,
        float *__restrict__ ws, int *__restrict__ counters, int *__restrict__ d_error)
@@ -253,6 +272,11 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = misc[0];
+    ptx::pdl_wait();                 // inputs written by the previous kernel are visible
+    ptx::pdl_launch_dependents();    // the next kernel may start its prologue
+    const bool cluster_split = sched.mode == 2 && sched.split > 1;
+    constexpr int PSTRIDE = BN * 4 + 16;   // bytes per row of the mode-2 partial tile in smem
+    static_assert(BM * PSTRIDE <= STAGES * L::STAGE_BYTES || MINB == 1, "partial tile must fit the ring");
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -365,6 +389,11 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                 for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(v[j]);
                 if (whole) {
                     store_chunk<SWAP>(C, ldc, R, Q, r, qb + c, f);
+                } else if (cluster_split) {
+                    float4 *prow = reinterpret_cast<float4 *>(smem + row * PSTRIDE + c * 4);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        prow[u] = make_float4(f[4 * u], f[4 * u + 1], f[4 * u + 2], f[4 * u + 3]);
                 } else {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) __stcg(part + (c + j) * BM + row, f[j]);
@@ -376,7 +405,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                 acc = 0;
                 acc_phase ^= 1u;
             }
-            if (whole) continue;
+            if (whole || cluster_split) continue;
 
             // ---- stream-K fixup: the last contributor of this tile sums the partials
             const int t = seg.tile;
@@ -398,17 +427,76 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                 float f[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) f[j] = 0.f;
+                // four contributors' loads in flight at once, summed in increasing-k order
 #pragma unroll 1
-                for (int cta = c_first; cta <= c_last; ++cta) {
-                    const int first_tile = (int)(range_begin(sched, cta) / sched.nk);
-                    const int slot = first_tile == t ? 0 : 1;
-                    const float *p = ws + (int64_t)(cta * 2 + slot) * (BM * BN) + (int64_t)c * BM + row;
+                for (int cta0 = c_first; cta0 <= c_last; cta0 += 4) {
+                    float v[4][16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) f[j] += __ldcg(p + j * BM);
+                    for (int u = 0; u < 4; ++u) {
+                        const int cta = cta0 + u;
+                        if (cta <= c_last) {
+                            const int first_tile = (int)(range_begin(sched, cta) / sched.nk);
+                            const int slot = first_tile == t ? 0 : 1;
+                            const float *p = ws + (int64_t)(cta * 2 + slot) * (BM * BN) + (int64_t)c * BM + row;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) v[u][j] = __ldcg(p + j * BM);
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        if (cta0 + u <= c_last) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) f[j] += v[u][j];
+                        }
                 }
                 store_chunk<SWAP>(C, ldc, R, Q, r, qb + c, f);
             }
         }
+    }
+
+    if (cluster_split) {
+        // every CTA's partial is in its shared memory; each CTA sums its slice
+        // of rows over the cluster, in rank order
+        ptx::cluster_sync();
+        if (warp >= 2) {
+            const int S = sched.split;
+            const int rank = (int)ptx::cluster_ctarank();
+            const int r0 = rank * BM / S, r1 = (rank + 1) * BM / S, nrows = r1 - r0;
+            int tr, tq;
+            tile_coords(sched, (int)blockIdx.x / S, tr, tq);
+            const int qb = tq * BN;
+            const int etid = threadIdx.x - 64;
+            for (int idx = etid; idx < nrows * (BN / 4); idx += kEpiThreads) {
+                const int rr = r0 + idx % nrows;   // neighbouring threads: neighbouring rows
+                const int c4 = idx / nrows;
+                const uint32_t local = sbase + (uint32_t)(rr * PSTRIDE + c4 * 16);
+                float4 v[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (q < S) v[q] = ptx::ld_cluster_v4(ptx::map_cluster(local, (uint32_t)q));
+                float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (q < S) {
+                        a[0] += v[q].x;
+                        a[1] += v[q].y;
+                        a[2] += v[q].z;
+                        a[3] += v[q].w;
+                    }
+                const int r = tr * BM + rr;
+                if (r < R) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int q = qb + c4 * 4 + j;
+                        if (q < Q) {
+                            if (SWAP) C[(int64_t)q * ldc + r] = f32_to_bf16_rn(a[j]);
+                            else C[(int64_t)r * ldc + q] = f32_to_bf16_rn(a[j]);
+                        }
+                    }
+                }
+            }
+        }
+        ptx::cluster_sync();    // no CTA leaves while others still read its shared memory
     }
 
     __syncthreads();
@@ -452,41 +540,50 @@ bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int64_t 
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES, bool SWAP>
+template <int BN, int STAGES, bool SWAP, int MINB>
 cudaError_t launch_t(const CUtensorMap &mx, const CUtensorMap &my, uint16_t *C, int R, int Q, int64_t ldc,
                      const Sched &s, const LaunchCtx &c)
 {
     using L = Layout<BN, STAGES>;
+    auto kern = k_umma<BN, STAGES, SWAP, MINB>;
     static std::once_flag once[64];
+    static cudaError_t attr_err[64];
     int dev = 0;
     cudaGetDevice(&dev);
-    cudaError_t attr = cudaSuccess;
     std::call_once(once[dev & 63], [&] {
-        attr = cudaFuncSetAttribute(k_umma<BN, STAGES, SWAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    L::SMEM);
+        attr_err[dev & 63] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
     });
-    if (attr != cudaSuccess) return attr;
-    k_umma<BN, STAGES, SWAP><<<s.grid, kThreads, L::SMEM, c.stream>>>(mx, my, C, R, Q, ldc, s, c.workspace,
-                                                                         c.counters, c.d_error);
-    return cudaGetLastError();
+    if (attr_err[dev & 63] != cudaSuccess) return attr_err[dev & 63];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)s.grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = L::SMEM;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute at[2];
+    int na = 0;
+    at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (s.mode == 2 && s.split > 1) {
+        at[na].id = cudaLaunchAttributeClusterDimension;
+        at[na].val.clusterDim.x = (unsigned)s.split;
+        at[na].val.clusterDim.y = 1;
+        at[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = at;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kern, mx, my, C, R, Q, ldc, s, c.workspace, c.counters, c.d_error);
 }
 
 }  // namespace
 
-int umma_stages(int bn)
+// Pipeline depth per tile width.  Skinny (decode) kernels keep two CTAs per
+// SM (about 100 KB of shared memory each); prefill uses one CTA per SM.
+int umma_stages(int bn, bool skinny)
 {
-    return bn <= 32 ? 8 : bn <= 128 ? 6 : 4;
-}
-
-int umma_smem_bytes(int bn)
-{
-    switch (bn) {
-    case 16: return Layout<16, 8>::SMEM;
-    case 32: return Layout<32, 8>::SMEM;
-    case 64: return Layout<64, 6>::SMEM;
-    case 128: return Layout<128, 6>::SMEM;
-    default: return Layout<256, 4>::SMEM;
-    }
+    if (!skinny) return 4;
+    return bn <= 16 ? 6 : bn <= 32 ? 5 : bn <= 64 ? 4 : 3;
 }
 
 int g_debug_stall = 0;
@@ -513,17 +610,18 @@ cudaError_t launch_umma_bf16(const GemmArgs &a, const Plan &p, const LaunchCtx &
     s.stall = g_debug_stall;
     uint16_t *C = (uint16_t *)a.C;
     const int r = (int)R, q = (int)Q;
+    s.split = p.split;
     if (swap) {
         switch (p.bn) {
-        case 16: return launch_t<16, 8, true>(mx, my, C, r, q, a.ldc, s, c);
-        case 32: return launch_t<32, 8, true>(mx, my, C, r, q, a.ldc, s, c);
-        case 64: return launch_t<64, 6, true>(mx, my, C, r, q, a.ldc, s, c);
-        case 128: return launch_t<128, 6, true>(mx, my, C, r, q, a.ldc, s, c);
+        case 16: return launch_t<16, 6, true, 2>(mx, my, C, r, q, a.ldc, s, c);
+        case 32: return launch_t<32, 5, true, 2>(mx, my, C, r, q, a.ldc, s, c);
+        case 64: return launch_t<64, 4, true, 2>(mx, my, C, r, q, a.ldc, s, c);
+        case 128: return launch_t<128, 3, true, 2>(mx, my, C, r, q, a.ldc, s, c);
         default: return cudaErrorInvalidValue;
         }
     }
     switch (p.bn) {
-    case 256: return launch_t<256, 4, false>(mx, my, C, r, q, a.ldc, s, c);
+    case 256: return launch_t<256, 4, false, 1>(mx, my, C, r, q, a.ldc, s, c);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -1,0 +1,91 @@
+"""Run one GEMM shape repeatedly on the GPU (for profiling and quick timing).
+
+    python -m dense_bit_weight_gb300.run_case --M 1 --N 24576 --K 4096 \
+        [--kind bf16|w4a16] [--variant auto|gemv|skinny|prefill] [--reps 4] [--copies 0]
+
+Weights are drawn on the device with torch's seeded generator; `--copies`
+weight copies (0 = enough to exceed three L2 sizes) are used round robin so
+every launch streams its weights from HBM.  Prints the plan and the mean
+device time per launch of a CUDA-graph replay.  Meant to be run under
+`ncu -k regex:<kernel> -s <skip> -c <count>`.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--M", type=int, required=True)
+    ap.add_argument("--N", type=int, required=True)
+    ap.add_argument("--K", type=int, required=True)
+    ap.add_argument("--kind", choices=["bf16", "w4a16"], default="bf16")
+    ap.add_argument("--variant", default="auto")
+    ap.add_argument("--group", type=int, default=128)
+    ap.add_argument("--reps", type=int, default=4)
+    ap.add_argument("--copies", type=int, default=0)
+    ap.add_argument("--no-graph", action="store_true", help="eager launches only (for ncu)")
+    a = ap.parse_args(argv)
+
+    import torch
+    from dense_bit_weight_gb300 import gemm as g
+
+    dev = torch.device("cuda")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    M, N, K = a.M, a.N, a.K
+    wbytes = N * K * 2 if a.kind == "bf16" else N * K // 2
+    copies = a.copies or max(1, min(16, math.ceil(3 * 130e6 / wbytes)))
+    A = torch.randn((M, K), generator=gen, device=dev).to(torch.bfloat16)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    if a.kind == "bf16":
+        Bs = [(torch.randn((N, K), generator=gen, device=dev) * K ** -0.5).to(torch.bfloat16)
+              for _ in range(copies)]
+        plan = g.gemm_bf16_plan(M, N, K, a.variant)
+        fn = lambda i: g.gemm_bf16(A, Bs[i % copies], C, variant=a.variant)
+        work = {"GB": 2 * (M * K + N * K + M * N) / 1e9, "TFLOP": 2 * M * N * K / 1e12}
+    else:
+        G = K // a.group
+        Bs = [(torch.randint(-2 ** 31, 2 ** 31 - 1, (N, K // 8), generator=gen, device=dev, dtype=torch.int32),
+               (torch.rand((N, G), generator=gen, device=dev) * 0.018 + 0.002).to(torch.bfloat16),
+               torch.randint(0, 16, (N, G), generator=gen, device=dev, dtype=torch.uint8))
+              for _ in range(copies)]
+        plan = g.gemm_w4a16_plan(M, N, K, a.group, a.variant)
+        fn = lambda i: g.gemm_w4a16(A, *Bs[i % copies], a.group, C, variant=a.variant)
+        work = {"GB": (N * K // 2 + 3 * N * K // a.group + 2 * M * K + 2 * M * N) / 1e9,
+                "TFLOP": 2 * M * N * K / 1e12}
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for i in range(a.reps):
+            fn(i)
+    torch.cuda.synchronize()
+    ms = None
+    if not a.no_graph:
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=s):
+            for i in range(a.reps):
+                fn(i)
+        gr.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            gr.replay()
+            e1.record(s)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / a.reps
+    err = g.gemm_last_device_error()
+    out = {"M": M, "N": N, "K": K, "kind": a.kind, "plan": plan, "copies": copies,
+           "ms_per_launch": ms, "device_error": err}
+    if ms:
+        out["GB/s"] = work["GB"] / (ms * 1e-3)
+        out["TFLOP/s"] = work["TFLOP"] / (ms * 1e-3)
+    print(json.dumps(out))
+    return 0 if err == 0 else 1
+
+
+if __name__ == "__main__":
+    raise SystemExit(main())
