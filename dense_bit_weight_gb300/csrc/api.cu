@@ -184,14 +184,28 @@ void to_public(const Plan &p, gemm_plan *out)
 
 namespace dbw {
 
+// Resident clusters of size `cs` for the skinny kernel: the device's answer
+// when planning for the current device, else an ideal-packing model.
+static int64_t cluster_capacity(int bn, bool deep, int cs, int sm_count, bool query)
+{
+    if (query) {
+        const int n = umma_cluster_capacity(bn, deep, cs);
+        if (n >= 0) return n;
+    }
+    return (int64_t)(deep ? 1 : 2) * sm_count / cs;
+}
+
 // tcgen05 planning.
-// Skinny (decode, swap AB): one 128-row weight tile per CTA, K split over a
-// cluster of S CTAs (mode 2), S the smallest value in 1..8 that gives every SM
-// a CTA; two CTAs fit per SM, so the whole grid is resident at once and the
-// HBM stream is shared evenly without stream-K.
+// Skinny (decode, swap AB): one 128-row weight tile per CTA with K split over
+// a cluster of S CTAs (mode 2).  When the tiles fit one wave the deep form
+// (one CTA per SM) takes the largest S <= 8 whose clusters are all resident at
+// once without exceeding one CTA per SM; otherwise the shallow form (two CTAs
+// per SM) runs every tile unsplit, all resident together, so the HBM stream
+// is shared evenly.  Beyond two tiles per SM, deep stream-K (mode 1).
 // Prefill: whole tiles round-robin when they fill the SMs in nearly whole
 // waves (mode 0), otherwise stream-K over (tile, k-block) units (mode 1).
-static void plan_umma(int64_t M, int64_t N, int64_t K, bool swap, int bn, int sm_count, Plan *p)
+static void plan_umma(int64_t M, int64_t N, int64_t K, bool swap, int bn, int sm_count, bool query,
+                      Plan *p)
 {
     const int64_t R = swap ? N : M, Q = swap ? M : N;
     const int64_t tiles_r = (R + kUmmaBM - 1) / kUmmaBM;
@@ -201,22 +215,33 @@ static void plan_umma(int64_t M, int64_t N, int64_t K, bool swap, int bn, int sm
     const int64_t G = sm_count;
     p->variant = swap ? GEMM_VARIANT_SKINNY : GEMM_VARIANT_PREFILL;
     p->bn = bn;
-    p->stages = umma_stages(bn, swap);
     p->tile_m = swap ? bn : kUmmaBM;
     p->tile_n = swap ? kUmmaBM : bn;
     p->group_r = swap ? (int)tiles_r : (int)std::min<int64_t>(tiles_r, 16);
     p->kernels = 1;
-    if (swap) {
+    p->ctas_per_sm = 1;
+    if (swap && tiles <= G) {
         int64_t S = 1;
-        while (S < 8 && S < nk && tiles * S < G) ++S;
+        for (int64_t s = 2; s <= 8 && s <= nk && tiles * s <= G; ++s)
+            if (cluster_capacity(bn, true, (int)s, sm_count, query) >= tiles) S = s;
         p->mode = 2;
         p->split = (int)S;
         p->grid = (int)(tiles * S);
+        p->stages = umma_stages(bn, true, true);
         return;
     }
+    if (swap && tiles <= 2 * G) {
+        p->mode = 2;
+        p->split = 1;
+        p->grid = (int)tiles;
+        p->ctas_per_sm = 2;
+        p->stages = umma_stages(bn, true, false);
+        return;
+    }
+    p->stages = umma_stages(bn, swap, true);
     const int64_t waves = (tiles + G - 1) / G;
     const double eff = (double)tiles / (double)(waves * G);
-    if (tiles >= G && eff >= 0.9) {
+    if (!swap && tiles >= G && eff >= 0.9) {
         p->mode = 0;
         p->grid = (int)G;
         p->split = 1;
@@ -230,7 +255,7 @@ static void plan_umma(int64_t M, int64_t N, int64_t K, bool swap, int bn, int sm
     }
 }
 
-bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan *p)
+bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan *p, bool query)
 {
     *p = Plan{};
     if (K == 0) {
@@ -256,11 +281,11 @@ bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan 
         if (M > 128) return false;
         int bn = 16;
         while (bn < M) bn *= 2;
-        plan_umma(M, N, K, true, bn, sm_count, p);
+        plan_umma(M, N, K, true, bn, sm_count, query, p);
         return true;
     }
     case GEMM_VARIANT_PREFILL:
-        plan_umma(M, N, K, false, 256, sm_count, p);
+        plan_umma(M, N, K, false, 256, sm_count, query, p);
         return true;
     default: return false;
     }
@@ -372,7 +397,7 @@ int gemm_bf16_plan(int64_t M, int64_t N, int64_t K, int variant, int num_sms, ge
     rc = sm_count_for_plan(num_sms, &sms);
     if (rc) return rc;
     Plan p;
-    if (!plan_bf16(M, N, K, variant, sms, &p)) return GEMM_ERR_VARIANT;
+    if (!plan_bf16(M, N, K, variant, sms, &p, num_sms == 0)) return GEMM_ERR_VARIANT;
     to_public(p, out);
     return GEMM_OK;
 }

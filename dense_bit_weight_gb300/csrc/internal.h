@@ -39,9 +39,12 @@ struct Plan {
     int mode;              // tcgen05: 0 whole tiles round-robin, 1 stream-K, 2 cluster split-K
     int bn;                // tcgen05: MMA N (columns of the Y operand per tile)
     int group_r;           // tcgen05: tile-rows per raster group
+    int ctas_per_sm;       // tcgen05 skinny: 1 = deep pipeline, 2 = shallow (two CTAs per SM)
 };
 
-bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan *p);
+// query = true: plan for the current device (asks it for cluster occupancy);
+// false: host-only model of a device with sm_count SMs.
+bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan *p, bool query = true);
 bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int sm_count, Plan *p);
 
 // Workspace need (floats, counters) for a plan; 0 when it needs none.
@@ -56,7 +59,9 @@ cudaError_t launch_umma_bf16(const GemmArgs &a, const Plan &p, const LaunchCtx &
 // tcgen05 kernel geometry (umma.cu)
 constexpr int kUmmaBM = 128;
 constexpr int kUmmaBK = 64;
-int umma_stages(int bn, bool skinny);
+int umma_stages(int bn, bool skinny, bool deep);
+// Resident clusters of the skinny kernel on the current device (-1 on failure).
+int umma_cluster_capacity(int bn, bool deep, int cluster);
 extern int g_debug_stall;   // test hook: producers issue no copies (forces the watchdog)
 
 }  // namespace dbw

@@ -377,7 +377,8 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
             const int qb = tq * BN;
             const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(acc * BN);
             const bool whole = seg.kb0 == 0 && seg.kb1 == sched.nk;
-            float *part = ws + (int64_t)(blockIdx.x * 2 + seg.slot) * (BM * BN);
+            // stream-K partial: float4 columns, [column/4][row], so a warp's store is 512 contiguous bytes
+            float4 *part = reinterpret_cast<float4 *>(ws) + (int64_t)(blockIdx.x * 2 + seg.slot) * (BM * BN / 4);
 #pragma unroll 1
             for (int c = 0; c < BN; c += 16) {
                 uint32_t v[16];
@@ -396,7 +397,9 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                         prow[u] = make_float4(f[4 * u], f[4 * u + 1], f[4 * u + 2], f[4 * u + 3]);
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) __stcg(part + (c + j) * BM + row, f[j]);
+                    for (int u = 0; u < 4; ++u)
+                        __stcg(part + (c / 4 + u) * BM + row,
+                               make_float4(f[4 * u], f[4 * u + 1], f[4 * u + 2], f[4 * u + 3]));
                 }
             }
             ptx::tc_fence_before();
@@ -422,34 +425,55 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
             ptx::named_bar_sync(1, kEpiThreads);
             if (!misc[2]) continue;
             __threadfence();
+            // many float4 loads in flight: CB4 float4 columns of BATCH contributors at a time,
+            // summed per column in increasing contributor (= increasing k) order
+            constexpr int CB4 = (BN / 4) < 16 ? (BN / 4) : 16;
+            constexpr int INFL = MINB == 1 ? 32 : 16;
+            constexpr int BATCH = INFL / CB4 > 0 ? INFL / CB4 : 1;
+            const float4 *wsv = reinterpret_cast<const float4 *>(ws);
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 16) {
-                float f[16];
+            for (int cb = 0; cb < BN / 4; cb += CB4) {
+                float4 a4[CB4];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) f[j] = 0.f;
-                // four contributors' loads in flight at once, summed in increasing-k order
+                for (int j = 0; j < CB4; ++j) a4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
-                for (int cta0 = c_first; cta0 <= c_last; cta0 += 4) {
-                    float v[4][16];
+                for (int cta0 = c_first; cta0 <= c_last; cta0 += BATCH) {
+                    float4 v[BATCH][CB4];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
+                    for (int u = 0; u < BATCH; ++u) {
                         const int cta = cta0 + u;
                         if (cta <= c_last) {
                             const int first_tile = (int)(range_begin(sched, cta) / sched.nk);
                             const int slot = first_tile == t ? 0 : 1;
-                            const float *p = ws + (int64_t)(cta * 2 + slot) * (BM * BN) + (int64_t)c * BM + row;
+                            const float4 *p = wsv + (int64_t)(cta * 2 + slot) * (BM * BN / 4) + (int64_t)cb * BM + row;
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) v[u][j] = __ldcg(p + j * BM);
+                            for (int j = 0; j < CB4; ++j) v[u][j] = __ldcg(p + j * BM);
                         }
                     }
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
+                    for (int u = 0; u < BATCH; ++u)
                         if (cta0 + u <= c_last) {
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) f[j] += v[u][j];
+                            for (int j = 0; j < CB4; ++j) {
+                                a4[j].x += v[u][j].x;
+                                a4[j].y += v[u][j].y;
+                                a4[j].z += v[u][j].z;
+                                a4[j].w += v[u][j].w;
+                            }
                         }
                 }
-                store_chunk<SWAP>(C, ldc, R, Q, r, qb + c, f);
+#pragma unroll
+                for (int j16 = 0; j16 < CB4 / 4; ++j16) {
+                    float f[16];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        f[4 * u] = a4[4 * j16 + u].x;
+                        f[4 * u + 1] = a4[4 * j16 + u].y;
+                        f[4 * u + 2] = a4[4 * j16 + u].z;
+                        f[4 * u + 3] = a4[4 * j16 + u].w;
+                    }
+                    store_chunk<SWAP>(C, ldc, R, Q, r, qb + cb * 4 + j16 * 16, f);
+                }
             }
         }
     }
@@ -578,12 +602,77 @@ cudaError_t launch_t(const CUtensorMap &mx, const CUtensorMap &my, uint16_t *C, 
 
 }  // namespace
 
-// Pipeline depth per tile width.  Skinny (decode) kernels keep two CTAs per
-// SM (about 100 KB of shared memory each); prefill uses one CTA per SM.
-int umma_stages(int bn, bool skinny)
+// Pipeline depth per tile width.  Skinny (decode) kernels come in a deep form
+// (one CTA per SM, about 190 KB of shared memory) used when the grid fits in
+// one wave, and a shallow form (two CTAs per SM, about 100 KB each) for grids
+// of up to two CTAs per SM.  Prefill uses one CTA per SM.
+int umma_stages(int bn, bool skinny, bool deep)
 {
     if (!skinny) return 4;
+    if (deep) return bn <= 64 ? 8 : 6;
     return bn <= 16 ? 6 : bn <= 32 ? 5 : bn <= 64 ? 4 : 3;
+}
+
+namespace {
+template <int BN, int STAGES, bool SWAP, int MINB>
+int cluster_capacity_t(int cluster)
+{
+    using L = Layout<BN, STAGES>;
+    auto kern = k_umma<BN, STAGES, SWAP, MINB>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM) != cudaSuccess)
+        return -1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(cluster * 64), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = L::SMEM;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)cluster;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return -1;
+    return n;
+}
+}  // namespace
+
+// Clusters of `cluster` CTAs of the skinny kernel that can be resident at
+// once on the current device (cached per device); -1 if the query fails.
+int umma_cluster_capacity(int bn, bool deep, int cluster)
+{
+    static std::mutex mu;
+    static int cache[64][5][2][9];
+    static bool have[64][5][2][9];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cluster < 1 || cluster > 8) return -1;
+    const int bi = bn <= 16 ? 0 : bn <= 32 ? 1 : bn <= 64 ? 2 : bn <= 128 ? 3 : 4;
+    std::lock_guard<std::mutex> lk(mu);
+    int &slot = cache[dev & 63][bi][deep][cluster];
+    if (!have[dev & 63][bi][deep][cluster]) {
+        int n = -1;
+        if (deep) {
+            switch (bi) {
+            case 0: n = cluster_capacity_t<16, 8, true, 1>(cluster); break;
+            case 1: n = cluster_capacity_t<32, 8, true, 1>(cluster); break;
+            case 2: n = cluster_capacity_t<64, 8, true, 1>(cluster); break;
+            case 3: n = cluster_capacity_t<128, 6, true, 1>(cluster); break;
+            default: break;
+            }
+        } else {
+            switch (bi) {
+            case 0: n = cluster_capacity_t<16, 6, true, 2>(cluster); break;
+            case 1: n = cluster_capacity_t<32, 5, true, 2>(cluster); break;
+            case 2: n = cluster_capacity_t<64, 4, true, 2>(cluster); break;
+            case 3: n = cluster_capacity_t<128, 3, true, 2>(cluster); break;
+            default: break;
+            }
+        }
+        slot = n;
+        have[dev & 63][bi][deep][cluster] = n >= 0;
+    }
+    return slot;
 }
 
 int g_debug_stall = 0;
@@ -611,6 +700,15 @@ cudaError_t launch_umma_bf16(const GemmArgs &a, const Plan &p, const LaunchCtx &
     uint16_t *C = (uint16_t *)a.C;
     const int r = (int)R, q = (int)Q;
     s.split = p.split;
+    if (swap && p.ctas_per_sm == 1) {
+        switch (p.bn) {
+        case 16: return launch_t<16, 8, true, 1>(mx, my, C, r, q, a.ldc, s, c);
+        case 32: return launch_t<32, 8, true, 1>(mx, my, C, r, q, a.ldc, s, c);
+        case 64: return launch_t<64, 8, true, 1>(mx, my, C, r, q, a.ldc, s, c);
+        case 128: return launch_t<128, 6, true, 1>(mx, my, C, r, q, a.ldc, s, c);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     if (swap) {
         switch (p.bn) {
         case 16: return launch_t<16, 6, true, 2>(mx, my, C, r, q, a.ldc, s, c);
