@@ -77,6 +77,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, 
         : "memory");
 }
 
+// Bring a tile into L2 without writing shared memory (safe before the grid
+// dependency wait: L2 is the coherence point, so nothing stale is consumed).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *m, int32_t c0, int32_t c1)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(m)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 // L2 eviction policies for TMA loads (createpolicy, fraction 1.0).
 __device__ __forceinline__ uint64_t policy_evict_first()
 {
@@ -190,15 +199,32 @@ __device__ __forceinline__ uint32_t map_cluster(uint32_t saddr, uint32_t rank)
     return r;
 }
 
+// Plain load from distributed shared memory (ordering comes from the cluster
+// barriers around it, so the compiler may keep several in flight).
 __device__ __forceinline__ float4 ld_cluster_v4(uint32_t caddr)
 {
     float4 v;
     asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
                  : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(caddr)
-                 : "memory");
+                 : "r"(caddr));
     return v;
 }
+
+// Bulk copy from this CTA's shared memory into another CTA's shared memory in
+// the cluster; completion (bytes) is counted on the destination's mbarrier.
+// Addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                                     uint32_t mbar_cluster)
+{
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst_cluster),
+                 "r"(src_cta), "r"(bytes), "r"(mbar_cluster)
+                 : "memory");
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the async
+// proxy (bulk copies, TMA) that will read them.
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // Programmatic dependent launch: wait for the grids this one depends on to
 // finish (and their memory to be visible); let dependents start their prologue.

@@ -38,11 +38,13 @@
 //           last one adds all partials in increasing-k order (deterministic,
 //           no float atomics) and resets the counter to zero.
 //   mode 2  cluster split-K (decode): the S CTAs that split one tile's K
-//           form a thread-block cluster; each leaves its fp32 partial in its
-//           own shared memory, and after a cluster barrier each CTA sums a
-//           slice of the tile's rows over distributed shared memory in rank
-//           order (deterministic, no global scratch).  One tile per CTA; the
-//           grid is small enough for every CTA to be resident at once.
+//           form a thread-block cluster.  Each writes its fp32 partial to its
+//           own shared memory; after a cluster barrier it sends row slice o
+//           of that partial to CTA o with one bulk shared-to-shared copy
+//           (completion counted on CTA o's mbarrier), and each CTA sums the S
+//           slices it owns from its own shared memory in rank order
+//           (deterministic, no global scratch).  One tile per CTA; the grid is
+//           small enough for every CTA to be resident at once.
 //
 // Launches use programmatic dependent launch: a kernel's prologue (barrier
 // set-up, TMEM allocation, descriptor prefetch) overlaps the tail of the
@@ -216,7 +218,7 @@ struct Layout {
     static constexpr int Y_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = X_BYTES + Y_BYTES;
     static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
-    static constexpr int NBARS = 2 * STAGES + 5;
+    static constexpr int NBARS = 2 * STAGES + 6;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int SMEM = MISC_OFF + 16 + 1024;   // + slack to align the base to 1024
 };
@@ -242,6 +244,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
     auto TFULL = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
     auto TEMPTY = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
     const uint32_t DONE = bar0 + 8u * (2 * STAGES + 4);
+    const uint32_t REDUCE = bar0 + 8u * (2 * STAGES + 5);   // mode 2: incoming partial slices
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile uint32_t *abort_flag = misc + 1;
@@ -256,6 +259,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
             ptx::mbar_init(TEMPTY(a), kEpiThreads);
         }
         ptx::mbar_init(DONE, 1);
+        ptx::mbar_init(REDUCE, 1);
         misc[1] = 0;
         misc[2] = 0;
         ptx::fence_mbar_init();
@@ -272,11 +276,20 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = misc[0];
-    ptx::pdl_wait();                 // inputs written by the previous kernel are visible
-    ptx::pdl_launch_dependents();    // the next kernel may start its prologue
-    const bool cluster_split = sched.mode == 2 && sched.split > 1;
+    // Programmatic dependent launch: let the next kernel start its prologue now;
+    // each role waits for the previous kernel (griddepcontrol.wait) just before
+    // its first global-memory access.  The MMA role touches only shared and
+    // tensor memory and does not wait.
+    ptx::pdl_launch_dependents();
+    // cluster split-K runs only in the deep skinny kernels (the planner never
+    // asks another instance for it; they lack the shared memory for it)
+    constexpr bool kCanClusterSplit = SWAP && MINB == 1;
+    const bool cluster_split = kCanClusterSplit && sched.mode == 2 && sched.split > 1;
     constexpr int PSTRIDE = BN * 4 + 16;   // bytes per row of the mode-2 partial tile in smem
-    static_assert(BM * PSTRIDE <= STAGES * L::STAGE_BYTES || MINB == 1, "partial tile must fit the ring");
+    // mode-2 partial [128][PSTRIDE] at ring offset 0, incoming slices after it
+    constexpr int IN_OFF = BM * PSTRIDE;
+    static_assert(!kCanClusterSplit || (BM + 8 + BM) * PSTRIDE <= STAGES * L::STAGE_BYTES,
+                  "partials must fit the ring");
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -286,6 +299,22 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
             int stage = 0;
             uint32_t phase = 0;
             long long issued = 0;
+            {
+                // warm L2 with the first stages of this CTA's work while the
+                // previous kernel drains, then wait for it
+                SegIter pre(sched, blockIdx.x);
+                Segment s0;
+                if (pre.next(sched, s0) && !sched.stall) {
+                    int tr, tq;
+                    tile_coords(sched, s0.tile, tr, tq);
+                    const int kend = min(s0.kb1, s0.kb0 + STAGES);
+                    for (int kb = s0.kb0; kb < kend; ++kb) {
+                        ptx::tma_prefetch_l2_2d(&tmX, kb * BK, tr * BM);
+                        ptx::tma_prefetch_l2_2d(&tmY, kb * BK, tq * BN);
+                    }
+                }
+                ptx::pdl_wait();
+            }
             SegIter it(sched, blockIdx.x);
             Segment seg;
             bool ok = true;
@@ -364,6 +393,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
         const int q4 = warp & 3;            // TMEM lane quarter this warp may read
         const int row = q4 * 32 + lane;     // accumulator row
         const int etid = threadIdx.x - 64;  // 0..127
+        ptx::pdl_wait();                    // C, workspace and counters may be in use by the previous kernel
         int acc = 0;
         uint32_t acc_phase = 0;
         SegIter it(sched, blockIdx.x);
@@ -395,6 +425,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
 #pragma unroll
                     for (int u = 0; u < 4; ++u)
                         prow[u] = make_float4(f[4 * u], f[4 * u + 1], f[4 * u + 2], f[4 * u + 3]);
+                    if (c + 16 >= BN) ptx::fence_proxy_async_smem();   // the bulk copies read these rows
                 } else {
 #pragma unroll
                     for (int u = 0; u < 4; ++u)
@@ -479,35 +510,44 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
     }
 
     if (cluster_split) {
-        // every CTA's partial is in its shared memory; each CTA sums its slice
-        // of rows over the cluster, in rank order
+        const int S = sched.split;
+        const int rank = (int)ptx::cluster_ctarank();
+        const int nmax = (BM + S - 1) / S;                    // rows per owner, at most
+        const int r0 = rank * BM / S, r1 = (rank + 1) * BM / S, nrows = r1 - r0;
+        if (threadIdx.x == 64)   // this CTA receives S-1 slices of its nrows rows
+            ptx::mbar_arrive_expect_tx(REDUCE, (uint32_t)((S - 1) * nrows * PSTRIDE));
+        // every CTA's pipeline has drained and its partial is in shared memory
         ptx::cluster_sync();
+        if (threadIdx.x == 64) {
+            for (int o = 0; o < S; ++o) {
+                if (o == rank) continue;
+                const int o0 = o * BM / S, o1 = (o + 1) * BM / S;
+                const uint32_t src = sbase + (uint32_t)(o0 * PSTRIDE);
+                const uint32_t dst = ptx::map_cluster(sbase + (uint32_t)(IN_OFF + rank * nmax * PSTRIDE), (uint32_t)o);
+                ptx::bulk_copy_to_cluster(dst, src, (uint32_t)((o1 - o0) * PSTRIDE), ptx::map_cluster(REDUCE, (uint32_t)o));
+            }
+        }
         if (warp >= 2) {
-            const int S = sched.split;
-            const int rank = (int)ptx::cluster_ctarank();
-            const int r0 = rank * BM / S, r1 = (rank + 1) * BM / S, nrows = r1 - r0;
+            const bool ok = wait_bar(REDUCE, 0, abort_flag, d_error);
             int tr, tq;
             tile_coords(sched, (int)blockIdx.x / S, tr, tq);
             const int qb = tq * BN;
             const int etid = threadIdx.x - 64;
-            for (int idx = etid; idx < nrows * (BN / 4); idx += kEpiThreads) {
-                const int rr = r0 + idx % nrows;   // neighbouring threads: neighbouring rows
+            const int items = nrows * (BN / 4);
+            for (int idx = etid; ok && idx < items; idx += kEpiThreads) {
+                const int rl = idx % nrows;   // neighbouring threads: neighbouring rows
                 const int c4 = idx / nrows;
-                const uint32_t local = sbase + (uint32_t)(rr * PSTRIDE + c4 * 16);
-                float4 v[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    if (q < S) v[q] = ptx::ld_cluster_v4(ptx::map_cluster(local, (uint32_t)q));
                 float a[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    if (q < S) {
-                        a[0] += v[q].x;
-                        a[1] += v[q].y;
-                        a[2] += v[q].z;
-                        a[3] += v[q].w;
-                    }
-                const int r = tr * BM + rr;
+                for (int q = 0; q < S; ++q) {   // rank order
+                    const float4 v = q == rank
+                        ? *reinterpret_cast<const float4 *>(smem + (r0 + rl) * PSTRIDE + c4 * 16)
+                        : *reinterpret_cast<const float4 *>(smem + IN_OFF + (q * nmax + rl) * PSTRIDE + c4 * 16);
+                    a[0] += v.x;
+                    a[1] += v.y;
+                    a[2] += v.z;
+                    a[3] += v.w;
+                }
+                const int r = tr * BM + r0 + rl;
                 if (r < R) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -520,7 +560,9 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                 }
             }
         }
-        ptx::cluster_sync();    // no CTA leaves while others still read its shared memory
+        // every incoming copy has landed (each owner waited for its bytes), so no
+        // CTA leaves while a copy still reads its shared memory
+        ptx::cluster_sync();
     }
 
     __syncthreads();
