@@ -144,8 +144,8 @@ int run(const GemmArgs &a, const Plan &p, cudaStream_t st, bool w4)
     case GEMM_VARIANT_GEMV: e = w4 ? launch_gemv_w4a16(a, p, c) : launch_gemv_bf16(a, p, c); break;
     case GEMM_VARIANT_SKINNY:
     case GEMM_VARIANT_PREFILL:
-        if (w4) return GEMM_ERR_VARIANT;
-        e = launch_umma_bf16(a, p, c);
+        if (w4 && p.variant != GEMM_VARIANT_SKINNY) return GEMM_ERR_VARIANT;
+        e = w4 ? launch_umma_w4a16(a, p, c) : launch_umma_bf16(a, p, c);
         break;
     default: return GEMM_ERR_VARIANT;
     }
@@ -291,13 +291,55 @@ bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan 
     }
 }
 
-bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int sm_count, Plan *p)
+// W4A16: CUDA-core GEMV for M <= 4; the tcgen05 skinny kernel with
+// in-kernel dequantisation for 5 <= M <= 128 (stages of 128 k): cluster
+// split-K (mode 2) when the weight tiles fit one wave, stream-K (mode 1)
+// beyond that.  Larger M runs the GEMV path (one pass per four rows).
+bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int sm_count, Plan *p, bool query)
 {
     (void)group;
     *p = Plan{};
-    if (variant == GEMM_VARIANT_AUTO) variant = GEMM_VARIANT_GEMV;
-    if (variant != GEMM_VARIANT_GEMV) return false;
     if (K == 0) return false;
+    if (variant == GEMM_VARIANT_AUTO)
+        variant = (M <= 4 || M > 128) ? GEMM_VARIANT_GEMV : GEMM_VARIANT_SKINNY;
+    if (variant == GEMM_VARIANT_SKINNY) {
+        if (M > 128) return false;
+        int bn = 16;
+        while (bn < M) bn *= 2;
+        const int64_t tiles = (N + kUmmaBM - 1) / kUmmaBM;
+        const int64_t nk = (K + 2 * kUmmaBK - 1) / (2 * kUmmaBK);
+        const int64_t G = sm_count;
+        p->variant = GEMM_VARIANT_SKINNY;
+        p->kernels = 1;
+        p->bn = bn;
+        p->tile_m = bn;
+        p->tile_n = kUmmaBM;
+        p->group_r = (int)tiles;
+        p->ctas_per_sm = 1;
+        p->stages = umma_w4_stages(bn);
+        if (tiles <= G) {
+            int64_t S = 1;
+            for (int64_t s = 2; s <= 8 && s <= nk && tiles * s <= G; ++s) {
+                int64_t cap = (int64_t)sm_count / s;
+                if (query) {
+                    const int n = umma_cluster_capacity(bn, true, (int)s, true);
+                    if (n >= 0) cap = n;
+                }
+                if (cap >= tiles) S = s;
+            }
+            p->mode = 2;
+            p->split = (int)S;
+            p->grid = (int)(tiles * S);
+        } else {
+            const int64_t units = tiles * nk;
+            p->mode = 1;
+            p->grid = (int)std::min<int64_t>(G, units);
+            const int64_t per_cta = units / p->grid;
+            p->split = (int)std::min<int64_t>(p->grid, (nk + per_cta - 1) / per_cta + 1);
+        }
+        return true;
+    }
+    if (variant != GEMM_VARIANT_GEMV) return false;
     p->variant = GEMM_VARIANT_GEMV;
     p->kernels = 1;
     p->split = 1;
@@ -414,7 +456,7 @@ int gemm_w4a16_plan(int64_t M, int64_t N, int64_t K, int64_t group, int variant,
     rc = sm_count_for_plan(num_sms, &sms);
     if (rc) return rc;
     Plan p;
-    if (!plan_w4a16(M, N, K, group, variant, sms, &p)) return GEMM_ERR_VARIANT;
+    if (!plan_w4a16(M, N, K, group, variant, sms, &p, num_sms == 0)) return GEMM_ERR_VARIANT;
     to_public(p, out);
     return GEMM_OK;
 }

@@ -45,7 +45,8 @@ struct Plan {
 // query = true: plan for the current device (asks it for cluster occupancy);
 // false: host-only model of a device with sm_count SMs.
 bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan *p, bool query = true);
-bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int sm_count, Plan *p);
+bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int sm_count, Plan *p,
+                bool query = true);
 
 // Workspace need (floats, counters) for a plan; 0 when it needs none.
 void workspace_need(const Plan &p, int64_t M, int64_t N, int64_t *floats, int64_t *counters);
@@ -61,7 +62,9 @@ constexpr int kUmmaBM = 128;
 constexpr int kUmmaBK = 64;
 int umma_stages(int bn, bool skinny, bool deep);
 // Resident clusters of the skinny kernel on the current device (-1 on failure).
-int umma_cluster_capacity(int bn, bool deep, int cluster);
+int umma_cluster_capacity(int bn, bool deep, int cluster, bool w4 = false);
+int umma_w4_stages(int bn);
+cudaError_t launch_umma_w4a16(const GemmArgs &a, const Plan &p, const LaunchCtx &c);
 extern int g_debug_stall;   // test hook: producers issue no copies (forces the watchdog)
 
 }  // namespace dbw

@@ -67,9 +67,17 @@ namespace dbw {
 namespace {
 
 constexpr int BM = 128;          // MMA M: rows of X per tile
-constexpr int BK = 64;           // k per stage (one 128-byte swizzle row of bf16)
-constexpr int kThreads = 192;
+constexpr int BK = 64;           // k per MMA tile (one 128-byte swizzle row of bf16)
 constexpr int kEpiThreads = 128;
+constexpr int kDqThreads = 256;  // W4A16: dequantising threads (warps 6-13)
+__host__ __device__ constexpr int threads_for(bool w4) { return w4 ? 448 : 192; }
+
+// W4A16 operands beyond the packed-weight tensor map.
+struct W4Args {
+    const uint16_t *scales;      // bf16 [N, K/group]
+    const uint8_t *zeros;        // uint8 [N, K/group]
+    int K, G, group;
+};
 constexpr uint64_t kTimeoutNs = 1000000000ull;
 
 struct Sched {
@@ -212,24 +220,32 @@ constexpr uint32_t tmem_cols_for(int n)
     return n <= 32 ? 32u : n <= 64 ? 64u : n <= 128 ? 128u : n <= 256 ? 256u : 512u;
 }
 
-template <int BN, int STAGES>
+// Shared memory: a ring of STAGES stages, each an X tile and a Y tile.
+// bf16: X = 128 x 64 bf16 (16 KB, TMA 128-B swizzle), Y = BN x 64 bf16.
+// W4A16: a stage covers 128 k: X = 128 rows x 128 packed 4-bit k (8 KB, plain
+// rows of 64 B), Y = two BN x 64 bf16 halves; the dequantised weights go to
+// XBUF, two buffers of two 128 x 64 bf16 tiles in the MMA's swizzled layout.
+template <int BN, int STAGES, bool W4 = false>
 struct Layout {
-    static constexpr int X_BYTES = BM * BK * 2;
-    static constexpr int Y_BYTES = BN * BK * 2;
+    static constexpr int KSTAGE = W4 ? 2 * BK : BK;
+    static constexpr int X_BYTES = W4 ? BM * KSTAGE / 2 : BM * BK * 2;
+    static constexpr int Y_BYTES = BN * KSTAGE * 2;
     static constexpr int STAGE_BYTES = X_BYTES + Y_BYTES;
-    static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
-    static constexpr int NBARS = 2 * STAGES + 6;
+    static constexpr int XBUF_OFF = STAGES * STAGE_BYTES;
+    static constexpr int XBUF_BYTES = W4 ? 4 * BM * BK * 2 : 0;
+    static constexpr int BAR_OFF = XBUF_OFF + XBUF_BYTES;
+    static constexpr int NBARS = 2 * STAGES + 6 + (W4 ? 4 : 0);
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int SMEM = MISC_OFF + 16 + 1024;   // + slack to align the base to 1024
 };
 
-template <int BN, int STAGES, bool SWAP, int MINB>
-__global__ void __launch_bounds__(kThreads, MINB)
+template <int BN, int STAGES, bool SWAP, int MINB, bool W4>
+__global__ void __launch_bounds__(threads_for(W4), MINB)
 k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
        uint16_t *__restrict__ C, int R, int Q, int64_t ldc, const Sched sched,
-       float *__restrict__ ws, int *__restrict__ counters, int *__restrict__ d_error)
+       float *__restrict__ ws, int *__restrict__ counters, int *__restrict__ d_error, const W4Args w4)
 {
-    using L = Layout<BN, STAGES>;
+    using L = Layout<BN, STAGES, W4>;
     constexpr uint32_t TMEM_COLS = tmem_cols_for(2 * BN);
     constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN);
 
@@ -245,6 +261,8 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
     auto TEMPTY = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
     const uint32_t DONE = bar0 + 8u * (2 * STAGES + 4);
     const uint32_t REDUCE = bar0 + 8u * (2 * STAGES + 5);   // mode 2: incoming partial slices
+    auto XFULL = [&](int b) { return bar0 + 8u * (2 * STAGES + 6 + b); };    // W4A16: dequantised tile ready
+    auto XEMPTY = [&](int b) { return bar0 + 8u * (2 * STAGES + 8 + b); };   // W4A16: MMA done with it
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile uint32_t *abort_flag = misc + 1;
@@ -260,6 +278,11 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
         }
         ptx::mbar_init(DONE, 1);
         ptx::mbar_init(REDUCE, 1);
+        if (W4)
+            for (int b = 0; b < 2; ++b) {
+                ptx::mbar_init(XFULL(b), kDqThreads);
+                ptx::mbar_init(XEMPTY(b), 1);
+            }
         misc[1] = 0;
         misc[2] = 0;
         ptx::fence_mbar_init();
@@ -309,8 +332,14 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                     tile_coords(sched, s0.tile, tr, tq);
                     const int kend = min(s0.kb1, s0.kb0 + STAGES);
                     for (int kb = s0.kb0; kb < kend; ++kb) {
-                        ptx::tma_prefetch_l2_2d(&tmX, kb * BK, tr * BM);
-                        ptx::tma_prefetch_l2_2d(&tmY, kb * BK, tq * BN);
+                        if (W4) {
+                            ptx::tma_prefetch_l2_2d(&tmX, kb * (L::KSTAGE / 8), tr * BM);
+                            ptx::tma_prefetch_l2_2d(&tmY, kb * L::KSTAGE, tq * BN);
+                            ptx::tma_prefetch_l2_2d(&tmY, kb * L::KSTAGE + BK, tq * BN);
+                        } else {
+                            ptx::tma_prefetch_l2_2d(&tmX, kb * BK, tr * BM);
+                            ptx::tma_prefetch_l2_2d(&tmY, kb * BK, tq * BN);
+                        }
                     }
                 }
                 ptx::pdl_wait();
@@ -329,8 +358,15 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                     if (!sched.stall) {
                         ptx::mbar_arrive_expect_tx(FULL(stage), L::STAGE_BYTES);
                         const uint32_t xs = sbase + stage * L::STAGE_BYTES;
-                        ptx::tma_load_2d(xs, &tmX, FULL(stage), kb * BK, tr * BM, pol_x);
-                        ptx::tma_load_2d(xs + L::X_BYTES, &tmY, FULL(stage), kb * BK, tq * BN, pol_y);
+                        if (W4) {   // packed words (8 k each), then the two activation halves
+                            ptx::tma_load_2d(xs, &tmX, FULL(stage), kb * (L::KSTAGE / 8), tr * BM, pol_x);
+                            ptx::tma_load_2d(xs + L::X_BYTES, &tmY, FULL(stage), kb * L::KSTAGE, tq * BN, pol_y);
+                            ptx::tma_load_2d(xs + L::X_BYTES + BN * BK * 2, &tmY, FULL(stage),
+                                             kb * L::KSTAGE + BK, tq * BN, pol_y);
+                        } else {
+                            ptx::tma_load_2d(xs, &tmX, FULL(stage), kb * BK, tr * BM, pol_x);
+                            ptx::tma_load_2d(xs + L::X_BYTES, &tmY, FULL(stage), kb * BK, tq * BN, pol_y);
+                        }
                         ++issued;
                     }
                     if (++stage == STAGES) {
@@ -351,8 +387,8 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            int stage = 0, acc = 0;
-            uint32_t phase = 0, acc_phase = 0;
+            int stage = 0, acc = 0, xb = 0;
+            uint32_t phase = 0, acc_phase = 0, xphase = 0;
             SegIter it(sched, blockIdx.x);
             Segment seg;
             bool ok = true;
@@ -365,13 +401,36 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                         ok = false;
                         break;
                     }
-                    ptx::tc_fence_after();
                     const uint32_t xs = sbase + stage * L::STAGE_BYTES;
-                    const uint64_t ad = ptx::sdesc_kmajor_sw128(xs);
-                    const uint64_t bd = ptx::sdesc_kmajor_sw128(xs + L::X_BYTES);
+                    if (W4) {
+                        // the dequantising warps have written this stage's weights to XBUF[xb]
+                        if (!wait_bar(XFULL(xb), xphase, abort_flag, d_error)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)   // +32 bytes along K per step
-                        ptx::mma_bf16(d, ad + 2u * k, bd + 2u * k, IDESC, (kb > seg.kb0 || k > 0) ? 1u : 0u);
+                        for (int h = 0; h < 2; ++h) {
+                            const uint64_t ad = ptx::sdesc_kmajor_sw128(sbase + L::XBUF_OFF + (xb * 2 + h) * BM * BK * 2);
+                            const uint64_t bd = ptx::sdesc_kmajor_sw128(xs + L::X_BYTES + h * BN * BK * 2);
+#pragma unroll
+                            for (int k = 0; k < BK / 16; ++k)
+                                ptx::mma_bf16(d, ad + 2u * k, bd + 2u * k, IDESC,
+                                              (kb > seg.kb0 || h > 0 || k > 0) ? 1u : 0u);
+                        }
+                        ptx::mma_commit(XEMPTY(xb));
+                        if (++xb == 2) {
+                            xb = 0;
+                            xphase ^= 1u;
+                        }
+                    } else {
+                        ptx::tc_fence_after();
+                        const uint64_t ad = ptx::sdesc_kmajor_sw128(xs);
+                        const uint64_t bd = ptx::sdesc_kmajor_sw128(xs + L::X_BYTES);
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k)   // +32 bytes along K per step
+                            ptx::mma_bf16(d, ad + 2u * k, bd + 2u * k, IDESC, (kb > seg.kb0 || k > 0) ? 1u : 0u);
+                    }
                     ptx::mma_commit(EMPTY(stage));
                     if (++stage == STAGES) {
                         stage = 0;
@@ -387,6 +446,94 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
             }
             ptx::mma_commit(DONE);          // every issued MMA retires before TMEM is freed
             wait_bar_drain(DONE, 0);
+        }
+    } else if (W4 && warp >= 6) {
+        // ------------------------------------------------------------ W4A16 dequantisation
+        // Thread d handles weight row r = d % 128 of the tile and the k-half
+        // h = d / 128 of each 128-k stage: it reads the row's 8 packed words
+        // (64 k), computes w = (q - z) * s in bf16 and writes the 128-byte row
+        // into XBUF in the MMA's swizzled K-major layout.
+        //   128 + q is exact in bf16 as (0x4300 | q); subtracting 128 + z is
+        //   exact (|q - z| <= 15); the product with s is rounded once (RNE).
+        const int d = threadIdx.x - 192;
+        const int r = d & (BM - 1), h = d >> 7;
+        ptx::pdl_wait();                    // scales and zeros are read from global memory
+        int stage = 0, xb = 0;
+        uint32_t phase = 0, xphase = 0;
+        SegIter it(sched, blockIdx.x);
+        Segment seg;
+        bool ok = true;
+        while (ok && it.next(sched, seg)) {
+            int tr, tq;
+            tile_coords(sched, seg.tile, tr, tq);
+            const int n = tr * BM + r;
+            const bool row_ok = n < R;
+            const uint16_t *srow = w4.scales + (int64_t)n * w4.G;
+            const uint8_t *zrow = w4.zeros + (int64_t)n * w4.G;
+            for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
+                const int k0 = kb * L::KSTAGE + h * BK;   // first k of this thread's 64
+                // scale/zero of the (one or two) groups covering k0 .. k0 + 63
+                const int g0 = k0 / w4.group;
+                const int g1 = (k0 + BK - 1) / w4.group;
+                uint32_t sraw0 = 0, sraw1 = 0, zr0 = 0, zr1 = 0;
+                if (row_ok && k0 < w4.K) {
+                    sraw0 = __ldg(srow + g0);
+                    zr0 = __ldg(zrow + g0);
+                    if (g1 != g0 && k0 + 32 < w4.K) {
+                        sraw1 = __ldg(srow + g1);
+                        zr1 = __ldg(zrow + g1);
+                    }
+                }
+                if (!wait_bar(FULL(stage), phase, abort_flag, d_error) ||
+                    !wait_bar(XEMPTY(xb), xphase ^ 1u, abort_flag, d_error)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t *pk = smem + stage * L::STAGE_BYTES + r * (L::KSTAGE / 2) + h * (BK / 2);
+                const uint4 q0 = *reinterpret_cast<const uint4 *>(pk);
+                const uint4 q1 = *reinterpret_cast<const uint4 *>(pk + 16);
+                const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                uint8_t *xrow = smem + L::XBUF_OFF + (xb * 2 + h) * BM * BK * 2 + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                    const bool second = (w >= 4) && (g1 != g0);
+                    const uint32_t sr = second ? sraw1 : sraw0;
+                    const uint32_t zr = second ? zr1 : zr0;
+                    uint4 out;
+                    if (row_ok && k0 + 8 * w < w4.K) {
+                        const __nv_bfloat162 s2 = __halves2bfloat162(__ushort_as_bfloat16((uint16_t)sr),
+                                                                     __ushort_as_bfloat16((uint16_t)sr));
+                        const uint32_t zb = (0x4300u + zr) * 0x00010001u;    // bf16x2 (128 + z)
+                        const __nv_bfloat162 z2 = *reinterpret_cast<const __nv_bfloat162 *>(&zb);
+                        const uint32_t x = words[w];
+                        uint32_t p[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {   // p[j] = (k j, k j+4) as bf16x2 128 + q
+                            const uint32_t t = ((x >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
+                            __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(&t);
+                            v = __hmul2(__hsub2(v, z2), s2);
+                            p[j] = *reinterpret_cast<const uint32_t *>(&v);
+                        }
+                        out.x = __byte_perm(p[0], p[1], 0x5410);   // (k0, k1)
+                        out.y = __byte_perm(p[2], p[3], 0x5410);   // (k2, k3)
+                        out.z = __byte_perm(p[0], p[1], 0x7632);   // (k4, k5)
+                        out.w = __byte_perm(p[2], p[3], 0x7632);   // (k6, k7)
+                    } else {
+                        out = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    *reinterpret_cast<uint4 *>(xrow + ((w ^ (r & 7)) << 4)) = out;
+                }
+                ptx::fence_proxy_async_smem();   // the MMA reads XBUF through the async proxy
+                ptx::mbar_arrive(XFULL(xb));
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                if (++xb == 2) {
+                    xb = 0;
+                    xphase ^= 1u;
+                }
+            }
         }
     } else {
         // ------------------------------------------------------------ epilogue
@@ -459,7 +606,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
             // many float4 loads in flight: CB4 float4 columns of BATCH contributors at a time,
             // summed per column in increasing contributor (= increasing k) order
             constexpr int CB4 = (BN / 4) < 16 ? (BN / 4) : 16;
-            constexpr int INFL = MINB == 1 ? 32 : 16;
+            constexpr int INFL = W4 ? 8 : (MINB == 1 ? 32 : 16);
             constexpr int BATCH = INFL / CB4 > 0 ? INFL / CB4 : 1;
             const float4 *wsv = reinterpret_cast<const float4 *>(ws);
 #pragma unroll 1
@@ -527,7 +674,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                 ptx::bulk_copy_to_cluster(dst, src, (uint32_t)((o1 - o0) * PSTRIDE), ptx::map_cluster(REDUCE, (uint32_t)o));
             }
         }
-        if (warp >= 2) {
+        if (warp >= 2 && warp < 6) {
             const bool ok = wait_bar(REDUCE, 0, abort_flag, d_error);
             int tr, tq;
             tile_coords(sched, (int)blockIdx.x / S, tr, tq);
@@ -606,12 +753,28 @@ bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int64_t 
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES, bool SWAP, int MINB>
-cudaError_t launch_t(const CUtensorMap &mx, const CUtensorMap &my, uint16_t *C, int R, int Q, int64_t ldc,
-                     const Sched &s, const LaunchCtx &c)
+// Packed 4-bit weights as uint32 words [rows, K/8]; box 16 words (128 k) x 128
+// rows, no swizzle (the dequantising warps read plain 64-byte rows).
+bool make_map_packed(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K)
 {
-    using L = Layout<BN, STAGES>;
-    auto kern = k_umma<BN, STAGES, SWAP, MINB>;
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)(K / 8), (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(K / 8) * 4};
+    cuuint32_t box[2] = {16, (cuuint32_t)BM};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int BN, int STAGES, bool SWAP, int MINB, bool W4 = false>
+cudaError_t launch_t(const CUtensorMap &mx, const CUtensorMap &my, uint16_t *C, int R, int Q, int64_t ldc,
+                     const Sched &s, const LaunchCtx &c, const W4Args &w4 = W4Args{})
+{
+    using L = Layout<BN, STAGES, W4>;
+    auto kern = k_umma<BN, STAGES, SWAP, MINB, W4>;
     static std::once_flag once[64];
     static cudaError_t attr_err[64];
     int dev = 0;
@@ -622,7 +785,7 @@ cudaError_t launch_t(const CUtensorMap &mx, const CUtensorMap &my, uint16_t *C, 
     if (attr_err[dev & 63] != cudaSuccess) return attr_err[dev & 63];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)s.grid, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(threads_for(W4), 1, 1);
     cfg.dynamicSmemBytes = L::SMEM;
     cfg.stream = c.stream;
     cudaLaunchAttribute at[2];
@@ -639,7 +802,7 @@ cudaError_t launch_t(const CUtensorMap &mx, const CUtensorMap &my, uint16_t *C, 
     }
     cfg.attrs = at;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, kern, mx, my, C, R, Q, ldc, s, c.workspace, c.counters, c.d_error);
+    return cudaLaunchKernelEx(&cfg, kern, mx, my, C, R, Q, ldc, s, c.workspace, c.counters, c.d_error, w4);
 }
 
 }  // namespace
@@ -655,17 +818,20 @@ int umma_stages(int bn, bool skinny, bool deep)
     return bn <= 16 ? 6 : bn <= 32 ? 5 : bn <= 64 ? 4 : 3;
 }
 
+// W4A16 skinny kernels: one CTA per SM; stages of 128 k.
+int umma_w4_stages(int bn) { return bn <= 32 ? 8 : bn <= 64 ? 6 : 4; }
+
 namespace {
-template <int BN, int STAGES, bool SWAP, int MINB>
+template <int BN, int STAGES, bool SWAP, int MINB, bool W4 = false>
 int cluster_capacity_t(int cluster)
 {
-    using L = Layout<BN, STAGES>;
-    auto kern = k_umma<BN, STAGES, SWAP, MINB>;
+    using L = Layout<BN, STAGES, W4>;
+    auto kern = k_umma<BN, STAGES, SWAP, MINB, W4>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM) != cudaSuccess)
         return -1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(cluster * 64), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(threads_for(W4), 1, 1);
     cfg.dynamicSmemBytes = L::SMEM;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
@@ -682,19 +848,28 @@ int cluster_capacity_t(int cluster)
 
 // Clusters of `cluster` CTAs of the skinny kernel that can be resident at
 // once on the current device (cached per device); -1 if the query fails.
-int umma_cluster_capacity(int bn, bool deep, int cluster)
+int umma_cluster_capacity(int bn, bool deep, int cluster, bool w4)
 {
     static std::mutex mu;
-    static int cache[64][5][2][9];
-    static bool have[64][5][2][9];
+    static int cache[64][5][3][9];
+    static bool have[64][5][3][9];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cluster < 1 || cluster > 8) return -1;
     const int bi = bn <= 16 ? 0 : bn <= 32 ? 1 : bn <= 64 ? 2 : bn <= 128 ? 3 : 4;
+    const int kind = w4 ? 2 : (deep ? 1 : 0);
     std::lock_guard<std::mutex> lk(mu);
-    int &slot = cache[dev & 63][bi][deep][cluster];
-    if (!have[dev & 63][bi][deep][cluster]) {
+    int &slot = cache[dev & 63][bi][kind][cluster];
+    if (!have[dev & 63][bi][kind][cluster]) {
         int n = -1;
-        if (deep) {
+        if (w4) {
+            switch (bi) {
+            case 0: n = cluster_capacity_t<16, 8, true, 1, true>(cluster); break;
+            case 1: n = cluster_capacity_t<32, 8, true, 1, true>(cluster); break;
+            case 2: n = cluster_capacity_t<64, 6, true, 1, true>(cluster); break;
+            case 3: n = cluster_capacity_t<128, 4, true, 1, true>(cluster); break;
+            default: break;
+            }
+        } else if (deep) {
             switch (bi) {
             case 0: n = cluster_capacity_t<16, 8, true, 1>(cluster); break;
             case 1: n = cluster_capacity_t<32, 8, true, 1>(cluster); break;
@@ -712,12 +887,41 @@ int umma_cluster_capacity(int bn, bool deep, int cluster)
             }
         }
         slot = n;
-        have[dev & 63][bi][deep][cluster] = n >= 0;
+        have[dev & 63][bi][kind][cluster] = n >= 0;
     }
     return slot;
 }
 
 int g_debug_stall = 0;
+
+cudaError_t launch_umma_w4a16(const GemmArgs &a, const Plan &p, const LaunchCtx &c)
+{
+    // skinny only: X = packed weights [N, K/8], Y = activations [M, K]
+    CUtensorMap mx, my;
+    if (!make_map_packed(&mx, a.B, a.N, a.K) || !make_map(&my, a.A, a.M, a.K, a.K, p.bn))
+        return cudaErrorInvalidValue;
+    Sched s{};
+    s.mode = p.mode;
+    s.tiles_r = (int)((a.N + BM - 1) / BM);
+    s.tiles_q = (int)((a.M + p.bn - 1) / p.bn);
+    s.tiles = s.tiles_r * s.tiles_q;
+    s.nk = (int)((a.K + 2 * BK - 1) / (2 * BK));
+    s.grid = p.grid;
+    s.group_r = p.group_r > 0 ? p.group_r : s.tiles_r;
+    s.units = (long long)s.tiles * s.nk;
+    s.stall = g_debug_stall;
+    s.split = p.split;
+    W4Args w4{(const uint16_t *)a.scales, (const uint8_t *)a.zeros, (int)a.K, (int)(a.K / a.group), (int)a.group};
+    uint16_t *C = (uint16_t *)a.C;
+    const int r = (int)a.N, q = (int)a.M;
+    switch (p.bn) {
+    case 16: return launch_t<16, 8, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
+    case 32: return launch_t<32, 8, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
+    case 64: return launch_t<64, 6, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
+    case 128: return launch_t<128, 4, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
+    default: return cudaErrorInvalidValue;
+    }
+}
 
 cudaError_t launch_umma_bf16(const GemmArgs &a, const Plan &p, const LaunchCtx &c)
 {

@@ -36,3 +36,25 @@ def test_forced_timeout_is_reported_and_recoverable(variant, M):
     torch.cuda.synchronize()
     assert_close(host_bits(C), oracle.gemm_bf16(A, B), what=f"after timeout {variant}")
     assert g.gemm_last_device_error() == 0
+
+
+def test_forced_timeout_w4a16_skinny():
+    import torch
+    from dense_bit_weight_gb300 import gemm as g, synth
+    from gpu_helpers import dev_raw
+    M, N, K, group = 16, 512, 1024, 128
+    A = synth.bf16_normal((M, K), 1.0, 3, synth.STREAM_A)
+    Bq, S, Z = synth.w4a16_operands(N, K, group, 3)
+    args = (dev_bf16(A), dev_raw(Bq), dev_bf16(S), dev_raw(Z), group)
+    g.gemm_debug_inject_timeout(True)
+    try:
+        g.gemm_w4a16(*args, variant="skinny")
+        torch.cuda.synchronize()
+    finally:
+        g.gemm_debug_inject_timeout(False)
+    assert g.gemm_last_device_error() == 7
+    g.gemm_shutdown()
+    C = g.gemm_w4a16(*args, variant="skinny")
+    torch.cuda.synchronize()
+    assert_close(host_bits(C), oracle.gemm_w4a16(A, Bq, S, Z, group), what="w4a16 after timeout")
+    assert g.gemm_last_device_error() == 0
