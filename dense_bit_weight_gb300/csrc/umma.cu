@@ -69,8 +69,9 @@ namespace {
 constexpr int BM = 128;          // MMA M: rows of X per tile
 constexpr int BK = 64;           // k per MMA tile (one 128-byte swizzle row of bf16)
 constexpr int kEpiThreads = 128;
-constexpr int kDqThreads = 256;  // W4A16: dequantising threads (warps 6-13)
-__host__ __device__ constexpr int threads_for(bool w4) { return w4 ? 448 : 192; }
+constexpr int kDqThreads = 512;  // W4A16: dequantising threads (warps 6-21)
+constexpr int kNX = 4;           // W4A16: dequantised-tile buffers (each two 128 x 64 bf16 halves)
+__host__ __device__ constexpr int threads_for(bool w4) { return w4 ? 192 + kDqThreads : 192; }
 
 // W4A16 operands beyond the packed-weight tensor map.
 struct W4Args {
@@ -158,20 +159,22 @@ struct SegIter {
     }
 };
 
+// Bounded wait on an mbarrier phase.  The thread is suspended in hardware
+// between polls (woken as soon as the phase completes), and every poll checks
+// the CTA's abort flag and the 1-second limit; on expiry it raises the abort
+// flag and the device error word and returns false.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
                                          int *d_error)
 {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::global_timer_ns();
-    for (uint32_t spins = 1;; ++spins) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
-        if ((spins & 31u) == 0) {
-            if (*abort_flag) return false;
-            if (ptx::global_timer_ns() - t0 > kTimeoutNs) {
-                *abort_flag = 1u;
-                atomicExch(d_error, (int)GEMM_ERR_DEVICE_TIMEOUT);
-                return false;
-            }
+    for (;;) {
+        if (ptx::mbar_try_wait_suspend(bar, parity, 100000u)) return true;
+        if (*abort_flag) return false;
+        if (ptx::global_timer_ns() - t0 > kTimeoutNs) {
+            *abort_flag = 1u;
+            atomicExch(d_error, (int)GEMM_ERR_DEVICE_TIMEOUT);
+            return false;
         }
     }
 }
@@ -180,7 +183,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 __device__ __forceinline__ void wait_bar_drain(uint32_t bar, uint32_t parity)
 {
     const uint64_t t0 = ptx::global_timer_ns();
-    while (!ptx::mbar_try_wait(bar, parity))
+    while (!ptx::mbar_try_wait_suspend(bar, parity, 100000u))
         if (ptx::global_timer_ns() - t0 > kTimeoutNs) return;
 }
 
@@ -222,9 +225,9 @@ constexpr uint32_t tmem_cols_for(int n)
 
 // Shared memory: a ring of STAGES stages, each an X tile and a Y tile.
 // bf16: X = 128 x 64 bf16 (16 KB, TMA 128-B swizzle), Y = BN x 64 bf16.
-// W4A16: a stage covers 128 k: X = 128 rows x 128 packed 4-bit k (8 KB, plain
-// rows of 64 B), Y = two BN x 64 bf16 halves; the dequantised weights go to
-// XBUF, two buffers of two 128 x 64 bf16 tiles in the MMA's swizzled layout.
+// W4A16: a stage covers 128 k: X = 128 rows x 128 packed 4-bit k (8 KB, rows
+// of 64 B, TMA 64-byte swizzle), Y = two BN x 64 bf16 halves; the dequantised weights go to
+// XBUF, kNX buffers of two 128 x 64 bf16 tiles in the MMA's swizzled layout.
 template <int BN, int STAGES, bool W4 = false>
 struct Layout {
     static constexpr int KSTAGE = W4 ? 2 * BK : BK;
@@ -232,9 +235,10 @@ struct Layout {
     static constexpr int Y_BYTES = BN * KSTAGE * 2;
     static constexpr int STAGE_BYTES = X_BYTES + Y_BYTES;
     static constexpr int XBUF_OFF = STAGES * STAGE_BYTES;
-    static constexpr int XBUF_BYTES = W4 ? 4 * BM * BK * 2 : 0;
-    static constexpr int BAR_OFF = XBUF_OFF + XBUF_BYTES;
-    static constexpr int NBARS = 2 * STAGES + 6 + (W4 ? 4 : 0);
+    static constexpr int XBUF_BYTES = W4 ? kNX * 2 * BM * BK * 2 : 0;
+    static constexpr int SZ_OFF = XBUF_OFF + XBUF_BYTES;   // end of the ring and dequantisation buffers
+    static constexpr int BAR_OFF = SZ_OFF;
+    static constexpr int NBARS = 2 * STAGES + 6 + (W4 ? 2 * kNX : 0);
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int SMEM = MISC_OFF + 16 + 1024;   // + slack to align the base to 1024
 };
@@ -261,8 +265,8 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
     auto TEMPTY = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
     const uint32_t DONE = bar0 + 8u * (2 * STAGES + 4);
     const uint32_t REDUCE = bar0 + 8u * (2 * STAGES + 5);   // mode 2: incoming partial slices
-    auto XFULL = [&](int b) { return bar0 + 8u * (2 * STAGES + 6 + b); };    // W4A16: dequantised tile ready
-    auto XEMPTY = [&](int b) { return bar0 + 8u * (2 * STAGES + 8 + b); };   // W4A16: MMA done with it
+    auto XFULL = [&](int b) { return bar0 + 8u * (2 * STAGES + 6 + b); };          // W4A16: dequantised tile ready
+    auto XEMPTY = [&](int b) { return bar0 + 8u * (2 * STAGES + 6 + kNX + b); };   // W4A16: MMA done with it
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile uint32_t *abort_flag = misc + 1;
@@ -279,7 +283,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
         ptx::mbar_init(DONE, 1);
         ptx::mbar_init(REDUCE, 1);
         if (W4)
-            for (int b = 0; b < 2; ++b) {
+            for (int b = 0; b < kNX; ++b) {
                 ptx::mbar_init(XFULL(b), kDqThreads);
                 ptx::mbar_init(XEMPTY(b), 1);
             }
@@ -311,10 +315,67 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
     constexpr int PSTRIDE = BN * 4 + 16;   // bytes per row of the mode-2 partial tile in smem
     // mode-2 partial [128][PSTRIDE] at ring offset 0, incoming slices after it
     constexpr int IN_OFF = BM * PSTRIDE;
-    static_assert(!kCanClusterSplit || (BM + 8 + BM) * PSTRIDE <= STAGES * L::STAGE_BYTES,
-                  "partials must fit the ring");
+    // (the ring and, for W4A16, the dequantisation buffers are free by then)
+    static_assert(!kCanClusterSplit || (BM + 8 + BM) * PSTRIDE <= L::SZ_OFF, "partials must fit the ring");
 
-    if (warp == 0) {
+    if (W4 && warp == 0) {
+        // ------------------------------------------------------------ W4A16 producer
+        if (lane == 0) {
+            const uint64_t pol_x = ptx::policy_evict_first();
+            const uint64_t pol_y = ptx::policy_evict_last();
+            int stage = 0;
+            uint32_t phase = 0;
+            long long issued = 0;
+            {
+                SegIter pre(sched, blockIdx.x);
+                Segment s0;
+                if (pre.next(sched, s0) && !sched.stall) {
+                    int tr, tq;
+                    tile_coords(sched, s0.tile, tr, tq);
+                    const int kend = min(s0.kb1, s0.kb0 + STAGES);
+                    for (int kb = s0.kb0; kb < kend; ++kb) {
+                        ptx::tma_prefetch_l2_2d(&tmX, kb * (L::KSTAGE / 8), tr * BM);
+                        ptx::tma_prefetch_l2_2d(&tmY, kb * L::KSTAGE, tq * BN);
+                        ptx::tma_prefetch_l2_2d(&tmY, kb * L::KSTAGE + BK, tq * BN);
+                    }
+                }
+                ptx::pdl_wait();
+            }
+            SegIter it(sched, blockIdx.x);
+            Segment seg;
+            bool ok = true;
+            while (ok && it.next(sched, seg)) {
+                int tr, tq;
+                tile_coords(sched, seg.tile, tr, tq);
+                for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
+                    if (!wait_bar(EMPTY(stage), phase ^ 1u, abort_flag, d_error)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!sched.stall) {   // packed words (8 k each), then the two activation halves
+                        ptx::mbar_arrive_expect_tx(FULL(stage), L::STAGE_BYTES);
+                        const uint32_t xs = sbase + stage * L::STAGE_BYTES;
+                        ptx::tma_load_2d(xs, &tmX, FULL(stage), kb * (L::KSTAGE / 8), tr * BM, pol_x);
+                        ptx::tma_load_2d(xs + L::X_BYTES, &tmY, FULL(stage), kb * L::KSTAGE, tq * BN, pol_y);
+                        ptx::tma_load_2d(xs + L::X_BYTES + BN * BK * 2, &tmY, FULL(stage), kb * L::KSTAGE + BK,
+                                         tq * BN, pol_y);
+                        ++issued;
+                    }
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                for (int s = 0; s < STAGES; ++s) {
+                    if (issued <= s) continue;
+                    const long long last = issued - 1 - ((issued - 1 - s) % STAGES);
+                    wait_bar_drain(FULL(s), (uint32_t)((last / STAGES) & 1));
+                }
+            }
+        }
+    } else if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             const uint64_t pol_x = SWAP ? ptx::policy_evict_first() : ptx::policy_evict_last();
@@ -419,7 +480,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                                               (kb > seg.kb0 || h > 0 || k > 0) ? 1u : 0u);
                         }
                         ptx::mma_commit(XEMPTY(xb));
-                        if (++xb == 2) {
+                        if (++xb == kNX) {
                             xb = 0;
                             xphase ^= 1u;
                         }
@@ -449,15 +510,23 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
         }
     } else if (W4 && warp >= 6) {
         // ------------------------------------------------------------ W4A16 dequantisation
-        // Thread d handles weight row r = d % 128 of the tile and the k-half
-        // h = d / 128 of each 128-k stage: it reads the row's 8 packed words
-        // (64 k), computes w = (q - z) * s in bf16 and writes the 128-byte row
-        // into XBUF in the MMA's swizzled K-major layout.
+        // Warp wd owns weight rows 8wd .. 8wd+7 of the tile; per stage (128 k),
+        // lane l takes row 8wd + l % 8 and the 32 k numbered l / 8: one 16-byte
+        // load of 4 packed words, w = (q - z) * s in bf16, four 16-byte stores
+        // into XBUF (half h = k / 64, chunk (k % 64) / 8) in the MMA's swizzled
+        // K-major layout.  Each quarter-warp covers 8 consecutive rows of one
+        // 32-k slice, so loads (64-byte swizzle) and stores (128-byte swizzle)
+        // are free of bank conflicts.
         //   128 + q is exact in bf16 as (0x4300 | q); subtracting 128 + z is
         //   exact (|q - z| <= 15); the product with s is rounded once (RNE).
         const int d = threadIdx.x - 192;
-        const int r = d & (BM - 1), h = d >> 7;
-        ptx::pdl_wait();                    // scales and zeros are read from global memory
+        const int wd = d >> 5;
+        const int r = 8 * wd + (lane & 7);
+        const int q4 = lane >> 3;                  // which 32 k of the stage
+        const int h = q4 >> 1, cbase = (q4 & 1) * 4;
+        const uint32_t pk_off = (uint32_t)(r * 64 + ((q4 ^ ((r >> 1) & 3)) << 4));
+        const uint32_t xrow_off = (uint32_t)(h * BM * BK * 2 + (r >> 3) * 1024 + (r & 7) * 128);
+        ptx::pdl_wait();                           // scales and zeros come from global memory
         int stage = 0, xb = 0;
         uint32_t phase = 0, xphase = 0;
         SegIter it(sched, blockIdx.x);
@@ -467,69 +536,61 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
             int tr, tq;
             tile_coords(sched, seg.tile, tr, tq);
             const int n = tr * BM + r;
-            const bool row_ok = n < R;
+            const bool nv = n < R;
             const uint16_t *srow = w4.scales + (int64_t)n * w4.G;
             const uint8_t *zrow = w4.zeros + (int64_t)n * w4.G;
+            // (scale, zero) of this thread's group, one stage ahead, through L1
+            auto load_sz = [&](int kb, uint32_t &sv, uint32_t &zv) {
+                const int kq = kb * L::KSTAGE + q4 * 32;
+                const bool in = nv && kq < w4.K;
+                const int gi = kq / w4.group;
+                sv = in ? __ldg(srow + gi) : 0u;
+                zv = in ? __ldg(zrow + gi) : 0u;
+            };
+            uint32_t sv, zv;
+            load_sz(seg.kb0, sv, zv);
             for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
-                const int k0 = kb * L::KSTAGE + h * BK;   // first k of this thread's 64
-                // scale/zero of the (one or two) groups covering k0 .. k0 + 63
-                const int g0 = k0 / w4.group;
-                const int g1 = (k0 + BK - 1) / w4.group;
-                uint32_t sraw0 = 0, sraw1 = 0, zr0 = 0, zr1 = 0;
-                if (row_ok && k0 < w4.K) {
-                    sraw0 = __ldg(srow + g0);
-                    zr0 = __ldg(zrow + g0);
-                    if (g1 != g0 && k0 + 32 < w4.K) {
-                        sraw1 = __ldg(srow + g1);
-                        zr1 = __ldg(zrow + g1);
-                    }
-                }
+                uint32_t sn = 0, zn = 0;
+                if (kb + 1 < seg.kb1) load_sz(kb + 1, sn, zn);
                 if (!wait_bar(FULL(stage), phase, abort_flag, d_error) ||
                     !wait_bar(XEMPTY(xb), xphase ^ 1u, abort_flag, d_error)) {
                     ok = false;
                     break;
                 }
-                const uint8_t *pk = smem + stage * L::STAGE_BYTES + r * (L::KSTAGE / 2) + h * (BK / 2);
-                const uint4 q0 = *reinterpret_cast<const uint4 *>(pk);
-                const uint4 q1 = *reinterpret_cast<const uint4 *>(pk + 16);
-                const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                uint8_t *xrow = smem + L::XBUF_OFF + (xb * 2 + h) * BM * BK * 2 + (r >> 3) * 1024 + (r & 7) * 128;
+                const uint4 wv = ptx::lds128(sbase + stage * L::STAGE_BYTES + pk_off);
+                const uint32_t s2u = sv * 0x00010001u;
+                const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162 *>(&s2u);
+                const uint32_t zbu = (0x4300u + zv) * 0x00010001u;   // bf16x2 (128 + z)
+                const __nv_bfloat162 z2 = *reinterpret_cast<const __nv_bfloat162 *>(&zbu);
+                const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
+                const uint32_t xrow = sbase + L::XBUF_OFF + xb * 2 * BM * BK * 2 + xrow_off;
 #pragma unroll
-                for (int w = 0; w < 8; ++w) {
-                    const bool second = (w >= 4) && (g1 != g0);
-                    const uint32_t sr = second ? sraw1 : sraw0;
-                    const uint32_t zr = second ? zr1 : zr0;
-                    uint4 out;
-                    if (row_ok && k0 + 8 * w < w4.K) {
-                        const __nv_bfloat162 s2 = __halves2bfloat162(__ushort_as_bfloat16((uint16_t)sr),
-                                                                     __ushort_as_bfloat16((uint16_t)sr));
-                        const uint32_t zb = (0x4300u + zr) * 0x00010001u;    // bf16x2 (128 + z)
-                        const __nv_bfloat162 z2 = *reinterpret_cast<const __nv_bfloat162 *>(&zb);
-                        const uint32_t x = words[w];
-                        uint32_t p[4];
+                for (int w = 0; w < 4; ++w) {
+                    const uint32_t x = words[w];
+                    uint32_t p[4];
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {   // p[j] = (k j, k j+4) as bf16x2 128 + q
-                            const uint32_t t = ((x >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
-                            __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(&t);
-                            v = __hmul2(__hsub2(v, z2), s2);
-                            p[j] = *reinterpret_cast<const uint32_t *>(&v);
-                        }
-                        out.x = __byte_perm(p[0], p[1], 0x5410);   // (k0, k1)
-                        out.y = __byte_perm(p[2], p[3], 0x5410);   // (k2, k3)
-                        out.z = __byte_perm(p[0], p[1], 0x7632);   // (k4, k5)
-                        out.w = __byte_perm(p[2], p[3], 0x7632);   // (k6, k7)
-                    } else {
-                        out = make_uint4(0u, 0u, 0u, 0u);
+                    for (int j = 0; j < 4; ++j) {   // p[j] = (k j, k j+4) as bf16x2 128 + q
+                        const uint32_t t = ((x >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
+                        __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(&t);
+                        v = __hmul2(__hsub2(v, z2), s2);
+                        p[j] = *reinterpret_cast<const uint32_t *>(&v);
                     }
-                    *reinterpret_cast<uint4 *>(xrow + ((w ^ (r & 7)) << 4)) = out;
+                    uint4 out;
+                    out.x = __byte_perm(p[0], p[1], 0x5410);   // (k0, k1)
+                    out.y = __byte_perm(p[2], p[3], 0x5410);   // (k2, k3)
+                    out.z = __byte_perm(p[0], p[1], 0x7632);   // (k4, k5)
+                    out.w = __byte_perm(p[2], p[3], 0x7632);   // (k6, k7)
+                    ptx::sts128(xrow + (((cbase + w) ^ (r & 7)) << 4), out);
                 }
                 ptx::fence_proxy_async_smem();   // the MMA reads XBUF through the async proxy
                 ptx::mbar_arrive(XFULL(xb));
+                sv = sn;
+                zv = zn;
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1u;
                 }
-                if (++xb == 2) {
+                if (++xb == kNX) {
                     xb = 0;
                     xphase ^= 1u;
                 }
@@ -605,8 +666,8 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
             __threadfence();
             // many float4 loads in flight: CB4 float4 columns of BATCH contributors at a time,
             // summed per column in increasing contributor (= increasing k) order
-            constexpr int CB4 = (BN / 4) < 16 ? (BN / 4) : 16;
-            constexpr int INFL = W4 ? 8 : (MINB == 1 ? 32 : 16);
+            constexpr int CB4 = (BN / 4) < (W4 ? 4 : 16) ? (BN / 4) : (W4 ? 4 : 16);
+            constexpr int INFL = W4 ? 4 : (MINB == 1 ? 32 : 16);
             constexpr int BATCH = INFL / CB4 > 0 ? INFL / CB4 : 1;
             const float4 *wsv = reinterpret_cast<const float4 *>(ws);
 #pragma unroll 1
@@ -754,7 +815,8 @@ bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int64_t 
 }
 
 // Packed 4-bit weights as uint32 words [rows, K/8]; box 16 words (128 k) x 128
-// rows, no swizzle (the dequantising warps read plain 64-byte rows).
+// rows with the 64-byte swizzle (16-byte piece c of row r lands at piece
+// c ^ ((r / 2) % 4)), so the dequantising warps read it without bank conflicts.
 bool make_map_packed(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K)
 {
     auto fn = encode_fn();
@@ -764,7 +826,7 @@ bool make_map_packed(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K)
     cuuint32_t box[2] = {16, (cuuint32_t)BM};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -819,7 +881,7 @@ int umma_stages(int bn, bool skinny, bool deep)
 }
 
 // W4A16 skinny kernels: one CTA per SM; stages of 128 k.
-int umma_w4_stages(int bn) { return bn <= 32 ? 8 : bn <= 64 ? 6 : 4; }
+int umma_w4_stages(int bn) { return bn <= 16 ? 6 : bn <= 32 ? 5 : bn <= 64 ? 3 : 2; }
 
 namespace {
 template <int BN, int STAGES, bool SWAP, int MINB, bool W4 = false>
@@ -863,10 +925,10 @@ int umma_cluster_capacity(int bn, bool deep, int cluster, bool w4)
         int n = -1;
         if (w4) {
             switch (bi) {
-            case 0: n = cluster_capacity_t<16, 8, true, 1, true>(cluster); break;
-            case 1: n = cluster_capacity_t<32, 8, true, 1, true>(cluster); break;
-            case 2: n = cluster_capacity_t<64, 6, true, 1, true>(cluster); break;
-            case 3: n = cluster_capacity_t<128, 4, true, 1, true>(cluster); break;
+            case 0: n = cluster_capacity_t<16, 6, true, 1, true>(cluster); break;
+            case 1: n = cluster_capacity_t<32, 5, true, 1, true>(cluster); break;
+            case 2: n = cluster_capacity_t<64, 3, true, 1, true>(cluster); break;
+            case 3: n = cluster_capacity_t<128, 2, true, 1, true>(cluster); break;
             default: break;
             }
         } else if (deep) {
@@ -915,10 +977,10 @@ cudaError_t launch_umma_w4a16(const GemmArgs &a, const Plan &p, const LaunchCtx 
     uint16_t *C = (uint16_t *)a.C;
     const int r = (int)a.N, q = (int)a.M;
     switch (p.bn) {
-    case 16: return launch_t<16, 8, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
-    case 32: return launch_t<32, 8, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
-    case 64: return launch_t<64, 6, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
-    case 128: return launch_t<128, 4, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
+    case 16: return launch_t<16, 6, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
+    case 32: return launch_t<32, 5, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
+    case 64: return launch_t<64, 3, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
+    case 128: return launch_t<128, 2, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
     default: return cudaErrorInvalidValue;
     }
 }
