@@ -49,6 +49,27 @@ WORKLOAD = ("decode projections, Qwen3-8B-like dims: bf16 A[M,4096], M in {1,8,3
             "B in {qkv 6144x4096, o 4096x4096, gate/up 24576x4096}, fp32 accumulate, bf16 out")
 
 
+# DRAM bytes (read + write) per launch of each decode GEMM, from one ncu pass
+# (profiles/decode_step_dram_traffic.md) over the kernel sources with this
+# SHA-256; reported only while the sources are unchanged.
+TRAFFIC_SOURCES_SHA256 = "8dd1a241e233e8949e48beff720e9caef78697c7406cbd2ee54405ef02591f3b"
+TRAFFIC_BYTES = {(1, 4096, 4096): 33.57e6, (1, 6144, 4096): 50.35e6, (1, 24576, 4096): 201.42e6,
+                 (8, 4096, 4096): 33.71e6, (8, 6144, 4096): 50.48e6, (8, 24576, 4096): 201.54e6,
+                 (32, 4096, 4096): 33.90e6, (32, 6144, 4096): 50.68e6, (32, 24576, 4096): 201.78e6,
+                 (128, 4096, 4096): 34.70e6, (128, 6144, 4096): 51.47e6, (128, 24576, 4096): 202.69e6}
+
+
+def kernel_sources_sha256():
+    import hashlib
+    csrc = os.path.join(ROOT, "dense_bit_weight_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()
+
+
 def bytes_bf16(M, N, K):
     return 2 * (M * K + N * K + M * N)
 
@@ -301,38 +322,42 @@ def run_ours(args):
             arm.step()
     torch.cuda.synchronize()
 
-    # One CUDA graph holds S steps with a pair of timing events around every
-    # GEMM; the timed region replays it K/S times (plus a graph of K % S steps),
-    # so exactly K steps run back to back without host launch gaps.
+    # The timed region replays a CUDA graph of S steps (plus one of K % S steps)
+    # so exactly K steps run back to back with no host launch gaps and no
+    # timing events between GEMMs.  A second graph of the same S steps, with a
+    # pair of events around each kernel family's GEMMs, is replayed afterwards
+    # over K steps for the per-kernel durations (an event between two kernels
+    # costs a launch gap, so it is kept out of the headline region).
     S = max(1, min(args.steps, args.graph_steps))
     try:
         mk = lambda: torch.cuda.Event(enable_timing=True, external=True)
         mk()
     except TypeError:
         mk = None
-
     n_groups = len(arm.groups)
 
-    def capture(nsteps):
-        evs = [[(mk(), mk()) for _ in range(n_groups)] for _ in range(nsteps)] if mk else None
+    def capture(nsteps, with_events):
+        evs = [[(mk(), mk()) for _ in range(n_groups)] for _ in range(nsteps)] if (with_events and mk) else None
         gr = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gr, stream=stream):
             for k in range(nsteps):
                 arm.step(evs[k] if evs else None)
         return gr, evs
 
-    graph, events = capture(S)
+    graph, _ = capture(S, False)
     rest = args.steps % S
-    graph_rest, _ = capture(rest) if rest else (None, None)
+    graph_rest, _ = capture(rest, False) if rest else (None, None)
+    graph_ev, events = capture(S, True)
     with torch.cuda.stream(stream):
         graph.replay()
+        graph_ev.replay()
     torch.cuda.synchronize()
 
-    def replay_steps():
+    def replay_steps(g_main, g_rest):
         for _ in range(args.steps // S):
-            graph.replay()
-        if graph_rest is not None:
-            graph_rest.replay()
+            g_main.replay()
+        if g_rest is not None:
+            g_rest.replay()
 
     clocks = Clocks(torch.cuda.current_device())
     clocks.start()
@@ -349,10 +374,22 @@ def run_ours(args):
     t1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         t0.record(stream)
-        replay_steps()
+        replay_steps(graph, graph_rest)
         t1.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
+    # the per-kernel replays (same load, inside the clock window)
+    group_ms = [0.0] * n_groups
+    nsteps = 0
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.steps // S)):
+            graph_ev.replay()
+            torch.cuda.synchronize()
+            if events is not None:
+                for k in range(S):
+                    for gi in range(n_groups):
+                        group_ms[gi] += events[k][gi][0].elapsed_time(events[k][gi][1])
+            nsteps += S
     t_end = time.time() + args.preroll
     with torch.cuda.stream(stream):
         while time.time() < t_end:
@@ -363,29 +400,26 @@ def run_ours(args):
     step_bytes = sum(it["bytes"] for it in arm.items)
     value = ws * step_bytes * args.steps / (ms_total * 1e-3) / 1e9
 
-    # per-kernel-family durations: the events of the last replay of the
-    # S-step graph (events in a graph are overwritten by each replay)
     per = {}
-    nsteps = S
-    group_ms = [0.0] * n_groups
     if events is None:
         # no external events in this torch: time each family alone in a graph of S steps
+        nsteps = S
         for gi, grp in enumerate(arm.groups):
             calls = [arm.items[i] for i in grp["idx"]]
             group_ms[gi] = graph_time_ms(torch, lambda _k, calls=calls: [arm.call(c) for c in calls], S) * S
-    else:
-        for k in range(S):
-            for gi in range(n_groups):
-                group_ms[gi] += events[k][gi][0].elapsed_time(events[k][gi][1])
     for gi, grp in enumerate(arm.groups):
         its = [arm.items[i] for i in grp["idx"]]
         per[grp["name"]] = {"ms": group_ms[gi], "bytes": sum(it["bytes"] for it in its) * nsteps,
                             "launches": sum(it["plan"]["kernels"] for it in its) * nsteps,
-                            "shapes": [[it["M"], it["N"], it["K"]] for it in its]}
+                            "shapes": [[it["M"], it["N"], it["K"]] for it in its],
+                            "traffic": [TRAFFIC_BYTES.get((it["M"], it["N"], it["K"])) for it in its]}
     dom_name = max(per, key=lambda k: per[k]["ms"])
     dom = per[dom_name]
     hbm, tf, tf_sus, src = peaks()
     achieved = dom["bytes"] / (dom["ms"] * 1e-3) / 1e9
+    traffic = None
+    if kernel_sources_sha256() == TRAFFIC_SOURCES_SHA256 and None not in dom["traffic"]:
+        traffic = round(sum(dom["traffic"]) / len(dom["traffic"]))     # bytes per launch, family average
     gpu_launches = sum(it["plan"]["kernels"] for it in arm.items) * args.steps
 
     # end to end through the public call, host buffers, copies inside the timing
@@ -454,14 +488,16 @@ def run_ours(args):
             "ms_per_step": round(ms_total / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": WORKLOAD, "gemms_per_step": n_items,
-                       "timing": f"CUDA graph of {S} steps replayed; timing events inside the graph "
-                                 "around each kernel family's GEMMs",
+                       "timing": f"CUDA graph of {S} steps replayed with no events between GEMMs; "
+                                 "per-kernel durations from a second replay with events around each "
+                                 "kernel family's GEMMs",
                        "l2": "inputs larger than L2: each GEMM has its own weight copy, "
                              f"{step_bytes / 1e9:.2f} GB streamed per step",
                        "parallelism": f"replicas x{ws}"},
             "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1),
                          "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                         "peak_source": src, "traffic": None},
+                         "peak_source": src, "traffic": traffic,
+                         "algorithmic_bytes_per_launch": round(dom["bytes"] / dom["launches"])},
             "e2e": {k: (round(v, 2) if isinstance(v, float) else v) for k, v in e2e.items()},
             "cpu_baseline": cpu,
             "gpu_launches": gpu_launches,
