@@ -292,7 +292,7 @@ bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan 
 }
 
 // W4A16: CUDA-core GEMV for M <= 4; the tcgen05 skinny kernel with
-// in-kernel dequantisation for 5 <= M <= 128 (stages of 128 k): cluster
+// in-kernel dequantisation for 5 <= M <= 128 (stages of 256 k): cluster
 // split-K (mode 2) when the weight tiles fit one wave, stream-K (mode 1)
 // beyond that.  Larger M runs the GEMV path (one pass per four rows).
 bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int sm_count, Plan *p, bool query)
@@ -307,7 +307,7 @@ bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int
         int bn = 16;
         while (bn < M) bn *= 2;
         const int64_t tiles = (N + kUmmaBM - 1) / kUmmaBM;
-        const int64_t nk = (K + 2 * kUmmaBK - 1) / (2 * kUmmaBK);
+        const int64_t nk = (K + 4 * kUmmaBK - 1) / (4 * kUmmaBK);   // 256-k stages
         const int64_t G = sm_count;
         p->variant = GEMM_VARIANT_SKINNY;
         p->kernels = 1;

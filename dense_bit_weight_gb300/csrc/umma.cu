@@ -70,8 +70,10 @@ constexpr int BM = 128;          // MMA M: rows of X per tile
 constexpr int BK = 64;           // k per MMA tile (one 128-byte swizzle row of bf16)
 constexpr int kEpiThreads = 128;
 constexpr int kDqThreads = 512;  // W4A16: dequantising threads (warps 6-21)
-constexpr int kNX = 4;           // W4A16: dequantised-tile buffers (each two 128 x 64 bf16 halves)
-__host__ __device__ constexpr int threads_for(bool w4) { return w4 ? 192 + kDqThreads : 192; }
+constexpr int kNX = 8;           // W4A16: dequantised 128 x 64 bf16 tiles in TMEM (two per 64-k sub-tile position)
+constexpr uint32_t kXCol = 256;  // W4A16: TMEM column of the first dequantised tile (32 columns each)
+constexpr int kActWarp = 22;     // W4A16: warp that loads the activation tiles
+__host__ __device__ constexpr int threads_for(bool w4) { return w4 ? 192 + kDqThreads + 32 : 192; }
 
 // W4A16 operands beyond the packed-weight tensor map.
 struct W4Args {
@@ -179,6 +181,16 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     }
 }
 
+// The same wait by every lane of a converged warp, with a warp-uniform result
+// (a lane that timed out makes the whole warp give up), so the warp can go on
+// to .sync.aligned tensor-memory operations and elected MMA issue together.
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                              int *d_error)
+{
+    const bool ok = wait_bar(bar, parity, abort_flag, d_error);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // Wait without looking at the abort flag (used when draining before exit).
 __device__ __forceinline__ void wait_bar_drain(uint32_t bar, uint32_t parity)
 {
@@ -223,22 +235,26 @@ constexpr uint32_t tmem_cols_for(int n)
     return n <= 32 ? 32u : n <= 64 ? 64u : n <= 128 ? 128u : n <= 256 ? 256u : 512u;
 }
 
-// Shared memory: a ring of STAGES stages, each an X tile and a Y tile.
-// bf16: X = 128 x 64 bf16 (16 KB, TMA 128-B swizzle), Y = BN x 64 bf16.
-// W4A16: a stage covers 128 k: X = 128 rows x 128 packed 4-bit k (8 KB, rows
-// of 64 B, TMA 64-byte swizzle), Y = two BN x 64 bf16 halves; the dequantised weights go to
-// XBUF, kNX buffers of two 128 x 64 bf16 tiles in the MMA's swizzled layout.
+// Shared memory.
+// bf16: a ring of STAGES stages, each an X tile (128 x 64 bf16, 16 KB, TMA
+// 128-B swizzle) and a Y tile (BN x 64 bf16).
+// W4A16: two rings.  Packed weights: STAGES stages of 128 rows x 256 k of
+// 4-bit codes (16 KB, TMA 128-B swizzle), released by the dequantising warps as
+// soon as they have read them.  Activations: AST tiles of BN x 64 bf16, released
+// by the MMA.  The dequantised weights live in tensor memory (kNX tiles of
+// 128 x 64 bf16 from column kXCol), where the MMA reads its A operand.
 template <int BN, int STAGES, bool W4 = false>
 struct Layout {
-    static constexpr int KSTAGE = W4 ? 2 * BK : BK;
+    static constexpr int KSTAGE = W4 ? 4 * BK : BK;                 // k per ring stage
     static constexpr int X_BYTES = W4 ? BM * KSTAGE / 2 : BM * BK * 2;
-    static constexpr int Y_BYTES = BN * KSTAGE * 2;
+    static constexpr int Y_BYTES = W4 ? 0 : BN * BK * 2;
     static constexpr int STAGE_BYTES = X_BYTES + Y_BYTES;
-    static constexpr int XBUF_OFF = STAGES * STAGE_BYTES;
-    static constexpr int XBUF_BYTES = W4 ? kNX * 2 * BM * BK * 2 : 0;
-    static constexpr int SZ_OFF = XBUF_OFF + XBUF_BYTES;   // end of the ring and dequantisation buffers
+    static constexpr int AST = !W4 ? 0 : BN <= 16 ? 12 : BN <= 32 ? 8 : BN <= 64 ? 6 : 3;
+    static constexpr int A_BYTES = BN * BK * 2;
+    static constexpr int A_OFF = STAGES * STAGE_BYTES;
+    static constexpr int SZ_OFF = A_OFF + AST * A_BYTES;   // end of the rings
     static constexpr int BAR_OFF = SZ_OFF;
-    static constexpr int NBARS = 2 * STAGES + 6 + (W4 ? 2 * kNX : 0);
+    static constexpr int NBARS = 2 * STAGES + 6 + (W4 ? 2 * kNX + 2 * AST : 0);
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int SMEM = MISC_OFF + 16 + 1024;   // + slack to align the base to 1024
 };
@@ -250,7 +266,12 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
        float *__restrict__ ws, int *__restrict__ counters, int *__restrict__ d_error, const W4Args w4)
 {
     using L = Layout<BN, STAGES, W4>;
-    constexpr uint32_t TMEM_COLS = tmem_cols_for(2 * BN);
+    // W4A16 takes all 512 columns: two accumulators below kXCol, the
+    // dequantised tiles above.  Its shared memory admits one CTA per SM, so
+    // the allocation never waits on a CTA of the same cluster.
+    constexpr uint32_t TMEM_COLS = W4 ? 512u : tmem_cols_for(2 * BN);
+    static_assert(!W4 || (2 * BN <= (int)kXCol && kXCol + kNX * 32 <= 512), "W4A16 TMEM map");
+    static_assert(!W4 || L::SMEM > 114 * 1024, "W4A16 needs one CTA per SM (it allocates all of TMEM)");
     constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN);
 
     extern __shared__ uint8_t smem_raw[];
@@ -267,6 +288,8 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
     const uint32_t REDUCE = bar0 + 8u * (2 * STAGES + 5);   // mode 2: incoming partial slices
     auto XFULL = [&](int b) { return bar0 + 8u * (2 * STAGES + 6 + b); };          // W4A16: dequantised tile ready
     auto XEMPTY = [&](int b) { return bar0 + 8u * (2 * STAGES + 6 + kNX + b); };   // W4A16: MMA done with it
+    auto AFULL = [&](int a) { return bar0 + 8u * (2 * STAGES + 6 + 2 * kNX + a); };              // W4A16
+    auto AEMPTY = [&](int a) { return bar0 + 8u * (2 * STAGES + 6 + 2 * kNX + L::AST + a); };   // W4A16
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile uint32_t *abort_flag = misc + 1;
@@ -274,7 +297,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(FULL(s), 1);
-            ptx::mbar_init(EMPTY(s), 1);
+            ptx::mbar_init(EMPTY(s), W4 ? kDqThreads : 1);   // W4A16: every dequantising thread releases
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(TFULL(a), 1);
@@ -282,11 +305,16 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
         }
         ptx::mbar_init(DONE, 1);
         ptx::mbar_init(REDUCE, 1);
-        if (W4)
+        if (W4) {
             for (int b = 0; b < kNX; ++b) {
-                ptx::mbar_init(XFULL(b), kDqThreads);
+                ptx::mbar_init(XFULL(b), kDqThreads / 4);   // the four warps writing that tile
                 ptx::mbar_init(XEMPTY(b), 1);
             }
+            for (int a = 0; a < L::AST; ++a) {
+                ptx::mbar_init(AFULL(a), 1);
+                ptx::mbar_init(AEMPTY(a), 1);
+            }
+        }
         misc[1] = 0;
         misc[2] = 0;
         ptx::fence_mbar_init();
@@ -315,29 +343,28 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
     constexpr int PSTRIDE = BN * 4 + 16;   // bytes per row of the mode-2 partial tile in smem
     // mode-2 partial [128][PSTRIDE] at ring offset 0, incoming slices after it
     constexpr int IN_OFF = BM * PSTRIDE;
-    // (the ring and, for W4A16, the dequantisation buffers are free by then)
+    // (the rings are free by then)
     static_assert(!kCanClusterSplit || (BM + 8 + BM) * PSTRIDE <= L::SZ_OFF, "partials must fit the ring");
 
-    if (W4 && warp == 0) {
-        // ------------------------------------------------------------ W4A16 producer
+    if (W4 && (warp == 0 || warp == kActWarp)) {
+        // ------------------------------------------------------------ W4A16 producers
+        // warp 0 streams the packed weights, warp kActWarp the activation tiles;
+        // the two rings are independent so weight loads never wait on the MMA.
         if (lane == 0) {
-            const uint64_t pol_x = ptx::policy_evict_first();
-            const uint64_t pol_y = ptx::policy_evict_last();
-            int stage = 0;
+            const bool packed = warp == 0;
+            const uint64_t pol = packed ? ptx::policy_evict_first() : ptx::policy_evict_last();
+            const int nslots = packed ? STAGES : L::AST;
+            int slot = 0;
             uint32_t phase = 0;
             long long issued = 0;
             {
                 SegIter pre(sched, blockIdx.x);
                 Segment s0;
-                if (pre.next(sched, s0) && !sched.stall) {
+                if (packed && pre.next(sched, s0) && !sched.stall) {
                     int tr, tq;
                     tile_coords(sched, s0.tile, tr, tq);
                     const int kend = min(s0.kb1, s0.kb0 + STAGES);
-                    for (int kb = s0.kb0; kb < kend; ++kb) {
-                        ptx::tma_prefetch_l2_2d(&tmX, kb * (L::KSTAGE / 8), tr * BM);
-                        ptx::tma_prefetch_l2_2d(&tmY, kb * L::KSTAGE, tq * BN);
-                        ptx::tma_prefetch_l2_2d(&tmY, kb * L::KSTAGE + BK, tq * BN);
-                    }
+                    for (int kb = s0.kb0; kb < kend; ++kb) ptx::tma_prefetch_l2_2d(&tmX, kb * (L::KSTAGE / 8), tr * BM);
                 }
                 ptx::pdl_wait();
             }
@@ -347,31 +374,38 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
             while (ok && it.next(sched, seg)) {
                 int tr, tq;
                 tile_coords(sched, seg.tile, tr, tq);
-                for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
-                    if (!wait_bar(EMPTY(stage), phase ^ 1u, abort_flag, d_error)) {
-                        ok = false;
-                        break;
-                    }
-                    if (!sched.stall) {   // packed words (8 k each), then the two activation halves
-                        ptx::mbar_arrive_expect_tx(FULL(stage), L::STAGE_BYTES);
-                        const uint32_t xs = sbase + stage * L::STAGE_BYTES;
-                        ptx::tma_load_2d(xs, &tmX, FULL(stage), kb * (L::KSTAGE / 8), tr * BM, pol_x);
-                        ptx::tma_load_2d(xs + L::X_BYTES, &tmY, FULL(stage), kb * L::KSTAGE, tq * BN, pol_y);
-                        ptx::tma_load_2d(xs + L::X_BYTES + BN * BK * 2, &tmY, FULL(stage), kb * L::KSTAGE + BK,
-                                         tq * BN, pol_y);
-                        ++issued;
-                    }
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
+                for (int kb = seg.kb0; ok && kb < seg.kb1; ++kb) {
+                    for (int u = 0; u < (packed ? 1 : L::KSTAGE / BK); ++u) {
+                        const uint32_t full = packed ? FULL(slot) : AFULL(slot);
+                        const uint32_t empty = packed ? EMPTY(slot) : AEMPTY(slot);
+                        if (!wait_bar(empty, phase ^ 1u, abort_flag, d_error)) {
+                            ok = false;
+                            break;
+                        }
+                        if (!sched.stall) {
+                            if (packed) {
+                                ptx::mbar_arrive_expect_tx(full, L::X_BYTES);
+                                ptx::tma_load_2d(sbase + slot * L::STAGE_BYTES, &tmX, full, kb * (L::KSTAGE / 8),
+                                                 tr * BM, pol);
+                            } else {
+                                ptx::mbar_arrive_expect_tx(full, L::A_BYTES);
+                                ptx::tma_load_2d(sbase + L::A_OFF + slot * L::A_BYTES, &tmY, full,
+                                                 kb * L::KSTAGE + u * BK, tq * BN, pol);
+                            }
+                            ++issued;
+                        }
+                        if (++slot == nslots) {
+                            slot = 0;
+                            phase ^= 1u;
+                        }
                     }
                 }
             }
             if (!ok) {
-                for (int s = 0; s < STAGES; ++s) {
+                for (int s = 0; s < nslots; ++s) {
                     if (issued <= s) continue;
-                    const long long last = issued - 1 - ((issued - 1 - s) % STAGES);
-                    wait_bar_drain(FULL(s), (uint32_t)((last / STAGES) & 1));
+                    const long long last = issued - 1 - ((issued - 1 - s) % nslots);
+                    wait_bar_drain(packed ? FULL(s) : AFULL(s), (uint32_t)((last / nslots) & 1));
                 }
             }
         }
@@ -393,14 +427,8 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                     tile_coords(sched, s0.tile, tr, tq);
                     const int kend = min(s0.kb1, s0.kb0 + STAGES);
                     for (int kb = s0.kb0; kb < kend; ++kb) {
-                        if (W4) {
-                            ptx::tma_prefetch_l2_2d(&tmX, kb * (L::KSTAGE / 8), tr * BM);
-                            ptx::tma_prefetch_l2_2d(&tmY, kb * L::KSTAGE, tq * BN);
-                            ptx::tma_prefetch_l2_2d(&tmY, kb * L::KSTAGE + BK, tq * BN);
-                        } else {
-                            ptx::tma_prefetch_l2_2d(&tmX, kb * BK, tr * BM);
-                            ptx::tma_prefetch_l2_2d(&tmY, kb * BK, tq * BN);
-                        }
+                        ptx::tma_prefetch_l2_2d(&tmX, kb * BK, tr * BM);
+                        ptx::tma_prefetch_l2_2d(&tmY, kb * BK, tq * BN);
                     }
                 }
                 ptx::pdl_wait();
@@ -419,15 +447,8 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                     if (!sched.stall) {
                         ptx::mbar_arrive_expect_tx(FULL(stage), L::STAGE_BYTES);
                         const uint32_t xs = sbase + stage * L::STAGE_BYTES;
-                        if (W4) {   // packed words (8 k each), then the two activation halves
-                            ptx::tma_load_2d(xs, &tmX, FULL(stage), kb * (L::KSTAGE / 8), tr * BM, pol_x);
-                            ptx::tma_load_2d(xs + L::X_BYTES, &tmY, FULL(stage), kb * L::KSTAGE, tq * BN, pol_y);
-                            ptx::tma_load_2d(xs + L::X_BYTES + BN * BK * 2, &tmY, FULL(stage),
-                                             kb * L::KSTAGE + BK, tq * BN, pol_y);
-                        } else {
-                            ptx::tma_load_2d(xs, &tmX, FULL(stage), kb * BK, tr * BM, pol_x);
-                            ptx::tma_load_2d(xs + L::X_BYTES, &tmY, FULL(stage), kb * BK, tq * BN, pol_y);
-                        }
+                        ptx::tma_load_2d(xs, &tmX, FULL(stage), kb * BK, tr * BM, pol_x);
+                        ptx::tma_load_2d(xs + L::X_BYTES, &tmY, FULL(stage), kb * BK, tq * BN, pol_y);
                         ++issued;
                     }
                     if (++stage == STAGES) {
@@ -447,87 +468,95 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            int stage = 0, acc = 0, xb = 0;
-            uint32_t phase = 0, acc_phase = 0, xphase = 0;
-            SegIter it(sched, blockIdx.x);
-            Segment seg;
-            bool ok = true;
-            while (ok && it.next(sched, seg)) {
-                if (!wait_bar(TEMPTY(acc), acc_phase ^ 1u, abort_flag, d_error)) break;
-                ptx::tc_fence_after();
-                const uint32_t d = tmem + (uint32_t)(acc * BN);
-                for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
-                    if (!wait_bar(FULL(stage), phase, abort_flag, d_error)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t xs = sbase + stage * L::STAGE_BYTES;
-                    if (W4) {
-                        // the dequantising warps have written this stage's weights to XBUF[xb]
-                        if (!wait_bar(XFULL(xb), xphase, abort_flag, d_error)) {
+        // The whole warp runs the loop; one elected lane issues each MMA and
+        // commit (see mma_bf16_warp).
+        int stage = 0, acc = 0, xb = 0;
+        uint32_t phase = 0, acc_phase = 0, xphase = 0;
+        SegIter it(sched, blockIdx.x);
+        Segment seg;
+        bool ok = true;
+        while (ok && it.next(sched, seg)) {
+            if (!wait_bar_warp(TEMPTY(acc), acc_phase ^ 1u, abort_flag, d_error)) break;
+            ptx::tc_fence_after();
+            const uint32_t d = tmem + (uint32_t)(acc * BN);
+            if (W4) {
+                // W4A16: per 64-k sub-tile, a dequantised weight tile (TMEM) and an activation tile
+                for (int kb = seg.kb0; ok && kb < seg.kb1; ++kb) {
+                    for (int u = 0; u < L::KSTAGE / BK; ++u) {
+                        if (!wait_bar_warp(XFULL(xb), xphase, abort_flag, d_error) ||
+                            !wait_bar_warp(AFULL(stage), phase, abort_flag, d_error)) {
                             ok = false;
                             break;
                         }
                         ptx::tc_fence_after();
+                        const uint32_t xa = tmem + kXCol + (uint32_t)(xb * 32);
+                        const uint64_t bd = ptx::sdesc_kmajor_sw128(sbase + L::A_OFF + stage * L::A_BYTES);
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const uint64_t ad = ptx::sdesc_kmajor_sw128(sbase + L::XBUF_OFF + (xb * 2 + h) * BM * BK * 2);
-                            const uint64_t bd = ptx::sdesc_kmajor_sw128(xs + L::X_BYTES + h * BN * BK * 2);
-#pragma unroll
-                            for (int k = 0; k < BK / 16; ++k)
-                                ptx::mma_bf16(d, ad + 2u * k, bd + 2u * k, IDESC,
-                                              (kb > seg.kb0 || h > 0 || k > 0) ? 1u : 0u);
-                        }
-                        ptx::mma_commit(XEMPTY(xb));
+                        for (int k = 0; k < BK / 16; ++k)   // 16 k = 8 TMEM columns of A, 32 bytes of B
+                            ptx::mma_bf16_ts_warp(d, xa + 8u * k, bd + 2u * k, IDESC,
+                                                  (kb > seg.kb0 || u > 0 || k > 0) ? 1u : 0u);
+                        ptx::mma_commit_warp(XEMPTY(xb));
+                        ptx::mma_commit_warp(AEMPTY(stage));
                         if (++xb == kNX) {
                             xb = 0;
                             xphase ^= 1u;
                         }
-                    } else {
-                        ptx::tc_fence_after();
-                        const uint64_t ad = ptx::sdesc_kmajor_sw128(xs);
-                        const uint64_t bd = ptx::sdesc_kmajor_sw128(xs + L::X_BYTES);
-#pragma unroll
-                        for (int k = 0; k < BK / 16; ++k)   // +32 bytes along K per step
-                            ptx::mma_bf16(d, ad + 2u * k, bd + 2u * k, IDESC, (kb > seg.kb0 || k > 0) ? 1u : 0u);
+                        if (++stage == L::AST) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
                     }
-                    ptx::mma_commit(EMPTY(stage));
+                }
+            } else {
+                for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
+                    if (!wait_bar_warp(FULL(stage), phase, abort_flag, d_error)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t xs = sbase + stage * L::STAGE_BYTES;
+                    ptx::tc_fence_after();
+                    const uint64_t ad = ptx::sdesc_kmajor_sw128(xs);
+                    const uint64_t bd = ptx::sdesc_kmajor_sw128(xs + L::X_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)   // +32 bytes along K per step
+                        ptx::mma_bf16_warp(d, ad + 2u * k, bd + 2u * k, IDESC, (kb > seg.kb0 || k > 0) ? 1u : 0u);
+                    ptx::mma_commit_warp(EMPTY(stage));
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
-                if (!ok) break;
-                ptx::mma_commit(TFULL(acc));
-                if (++acc == 2) {
-                    acc = 0;
-                    acc_phase ^= 1u;
-                }
             }
-            ptx::mma_commit(DONE);          // every issued MMA retires before TMEM is freed
-            wait_bar_drain(DONE, 0);
+            if (!ok) break;
+            ptx::mma_commit_warp(TFULL(acc));
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
         }
+        ptx::mma_commit_warp(DONE);          // every issued MMA retires before TMEM is freed
+        wait_bar_drain(DONE, 0);
     } else if (W4 && warp >= 6) {
         // ------------------------------------------------------------ W4A16 dequantisation
-        // Warp wd owns weight rows 8wd .. 8wd+7 of the tile; per stage (128 k),
-        // lane l takes row 8wd + l % 8 and the 32 k numbered l / 8: one 16-byte
-        // load of 4 packed words, w = (q - z) * s in bf16, four 16-byte stores
-        // into XBUF (half h = k / 64, chunk (k % 64) / 8) in the MMA's swizzled
-        // K-major layout.  Each quarter-warp covers 8 consecutive rows of one
-        // 32-k slice, so loads (64-byte swizzle) and stores (128-byte swizzle)
-        // are free of bank conflicts.
+        // Warps 6-21: group u = (warp - 6) / 4 owns the 64-k sub-tile u of every
+        // 256-k stage, and lane l of warp w the weight row 32 (w % 4) + l, which is
+        // the TMEM lane that warp may write.  A thread reads its row's 8 packed
+        // words (two 16-byte pieces of the 128-B-swizzled stage; every
+        // quarter-warp touches eight consecutive rows, so the loads are free of
+        // bank conflicts), releases the stage, computes w = (q - z) * s in bf16
+        // and stores the row's 64 weights into dequantised tile u (or u + 4) of
+        // tensor memory as 32 columns of k pairs -- the A layout the MMA reads.
         //   128 + q is exact in bf16 as (0x4300 | q); subtracting 128 + z is
         //   exact (|q - z| <= 15); the product with s is rounded once (RNE).
-        const int d = threadIdx.x - 192;
-        const int wd = d >> 5;
-        const int r = 8 * wd + (lane & 7);
-        const int q4 = lane >> 3;                  // which 32 k of the stage
-        const int h = q4 >> 1, cbase = (q4 & 1) * 4;
-        const uint32_t pk_off = (uint32_t)(r * 64 + ((q4 ^ ((r >> 1) & 3)) << 4));
-        const uint32_t xrow_off = (uint32_t)(h * BM * BK * 2 + (r >> 3) * 1024 + (r & 7) * 128);
+        const int u = (warp - 6) >> 2;
+        const int q4 = warp & 3;
+        const int r = 32 * q4 + lane;
+        const uint32_t pk_off0 = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + (((2 * u) ^ (r & 7)) << 4));
+        const uint32_t pk_off1 = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + (((2 * u + 1) ^ (r & 7)) << 4));
+        const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16) + kXCol;
         ptx::pdl_wait();                           // scales and zeros come from global memory
-        int stage = 0, xb = 0;
+        // tiles u and u + 4 alternate between consecutive stages
+        int stage = 0, xsel = 0;
         uint32_t phase = 0, xphase = 0;
         SegIter it(sched, blockIdx.x);
         Segment seg;
@@ -539,64 +568,86 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
             const bool nv = n < R;
             const uint16_t *srow = w4.scales + (int64_t)n * w4.G;
             const uint8_t *zrow = w4.zeros + (int64_t)n * w4.G;
-            // (scale, zero) of this thread's group, one stage ahead, through L1
-            auto load_sz = [&](int kb, uint32_t &sv, uint32_t &zv) {
-                const int kq = kb * L::KSTAGE + q4 * 32;
-                const bool in = nv && kq < w4.K;
-                const int gi = kq / w4.group;
-                sv = in ? __ldg(srow + gi) : 0u;
-                zv = in ? __ldg(zrow + gi) : 0u;
+            // (scale, zero) of the groups covering this thread's two 32-k halves
+            // (different groups when g = 32), one stage ahead, through L1.  A half
+            // at or beyond K gets scale 0 (its activations are zero-filled too).
+            auto load_sz = [&](int kb, uint32_t &s0, uint32_t &z0, uint32_t &s1, uint32_t &z1) {
+                const int k0 = kb * L::KSTAGE + u * BK;
+                const bool in0 = nv && k0 < w4.K, in1 = nv && k0 + 32 < w4.K;
+                const int g0 = k0 / w4.group, g1 = (k0 + 32) / w4.group;
+                s0 = in0 ? __ldg(srow + g0) : 0u;
+                z0 = in0 ? __ldg(zrow + g0) : 0u;
+                if (g1 != g0 || !in1) {
+                    s1 = in1 ? __ldg(srow + g1) : 0u;
+                    z1 = in1 ? __ldg(zrow + g1) : 0u;
+                } else {
+                    s1 = s0;
+                    z1 = z0;
+                }
             };
-            uint32_t sv, zv;
-            load_sz(seg.kb0, sv, zv);
+            uint32_t s0, z0, s1, z1;
+            load_sz(seg.kb0, s0, z0, s1, z1);
             for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
-                uint32_t sn = 0, zn = 0;
-                if (kb + 1 < seg.kb1) load_sz(kb + 1, sn, zn);
-                if (!wait_bar(FULL(stage), phase, abort_flag, d_error) ||
-                    !wait_bar(XEMPTY(xb), xphase ^ 1u, abort_flag, d_error)) {
+                uint32_t ns0 = 0, nz0 = 0, ns1 = 0, nz1 = 0;
+                if (kb + 1 < seg.kb1) load_sz(kb + 1, ns0, nz0, ns1, nz1);
+                if (!wait_bar_warp(FULL(stage), phase, abort_flag, d_error)) {
                     ok = false;
                     break;
                 }
-                const uint4 wv = ptx::lds128(sbase + stage * L::STAGE_BYTES + pk_off);
-                const uint32_t s2u = sv * 0x00010001u;
-                const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162 *>(&s2u);
-                const uint32_t zbu = (0x4300u + zv) * 0x00010001u;   // bf16x2 (128 + z)
-                const __nv_bfloat162 z2 = *reinterpret_cast<const __nv_bfloat162 *>(&zbu);
-                const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
-                const uint32_t xrow = sbase + L::XBUF_OFF + xb * 2 * BM * BK * 2 + xrow_off;
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const uint32_t x = words[w];
-                    uint32_t p[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {   // p[j] = (k j, k j+4) as bf16x2 128 + q
-                        const uint32_t t = ((x >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
-                        __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(&t);
-                        v = __hmul2(__hsub2(v, z2), s2);
-                        p[j] = *reinterpret_cast<const uint32_t *>(&v);
-                    }
-                    uint4 out;
-                    out.x = __byte_perm(p[0], p[1], 0x5410);   // (k0, k1)
-                    out.y = __byte_perm(p[2], p[3], 0x5410);   // (k2, k3)
-                    out.z = __byte_perm(p[0], p[1], 0x7632);   // (k4, k5)
-                    out.w = __byte_perm(p[2], p[3], 0x7632);   // (k6, k7)
-                    ptx::sts128(xrow + (((cbase + w) ^ (r & 7)) << 4), out);
+                const uint32_t sb = sbase + stage * L::STAGE_BYTES;
+                const uint4 wa = ptx::lds128(sb + pk_off0);
+                const uint4 wb = ptx::lds128(sb + pk_off1);
+                ptx::mbar_arrive(EMPTY(stage));          // the packed stage may be refilled now
+                const int xb = u + 4 * xsel;
+                if (!wait_bar_warp(XEMPTY(xb), xphase ^ 1u, abort_flag, d_error)) {
+                    ok = false;
+                    break;
                 }
-                ptx::fence_proxy_async_smem();   // the MMA reads XBUF through the async proxy
+                ptx::tc_fence_after();
+                const uint32_t words[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {          // 32 k = 16 columns per store
+                    const uint32_t s2u = (h == 0 ? s0 : s1) * 0x00010001u;
+                    const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162 *>(&s2u);
+                    const uint32_t zbu = (0x4300u + (h == 0 ? z0 : z1)) * 0x00010001u;   // bf16x2 (128 + z)
+                    const __nv_bfloat162 z2 = *reinterpret_cast<const __nv_bfloat162 *>(&zbu);
+                    uint32_t v[16];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t x = words[4 * h + j];
+                        uint32_t p[4];
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) {   // p[jj] = (k jj, k jj+4) as bf16x2 128 + q
+                            const uint32_t t = ((x >> (4 * jj)) & 0x000F000Fu) | 0x43004300u;
+                            __nv_bfloat162 w2 = *reinterpret_cast<const __nv_bfloat162 *>(&t);
+                            w2 = __hmul2(__hsub2(w2, z2), s2);
+                            p[jj] = *reinterpret_cast<const uint32_t *>(&w2);
+                        }
+                        v[4 * j + 0] = __byte_perm(p[0], p[1], 0x5410);   // (k0, k1)
+                        v[4 * j + 1] = __byte_perm(p[2], p[3], 0x5410);   // (k2, k3)
+                        v[4 * j + 2] = __byte_perm(p[0], p[1], 0x7632);   // (k4, k5)
+                        v[4 * j + 3] = __byte_perm(p[2], p[3], 0x7632);   // (k6, k7)
+                    }
+                    ptx::tmem_st16(trow + (uint32_t)(xb * 32 + 16 * h), v);
+                }
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();              // the MMA reads these columns after XFULL
                 ptx::mbar_arrive(XFULL(xb));
-                sv = sn;
-                zv = zn;
+                s0 = ns0;
+                z0 = nz0;
+                s1 = ns1;
+                z1 = nz1;
+                if (++xsel == 2) {
+                    xsel = 0;
+                    xphase ^= 1u;
+                }
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1u;
                 }
-                if (++xb == kNX) {
-                    xb = 0;
-                    xphase ^= 1u;
-                }
             }
         }
-    } else {
+    } else if (warp >= 2 && warp < 6) {
         // ------------------------------------------------------------ epilogue
         const int q4 = warp & 3;            // TMEM lane quarter this warp may read
         const int row = q4 * 32 + lane;     // accumulator row
@@ -607,7 +658,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
         SegIter it(sched, blockIdx.x);
         Segment seg;
         while (it.next(sched, seg)) {
-            if (!wait_bar(TFULL(acc), acc_phase, abort_flag, d_error)) break;
+            if (!wait_bar_warp(TFULL(acc), acc_phase, abort_flag, d_error)) break;
             ptx::tc_fence_after();
             int tr, tq;
             tile_coords(sched, seg.tile, tr, tq);
@@ -814,19 +865,19 @@ bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int64_t 
     return r == CUDA_SUCCESS;
 }
 
-// Packed 4-bit weights as uint32 words [rows, K/8]; box 16 words (128 k) x 128
-// rows with the 64-byte swizzle (16-byte piece c of row r lands at piece
-// c ^ ((r / 2) % 4)), so the dequantising warps read it without bank conflicts.
+// Packed 4-bit weights as uint32 words [rows, K/8]; box 32 words (256 k) x 128
+// rows with the 128-byte swizzle (16-byte piece c of row r lands at piece
+// c ^ (r % 8)), so the dequantising warps read it without bank conflicts.
 bool make_map_packed(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K)
 {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)(K / 8), (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)(K / 8) * 4};
-    cuuint32_t box[2] = {16, (cuuint32_t)BM};
+    cuuint32_t box[2] = {32, (cuuint32_t)BM};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -880,8 +931,8 @@ int umma_stages(int bn, bool skinny, bool deep)
     return bn <= 16 ? 6 : bn <= 32 ? 5 : bn <= 64 ? 4 : 3;
 }
 
-// W4A16 skinny kernels: one CTA per SM; stages of 128 k.
-int umma_w4_stages(int bn) { return bn <= 16 ? 6 : bn <= 32 ? 5 : bn <= 64 ? 3 : 2; }
+// W4A16 skinny kernels: one CTA per SM; packed stages of 256 k (16 KB).
+int umma_w4_stages(int bn) { return bn <= 64 ? 8 : 6; }
 
 namespace {
 template <int BN, int STAGES, bool SWAP, int MINB, bool W4 = false>
@@ -925,10 +976,10 @@ int umma_cluster_capacity(int bn, bool deep, int cluster, bool w4)
         int n = -1;
         if (w4) {
             switch (bi) {
-            case 0: n = cluster_capacity_t<16, 6, true, 1, true>(cluster); break;
-            case 1: n = cluster_capacity_t<32, 5, true, 1, true>(cluster); break;
-            case 2: n = cluster_capacity_t<64, 3, true, 1, true>(cluster); break;
-            case 3: n = cluster_capacity_t<128, 2, true, 1, true>(cluster); break;
+            case 0: n = cluster_capacity_t<16, 8, true, 1, true>(cluster); break;
+            case 1: n = cluster_capacity_t<32, 8, true, 1, true>(cluster); break;
+            case 2: n = cluster_capacity_t<64, 8, true, 1, true>(cluster); break;
+            case 3: n = cluster_capacity_t<128, 6, true, 1, true>(cluster); break;
             default: break;
             }
         } else if (deep) {
@@ -967,7 +1018,7 @@ cudaError_t launch_umma_w4a16(const GemmArgs &a, const Plan &p, const LaunchCtx 
     s.tiles_r = (int)((a.N + BM - 1) / BM);
     s.tiles_q = (int)((a.M + p.bn - 1) / p.bn);
     s.tiles = s.tiles_r * s.tiles_q;
-    s.nk = (int)((a.K + 2 * BK - 1) / (2 * BK));
+    s.nk = (int)((a.K + 4 * BK - 1) / (4 * BK));   // 256-k stages
     s.grid = p.grid;
     s.group_r = p.group_r > 0 ? p.group_r : s.tiles_r;
     s.units = (long long)s.tiles * s.nk;
@@ -977,10 +1028,10 @@ cudaError_t launch_umma_w4a16(const GemmArgs &a, const Plan &p, const LaunchCtx 
     uint16_t *C = (uint16_t *)a.C;
     const int r = (int)a.N, q = (int)a.M;
     switch (p.bn) {
-    case 16: return launch_t<16, 6, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
-    case 32: return launch_t<32, 5, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
-    case 64: return launch_t<64, 3, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
-    case 128: return launch_t<128, 2, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
+    case 16: return launch_t<16, 8, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
+    case 32: return launch_t<32, 8, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
+    case 64: return launch_t<64, 8, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
+    case 128: return launch_t<128, 6, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -53,7 +53,9 @@ def run(g, A, Bq, S, Z, group, variant="auto"):
 
 SMALL = [(1, 8, 128, 32), (1, 64, 256, 64), (2, 136, 384, 128), (3, 520, 1024, 32),
          (4, 1000, 2048, 128), (8, 264, 640, 128), (16, 136, 512, 64), (17, 4104, 256, 128),
-         (64, 512, 1024, 128), (128, 392, 1280, 128), (129, 136, 512, 32)]
+         (64, 512, 1024, 128), (128, 392, 1280, 128), (129, 136, 512, 32),
+         # K % 64 == 32: the last 64-k sub-tile is half past K (its second group is absent)
+         (16, 264, 608, 32), (40, 136, 4128, 32)]
 
 
 @pytest.mark.parametrize("M,N,K,group", SMALL)
