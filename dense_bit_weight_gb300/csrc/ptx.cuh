@@ -61,6 +61,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 // As mbar_try_wait, but the thread may be suspended (woken when the phase
 // completes) for up to `ns` nanoseconds instead of returning at once, so
 // waiting warps do not take issue slots from working ones.
+// Non-blocking test of a phase (never suspends).  Issued early, its result can
+// be consumed after independent work, hiding the barrier's access latency.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t ns)
 {
     uint32_t ok;

@@ -70,8 +70,8 @@ constexpr int BM = 128;          // MMA M: rows of X per tile
 constexpr int BK = 64;           // k per MMA tile (one 128-byte swizzle row of bf16)
 constexpr int kEpiThreads = 128;
 constexpr int kDqThreads = 512;  // W4A16: dequantising threads (warps 6-21)
-constexpr int kNX = 8;           // W4A16: dequantised 128 x 64 bf16 tiles in TMEM (two per 64-k sub-tile position)
-constexpr uint32_t kXCol = 256;  // W4A16: TMEM column of the first dequantised tile (32 columns each)
+constexpr int kNX = 2;           // W4A16: dequantised 128 x 256 bf16 stages in TMEM (128 columns each)
+constexpr uint32_t kXCol = 256;  // W4A16: TMEM column of the first dequantised stage
 constexpr int kActWarp = 22;     // W4A16: warp that loads the activation tiles
 __host__ __device__ constexpr int threads_for(bool w4) { return w4 ? 192 + kDqThreads + 32 : 192; }
 
@@ -80,6 +80,7 @@ struct W4Args {
     const uint16_t *scales;      // bf16 [N, K/group]
     const uint8_t *zeros;        // uint8 [N, K/group]
     int K, G, group;
+    int lg_group;                // log2(group); group is 32, 64 or 128
 };
 constexpr uint64_t kTimeoutNs = 1000000000ull;
 
@@ -184,11 +185,29 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 // The same wait by every lane of a converged warp, with a warp-uniform result
 // (a lane that timed out makes the whole warp give up), so the warp can go on
 // to .sync.aligned tensor-memory operations and elected MMA issue together.
+// (Polling from lane 0 alone and broadcasting the outcome measured slower.)
 __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
                                               int *d_error)
 {
     const bool ok = wait_bar(bar, parity, abort_flag, d_error);
     return __all_sync(0xffffffffu, ok);
+}
+
+// Consume a probe taken earlier with mbar_test_wait: if any lane saw the phase
+// incomplete, the warp falls back to the bounded blocking wait.
+__device__ __forceinline__ bool settle_warp(bool probe, uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                            int *d_error)
+{
+    if (__all_sync(0xffffffffu, probe)) return true;
+    return wait_bar_warp(bar, parity, abort_flag, d_error);
+}
+
+// One arrival for the whole (converged) warp, after every lane's prior
+// accesses: the barrier counts warps, not threads.
+__device__ __forceinline__ void arrive_warp(uint32_t bar)
+{
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(bar);
 }
 
 // Wait without looking at the abort flag (used when draining before exit).
@@ -238,19 +257,20 @@ constexpr uint32_t tmem_cols_for(int n)
 // Shared memory.
 // bf16: a ring of STAGES stages, each an X tile (128 x 64 bf16, 16 KB, TMA
 // 128-B swizzle) and a Y tile (BN x 64 bf16).
-// W4A16: two rings.  Packed weights: STAGES stages of 128 rows x 256 k of
-// 4-bit codes (16 KB, TMA 128-B swizzle), released by the dequantising warps as
-// soon as they have read them.  Activations: AST tiles of BN x 64 bf16, released
-// by the MMA.  The dequantised weights live in tensor memory (kNX tiles of
-// 128 x 64 bf16 from column kXCol), where the MMA reads its A operand.
+// W4A16: two rings of 256-k stages.  Packed weights: STAGES stages of 128 rows
+// of 4-bit codes (16 KB, TMA 128-B swizzle), released by the dequantising warps
+// as soon as they have read them.  Activations: AST stages of four BN x 64 bf16
+// tiles, released by the MMA.  The dequantised weights live in tensor memory
+// (kNX stages of 128 x 256 bf16 from column kXCol), where the MMA reads its A
+// operand.
 template <int BN, int STAGES, bool W4 = false>
 struct Layout {
     static constexpr int KSTAGE = W4 ? 4 * BK : BK;                 // k per ring stage
     static constexpr int X_BYTES = W4 ? BM * KSTAGE / 2 : BM * BK * 2;
     static constexpr int Y_BYTES = W4 ? 0 : BN * BK * 2;
     static constexpr int STAGE_BYTES = X_BYTES + Y_BYTES;
-    static constexpr int AST = !W4 ? 0 : BN <= 16 ? 12 : BN <= 32 ? 8 : BN <= 64 ? 6 : 3;
-    static constexpr int A_BYTES = BN * BK * 2;
+    static constexpr int AST = !W4 ? 0 : BN <= 16 ? 4 : BN <= 32 ? 3 : 2;
+    static constexpr int A_BYTES = BN * KSTAGE * 2;                 // W4A16: one activation stage
     static constexpr int A_OFF = STAGES * STAGE_BYTES;
     static constexpr int SZ_OFF = A_OFF + AST * A_BYTES;   // end of the rings
     static constexpr int BAR_OFF = SZ_OFF;
@@ -270,7 +290,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
     // dequantised tiles above.  Its shared memory admits one CTA per SM, so
     // the allocation never waits on a CTA of the same cluster.
     constexpr uint32_t TMEM_COLS = W4 ? 512u : tmem_cols_for(2 * BN);
-    static_assert(!W4 || (2 * BN <= (int)kXCol && kXCol + kNX * 32 <= 512), "W4A16 TMEM map");
+    static_assert(!W4 || (2 * BN <= (int)kXCol && kXCol + kNX * 128 <= 512), "W4A16 TMEM map");
     static_assert(!W4 || L::SMEM > 114 * 1024, "W4A16 needs one CTA per SM (it allocates all of TMEM)");
     constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN);
 
@@ -297,17 +317,17 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(FULL(s), 1);
-            ptx::mbar_init(EMPTY(s), W4 ? kDqThreads : 1);   // W4A16: every dequantising thread releases
+            ptx::mbar_init(EMPTY(s), W4 ? kDqThreads / 32 : 1);   // W4A16: every dequantising warp releases
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(TFULL(a), 1);
-            ptx::mbar_init(TEMPTY(a), kEpiThreads);
+            ptx::mbar_init(TEMPTY(a), kEpiThreads / 32);   // one arrival per epilogue warp
         }
         ptx::mbar_init(DONE, 1);
         ptx::mbar_init(REDUCE, 1);
         if (W4) {
             for (int b = 0; b < kNX; ++b) {
-                ptx::mbar_init(XFULL(b), kDqThreads / 4);   // the four warps writing that tile
+                ptx::mbar_init(XFULL(b), kDqThreads / 32);   // every dequantising warp
                 ptx::mbar_init(XEMPTY(b), 1);
             }
             for (int a = 0; a < L::AST; ++a) {
@@ -374,30 +394,29 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
             while (ok && it.next(sched, seg)) {
                 int tr, tq;
                 tile_coords(sched, seg.tile, tr, tq);
-                for (int kb = seg.kb0; ok && kb < seg.kb1; ++kb) {
-                    for (int u = 0; u < (packed ? 1 : L::KSTAGE / BK); ++u) {
-                        const uint32_t full = packed ? FULL(slot) : AFULL(slot);
-                        const uint32_t empty = packed ? EMPTY(slot) : AEMPTY(slot);
-                        if (!wait_bar(empty, phase ^ 1u, abort_flag, d_error)) {
-                            ok = false;
-                            break;
-                        }
-                        if (!sched.stall) {
-                            if (packed) {
-                                ptx::mbar_arrive_expect_tx(full, L::X_BYTES);
-                                ptx::tma_load_2d(sbase + slot * L::STAGE_BYTES, &tmX, full, kb * (L::KSTAGE / 8),
-                                                 tr * BM, pol);
-                            } else {
-                                ptx::mbar_arrive_expect_tx(full, L::A_BYTES);
-                                ptx::tma_load_2d(sbase + L::A_OFF + slot * L::A_BYTES, &tmY, full,
+                for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
+                    const uint32_t full = packed ? FULL(slot) : AFULL(slot);
+                    const uint32_t empty = packed ? EMPTY(slot) : AEMPTY(slot);
+                    if (!wait_bar(empty, phase ^ 1u, abort_flag, d_error)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!sched.stall) {
+                        if (packed) {
+                            ptx::mbar_arrive_expect_tx(full, L::X_BYTES);
+                            ptx::tma_load_2d(sbase + slot * L::STAGE_BYTES, &tmX, full, kb * (L::KSTAGE / 8),
+                                             tr * BM, pol);
+                        } else {   // four 64-k tiles, BN rows of 128 B each
+                            ptx::mbar_arrive_expect_tx(full, L::A_BYTES);
+                            for (int u = 0; u < L::KSTAGE / BK; ++u)
+                                ptx::tma_load_2d(sbase + L::A_OFF + slot * L::A_BYTES + u * BN * BK * 2, &tmY, full,
                                                  kb * L::KSTAGE + u * BK, tq * BN, pol);
-                            }
-                            ++issued;
                         }
-                        if (++slot == nslots) {
-                            slot = 0;
-                            phase ^= 1u;
-                        }
+                        ++issued;
+                    }
+                    if (++slot == nslots) {
+                        slot = 0;
+                        phase ^= 1u;
                     }
                 }
             }
@@ -480,31 +499,44 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
             ptx::tc_fence_after();
             const uint32_t d = tmem + (uint32_t)(acc * BN);
             if (W4) {
-                // W4A16: per 64-k sub-tile, a dequantised weight tile (TMEM) and an activation tile
-                for (int kb = seg.kb0; ok && kb < seg.kb1; ++kb) {
+                // W4A16: per 256-k stage, one wait: the dequantising threads arrive on
+                // XFULL only after their weights are in TMEM and the stage's
+                // activations have landed (they wait for AFULL themselves), so the
+                // 16 MMAs of a stage run back to back.  Each synchronisation point
+                // of the issuing warp costs about as much as four N = 16 MMAs.
+                // The next stage's XFULL is probed (non-blocking) before the last
+                // sub-tile's MMAs and settled at the top of the next iteration, so
+                // the barrier's latency overlaps MMA execution.
+                bool probe = false;
+                for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
+                    if (!settle_warp(probe, XFULL(xb), xphase, abort_flag, d_error)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t xa = tmem + kXCol + (uint32_t)(xb * 128);
+                    const uint32_t ab = sbase + L::A_OFF + stage * L::A_BYTES;
+                    const int nxb = xb + 1 == kNX ? 0 : xb + 1;
+                    const uint32_t nxphase = nxb == 0 ? xphase ^ 1u : xphase;
+#pragma unroll
                     for (int u = 0; u < L::KSTAGE / BK; ++u) {
-                        if (!wait_bar_warp(XFULL(xb), xphase, abort_flag, d_error) ||
-                            !wait_bar_warp(AFULL(stage), phase, abort_flag, d_error)) {
-                            ok = false;
-                            break;
-                        }
-                        ptx::tc_fence_after();
-                        const uint32_t xa = tmem + kXCol + (uint32_t)(xb * 32);
-                        const uint64_t bd = ptx::sdesc_kmajor_sw128(sbase + L::A_OFF + stage * L::A_BYTES);
+                        if (u == L::KSTAGE / BK - 1)
+                            probe = kb + 1 < seg.kb1 && ptx::mbar_test_wait(XFULL(nxb), nxphase);
+                        const uint64_t bd = ptx::sdesc_kmajor_sw128(ab + u * BN * BK * 2);
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k)   // 16 k = 8 TMEM columns of A, 32 bytes of B
-                            ptx::mma_bf16_ts_warp(d, xa + 8u * k, bd + 2u * k, IDESC,
+                            ptx::mma_bf16_ts_warp(d, xa + (uint32_t)(32 * u + 8 * k), bd + 2u * k, IDESC,
                                                   (kb > seg.kb0 || u > 0 || k > 0) ? 1u : 0u);
-                        ptx::mma_commit_warp(XEMPTY(xb));
-                        ptx::mma_commit_warp(AEMPTY(stage));
-                        if (++xb == kNX) {
-                            xb = 0;
-                            xphase ^= 1u;
-                        }
-                        if (++stage == L::AST) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
+                    }
+                    ptx::mma_commit_warp(XEMPTY(xb));
+                    ptx::mma_commit_warp(AEMPTY(stage));
+                    if (++xb == kNX) {
+                        xb = 0;
+                        xphase ^= 1u;
+                    }
+                    if (++stage == L::AST) {
+                        stage = 0;
+                        phase ^= 1u;
                     }
                 }
             } else {
@@ -544,8 +576,10 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
         // words (two 16-byte pieces of the 128-B-swizzled stage; every
         // quarter-warp touches eight consecutive rows, so the loads are free of
         // bank conflicts), releases the stage, computes w = (q - z) * s in bf16
-        // and stores the row's 64 weights into dequantised tile u (or u + 4) of
-        // tensor memory as 32 columns of k pairs -- the A layout the MMA reads.
+        // and stores the row's 64 weights into sub-tile u of a TMEM stage buffer
+        // as 32 columns of k pairs -- the A layout the MMA reads.  Before it
+        // signals the MMA it also waits for the stage's activations, so the MMA
+        // warp waits once per stage.
         //   128 + q is exact in bf16 as (0x4300 | q); subtracting 128 + z is
         //   exact (|q - z| <= 15); the product with s is rounded once (RNE).
         const int u = (warp - 6) >> 2;
@@ -555,9 +589,8 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
         const uint32_t pk_off1 = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + (((2 * u + 1) ^ (r & 7)) << 4));
         const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16) + kXCol;
         ptx::pdl_wait();                           // scales and zeros come from global memory
-        // tiles u and u + 4 alternate between consecutive stages
-        int stage = 0, xsel = 0;
-        uint32_t phase = 0, xphase = 0;
+        int stage = 0, xsel = 0, astage = 0;
+        uint32_t phase = 0, xphase = 0, aphase = 0;
         SegIter it(sched, blockIdx.x);
         Segment seg;
         bool ok = true;
@@ -574,7 +607,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
             auto load_sz = [&](int kb, uint32_t &s0, uint32_t &z0, uint32_t &s1, uint32_t &z1) {
                 const int k0 = kb * L::KSTAGE + u * BK;
                 const bool in0 = nv && k0 < w4.K, in1 = nv && k0 + 32 < w4.K;
-                const int g0 = k0 / w4.group, g1 = (k0 + 32) / w4.group;
+                const int g0 = k0 >> w4.lg_group, g1 = (k0 + 32) >> w4.lg_group;
                 s0 = in0 ? __ldg(srow + g0) : 0u;
                 z0 = in0 ? __ldg(zrow + g0) : 0u;
                 if (g1 != g0 || !in1) {
@@ -587,31 +620,33 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
             };
             uint32_t s0, z0, s1, z1;
             load_sz(seg.kb0, s0, z0, s1, z1);
+            // Barriers are probed (non-blocking) ahead of the arithmetic and settled
+            // where their data is needed, so their latency overlaps the work.
+            bool pfull = false;   // probe of this stage's FULL, taken in the previous iteration
             for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
                 uint32_t ns0 = 0, nz0 = 0, ns1 = 0, nz1 = 0;
                 if (kb + 1 < seg.kb1) load_sz(kb + 1, ns0, nz0, ns1, nz1);
-                if (!wait_bar_warp(FULL(stage), phase, abort_flag, d_error)) {
+                if (!settle_warp(pfull, FULL(stage), phase, abort_flag, d_error)) {
                     ok = false;
                     break;
                 }
                 const uint32_t sb = sbase + stage * L::STAGE_BYTES;
                 const uint4 wa = ptx::lds128(sb + pk_off0);
                 const uint4 wb = ptx::lds128(sb + pk_off1);
-                ptx::mbar_arrive(EMPTY(stage));          // the packed stage may be refilled now
-                const int xb = u + 4 * xsel;
-                if (!wait_bar_warp(XEMPTY(xb), xphase ^ 1u, abort_flag, d_error)) {
-                    ok = false;
-                    break;
-                }
-                ptx::tc_fence_after();
+                arrive_warp(EMPTY(stage));               // the packed stage may be refilled now
+                const int nstage = stage + 1 == STAGES ? 0 : stage + 1;
+                const uint32_t nphase = nstage == 0 ? phase ^ 1u : phase;
+                const bool pxe = ptx::mbar_test_wait(XEMPTY(xsel), xphase ^ 1u);
+                const bool pact = ptx::mbar_test_wait(AFULL(astage), aphase);
+                pfull = kb + 1 < seg.kb1 && ptx::mbar_test_wait(FULL(nstage), nphase);
                 const uint32_t words[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+                uint32_t v[2][16];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {          // 32 k = 16 columns per store
                     const uint32_t s2u = (h == 0 ? s0 : s1) * 0x00010001u;
                     const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162 *>(&s2u);
                     const uint32_t zbu = (0x4300u + (h == 0 ? z0 : z1)) * 0x00010001u;   // bf16x2 (128 + z)
                     const __nv_bfloat162 z2 = *reinterpret_cast<const __nv_bfloat162 *>(&zbu);
-                    uint32_t v[16];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const uint32_t x = words[4 * h + j];
@@ -623,23 +658,37 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                             w2 = __hmul2(__hsub2(w2, z2), s2);
                             p[jj] = *reinterpret_cast<const uint32_t *>(&w2);
                         }
-                        v[4 * j + 0] = __byte_perm(p[0], p[1], 0x5410);   // (k0, k1)
-                        v[4 * j + 1] = __byte_perm(p[2], p[3], 0x5410);   // (k2, k3)
-                        v[4 * j + 2] = __byte_perm(p[0], p[1], 0x7632);   // (k4, k5)
-                        v[4 * j + 3] = __byte_perm(p[2], p[3], 0x7632);   // (k6, k7)
+                        v[h][4 * j + 0] = __byte_perm(p[0], p[1], 0x5410);   // (k0, k1)
+                        v[h][4 * j + 1] = __byte_perm(p[2], p[3], 0x5410);   // (k2, k3)
+                        v[h][4 * j + 2] = __byte_perm(p[0], p[1], 0x7632);   // (k4, k5)
+                        v[h][4 * j + 3] = __byte_perm(p[2], p[3], 0x7632);   // (k6, k7)
                     }
-                    ptx::tmem_st16(trow + (uint32_t)(xb * 32 + 16 * h), v);
                 }
+                if (!settle_warp(pxe, XEMPTY(xsel), xphase ^ 1u, abort_flag, d_error)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                ptx::tmem_st16(trow + (uint32_t)(xsel * 128 + u * 32), v[0]);
+                ptx::tmem_st16(trow + (uint32_t)(xsel * 128 + u * 32 + 16), v[1]);
                 ptx::tmem_wait_st();
+                if (!settle_warp(pact, AFULL(astage), aphase, abort_flag, d_error)) {
+                    ok = false;
+                    break;
+                }
                 ptx::tc_fence_before();              // the MMA reads these columns after XFULL
-                ptx::mbar_arrive(XFULL(xb));
+                arrive_warp(XFULL(xsel));
                 s0 = ns0;
                 z0 = nz0;
                 s1 = ns1;
                 z1 = nz1;
-                if (++xsel == 2) {
+                if (++xsel == kNX) {
                     xsel = 0;
                     xphase ^= 1u;
+                }
+                if (++astage == L::AST) {
+                    astage = 0;
+                    aphase ^= 1u;
                 }
                 if (++stage == STAGES) {
                     stage = 0;
@@ -693,7 +742,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                 }
             }
             ptx::tc_fence_before();
-            ptx::mbar_arrive(TEMPTY(acc));
+            arrive_warp(TEMPTY(acc));
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
@@ -932,7 +981,7 @@ int umma_stages(int bn, bool skinny, bool deep)
 }
 
 // W4A16 skinny kernels: one CTA per SM; packed stages of 256 k (16 KB).
-int umma_w4_stages(int bn) { return bn <= 64 ? 8 : 6; }
+int umma_w4_stages(int bn) { return bn <= 32 ? 8 : bn <= 64 ? 6 : 5; }
 
 namespace {
 template <int BN, int STAGES, bool SWAP, int MINB, bool W4 = false>
@@ -978,8 +1027,8 @@ int umma_cluster_capacity(int bn, bool deep, int cluster, bool w4)
             switch (bi) {
             case 0: n = cluster_capacity_t<16, 8, true, 1, true>(cluster); break;
             case 1: n = cluster_capacity_t<32, 8, true, 1, true>(cluster); break;
-            case 2: n = cluster_capacity_t<64, 8, true, 1, true>(cluster); break;
-            case 3: n = cluster_capacity_t<128, 6, true, 1, true>(cluster); break;
+            case 2: n = cluster_capacity_t<64, 6, true, 1, true>(cluster); break;
+            case 3: n = cluster_capacity_t<128, 5, true, 1, true>(cluster); break;
             default: break;
             }
         } else if (deep) {
@@ -1024,14 +1073,15 @@ cudaError_t launch_umma_w4a16(const GemmArgs &a, const Plan &p, const LaunchCtx 
     s.units = (long long)s.tiles * s.nk;
     s.stall = g_debug_stall;
     s.split = p.split;
-    W4Args w4{(const uint16_t *)a.scales, (const uint8_t *)a.zeros, (int)a.K, (int)(a.K / a.group), (int)a.group};
+    W4Args w4{(const uint16_t *)a.scales, (const uint8_t *)a.zeros, (int)a.K, (int)(a.K / a.group), (int)a.group,
+              a.group == 32 ? 5 : a.group == 64 ? 6 : 7};
     uint16_t *C = (uint16_t *)a.C;
     const int r = (int)a.N, q = (int)a.M;
     switch (p.bn) {
     case 16: return launch_t<16, 8, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
     case 32: return launch_t<32, 8, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
-    case 64: return launch_t<64, 8, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
-    case 128: return launch_t<128, 6, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
+    case 64: return launch_t<64, 6, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
+    case 128: return launch_t<128, 5, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
     default: return cudaErrorInvalidValue;
     }
 }
