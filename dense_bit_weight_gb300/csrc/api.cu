@@ -291,17 +291,20 @@ bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan 
     }
 }
 
-// W4A16: CUDA-core GEMV for M <= 4; the tcgen05 skinny kernel with
-// in-kernel dequantisation for 5 <= M <= 128 (stages of 256 k): cluster
+// W4A16: CUDA-core GEMV for M == 1; the tcgen05 skinny kernel with
+// in-kernel dequantisation for 2 <= M <= 128 (stages of 256 k): cluster
 // split-K (mode 2) when the weight tiles fit one wave, stream-K (mode 1)
 // beyond that.  Larger M runs the GEMV path (one pass per four rows).
+// (Measured on GB300: the GEMV's time grows with M -- 87 us at M = 2 and
+// 159 us at M = 4 for N = 34816, K = 5120 -- while the tcgen05 kernel's stays
+// at 46 us for any M <= 16; at M = 1 the GEMV is as fast or faster.)
 bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int sm_count, Plan *p, bool query)
 {
     (void)group;
     *p = Plan{};
     if (K == 0) return false;
     if (variant == GEMM_VARIANT_AUTO)
-        variant = (M <= 4 || M > 128) ? GEMM_VARIANT_GEMV : GEMM_VARIANT_SKINNY;
+        variant = (M == 1 || M > 128) ? GEMM_VARIANT_GEMV : GEMM_VARIANT_SKINNY;
     if (variant == GEMM_VARIANT_SKINNY) {
         if (M > 128) return false;
         int bn = 16;
