@@ -128,7 +128,7 @@ int run(const GemmArgs &a, const Plan &p, cudaStream_t st, bool w4)
     c.sm_count = s->sm_count;
     c.d_error = s->d_error;
     int64_t nf = 0, nc = 0;
-    workspace_need(p, a.M, a.N, &nf, &nc);
+    workspace_need(p, a.M, a.N, a.K, &nf, &nc);
     if (nf > 0 || nc > 0) {
         StreamWorkspace *w = nullptr;
         rc = stream_workspace(*s, st, nf, nc, &w);
@@ -137,6 +137,7 @@ int run(const GemmArgs &a, const Plan &p, cudaStream_t st, bool w4)
         c.counters = w->counters;
         c.ws_floats = w->floats;
         c.n_counters = w->n_counters;
+        if (p.act_copy) c.act_copy = w->partials + act_copy_offset(p);
     }
     cudaError_t e = cudaSuccess;
     switch (p.variant) {
@@ -313,7 +314,8 @@ bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int
         const int64_t nk = (K + 4 * kUmmaBK - 1) / (4 * kUmmaBK);   // 256-k stages
         const int64_t G = sm_count;
         p->variant = GEMM_VARIANT_SKINNY;
-        p->kernels = 1;
+        p->kernels = 2;                      // activation k-order copy, then the GEMM
+        p->act_copy = 1;
         p->bn = bn;
         p->tile_m = bn;
         p->tile_n = kUmmaBM;
@@ -353,16 +355,22 @@ bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int
     return true;
 }
 
-void workspace_need(const Plan &p, int64_t M, int64_t N, int64_t *floats, int64_t *counters)
+int64_t act_copy_offset(const Plan &p)
 {
-    (void)M;
-    (void)N;
+    const bool split = (p.variant == GEMM_VARIANT_SKINNY || p.variant == GEMM_VARIANT_PREFILL) && p.mode == 1;
+    const int64_t partials = split ? (int64_t)p.grid * 2 * kUmmaBM * p.bn : 0;
+    return (partials + 63) / 64 * 64;   // 256-byte aligned
+}
+
+void workspace_need(const Plan &p, int64_t M, int64_t N, int64_t K, int64_t *floats, int64_t *counters)
+{
     *floats = 0;
     *counters = 0;
     if ((p.variant == GEMM_VARIANT_SKINNY || p.variant == GEMM_VARIANT_PREFILL) && p.mode == 1) {
         *floats = (int64_t)p.grid * 2 * kUmmaBM * p.bn;
         *counters = ((M + p.tile_m - 1) / p.tile_m) * ((N + p.tile_n - 1) / p.tile_n);
     }
+    if (p.act_copy) *floats = act_copy_offset(p) + (M * K + 1) / 2;   // bf16 [M, K]
 }
 
 }  // namespace dbw

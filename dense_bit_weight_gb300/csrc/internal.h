@@ -18,6 +18,7 @@ struct LaunchCtx {
     int *counters;         // per-tile arrival counters, zero between calls
     int64_t ws_floats;     // capacity of `workspace` in floats
     int64_t n_counters;    // capacity of `counters`
+    void *act_copy;        // W4A16 tcgen05: bf16 [M, K] activations in the kernel's k order (workspace)
 };
 
 struct GemmArgs {
@@ -40,6 +41,7 @@ struct Plan {
     int bn;                // tcgen05: MMA N (columns of the Y operand per tile)
     int group_r;           // tcgen05: tile-rows per raster group
     int ctas_per_sm;       // tcgen05 skinny: 1 = deep pipeline, 2 = shallow (two CTAs per SM)
+    int act_copy;          // W4A16 tcgen05: activations are first copied into the kernel's k order
 };
 
 // query = true: plan for the current device (asks it for cluster occupancy);
@@ -48,8 +50,11 @@ bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan 
 bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int sm_count, Plan *p,
                 bool query = true);
 
-// Workspace need (floats, counters) for a plan; 0 when it needs none.
-void workspace_need(const Plan &p, int64_t M, int64_t N, int64_t *floats, int64_t *counters);
+// Workspace need (floats, counters) for a plan; 0 when it needs none.  The
+// permuted activation copy of a W4A16 tcgen05 plan sits after the split-K
+// partials, at float offset act_copy_offset(p).
+void workspace_need(const Plan &p, int64_t M, int64_t N, int64_t K, int64_t *floats, int64_t *counters);
+int64_t act_copy_offset(const Plan &p);
 
 // Kernel launchers: return cudaSuccess or the launch error.
 cudaError_t launch_zero_fill(const GemmArgs &a, const LaunchCtx &c);

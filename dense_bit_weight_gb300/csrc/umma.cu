@@ -577,7 +577,11 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
         // quarter-warp touches eight consecutive rows, so the loads are free of
         // bank conflicts), releases the stage, computes w = (q - z) * s in bf16
         // and stores the row's 64 weights into sub-tile u of a TMEM stage buffer
-        // as 32 columns of k pairs -- the A layout the MMA reads.  Before it
+        // as 32 columns of k pairs -- the A layout the MMA reads.  Within each
+        // 8-k block the pairs are (k, k + 4), k = 0..3, as two nibbles one 16-bit
+        // half apart extract with one shift and one mask; the activations are
+        // copied into the same k order beforehand (k_permute_k8), so the MMA's
+        // sum runs over the same products.  Before it
         // signals the MMA it also waits for the stage's activations, so the MMA
         // warp waits once per stage.
         //   128 + q is exact in bf16 as (0x4300 | q); subtracting 128 + z is
@@ -650,18 +654,13 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const uint32_t x = words[4 * h + j];
-                        uint32_t p[4];
 #pragma unroll
-                        for (int jj = 0; jj < 4; ++jj) {   // p[jj] = (k jj, k jj+4) as bf16x2 128 + q
-                            const uint32_t t = ((x >> (4 * jj)) & 0x000F000Fu) | 0x43004300u;
+                        for (int jj = 0; jj < 4; ++jj) {   // column 4j + jj = (k jj, k jj+4) of this 8-k block
+                            const uint32_t t = ((x >> (4 * jj)) & 0x000F000Fu) | 0x43004300u;   // bf16x2 128 + q
                             __nv_bfloat162 w2 = *reinterpret_cast<const __nv_bfloat162 *>(&t);
                             w2 = __hmul2(__hsub2(w2, z2), s2);
-                            p[jj] = *reinterpret_cast<const uint32_t *>(&w2);
+                            v[h][4 * j + jj] = *reinterpret_cast<const uint32_t *>(&w2);
                         }
-                        v[h][4 * j + 0] = __byte_perm(p[0], p[1], 0x5410);   // (k0, k1)
-                        v[h][4 * j + 1] = __byte_perm(p[2], p[3], 0x5410);   // (k2, k3)
-                        v[h][4 * j + 2] = __byte_perm(p[0], p[1], 0x7632);   // (k4, k5)
-                        v[h][4 * j + 3] = __byte_perm(p[2], p[3], 0x7632);   // (k6, k7)
                     }
                 }
                 if (!settle_warp(pxe, XEMPTY(xsel), xphase ^ 1u, abort_flag, d_error)) {
@@ -1056,11 +1055,55 @@ int umma_cluster_capacity(int bn, bool deep, int cluster, bool w4)
 
 int g_debug_stall = 0;
 
+namespace {
+// Activations [M, K] (K % 8 == 0) copied with every 8-k block reordered to
+// k = 0, 4, 1, 5, 2, 6, 3, 7: the order in which the W4A16 kernel lays the
+// dequantised weights along K.  One thread per 16-byte block.
+__global__ void __launch_bounds__(256) k_permute_k8(const uint4 *__restrict__ in, uint4 *__restrict__ out,
+                                                    int64_t blocks)
+{
+    ptx::pdl_wait();                 // the workspace may still be read by the previous kernel
+    ptx::pdl_launch_dependents();
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < blocks;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 a = ld_ro_v4(reinterpret_cast<const uint16_t *>(in + i));   // (a0 a1)(a2 a3)(a4 a5)(a6 a7)
+        uint4 b;
+        b.x = __byte_perm(a.x, a.z, 0x5410);   // (a0, a4)
+        b.y = __byte_perm(a.x, a.z, 0x7632);   // (a1, a5)
+        b.z = __byte_perm(a.y, a.w, 0x5410);   // (a2, a6)
+        b.w = __byte_perm(a.y, a.w, 0x7632);   // (a3, a7)
+        out[i] = b;
+    }
+}
+
+cudaError_t launch_permute_k8(const void *in, void *out, int64_t M, int64_t K, const LaunchCtx &c)
+{
+    const int64_t blocks = M * K / 8;
+    int64_t grid = (blocks + 255) / 256;
+    if (grid > (int64_t)c.sm_count * 4) grid = (int64_t)c.sm_count * 4;
+    if (grid < 1) grid = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = c.stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_permute_k8, reinterpret_cast<const uint4 *>(in), reinterpret_cast<uint4 *>(out),
+                              blocks);
+}
+}  // namespace
+
 cudaError_t launch_umma_w4a16(const GemmArgs &a, const Plan &p, const LaunchCtx &c)
 {
-    // skinny only: X = packed weights [N, K/8], Y = activations [M, K]
+    // skinny only: X = packed weights [N, K/8], Y = activations [M, K] in the kernel's k order
+    if (!c.act_copy) return cudaErrorInvalidValue;
+    cudaError_t e = launch_permute_k8(a.A, c.act_copy, a.M, a.K, c);
+    if (e != cudaSuccess) return e;
     CUtensorMap mx, my;
-    if (!make_map_packed(&mx, a.B, a.N, a.K) || !make_map(&my, a.A, a.M, a.K, a.K, p.bn))
+    if (!make_map_packed(&mx, a.B, a.N, a.K) || !make_map(&my, c.act_copy, a.M, a.K, a.K, p.bn))
         return cudaErrorInvalidValue;
     Sched s{};
     s.mode = p.mode;
