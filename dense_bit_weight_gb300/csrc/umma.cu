@@ -835,27 +835,58 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
             }
         }
         if (warp >= 2 && warp < 6) {
-            const bool ok = wait_bar(REDUCE, 0, abort_flag, d_error);
+            const bool ok = wait_bar_warp(REDUCE, 0, abort_flag, d_error);   // warp-uniform: shuffles below
             int tr, tq;
             tile_coords(sched, (int)blockIdx.x / S, tr, tq);
             const int qb = tq * BN;
+            // thread -> (row rl, first float4 column c4); rows per owner padded to a
+            // power of two so the mapping is shifts and masks
             const int etid = threadIdx.x - 64;
-            const int items = nrows * (BN / 4);
-            for (int idx = etid; ok && idx < items; idx += kEpiThreads) {
-                const int rl = idx % nrows;   // neighbouring threads: neighbouring rows
-                const int c4 = idx / nrows;
+            const int lg = nrows <= 16 ? 4 : nrows <= 32 ? 5 : nrows <= 64 ? 6 : 7;
+            const int rl = etid & ((1 << lg) - 1);   // neighbouring threads: neighbouring rows
+            const int cstep = kEpiThreads >> lg;
+            const uint32_t own = sbase + (uint32_t)((r0 + rl) * PSTRIDE);
+            const uint32_t inb = sbase + (uint32_t)(IN_OFF + rl * PSTRIDE);
+            // S in {2, 4, 8}: the owner's rows are a power of two and start even, every
+            // lane of a warp runs the same iterations, and neighbouring lanes (rows r,
+            // r + 1) pair their values into 4-byte stores of C
+            const bool paired = SWAP && (S == 2 || S == 4 || S == 8);
+            for (int c4 = etid >> lg; ok && rl < nrows && c4 < BN / 4; c4 += cstep) {
+                uint4 u[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q)   // all slices' loads in flight before the sums
+                    if (q < S)
+                        u[q] = ptx::lds128((q == rank ? own : inb + (uint32_t)(q * nmax * PSTRIDE)) +
+                                           (uint32_t)(c4 * 16));
                 float a[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int q = 0; q < S; ++q) {   // rank order
-                    const float4 v = q == rank
-                        ? *reinterpret_cast<const float4 *>(smem + (r0 + rl) * PSTRIDE + c4 * 16)
-                        : *reinterpret_cast<const float4 *>(smem + IN_OFF + (q * nmax + rl) * PSTRIDE + c4 * 16);
-                    a[0] += v.x;
-                    a[1] += v.y;
-                    a[2] += v.z;
-                    a[3] += v.w;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {   // rank order
+                    if (q < S) {
+                        a[0] += __uint_as_float(u[q].x);
+                        a[1] += __uint_as_float(u[q].y);
+                        a[2] += __uint_as_float(u[q].z);
+                        a[3] += __uint_as_float(u[q].w);
+                    }
                 }
                 const int r = tr * BM + r0 + rl;
-                if (r < R) {
+                if (paired) {
+                    float x[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) x[j] = __shfl_xor_sync(0xffffffffu, a[j], 1);
+                    const bool odd = rl & 1;
+                    const int re = r - (odd ? 1 : 0);   // the pair's even row
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj) {    // even lane: tokens 0, 1; odd lane: tokens 2, 3
+                        const int j = odd ? 2 + jj : jj;
+                        const float lo = odd ? x[j] : a[j], hi = odd ? a[j] : x[j];
+                        const int q = qb + c4 * 4 + j;
+                        if (q < Q && re < R) {
+                            uint16_t *dst = C + (int64_t)q * ldc + re;
+                            if (re + 1 < R) *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2_rn(lo, hi);
+                            else *dst = f32_to_bf16_rn(lo);
+                        }
+                    }
+                } else if (r < R) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const int q = qb + c4 * 4 + j;

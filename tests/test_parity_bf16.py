@@ -76,6 +76,27 @@ def test_leading_dimensions_and_views(g):
     assert not host_bits(Cbig[:, N:]).any()     # nothing written past N
 
 
+# Odd N (C padded to a leading dimension that is a multiple of 8) under cluster
+# split-K of 8, 4, 2 and 3 CTAs: the reduction stores neighbouring output columns
+# in pairs where the split allows, and the last column of an odd N pairs with none.
+ODD_N = [(8, 1001, 4096), (64, 255, 2048), (128, 383, 8192), (8, 4863, 1024), (32, 9727, 512),
+         (16, 6399, 768)]
+
+
+@pytest.mark.parametrize("M,N,K", ODD_N)
+@pytest.mark.parametrize("kind", ["normal", "int"])
+def test_odd_n_split_reduction(g, M, N, K, kind):
+    import torch
+    A, B = bf16_inputs(M, N, K, seed=M + N, kind=kind)
+    ldc = (N + 7) // 8 * 8 + 8
+    Cbig = torch.zeros((M, ldc), dtype=torch.bfloat16, device="cuda")
+    C = Cbig[:, :N]
+    g.gemm_bf16(dev_bf16(A), dev_bf16(B), C, variant="skinny")
+    ref = oracle.gemm_bf16(A, B)
+    (assert_exact if kind == "int" else assert_close)(host_bits(C), ref, what=f"odd N {M}x{N}x{K}")
+    assert not host_bits(Cbig[:, N:]).any()     # nothing written past N
+
+
 def test_k_zero_and_empty(g):
     import torch
     C = torch.full((5, 24), 3.0, dtype=torch.bfloat16, device="cuda")
