@@ -39,7 +39,8 @@ def runnable(g, M, N, K, variant):
 
 SMALL = [(1, 8, 8), (1, 136, 24), (3, 8, 16), (4, 4104, 136), (8, 520, 64), (16, 136, 136),
          (17, 1000, 264), (33, 8, 1032), (129, 264, 72), (256, 256, 256), (255, 392, 520),
-         (1000, 136, 136), (129, 4104, 8), (300, 1200, 4096)]
+         (1000, 136, 136), (129, 4104, 8), (300, 1200, 4096),
+         (8, 40960, 512)]   # skinny stream-K: 320 weight tiles, more than two per SM
 
 
 @pytest.mark.parametrize("M,N,K", SMALL)
