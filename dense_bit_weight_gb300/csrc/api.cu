@@ -143,6 +143,10 @@ int run(const GemmArgs &a, const Plan &p, cudaStream_t st, bool w4)
     switch (p.variant) {
     case GEMM_VARIANT_ZERO: e = launch_zero_fill(a, c); break;
     case GEMM_VARIANT_GEMV: e = w4 ? launch_gemv_w4a16(a, p, c) : launch_gemv_bf16(a, p, c); break;
+    case GEMM_VARIANT_REGISTER:
+        if (!w4) return GEMM_ERR_VARIANT;
+        e = launch_w4_register(a, p, c);
+        break;
     case GEMM_VARIANT_SKINNY:
     case GEMM_VARIANT_PREFILL:
         if (w4 && p.variant != GEMM_VARIANT_SKINNY) return GEMM_ERR_VARIANT;
@@ -293,20 +297,37 @@ bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan 
     }
 }
 
-// W4A16: CUDA-core GEMV for M == 1; the tcgen05 skinny kernel with
-// in-kernel dequantisation for 2 <= M <= 128 (stages of 256 k): cluster
-// split-K (mode 2) when the weight tiles fit one wave, stream-K (mode 1)
-// beyond that.  Larger M runs the GEMV path (one pass per four rows).
-// (Measured on GB300: the GEMV's time grows with M -- 87 us at M = 2 and
-// 159 us at M = 4 for N = 34816, K = 5120 -- while the tcgen05 kernel's stays
-// at 46 us for any M <= 16; at M = 1 the GEMV is as fast or faster.)
+// W4A16 routing (AUTO), from GB300 timings over the four decode shapes
+// (N, K) in {(7168, 5120), (5120, 5120), (34816, 5120), (5120, 17408)}:
+//   M <= 4       register-fragment kernel (w4mma.cu): 92 us summed at M = 1
+//                against 103 for the CUDA-core GEMV and 106 for tcgen05
+//   5..128       tcgen05 skinny kernel with in-kernel dequantisation into
+//                TMEM (stages of 256 k): cluster split-K (mode 2) when the
+//                weight tiles fit one wave, stream-K (mode 1) beyond; at
+//                M = 8 and 16 it leads the register kernel (106 vs 109 us,
+//                108 vs 130 us), whose activation loads grow with M
+//   > 128        GEMV path (one pass per four rows)
 bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int sm_count, Plan *p, bool query)
 {
-    (void)group;
     *p = Plan{};
     if (K == 0) return false;
     if (variant == GEMM_VARIANT_AUTO)
-        variant = (M == 1 || M > 128) ? GEMM_VARIANT_GEMV : GEMM_VARIANT_SKINNY;
+        variant = M > 128                                       ? GEMM_VARIANT_GEMV
+                  : (M <= 4 && K / group <= kW4RegisterMaxGroups) ? GEMM_VARIANT_REGISTER
+                                                                  : GEMM_VARIANT_SKINNY;
+    if (variant == GEMM_VARIANT_REGISTER) {
+        if (M > 32 || K / group > kW4RegisterMaxGroups) return false;
+        p->variant = GEMM_VARIANT_REGISTER;
+        p->kernels = 2;                      // activation copy and group sums, then the GEMM
+        p->act_copy = 1;
+        p->ws_extra = 32 * (K / group);   // group sums, tokens padded to the MMAs' 8, 16 or 32
+        p->split = 1;
+        p->m_per_pass = M <= 8 ? 1 : M <= 16 ? 2 : 4;   // MMAs of 8 tokens
+        p->tile_m = 8 * p->m_per_pass;
+        p->tile_n = 16;
+        p->grid = w4_register_grid(N);
+        return true;
+    }
     if (variant == GEMM_VARIANT_SKINNY) {
         if (M > 128) return false;
         int bn = 16;
@@ -371,7 +392,7 @@ void workspace_need(const Plan &p, int64_t M, int64_t N, int64_t K, int64_t *flo
         *floats = (int64_t)p.grid * 2 * kUmmaBM * p.bn;
         *counters = ((M + p.tile_m - 1) / p.tile_m) * ((N + p.tile_n - 1) / p.tile_n);
     }
-    if (p.act_copy) *floats = act_copy_offset(p) + (M * K + 1) / 2;   // bf16 [M, K]
+    if (p.act_copy) *floats = act_copy_offset(p) + (M * K + 127) / 128 * 64 + p.ws_extra;   // bf16 [M, K] (+ sums)
 }
 
 }  // namespace dbw

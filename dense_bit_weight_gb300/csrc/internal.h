@@ -41,7 +41,8 @@ struct Plan {
     int bn;                // tcgen05: MMA N (columns of the Y operand per tile)
     int group_r;           // tcgen05: tile-rows per raster group
     int ctas_per_sm;       // tcgen05 skinny: 1 = deep pipeline, 2 = shallow (two CTAs per SM)
-    int act_copy;          // W4A16 tcgen05: activations are first copied into the kernel's k order
+    int act_copy;          // W4A16: activations are first copied into the kernels' k order
+    int64_t ws_extra;      // W4A16 register variant: fp32 group sums after the copy (floats)
 };
 
 // query = true: plan for the current device (asks it for cluster occupancy);
@@ -61,6 +62,12 @@ cudaError_t launch_zero_fill(const GemmArgs &a, const LaunchCtx &c);
 cudaError_t launch_gemv_bf16(const GemmArgs &a, const Plan &p, const LaunchCtx &c);
 cudaError_t launch_gemv_w4a16(const GemmArgs &a, const Plan &p, const LaunchCtx &c);
 cudaError_t launch_umma_bf16(const GemmArgs &a, const Plan &p, const LaunchCtx &c);
+// W4A16, M <= 32: dequantisation into mma.sync fragments (w4mma.cu); the
+// kernel stages a CTA's scales and zeros in shared memory, up to this many
+// groups per row
+constexpr int kW4RegisterMaxGroups = 544;
+cudaError_t launch_w4_register(const GemmArgs &a, const Plan &p, const LaunchCtx &c);
+int w4_register_grid(int64_t N);
 
 // tcgen05 kernel geometry (umma.cu)
 constexpr int kUmmaBM = 128;

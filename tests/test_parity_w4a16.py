@@ -15,7 +15,7 @@ from gpu_helpers import assert_close, assert_exact, dev_bf16, dev_raw, host_bits
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = ["gemv", "skinny", "prefill"]
+VARIANTS = ["gemv", "skinny", "prefill", "register"]
 
 
 @pytest.fixture(scope="module")
