@@ -207,11 +207,12 @@ static int64_t cluster_capacity(int bn, bool deep, int cs, int sm_count, bool qu
 // once without exceeding one CTA per SM; otherwise the shallow form (two CTAs
 // per SM) runs every tile unsplit, all resident together, so the HBM stream
 // is shared evenly.  Beyond two tiles per SM, deep stream-K (mode 1).
-// Prefill: whole tiles round-robin (mode 0), min(tiles, SMs) CTAs.  Measured
-// on GB300 against stream-K (mode 1) over the fifteen prefill shapes and the
-// M = 512 down projection, whole tiles were as fast or faster on every shape
-// (1.3-1.4x at M = 1024): stream-K's fp32 fixup of a 128 x 256 tile costs more
-// than the wave quantisation it removes.
+// Prefill: whole tiles round-robin (mode 0), min(tiles, SMs) CTAs, whenever the
+// tiles fill at least half the SMs; stream-K (mode 1) below that.  Measured on
+// GB300 over the fifteen prefill shapes, whole tiles were as fast or faster on
+// every shape (1.3-1.4x at M = 1024: stream-K's fp32 fixup of a 128 x 256 tile
+// costs more than the wave quantisation it removes); the M = 512 down
+// projection (64 tiles) is 1.13x faster with stream-K spreading it over every SM.
 static void plan_umma(int64_t M, int64_t N, int64_t K, bool swap, int bn, int sm_count, bool query,
                       Plan *p)
 {
@@ -247,7 +248,7 @@ static void plan_umma(int64_t M, int64_t N, int64_t K, bool swap, int bn, int sm
         return;
     }
     p->stages = umma_stages(bn, swap, true);
-    if (!swap) {
+    if (!swap && 2 * tiles >= G) {
         p->mode = 0;
         p->grid = (int)std::min<int64_t>(tiles, G);
         p->split = 1;
