@@ -147,6 +147,10 @@ int run(const GemmArgs &a, const Plan &p, cudaStream_t st, bool w4)
         if (!w4) return GEMM_ERR_VARIANT;
         e = launch_w4_register(a, p, c);
         break;
+    case GEMM_VARIANT_FRAGMENT:
+        if (!w4) return GEMM_ERR_VARIANT;
+        e = launch_w4_frag(a, p, c);
+        break;
     case GEMM_VARIANT_SKINNY:
     case GEMM_VARIANT_PREFILL:
         if (w4 && p.variant != GEMM_VARIANT_SKINNY) return GEMM_ERR_VARIANT;
@@ -300,22 +304,21 @@ bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan 
 
 // W4A16 routing (AUTO), from GB300 timings over the four decode shapes
 // (N, K) in {(7168, 5120), (5120, 5120), (34816, 5120), (5120, 17408)}:
-//   M <= 4       register-fragment kernel (w4mma.cu): 92 us summed at M = 1
-//                against 103 for the CUDA-core GEMV and 106 for tcgen05
-//   5..128       tcgen05 skinny kernel with in-kernel dequantisation into
+//   M <= 8       TMA-fed fragment kernel (w4frag.cu): 31.7 / 11.4 / 10.8 /
+//                30.8 us at M = 1 against 39.5 / 12.6 / 12.2 / 28.2 for the
+//                register-fragment kernel and 43 / 18 / 15 / 30 for tcgen05
+//   9..128       tcgen05 skinny kernel with in-kernel dequantisation into
 //                TMEM (stages of 256 k): cluster split-K (mode 2) when the
 //                weight tiles fit one wave, stream-K (mode 1) beyond; at
-//                M = 8 and 16 it leads the register kernel (106 vs 109 us,
-//                108 vs 130 us), whose activation loads grow with M
+//                M = 16 it leads the fragment kernel (44 vs 52 us on
+//                34816 x 5120), whose activation loads grow with M
 //   > 128        GEMV path (one pass per four rows)
 bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int sm_count, Plan *p, bool query)
 {
     *p = Plan{};
     if (K == 0) return false;
     if (variant == GEMM_VARIANT_AUTO)
-        variant = M > 128                                       ? GEMM_VARIANT_GEMV
-                  : (M <= 4 && K / group <= kW4RegisterMaxGroups) ? GEMM_VARIANT_REGISTER
-                                                                  : GEMM_VARIANT_SKINNY;
+        variant = M > 128 ? GEMM_VARIANT_GEMV : M <= 8 ? GEMM_VARIANT_FRAGMENT : GEMM_VARIANT_SKINNY;
     if (variant == GEMM_VARIANT_REGISTER) {
         if (M > 32 || K / group > kW4RegisterMaxGroups) return false;
         p->variant = GEMM_VARIANT_REGISTER;
@@ -327,6 +330,18 @@ bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int
         p->tile_m = 8 * p->m_per_pass;
         p->tile_n = 16;
         p->grid = w4_register_grid(N);
+        return true;
+    }
+    if (variant == GEMM_VARIANT_FRAGMENT) {
+        if (M > 16) return false;
+        p->variant = GEMM_VARIANT_FRAGMENT;
+        p->kernels = 2;                      // activation copy and group sums, then the GEMM
+        p->act_copy = 1;
+        p->tile_m = M <= 8 ? 8 : 16;         // tokens of the MMAs (N side)
+        p->split = w4_frag_split(N, K, sm_count, p->tile_m);   // warps per tile
+        p->tile_n = kW4FragRows;
+        p->grid = w4_frag_grid(N, p->split);
+        p->ws_extra = w4_frag_workspace_floats(M, p->tile_m, K, group);   // activation copy and group sums
         return true;
     }
     if (variant == GEMM_VARIANT_SKINNY) {
@@ -393,7 +408,11 @@ void workspace_need(const Plan &p, int64_t M, int64_t N, int64_t K, int64_t *flo
         *floats = (int64_t)p.grid * 2 * kUmmaBM * p.bn;
         *counters = ((M + p.tile_m - 1) / p.tile_m) * ((N + p.tile_n - 1) / p.tile_n);
     }
-    if (p.act_copy) *floats = act_copy_offset(p) + (M * K + 127) / 128 * 64 + p.ws_extra;   // bf16 [M, K] (+ sums)
+    if (p.variant == GEMM_VARIANT_FRAGMENT) {
+        *floats = p.ws_extra;
+        return;
+    }
+    else if (p.act_copy) *floats = act_copy_offset(p) + (M * K + 127) / 128 * 64 + p.ws_extra;   // bf16 [M, K] (+ sums)
 }
 
 }  // namespace dbw

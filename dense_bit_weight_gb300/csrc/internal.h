@@ -2,6 +2,7 @@
 // translation units.  Not installed; not part of the C ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -68,6 +69,17 @@ cudaError_t launch_umma_bf16(const GemmArgs &a, const Plan &p, const LaunchCtx &
 constexpr int kW4RegisterMaxGroups = 544;
 cudaError_t launch_w4_register(const GemmArgs &a, const Plan &p, const LaunchCtx &c);
 int w4_register_grid(int64_t N);
+// W4A16, M <= 16: weights dequantised into mma.sync fragments, streamed by
+// TMA (w4frag.cu): CTAs of kW4FragWarps warps; a tile of kW4FragRows weight
+// rows is shared by w4_frag_split warps of a CTA.  The workspace holds the
+// activation copy and the group sums (w4_frag_workspace_floats floats;
+// tile_m = the MMAs' token count, 8 or 16).
+constexpr int kW4FragRows = 32;
+constexpr int kW4FragWarps = 4;
+cudaError_t launch_w4_frag(const GemmArgs &a, const Plan &p, const LaunchCtx &c);
+int w4_frag_split(int64_t N, int64_t K, int sm_count, int tile_m);
+int w4_frag_grid(int64_t N, int P);
+int64_t w4_frag_workspace_floats(int64_t M, int64_t TP, int64_t K, int64_t group);
 
 // tcgen05 kernel geometry (umma.cu)
 constexpr int kUmmaBM = 128;
@@ -77,6 +89,8 @@ int umma_stages(int bn, bool skinny, bool deep);
 int umma_cluster_capacity(int bn, bool deep, int cluster, bool w4 = false);
 int umma_w4_stages(int bn);
 cudaError_t launch_umma_w4a16(const GemmArgs &a, const Plan &p, const LaunchCtx &c);
+// TMA map of packed 4-bit weights [rows, K/8] (uint32): 32-word x box_rows boxes, 128-byte swizzle.
+bool make_map_words(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int box_rows);
 extern int g_debug_stall;   // test hook: producers issue no copies (forces the watchdog)
 
 }  // namespace dbw

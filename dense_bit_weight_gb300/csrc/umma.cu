@@ -62,6 +62,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
+#include "waits.cuh"
 
 namespace dbw {
 namespace {
@@ -82,7 +83,6 @@ struct W4Args {
     int K, G, group;
     int lg_group;                // log2(group); group is 32, 64 or 128
 };
-constexpr uint64_t kTimeoutNs = 1000000000ull;
 
 struct Sched {
     int mode;                    // 0 whole tiles, 1 stream-K ranges
@@ -161,62 +161,6 @@ struct SegIter {
         return true;
     }
 };
-
-// Bounded wait on an mbarrier phase.  The thread is suspended in hardware
-// between polls (woken as soon as the phase completes), and every poll checks
-// the CTA's abort flag and the 1-second limit; on expiry it raises the abort
-// flag and the device error word and returns false.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
-                                         int *d_error)
-{
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = ptx::global_timer_ns();
-    for (;;) {
-        if (ptx::mbar_try_wait_suspend(bar, parity, 100000u)) return true;
-        if (*abort_flag) return false;
-        if (ptx::global_timer_ns() - t0 > kTimeoutNs) {
-            *abort_flag = 1u;
-            atomicExch(d_error, (int)GEMM_ERR_DEVICE_TIMEOUT);
-            return false;
-        }
-    }
-}
-
-// The same wait by every lane of a converged warp, with a warp-uniform result
-// (a lane that timed out makes the whole warp give up), so the warp can go on
-// to .sync.aligned tensor-memory operations and elected MMA issue together.
-// (Polling from lane 0 alone and broadcasting the outcome measured slower.)
-__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
-                                              int *d_error)
-{
-    const bool ok = wait_bar(bar, parity, abort_flag, d_error);
-    return __all_sync(0xffffffffu, ok);
-}
-
-// Consume a probe taken earlier with mbar_test_wait: if any lane saw the phase
-// incomplete, the warp falls back to the bounded blocking wait.
-__device__ __forceinline__ bool settle_warp(bool probe, uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
-                                            int *d_error)
-{
-    if (__all_sync(0xffffffffu, probe)) return true;
-    return wait_bar_warp(bar, parity, abort_flag, d_error);
-}
-
-// One arrival for the whole (converged) warp, after every lane's prior
-// accesses: the barrier counts warps, not threads.
-__device__ __forceinline__ void arrive_warp(uint32_t bar)
-{
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(bar);
-}
-
-// Wait without looking at the abort flag (used when draining before exit).
-__device__ __forceinline__ void wait_bar_drain(uint32_t bar, uint32_t parity)
-{
-    const uint64_t t0 = ptx::global_timer_ns();
-    while (!ptx::mbar_try_wait_suspend(bar, parity, 100000u))
-        if (ptx::global_timer_ns() - t0 > kTimeoutNs) return;
-}
 
 template <bool SWAP>
 __device__ __forceinline__ void store_chunk(uint16_t *__restrict__ C, int64_t ldc, int R, int Q, int r,
@@ -944,21 +888,10 @@ bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int64_t 
     return r == CUDA_SUCCESS;
 }
 
-// Packed 4-bit weights as uint32 words [rows, K/8]; box 32 words (256 k) x 128
-// rows with the 128-byte swizzle (16-byte piece c of row r lands at piece
-// c ^ (r % 8)), so the dequantising warps read it without bank conflicts.
+// Packed 4-bit weights for the tcgen05 kernel: boxes of 32 words x 128 rows.
 bool make_map_packed(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K)
 {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)(K / 8), (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)(K / 8) * 4};
-    cuuint32_t box[2] = {32, (cuuint32_t)BM};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    return make_map_words(m, ptr, rows, K, BM);
 }
 
 template <int BN, int STAGES, bool SWAP, int MINB, bool W4 = false>
@@ -998,6 +931,23 @@ cudaError_t launch_t(const CUtensorMap &mx, const CUtensorMap &my, uint16_t *C, 
 }
 
 }  // namespace
+
+// Packed 4-bit weights as uint32 words [rows, K/8]; box 32 words (256 k) x
+// box_rows rows with the 128-byte swizzle (16-byte piece c of row r lands at
+// piece c ^ (r % 8)), out-of-range words read as zero.
+bool make_map_words(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)(K / 8), (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(K / 8) * 4};
+    cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
 
 // Pipeline depth per tile width.  Skinny (decode) kernels come in a deep form
 // (one CTA per SM, about 190 KB of shared memory) used when the grid fits in

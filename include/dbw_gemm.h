@@ -61,8 +61,10 @@ typedef enum {
     GEMM_VARIANT_SKINNY = 2,     /* tcgen05, weights as the MMA M side (swap AB)   */
     GEMM_VARIANT_PREFILL = 3,    /* tcgen05, persistent warp-specialised tiles     */
     GEMM_VARIANT_ZERO = 4,       /* K == 0: C is the empty sum, written as zeros   */
-    GEMM_VARIANT_REGISTER = 5    /* W4A16, M <= 32: weights dequantised into       */
+    GEMM_VARIANT_REGISTER = 5,   /* W4A16, M <= 32: weights dequantised into       */
                                  /* registers for warp-level MMAs (mma.sync)       */
+    GEMM_VARIANT_FRAGMENT = 6    /* W4A16, M <= 16: weights streamed by TMA and    */
+                                 /* dequantised into mma.sync fragments            */
 } gemm_variant;
 
 typedef struct {

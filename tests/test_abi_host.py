@@ -112,14 +112,22 @@ def test_plans_are_host_only_and_cover_the_workloads(g):
     assert g.gemm_bf16_plan(5, 7, 0, num_sms=sms)["variant"] == 4
     for M in (1, 16, 64, 128):
         p = g.gemm_w4a16_plan(M, 7168, 5120, 128, num_sms=sms)
-        assert p["variant"] in (1, 2, 3, 5)
-    # W4A16: M <= 4 the register-fragment kernel, 5 <= M <= 128 tcgen05
-    for M in (1, 2, 4):
-        assert g.gemm_w4a16_plan(M, 34816, 5120, 128, num_sms=sms)["variant"] == 5
-    for M in (5, 16, 128):
+        assert p["variant"] in (1, 2, 3, 5, 6)
+    # W4A16: M <= 8 the TMA-fed fragment kernel, 9 <= M <= 128 tcgen05
+    for M in (1, 2, 4, 5, 8):
+        p = g.gemm_w4a16_plan(M, 34816, 5120, 128, num_sms=sms)
+        assert p["variant"] == 6 and p["tile_m"] == 8 and p["kernels"] == 2
+    for M in (9, 16, 128):
         assert g.gemm_w4a16_plan(M, 34816, 5120, 128, num_sms=sms)["variant"] == 2
+    # the fragment kernel stages scales per stage: any number of groups plans
+    assert g.gemm_w4a16_plan(1, 4096, 32 * 545, 32, num_sms=sms)["variant"] == 6
     # beyond the staged-scale limit (K / group > 544 groups) the register kernel does not plan
-    assert g.gemm_w4a16_plan(1, 4096, 32 * 545, 32, num_sms=sms)["variant"] == 2
+    with pytest.raises(g.GemmError):
+        g.gemm_w4a16_plan(1, 4096, 32 * 545, 32, "register", num_sms=sms)
+    # warps per 32-row tile: enough to fill the device, never more than the 256-k stages
+    assert g.gemm_w4a16_plan(1, 34816, 5120, 128, num_sms=sms)["split"] == 2
+    assert g.gemm_w4a16_plan(1, 5120, 5120, 128, num_sms=sms)["split"] == 4
+    assert g.gemm_w4a16_plan(1, 5120, 256, 128, num_sms=sms)["split"] == 1
     with pytest.raises(g.GemmError):
         g.gemm_bf16_plan(4, 4, 4, num_sms=sms)       # K % 8
     with pytest.raises(g.GemmError):

@@ -15,7 +15,7 @@ from gpu_helpers import assert_close, assert_exact, dev_bf16, dev_raw, host_bits
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = ["gemv", "skinny", "prefill", "register"]
+VARIANTS = ["gemv", "skinny", "prefill", "register", "fragment"]
 
 
 @pytest.fixture(scope="module")

@@ -1,4 +1,4 @@
-"""The tcgen05 kernels' bounded waits: a forced stall must end in a recorded
+"""The TMA-fed kernels' bounded waits: a forced stall must end in a recorded
 GEMM_ERR_DEVICE_TIMEOUT and a clean exit, leaving the context usable.
 
 The stall is a test hook (gemm_debug_inject_timeout): the producer issues no
@@ -38,7 +38,8 @@ def test_forced_timeout_is_reported_and_recoverable(variant, M):
     assert g.gemm_last_device_error() == 0
 
 
-def test_forced_timeout_w4a16_skinny():
+@pytest.mark.parametrize("variant", ["skinny", "fragment"])
+def test_forced_timeout_w4a16(variant):
     import torch
     from dense_bit_weight_gb300 import gemm as g, synth
     from gpu_helpers import dev_raw
@@ -48,13 +49,13 @@ def test_forced_timeout_w4a16_skinny():
     args = (dev_bf16(A), dev_raw(Bq), dev_bf16(S), dev_raw(Z), group)
     g.gemm_debug_inject_timeout(True)
     try:
-        g.gemm_w4a16(*args, variant="skinny")
+        g.gemm_w4a16(*args, variant=variant)
         torch.cuda.synchronize()
     finally:
         g.gemm_debug_inject_timeout(False)
     assert g.gemm_last_device_error() == 7
     g.gemm_shutdown()
-    C = g.gemm_w4a16(*args, variant="skinny")
+    C = g.gemm_w4a16(*args, variant=variant)
     torch.cuda.synchronize()
     assert_close(host_bits(C), oracle.gemm_w4a16(A, Bq, S, Z, group), what="w4a16 after timeout")
     assert g.gemm_last_device_error() == 0
