@@ -57,6 +57,8 @@ def _load():
             lib.oracle_dequant_w4.restype = ctypes.c_int
             lib.oracle_round_to_bf16.argtypes = [p, p, i64]
             lib.oracle_round_to_bf16.restype = None
+            lib.oracle_epilogue.argtypes = [ctypes.c_int, p, p, p, p, i64, i64]
+            lib.oracle_epilogue.restype = ctypes.c_int
             lib.oracle_hardware_threads.argtypes = []
             lib.oracle_hardware_threads.restype = ctypes.c_int
             _lib = lib
@@ -117,6 +119,50 @@ def gemm_w4a16(A_bits: np.ndarray, Bq: np.ndarray, scales_bits: np.ndarray,
     rc = _load().oracle_gemm_w4a16(_ptr(A), _ptr(Q), _ptr(S), _ptr(Z), _ptr(R), M, N, K, group, K, t)
     if rc != 0:
         raise RuntimeError(f"oracle_gemm_w4a16 returned {rc}")
+    return R
+
+
+def gemm_bf16_bias(A_bits: np.ndarray, B_bits: np.ndarray, bias_bits: np.ndarray,
+                   threads: int | None = None) -> np.ndarray:
+    """R[m,n] = sum_k A[m,k]*B[n,k] + bias[n] in fp64 (unrounded); bias_bits uint16 [N]."""
+    S = gemm_bf16(A_bits, B_bits, threads)
+    b = _as(bias_bits, np.uint16, "bias")
+    if b.shape != (S.shape[1],):
+        raise ValueError("bias must have one entry per column of C")
+    R = np.empty_like(S)
+    rc = _load().oracle_epilogue(1, _ptr(S), None, _ptr(b), _ptr(R), S.shape[0], S.shape[1])
+    if rc != 0:
+        raise RuntimeError(f"oracle_epilogue returned {rc}")
+    return R
+
+
+def gemm_bf16_silu_mul(A_bits: np.ndarray, B_bits: np.ndarray, threads: int | None = None) -> np.ndarray:
+    """The fused gate/up projection: B_bits uint16 [2N,K] holds the gate rows
+    0..N-1 and the up rows N..2N-1; R[m,n] = silu(g)*u in fp64 (unrounded)
+    with g = sum_k A[m,k]*B[n,k], u = sum_k A[m,k]*B[N+n,k]."""
+    B = _as(B_bits, np.uint16, "B")
+    if B.ndim != 2 or B.shape[0] % 2:
+        raise ValueError("B must hold 2N rows (gate, then up)")
+    N = B.shape[0] // 2
+    G = gemm_bf16(A_bits, B[:N], threads)
+    U = gemm_bf16(A_bits, B[N:], threads)
+    R = np.empty_like(G)
+    rc = _load().oracle_epilogue(2, _ptr(G), _ptr(U), None, _ptr(R), G.shape[0], G.shape[1])
+    if rc != 0:
+        raise RuntimeError(f"oracle_epilogue returned {rc}")
+    return R
+
+
+def silu_mul(g: np.ndarray, u: np.ndarray) -> np.ndarray:
+    """silu(g)*u elementwise in fp64 (the epilogue alone, for pins)."""
+    G = np.ascontiguousarray(g, dtype=np.float64)
+    U = np.ascontiguousarray(u, dtype=np.float64)
+    if G.shape != U.shape:
+        raise ValueError("shape mismatch")
+    R = np.empty_like(G)
+    rc = _load().oracle_epilogue(2, _ptr(G), _ptr(U), None, _ptr(R), 1, G.size)
+    if rc != 0:
+        raise RuntimeError(f"oracle_epilogue returned {rc}")
     return R
 
 

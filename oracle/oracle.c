@@ -37,6 +37,15 @@
  *
  *   oracle_dequant_w4      fp64 [N,K] weights (q - z) * s, for invariant checks.
  *
+ *   oracle_epilogue        the fused epilogues, applied to unrounded fp64 sums:
+ *       bias      R[m,n] = S[m,n] + bias[n]   (FlyDSL prebuilt kernels guide,
+ *                 section 3.1 "Preshuffle GEMM", the epilogue parameter:
+ *                 "bias" and bias + activation fused into the GEMM)
+ *       silu_mul  R[m,n] = silu(G[m,n]) * U[m,n], silu(x) = x / (1 + e^-x),
+ *                 with G and U the gate and up halves of a fused gate/up
+ *                 projection (hk-dsl PyPI page: the fused SiLU-mul kernel)
+ *       exp is the C library's fp64 exp.
+ *
  * Threads: outputs are split into contiguous ranges of the flattened (m,n)
  * index over POSIX threads; each output is computed by exactly one thread in
  * the same k order, so the result does not depend on the thread count.
@@ -229,4 +238,28 @@ static uint16_t round_one(double x)
 void oracle_round_to_bf16(const double *x, uint16_t *out, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i) out[i] = round_one(x[i]);
+}
+
+/* -------------------------------------------------------------- epilogues */
+
+/* kind 1: R[m,n] = S[m,n] + bias[n] (bias bf16 bits [N]); S is [M,N].
+ * kind 2: R[m,n] = silu(S[m,n]) * U[m,n], both [M,N].
+ * R may alias S.  Returns 0 on success, 2 on a bad kind or size. */
+int oracle_epilogue(int kind, const double *S, const double *U, const uint16_t *bias, double *R,
+                    int64_t M, int64_t N)
+{
+    if (M < 0 || N < 0) return 2;
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            const double s = S[m * N + n];
+            if (kind == 1) {
+                R[m * N + n] = s + bf16_to_f64(bias[n]);
+            } else if (kind == 2) {
+                R[m * N + n] = s / (1.0 + exp(-s)) * U[m * N + n];
+            } else {
+                return 2;
+            }
+        }
+    }
+    return 0;
 }

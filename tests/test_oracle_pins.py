@@ -257,6 +257,67 @@ def test_w4_general_vs_dequant_and_blas():
 
 # ------------------------------------------------------------- tolerance helper
 
+# ------------------------------------------------------ fused epilogues
+
+def test_silu_textbook_values():
+    # silu(x) = x * sigmoid(x); sigmoid(1) = 1 / (1 + 1/e) = 0.7310585786300049
+    g = np.array([0.0, 1.0, -1.0, 2.0])
+    got = oracle.silu_mul(g, np.array([1.0, 1.0, 1.0, 0.5]))
+    want = [0.0, 0.7310585786300049, -0.2689414213699951, 0.5 * 2.0 * 0.8807970779778823]
+    assert np.allclose(got, want, rtol=1e-15, atol=0)
+
+
+def test_silu_tanh_form_and_odd_part():
+    # two closed forms independent of the oracle's: silu(x) = (x/2)(1 + tanh(x/2)),
+    # and silu(x) - silu(-x) = x (a sign or exponent error breaks both)
+    # (the tanh form cancels for large negative x; there x e^x / (1 + e^x) is exact-ish)
+    x = np.linspace(-30.0, 30.0, 1201)
+    one = np.ones_like(x)
+    s = oracle.silu_mul(x, one)
+    pos = x >= -4.0
+    assert np.allclose(s[pos], 0.5 * x[pos] * (1.0 + np.tanh(0.5 * x[pos])), rtol=1e-13, atol=1e-300)
+    neg = x < 0.0
+    ex = np.exp(x[neg])
+    assert np.allclose(s[neg], x[neg] * ex / (1.0 + ex), rtol=1e-13, atol=1e-300)
+    assert np.allclose(s - oracle.silu_mul(-x, one), x, rtol=1e-14, atol=1e-14)
+    # saturation: silu(-1000) is -0 (not NaN), silu(1000) = 1000
+    assert np.array_equal(oracle.silu_mul(np.array([-1000.0, 1000.0]), np.ones(2)), [-0.0, 1000.0])
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 8, 16), (5, 24, 40), (33, 136, 264)])
+def test_bias_epilogue_integer_exact(M, N, K):
+    a, A = ints((M, K), 11)
+    b, B = ints((N, K), 12)
+    c, Cb = ints((N,), 13, -40, 40)
+    R = oracle.gemm_bf16_bias(A, B, Cb)
+    assert np.array_equal(R, (a @ b.T + c[None, :]).astype(np.float64))
+
+
+def test_bias_epilogue_vs_blas():
+    A = synth.bf16_normal((17, 96), 1.0, 4, 1)
+    B = synth.bf16_normal((40, 96), 0.1, 4, 2)
+    bias = synth.bf16_normal((40,), 1.0, 4, 3)
+    want = F64(A) @ F64(B).T + F64(bias)[None, :]
+    assert np.allclose(oracle.gemm_bf16_bias(A, B, bias), want, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 8, 16), (7, 24, 40), (16, 72, 128)])
+def test_silu_mul_gate_up_layout(M, N, K):
+    # B stacks the gate rows (0..N-1) over the up rows (N..2N-1): g and u are
+    # exact integer sums here, and the tanh form is independent of the oracle
+    a, A = ints((M, K), 21)
+    b, B = ints((2 * N, K), 22)
+    g = (a @ b[:N].T).astype(np.float64)
+    u = (a @ b[N:].T).astype(np.float64)
+    want = 0.5 * g * (1.0 + np.tanh(0.5 * g)) * u
+    got = oracle.gemm_bf16_silu_mul(A, B)
+    assert got.shape == (M, N)
+    assert np.allclose(got, want, rtol=1e-13, atol=1e-12)
+    # the halves are not interchangeable (the test would catch a swapped layout)
+    swapped = 0.5 * u * (1.0 + np.tanh(0.5 * u)) * g
+    assert not np.allclose(got, swapped, rtol=1e-6, atol=1e-6)
+
+
 def test_tolerance_flags_planted_error():
     ref = synth.normal_f64(1000, 0, 9).reshape(10, 100)
     out = ref.copy()
