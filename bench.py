@@ -17,7 +17,9 @@ The JSON line also carries:
                 each step copies its activations host->device (pinned) and
                 its outputs device->host; weights stay resident
   cpu_baseline  the fp64 CPU oracle on this host, on a bounded sample
-  sweeps        prefill (TFLOP/s), down-projection and W4A16 (GB/s) shapes
+  sweeps        prefill (TFLOP/s), down-projection and W4A16 (GB/s) shapes, and the
+                fused gate/up projection with the SiLU-mul epilogue (decode GB/s,
+                prefill TFLOP/s)
   clocks        nvidia-smi samples taken during the timed region
 
 --impl reference times the oracle (the method's plain definition on the
@@ -45,6 +47,9 @@ PREFILL = [(M, N, K) for M in (1024, 4096, 16384)
            for (N, K) in ((4096, 4096), (6144, 4096), (24576, 4096), (4096, 12288), (8192, 8192))]
 W4 = [(M, N, K) for M in (1, 16, 64, 128)
       for (N, K) in ((7168, 5120), (5120, 5120), (34816, 5120), (5120, 17408))]
+# fused gate/up projection with the SiLU-mul epilogue (C has N = 12288 columns, B 2N rows)
+GATE_UP_DECODE = [(M, 12288, 4096) for M in (1, 8, 32, 128)]
+GATE_UP_PREFILL = [(M, 12288, 4096) for M in (1024, 4096)]
 WORKLOAD = ("decode projections, Qwen3-8B-like dims: bf16 A[M,4096], M in {1,8,32,128}, "
             "B in {qkv 6144x4096, o 4096x4096, gate/up 24576x4096}, fp32 accumulate, bf16 out")
 
@@ -255,11 +260,13 @@ def timed_sweep(g, torch, shapes, kind, reps=20):
     gen.manual_seed(1)
     out = []
     for (M, N, K) in shapes:
-        plan = (g.gemm_w4a16_plan(M, N, K, 128) if kind == "w4" else g.gemm_bf16_plan(M, N, K))
+        silu = kind.startswith("silu")
+        NB = 2 * N if silu else N   # weight rows
+        plan = (g.gemm_w4a16_plan(M, N, K, 128) if kind == "w4" else g.gemm_bf16_plan(M, NB, K))
         if plan["variant"] == 1 and M > 64:
             continue            # no tensor-core plan for this shape
         # enough weight copies that consecutive launches miss L2
-        wbytes = N * K * 2 if kind != "w4" else N * K // 2
+        wbytes = NB * K * 2 if kind != "w4" else N * K // 2
         copies = max(1, min(8, int(np.ceil(3 * 126e6 / wbytes))))
         A = torch.randn((M, K), generator=gen, device=dev).to(torch.bfloat16)
         C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
@@ -270,6 +277,12 @@ def timed_sweep(g, torch, shapes, kind, reps=20):
                   for _ in range(copies)]
             fn = lambda i: g.gemm_w4a16(A, *Bs[i % copies], 128, C)
             work = bytes_w4(M, N, K)
+        elif silu:
+            Bs = [(torch.randn((NB, K), generator=gen, device=dev) * K ** -0.5).to(torch.bfloat16)
+                  for _ in range(copies)]
+            fn = lambda i: g.gemm_bf16_fused(A, Bs[i % copies], C=C, epilogue="silu_mul")
+            # algorithmic work: the 2N-row contraction; bytes read A and B, write C [M, N]
+            work = flops(M, NB, K) if kind == "silu_prefill" else 2 * (M * K + NB * K + M * N)
         else:
             Bs = [(torch.randn((N, K), generator=gen, device=dev) * K ** -0.5).to(torch.bfloat16)
                   for _ in range(copies)]
@@ -468,6 +481,19 @@ def run_ours(args):
                            "frac_of_peak": tot_b / (tot_ms * 1e-3) / 1e9 / hbm,
                            "shapes": [[r["M"], r["N"], r["K"], round(r["work"] / (r["ms"] * 1e-3) / 1e9, 1),
                                        r["variant"]] for r in rs]}
+        # the fused gate/up projection with the SiLU-mul epilogue
+        rs = timed_sweep(g, torch, GATE_UP_DECODE, "silu")
+        tot_b, tot_ms = sum(r["work"] for r in rs), sum(r["ms"] for r in rs)
+        sweeps["gate_up_silu_decode"] = {
+            "unit": "GB/s", "aggregate": tot_b / (tot_ms * 1e-3) / 1e9, "frac_of_peak": tot_b / (tot_ms * 1e-3) / 1e9 / hbm,
+            "shapes": [[r["M"], r["N"], r["K"], round(r["work"] / (r["ms"] * 1e-3) / 1e9, 1), r["variant"]] for r in rs]}
+        rs = timed_sweep(g, torch, GATE_UP_PREFILL, "silu_prefill") if not args.quick else []
+        if rs:
+            tot_f, tot_ms = sum(r["work"] for r in rs), sum(r["ms"] for r in rs)
+            sweeps["gate_up_silu_prefill"] = {
+                "unit": "TFLOP/s", "aggregate": tot_f / (tot_ms * 1e-3) / 1e12, "frac_of_peak": tot_f / (tot_ms * 1e-3) / 1e12 / tf,
+                "shapes": [[r["M"], r["N"], r["K"], round(r["work"] / (r["ms"] * 1e-3) / 1e12, 1), r["variant"]]
+                           for r in rs]}
         # each decode shape alone, graph-timed back to back (no events between launches)
         dec = timed_sweep(g, torch, DECODE, "bf16")
         sweeps["decode_per_shape"] = {"unit": "GB/s", "shapes": [

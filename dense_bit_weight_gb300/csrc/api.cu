@@ -218,7 +218,7 @@ static int64_t cluster_capacity(int bn, bool deep, int cs, int sm_count, bool qu
 // costs more than the wave quantisation it removes); the M = 512 down
 // projection (64 tiles) is 1.13x faster with stream-K spreading it over every SM.
 static void plan_umma(int64_t M, int64_t N, int64_t K, bool swap, int bn, int sm_count, bool query,
-                      Plan *p)
+                      Plan *p, bool pairs = false)
 {
     const int64_t R = swap ? N : M, Q = swap ? M : N;
     const int64_t tiles_r = (R + kUmmaBM - 1) / kUmmaBM;
@@ -235,8 +235,11 @@ static void plan_umma(int64_t M, int64_t N, int64_t K, bool swap, int bn, int sm
     p->ctas_per_sm = 1;
     if (swap && tiles <= G) {
         int64_t S = 1;
+        // (gate, up) row pairs: each CTA of a cluster reduces a block of rows
+        // of the tile, so the split must divide 128 into even blocks
         for (int64_t s = 2; s <= 8 && s <= nk && tiles * s <= G; ++s)
-            if (cluster_capacity(bn, true, (int)s, sm_count, query) >= tiles) S = s;
+            if ((!pairs || (s & (s - 1)) == 0) && cluster_capacity(bn, true, (int)s, sm_count, query) >= tiles)
+                S = s;
         p->mode = 2;
         p->split = (int)S;
         p->grid = (int)(tiles * S);
@@ -266,7 +269,7 @@ static void plan_umma(int64_t M, int64_t N, int64_t K, bool swap, int bn, int sm
     }
 }
 
-bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan *p, bool query)
+bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan *p, bool query, bool pairs)
 {
     *p = Plan{};
     if (K == 0) {
@@ -286,17 +289,17 @@ bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan 
         p->m_per_pass = (int)std::min<int64_t>(M, 4);
         p->tile_m = p->m_per_pass;
         p->tile_n = 8;
-        p->grid = gemv_grid(N, sm_count);
+        p->grid = gemv_grid(pairs ? N / 2 : N, sm_count);   // pairs: one warp per (gate, up) row pair
         return true;
     case GEMM_VARIANT_SKINNY: {
         if (M > 128) return false;
         int bn = 16;
         while (bn < M) bn *= 2;
-        plan_umma(M, N, K, true, bn, sm_count, query, p);
+        plan_umma(M, N, K, true, bn, sm_count, query, p, pairs);
         return true;
     }
     case GEMM_VARIANT_PREFILL:
-        plan_umma(M, N, K, false, 256, sm_count, query, p);
+        plan_umma(M, N, K, false, 256, sm_count, query, p, pairs);
         return true;
     default: return false;
     }
@@ -450,6 +453,44 @@ int gemm_bf16(const void *A, const void *B, void *C, int64_t M, int64_t N, int64
     return gemm_bf16_ex(A, B, C, M, N, K, lda, ldb, ldc, stream, GEMM_VARIANT_AUTO);
 }
 
+int gemm_bf16_fused_ex(const void *A, const void *B, const void *bias, void *C, int64_t M, int64_t N,
+                       int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int epilogue, void *stream,
+                       int variant)
+{
+    if (epilogue != GEMM_EPI_NONE && epilogue != GEMM_EPI_BIAS && epilogue != GEMM_EPI_SILU_MUL)
+        return GEMM_ERR_EPILOGUE;
+    if ((epilogue == GEMM_EPI_BIAS) != (bias != nullptr)) return GEMM_ERR_EPILOGUE;
+    if (epilogue == GEMM_EPI_NONE) return gemm_bf16_ex(A, B, C, M, N, K, lda, ldb, ldc, stream, variant);
+    int rc = check_sizes(M, N, K);
+    if (rc) return rc;
+    const bool pairs = epilogue == GEMM_EPI_SILU_MUL;
+    const int64_t NB = pairs ? 2 * N : N;   // rows of B
+    if (NB > kMaxDim) return GEMM_ERR_SHAPE;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (!C || (K > 0 && (!A || !B))) return GEMM_ERR_NULL;
+    if (ldc < N || ldc % 8 || (K > 0 && (lda < K || ldb < K || lda % 8 || ldb % 8))) return GEMM_ERR_LD;
+    if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B)))) return GEMM_ERR_ALIGN;
+    if (bias && ((uintptr_t)bias & 1u)) return GEMM_ERR_ALIGN;
+    const int64_t cb = extent(M, N, ldc, 2);
+    if (K > 0 && (overlaps(C, cb, A, extent(M, K, lda, 2)) || overlaps(C, cb, B, extent(NB, K, ldb, 2))))
+        return GEMM_ERR_ALIAS;
+    if (bias && overlaps(C, cb, bias, N * 2)) return GEMM_ERR_ALIAS;
+    DeviceState *s = nullptr;
+    int dev = 0;
+    rc = device_state(&s, &dev);
+    if (rc) return rc;
+    Plan p;
+    if (!plan_bf16(M, NB, K, variant, s->sm_count, &p, true, pairs)) return GEMM_ERR_VARIANT;
+    GemmArgs a{A, B, nullptr, nullptr, C, M, N, K, lda, ldb, ldc, 0, bias, epilogue};
+    return run(a, p, (cudaStream_t)stream, false);
+}
+
+int gemm_bf16_fused(const void *A, const void *B, const void *bias, void *C, int64_t M, int64_t N, int64_t K,
+                    int64_t lda, int64_t ldb, int64_t ldc, int epilogue, void *stream)
+{
+    return gemm_bf16_fused_ex(A, B, bias, C, M, N, K, lda, ldb, ldc, epilogue, stream, GEMM_VARIANT_AUTO);
+}
+
 int gemm_w4a16_ex(const void *A, const void *Bq, const void *scales, const void *zeros, void *C,
                   int64_t M, int64_t N, int64_t K, int64_t group, void *stream, int variant)
 {
@@ -541,6 +582,7 @@ const char *gemm_status_string(int status)
     case GEMM_ERR_ARCH: return "device is not compute capability 10.3";
     case GEMM_ERR_ALIAS: return "output overlaps an input";
     case GEMM_ERR_VARIANT: return "variant cannot run this shape";
+    case GEMM_ERR_EPILOGUE: return "unknown epilogue, or bias missing or not used";
     default: return "unknown status";
     }
 }

@@ -40,6 +40,10 @@ __device__ __forceinline__ uint4 ld_ro_v4(const void *p)
     return __ldg(reinterpret_cast<const uint4 *>(p));
 }
 
+// The gated-MLP epilogue: silu(g) * u with silu(x) = x / (1 + e^-x), in fp32
+// (IEEE division, so a huge negative g gives -0, not NaN).
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + __expf(-g)) * u; }
+
 __device__ __forceinline__ float warp_sum(float v)
 {
 #pragma unroll

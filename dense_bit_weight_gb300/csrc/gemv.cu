@@ -11,6 +11,9 @@
 //
 // For M larger than the per-pass row count the kernel makes one pass over the
 // weight row per group of rows (the tcgen05 kernels serve those shapes).
+// Fused epilogues: EPI = 1 adds bias[n] to the fp32 sum; EPI = 2 has the warp
+// take the weight rows n (gate) and N + n (up) together and store
+// silu(gate) * up.
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
@@ -20,51 +23,64 @@ namespace {
 
 constexpr int kWarps = 8;
 
-template <int MT, int U>
+template <int MT, int U, int EPI>
 __global__ void __launch_bounds__(kWarps * 32)
 k_gemv_bf16(const uint16_t *__restrict__ A, const uint16_t *__restrict__ B,
-            uint16_t *__restrict__ C, int M, int N, int K, int64_t lda, int64_t ldb, int64_t ldc)
+            uint16_t *__restrict__ C, int M, int N, int K, int64_t lda, int64_t ldb, int64_t ldc,
+            const uint16_t *__restrict__ bias)
 {
     ptx::pdl_wait();
     ptx::pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int chunks = K >> 3;  // 8 bf16 per 16-byte chunk
+    constexpr int NR = EPI == 2 ? 2 : 1;   // weight rows per output column
     for (int n = blockIdx.x * kWarps + (threadIdx.x >> 5); n < N; n += gridDim.x * kWarps) {
-        const uint16_t *brow = B + (int64_t)n * ldb;
+        const uint16_t *brow[NR];
+#pragma unroll
+        for (int r = 0; r < NR; ++r) brow[r] = B + (int64_t)(n + r * N) * ldb;
         for (int m0 = 0; m0 < M; m0 += MT) {
-            float acc[MT];
+            float acc[NR][MT];
 #pragma unroll
-            for (int i = 0; i < MT; ++i) acc[i] = 0.f;
+            for (int r = 0; r < NR; ++r)
+#pragma unroll
+                for (int i = 0; i < MT; ++i) acc[r][i] = 0.f;
             for (int c0 = lane; c0 < chunks; c0 += 32 * U) {
-                uint4 bv[U];
+                uint4 bv[NR][U];
 #pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int c = c0 + 32 * u;
-                    bv[u] = c < chunks ? ld_stream_v4(brow + (int64_t)c * 8) : make_uint4(0, 0, 0, 0);
-                }
+                for (int r = 0; r < NR; ++r)
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int c = c0 + 32 * u;
+                        bv[r][u] = c < chunks ? ld_stream_v4(brow[r] + (int64_t)c * 8) : make_uint4(0, 0, 0, 0);
+                    }
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int c = c0 + 32 * u;
                     if (c >= chunks) break;
-                    const uint32_t bw[4] = {bv[u].x, bv[u].y, bv[u].z, bv[u].w};
 #pragma unroll
                     for (int i = 0; i < MT; ++i) {
                         if (m0 + i >= M) break;
                         const uint4 av = ld_ro_v4(A + (int64_t)(m0 + i) * lda + (int64_t)c * 8);
                         const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
-                        float s = acc[i];
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            s = fmaf(bf16lo(aw[j]), bf16lo(bw[j]), s);
-                            s = fmaf(bf16hi(aw[j]), bf16hi(bw[j]), s);
+                        for (int r = 0; r < NR; ++r) {
+                            const uint32_t bw[4] = {bv[r][u].x, bv[r][u].y, bv[r][u].z, bv[r][u].w};
+                            float s = acc[r][i];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                s = fmaf(bf16lo(aw[j]), bf16lo(bw[j]), s);
+                                s = fmaf(bf16hi(aw[j]), bf16hi(bw[j]), s);
+                            }
+                            acc[r][i] = s;
                         }
-                        acc[i] = s;
                     }
                 }
             }
 #pragma unroll
             for (int i = 0; i < MT; ++i) {
-                const float v = warp_sum(acc[i]);
+                float v = warp_sum(acc[0][i]);
+                if (EPI == 1) v += bf16lo(bias[n]);
+                if (EPI == 2) v = silu_mul(v, warp_sum(acc[NR - 1][i]));
                 if (lane == 0 && m0 + i < M) C[(int64_t)(m0 + i) * ldc + n] = f32_to_bf16_rn(v);
             }
         }
@@ -141,11 +157,12 @@ k_gemv_w4a16(const uint16_t *__restrict__ A, const uint32_t *__restrict__ Bq,
     }
 }
 
-__global__ void k_zero_fill(uint16_t *C, int M, int N, int64_t ldc)
+// K == 0: the empty sum (plus the bias, if one is fused; silu(0) * 0 = 0).
+__global__ void k_zero_fill(uint16_t *C, int M, int N, int64_t ldc, const uint16_t *bias)
 {
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < (int64_t)M * N;
          i += (int64_t)gridDim.x * blockDim.x)
-        C[(i / N) * ldc + (i % N)] = 0;
+        C[(i / N) * ldc + (i % N)] = bias ? bias[i % N] : (uint16_t)0;
 }
 
 template <typename Kern, typename... Args>
@@ -179,20 +196,33 @@ cudaError_t launch_zero_fill(const GemmArgs &a, const LaunchCtx &c)
     int grid = (int)((total + 255) / 256);
     if (grid > c.sm_count * 8) grid = c.sm_count * 8;
     if (grid < 1) grid = 1;
-    k_zero_fill<<<grid, 256, 0, c.stream>>>((uint16_t *)a.C, (int)a.M, (int)a.N, a.ldc);
+    k_zero_fill<<<grid, 256, 0, c.stream>>>((uint16_t *)a.C, (int)a.M, (int)a.N, a.ldc,
+                                           a.epi == GEMM_EPI_BIAS ? (const uint16_t *)a.bias : nullptr);
     return cudaGetLastError();
+}
+
+template <int EPI>
+cudaError_t launch_gemv_mt(const GemmArgs &a, const Plan &p, const LaunchCtx &c, const uint16_t *A,
+                           const uint16_t *B, uint16_t *C)
+{
+    const int M = (int)a.M, N = (int)a.N, K = (int)a.K;
+    const uint16_t *bias = (const uint16_t *)a.bias;
+    switch (p.m_per_pass) {
+    case 1: return launch_pdl(k_gemv_bf16<1, 8, EPI>, p.grid, c.stream, A, B, C, M, N, K, a.lda, a.ldb, a.ldc, bias);
+    case 2: return launch_pdl(k_gemv_bf16<2, 8, EPI>, p.grid, c.stream, A, B, C, M, N, K, a.lda, a.ldb, a.ldc, bias);
+    case 3: return launch_pdl(k_gemv_bf16<3, 4, EPI>, p.grid, c.stream, A, B, C, M, N, K, a.lda, a.ldb, a.ldc, bias);
+    default: return launch_pdl(k_gemv_bf16<4, 4, EPI>, p.grid, c.stream, A, B, C, M, N, K, a.lda, a.ldb, a.ldc, bias);
+    }
 }
 
 cudaError_t launch_gemv_bf16(const GemmArgs &a, const Plan &p, const LaunchCtx &c)
 {
     const uint16_t *A = (const uint16_t *)a.A, *B = (const uint16_t *)a.B;
     uint16_t *C = (uint16_t *)a.C;
-    const int M = (int)a.M, N = (int)a.N, K = (int)a.K;
-    switch (p.m_per_pass) {
-    case 1: return launch_pdl(k_gemv_bf16<1, 8>, p.grid, c.stream, A, B, C, M, N, K, a.lda, a.ldb, a.ldc);
-    case 2: return launch_pdl(k_gemv_bf16<2, 8>, p.grid, c.stream, A, B, C, M, N, K, a.lda, a.ldb, a.ldc);
-    case 3: return launch_pdl(k_gemv_bf16<3, 4>, p.grid, c.stream, A, B, C, M, N, K, a.lda, a.ldb, a.ldc);
-    default: return launch_pdl(k_gemv_bf16<4, 4>, p.grid, c.stream, A, B, C, M, N, K, a.lda, a.ldb, a.ldc);
+    switch (a.epi) {
+    case GEMM_EPI_BIAS: return launch_gemv_mt<1>(a, p, c, A, B, C);
+    case GEMM_EPI_SILU_MUL: return launch_gemv_mt<2>(a, p, c, A, B, C);
+    default: return launch_gemv_mt<0>(a, p, c, A, B, C);
     }
 }
 

@@ -27,6 +27,8 @@ struct GemmArgs {
     const void *scales, *zeros;
     void *C;
     int64_t M, N, K, lda, ldb, ldc, group;
+    const void *bias = nullptr;   // bf16 [N] for GEMM_EPI_BIAS
+    int epi = GEMM_EPI_NONE;      // bf16 only; for GEMM_EPI_SILU_MUL, N counts the columns of C and B has 2N rows
 };
 
 // Host-side plan (pure function of the sizes and the SM count).
@@ -48,7 +50,10 @@ struct Plan {
 
 // query = true: plan for the current device (asks it for cluster occupancy);
 // false: host-only model of a device with sm_count SMs.
-bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan *p, bool query = true);
+// pairs: the weight rows come in (gate, up) pairs (GEMM_EPI_SILU_MUL; N is
+// then the kernel's row count 2 * columns of C): splits keep pairs together.
+bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan *p, bool query = true,
+               bool pairs = false);
 bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int sm_count, Plan *p,
                 bool query = true);
 

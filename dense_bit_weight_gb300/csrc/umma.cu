@@ -93,6 +93,9 @@ struct Sched {
     int stall;                   // test hook: producer issues nothing (forces the watchdog)
     int split;                   // mode 2: CTAs per tile (cluster size)
     long long units;             // tiles * nk
+    int epi;                     // fused epilogue (GEMM_EPI_*)
+    int pairs;                   // the weight operand's map interleaves (gate, up) rows: 3-D copies
+    const uint16_t *bias;        // GEMM_EPI_BIAS: bf16 per weight row (output column)
 };
 
 struct Segment {
@@ -191,6 +194,58 @@ __device__ __forceinline__ void store_chunk(uint16_t *__restrict__ C, int64_t ld
         for (int j = 0; j < 16; ++j)
             if (q0 + j < Q) C[(int64_t)(q0 + j) * ldc + r] = f32_to_bf16_rn(f[j]);
     }
+}
+
+// store_chunk with the fused epilogue.  Rows of X (SWAP) or columns of Y hold
+// weight rows; with GEMM_EPI_SILU_MUL they come as (gate, up) pairs 2j, 2j + 1
+// for output column j.  SWAP: a thread owns one weight row and its pair
+// partner is the neighbouring lane (every lane of the warp must call this).
+template <bool SWAP>
+__device__ __forceinline__ void store_chunk_epi(uint16_t *__restrict__ C, int64_t ldc, int R, int Q, int r,
+                                                int q0, float (&f)[16], const Sched &s)
+{
+    if (s.epi == GEMM_EPI_SILU_MUL) {
+        if (SWAP) {
+            float u[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) u[j] = __shfl_down_sync(0xffffffffu, f[j], 1);
+            if ((r & 1) == 0 && r < R) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (q0 + j < Q) C[(int64_t)(q0 + j) * ldc + (r >> 1)] = f32_to_bf16_rn(silu_mul(f[j], u[j]));
+            }
+        } else if (r < R) {
+            float o[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) o[j] = silu_mul(f[2 * j], f[2 * j + 1]);
+            uint16_t *dst = C + (int64_t)r * ldc + (q0 >> 1);
+            if (q0 + 16 <= Q) {
+                uint4 w;
+                w.x = pack_bf16x2_rn(o[0], o[1]);
+                w.y = pack_bf16x2_rn(o[2], o[3]);
+                w.z = pack_bf16x2_rn(o[4], o[5]);
+                w.w = pack_bf16x2_rn(o[6], o[7]);
+                *reinterpret_cast<uint4 *>(dst) = w;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (q0 + 2 * j < Q) dst[j] = f32_to_bf16_rn(o[j]);
+            }
+        }
+        return;
+    }
+    if (s.epi == GEMM_EPI_BIAS) {
+        if (SWAP) {
+            const float b = r < R ? bf16lo(s.bias[r]) : 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) f[j] += b;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (q0 + j < Q) f[j] += bf16lo(s.bias[q0 + j]);
+        }
+    }
+    store_chunk<SWAP>(C, ldc, R, Q, r, q0, f);
 }
 
 constexpr uint32_t tmem_cols_for(int n)
@@ -390,8 +445,10 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                     tile_coords(sched, s0.tile, tr, tq);
                     const int kend = min(s0.kb1, s0.kb0 + STAGES);
                     for (int kb = s0.kb0; kb < kend; ++kb) {
-                        ptx::tma_prefetch_l2_2d(&tmX, kb * BK, tr * BM);
-                        ptx::tma_prefetch_l2_2d(&tmY, kb * BK, tq * BN);
+                        if (SWAP && sched.pairs) ptx::tma_prefetch_l2_3d(&tmX, kb * BK, 0, tr * (BM / 2));
+                        else ptx::tma_prefetch_l2_2d(&tmX, kb * BK, tr * BM);
+                        if (!SWAP && sched.pairs) ptx::tma_prefetch_l2_3d(&tmY, kb * BK, 0, tq * (BN / 2));
+                        else ptx::tma_prefetch_l2_2d(&tmY, kb * BK, tq * BN);
                     }
                 }
                 ptx::pdl_wait();
@@ -410,8 +467,13 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                     if (!sched.stall) {
                         ptx::mbar_arrive_expect_tx(FULL(stage), L::STAGE_BYTES);
                         const uint32_t xs = sbase + stage * L::STAGE_BYTES;
-                        ptx::tma_load_2d(xs, &tmX, FULL(stage), kb * BK, tr * BM, pol_x);
-                        ptx::tma_load_2d(xs + L::X_BYTES, &tmY, FULL(stage), kb * BK, tq * BN, pol_y);
+                        // (gate, up) pairs: the 3-D view [row / 2][gate or up][k] puts the
+                        // pair's rows next to each other in the tile
+                        if (SWAP && sched.pairs) ptx::tma_load_3d(xs, &tmX, FULL(stage), kb * BK, 0, tr * (BM / 2), pol_x);
+                        else ptx::tma_load_2d(xs, &tmX, FULL(stage), kb * BK, tr * BM, pol_x);
+                        if (!SWAP && sched.pairs)
+                            ptx::tma_load_3d(xs + L::X_BYTES, &tmY, FULL(stage), kb * BK, 0, tq * (BN / 2), pol_y);
+                        else ptx::tma_load_2d(xs + L::X_BYTES, &tmY, FULL(stage), kb * BK, tq * BN, pol_y);
                         ++issued;
                     }
                     if (++stage == STAGES) {
@@ -670,7 +732,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
 #pragma unroll
                 for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(v[j]);
                 if (whole) {
-                    store_chunk<SWAP>(C, ldc, R, Q, r, qb + c, f);
+                    store_chunk_epi<SWAP>(C, ldc, R, Q, r, qb + c, f, sched);
                 } else if (cluster_split) {
                     float4 *prow = reinterpret_cast<float4 *>(smem + row * PSTRIDE + c * 4);
 #pragma unroll
@@ -754,7 +816,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                         f[4 * u + 2] = a4[4 * j16 + u].z;
                         f[4 * u + 3] = a4[4 * j16 + u].w;
                     }
-                    store_chunk<SWAP>(C, ldc, R, Q, r, qb + cb * 4 + j16 * 16, f);
+                    store_chunk_epi<SWAP>(C, ldc, R, Q, r, qb + cb * 4 + j16 * 16, f, sched);
                 }
             }
         }
@@ -822,21 +884,30 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
 #pragma unroll
                     for (int jj = 0; jj < 2; ++jj) {    // even lane: tokens 0, 1; odd lane: tokens 2, 3
                         const int j = odd ? 2 + jj : jj;
-                        const float lo = odd ? x[j] : a[j], hi = odd ? a[j] : x[j];
+                        float lo = odd ? x[j] : a[j], hi = odd ? a[j] : x[j];
                         const int q = qb + c4 * 4 + j;
                         if (q < Q && re < R) {
+                            if (sched.epi == GEMM_EPI_SILU_MUL) {   // rows re, re + 1: gate and up of column re / 2
+                                C[(int64_t)q * ldc + (re >> 1)] = f32_to_bf16_rn(silu_mul(lo, hi));
+                                continue;
+                            }
+                            if (sched.epi == GEMM_EPI_BIAS) {
+                                lo += bf16lo(sched.bias[re]);
+                                if (re + 1 < R) hi += bf16lo(sched.bias[re + 1]);
+                            }
                             uint16_t *dst = C + (int64_t)q * ldc + re;
                             if (re + 1 < R) *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2_rn(lo, hi);
                             else *dst = f32_to_bf16_rn(lo);
                         }
                     }
-                } else if (r < R) {
+                } else if (r < R && sched.epi != GEMM_EPI_SILU_MUL) {   // (pairs are only split in twos)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const int q = qb + c4 * 4 + j;
                         if (q < Q) {
-                            if (SWAP) C[(int64_t)q * ldc + r] = f32_to_bf16_rn(a[j]);
-                            else C[(int64_t)r * ldc + q] = f32_to_bf16_rn(a[j]);
+                            const float b = sched.epi == GEMM_EPI_BIAS ? bf16lo(sched.bias[SWAP ? r : q]) : 0.f;
+                            if (SWAP) C[(int64_t)q * ldc + r] = f32_to_bf16_rn(a[j] + b);
+                            else C[(int64_t)r * ldc + q] = f32_to_bf16_rn(a[j] + b);
                         }
                     }
                 }
@@ -883,6 +954,24 @@ bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int64_t 
     cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Fused gate/up weights [2N, K] bf16 (gate rows 0..N-1, up rows N..2N-1) as
+// the 3-D view [N][2][K]: a box of 64 k x 2 x box_pairs puts the gate and up
+// rows of output column j next to each other (rows 2j, 2j + 1 of the tile),
+// 128-byte swizzle as make_map.
+bool make_map_pairs(CUtensorMap *m, const void *ptr, int64_t N, int64_t K, int64_t ld, int box_pairs)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)K, 2, (cuuint64_t)N};
+    cuuint64_t strides[2] = {(cuuint64_t)(N * ld * 2), (cuuint64_t)ld * 2};
+    cuuint32_t box[3] = {(cuuint32_t)BK, 2, (cuuint32_t)box_pairs};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -1113,13 +1202,16 @@ cudaError_t launch_umma_w4a16(const GemmArgs &a, const Plan &p, const LaunchCtx 
 cudaError_t launch_umma_bf16(const GemmArgs &a, const Plan &p, const LaunchCtx &c)
 {
     const bool swap = p.variant == GEMM_VARIANT_SKINNY;
+    const bool pairs = a.epi == GEMM_EPI_SILU_MUL;
+    const int64_t NW = pairs ? 2 * a.N : a.N;   // weight rows the kernel multiplies
     const void *X = swap ? a.B : a.A;
     const void *Y = swap ? a.A : a.B;
-    const int64_t R = swap ? a.N : a.M, Q = swap ? a.M : a.N;
+    const int64_t R = swap ? NW : a.M, Q = swap ? a.M : NW;
     const int64_t ldx = swap ? a.ldb : a.lda, ldy = swap ? a.lda : a.ldb;
     CUtensorMap mx, my;
-    if (!make_map(&mx, X, R, a.K, ldx, BM) || !make_map(&my, Y, Q, a.K, ldy, p.bn))
-        return cudaErrorInvalidValue;
+    const bool okx = swap && pairs ? make_map_pairs(&mx, X, a.N, a.K, ldx, BM / 2) : make_map(&mx, X, R, a.K, ldx, BM);
+    const bool oky = !swap && pairs ? make_map_pairs(&my, Y, a.N, a.K, ldy, p.bn / 2) : make_map(&my, Y, Q, a.K, ldy, p.bn);
+    if (!okx || !oky) return cudaErrorInvalidValue;
     Sched s{};
     s.mode = p.mode;
     s.tiles_r = (int)((R + BM - 1) / BM);
@@ -1130,6 +1222,9 @@ cudaError_t launch_umma_bf16(const GemmArgs &a, const Plan &p, const LaunchCtx &
     s.group_r = p.group_r > 0 ? p.group_r : s.tiles_r;
     s.units = (long long)s.tiles * s.nk;
     s.stall = g_debug_stall;
+    s.epi = a.epi;
+    s.pairs = pairs ? 1 : 0;
+    s.bias = (const uint16_t *)a.bias;
     uint16_t *C = (uint16_t *)a.C;
     const int r = (int)R, q = (int)Q;
     s.split = p.split;

@@ -20,13 +20,13 @@ GEMM_OK = 0
 STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_NULL", 2: "GEMM_ERR_SHAPE", 3: "GEMM_ERR_LD",
           4: "GEMM_ERR_ALIGN", 5: "GEMM_ERR_GROUP", 6: "GEMM_ERR_CUDA",
           7: "GEMM_ERR_DEVICE_TIMEOUT", 8: "GEMM_ERR_ARCH", 9: "GEMM_ERR_ALIAS",
-          10: "GEMM_ERR_VARIANT"}
+          10: "GEMM_ERR_VARIANT", 11: "GEMM_ERR_EPILOGUE"}
 VARIANT = {"auto": 0, "gemv": 1, "skinny": 2, "prefill": 3, "zero": 4, "register": 5, "fragment": 6}
 VARIANT_NAME = {v: k for k, v in VARIANT.items()}
 
 EXPORTS = ["gemm_bf16", "gemm_w4a16", "gemm_bf16_ex", "gemm_w4a16_ex", "gemm_bf16_plan",
            "gemm_w4a16_plan", "gemm_last_device_error", "gemm_status_string", "gemm_shutdown",
-           "gemm_debug_inject_timeout", "gemm_bf16_noalloc"]
+           "gemm_debug_inject_timeout", "gemm_bf16_noalloc", "gemm_bf16_fused", "gemm_bf16_fused_ex"]
 
 
 class gemm_plan(ctypes.Structure):
@@ -43,6 +43,8 @@ class gemm_plan(ctypes.Structure):
 _p, _i64, _i = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
 lib.gemm_bf16.argtypes = [_p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _p]
 lib.gemm_bf16_ex.argtypes = lib.gemm_bf16.argtypes + [_i]
+lib.gemm_bf16_fused_ex.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _i, _p, _i]
+lib.gemm_bf16_fused_ex.restype = _i
 lib.gemm_bf16_noalloc.argtypes = lib.gemm_bf16.argtypes
 lib.gemm_bf16_noalloc.restype = _i
 lib.gemm_w4a16.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _p]
@@ -147,6 +149,45 @@ def gemm_bf16(A, B, C=None, stream=None, variant="auto"):
     return C
 
 
+EPILOGUE = {"none": 0, "bias": 1, "silu_mul": 2}
+
+
+def gemm_bf16_fused(A, B, bias=None, C=None, epilogue="bias", stream=None, variant="auto"):
+    """gemm_bf16 with a fused epilogue (applied in fp32 to the full K sum).
+
+    epilogue "bias": C[m,n] = (A @ B^T)[m,n] + bias[n] (bias bf16 [N]).
+    epilogue "silu_mul": B is the fused gate/up weight [2N,K] (gate rows, then
+    up rows) and C[m,n] = silu(g) * u with g, u the two halves of A @ B^T.
+    Returns C bf16 [M,N].
+    """
+    import torch
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
+        raise TypeError("A and B must be bfloat16")
+    if not (A.is_cuda and B.is_cuda):
+        raise ValueError("A and B must be CUDA tensors")
+    epi = EPILOGUE[epilogue] if isinstance(epilogue, str) else int(epilogue)
+    M, K = A.shape
+    NB, K2 = B.shape
+    if K != K2:
+        raise ValueError(f"K mismatch: {A.shape} vs {B.shape}")
+    if epi == 2 and NB % 2:
+        raise ValueError("silu_mul: B must hold 2N rows (gate, then up)")
+    N = NB // 2 if epi == 2 else NB
+    if bias is not None and (bias.dtype != torch.bfloat16 or not bias.is_cuda or tuple(bias.shape) != (N,)
+                             or bias.stride(0) != 1):
+        raise ValueError("bias must be a contiguous CUDA bfloat16 [N] tensor")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    if C.dtype != torch.bfloat16 or tuple(C.shape) != (M, N):
+        raise ValueError("C must be bfloat16 [M,N]")
+    lda, ldb, ldc = _row_major_2d(A, "A"), _row_major_2d(B, "B"), _row_major_2d(C, "C")
+    rc = lib.gemm_bf16_fused_ex(A.data_ptr(), B.data_ptr(), bias.data_ptr() if bias is not None else None,
+                                C.data_ptr(), M, N, K, lda, ldb, ldc, epi, _stream_handle(stream),
+                                _variant(variant))
+    _check(rc, "gemm_bf16_fused")
+    return C
+
+
 def gemm_w4a16(A, Bq, scales, zeros, group: int, C=None, stream=None, variant="auto"):
     """C[M,N] = A[M,K] @ W[N,K]^T with W = (q - z) * s, q packed 8 per int32 along K.
 
@@ -180,6 +221,13 @@ def gemm_bf16_ptr(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb:
     """The C call on raw device addresses; returns the gemm_status."""
     return int(lib.gemm_bf16_ex(A, B, C, M, N, K, lda, ldb, ldc, ctypes.c_void_p(stream),
                                 _variant(variant)))
+
+
+def gemm_bf16_fused_ptr(A: int, B: int, bias: int, C: int, M: int, N: int, K: int, lda: int, ldb: int,
+                        ldc: int, epilogue: int, stream: int = 0, variant="auto") -> int:
+    """gemm_bf16_fused_ex on raw device addresses (bias 0 = NULL); returns the gemm_status."""
+    return int(lib.gemm_bf16_fused_ex(A, B, bias or None, C, M, N, K, lda, ldb, ldc, epilogue,
+                                      ctypes.c_void_p(stream), _variant(variant)))
 
 
 def gemm_bf16_noalloc_ptr(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int,

@@ -51,7 +51,8 @@ typedef enum {
     GEMM_ERR_DEVICE_TIMEOUT = 7, /* a kernel's bounded wait expired (see below)    */
     GEMM_ERR_ARCH = 8,           /* current device is not compute capability 10.3  */
     GEMM_ERR_ALIAS = 9,          /* C overlaps an input                            */
-    GEMM_ERR_VARIANT = 10        /* a forced variant cannot run this shape         */
+    GEMM_ERR_VARIANT = 10,       /* a forced variant cannot run this shape         */
+    GEMM_ERR_EPILOGUE = 11       /* unknown epilogue, or bias missing / not used   */
 } gemm_status;
 
 /* Kernel variants (what gemm_*_plan reports and gemm_*_ex may force). */
@@ -113,6 +114,41 @@ int gemm_bf16(const void *A, const void *B, void *C, int64_t M, int64_t N, int64
  */
 int gemm_w4a16(const void *A, const void *Bq, const void *scales, const void *zeros, void *C,
                int64_t M, int64_t N, int64_t K, int64_t group, void *stream);
+
+/*
+ * gemm_bf16_fused -- gemm_bf16 with the epilogue fused into the GEMM's store.
+ * The FlyDSL prebuilt-kernels guide (section 3.1, Preshuffle GEMM, the
+ * `epilogue` parameter) fuses a bias and an activation into the GEMM; the
+ * hk-dsl PyPI page lists a fused SiLU-mul for the gated MLP.  The epilogue is
+ * applied in fp32 to the complete K sum, and the result is rounded to bf16
+ * once (nearest, ties to even).
+ *
+ *   GEMM_EPI_NONE      C[m,n] = sum_k A[m,k] B[n,k]                (as gemm_bf16)
+ *   GEMM_EPI_BIAS      C[m,n] = sum_k A[m,k] B[n,k] + bias[n]
+ *                      bias: bf16 [N], 2-byte aligned, device memory.
+ *   GEMM_EPI_SILU_MUL  B is the fused gate/up projection with 2N rows: gate
+ *                      rows 0..N-1, then up rows N..2N-1 (row j at B + j*ldb).
+ *                      g = sum_k A[m,k] B[n,k], u = sum_k A[m,k] B[N+n,k],
+ *                      C[m,n] = silu(g) * u, silu(x) = x / (1 + exp(-x)).
+ *                      C is [M, N]; bias must be NULL.
+ *
+ * Sizes, leading dimensions, alignment and errors as for gemm_bf16 (N counts
+ * the columns of C; B spans 2N rows for GEMM_EPI_SILU_MUL).  An unknown
+ * epilogue, or a bias that is NULL for GEMM_EPI_BIAS or not NULL otherwise,
+ * returns GEMM_ERR_EPILOGUE; C overlapping bias returns GEMM_ERR_ALIAS.
+ * gemm_bf16_fused_ex forces a kernel family like gemm_bf16_ex.
+ */
+typedef enum {
+    GEMM_EPI_NONE = 0,
+    GEMM_EPI_BIAS = 1,
+    GEMM_EPI_SILU_MUL = 2
+} gemm_epilogue;
+
+int gemm_bf16_fused(const void *A, const void *B, const void *bias, void *C, int64_t M, int64_t N,
+                    int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int epilogue, void *stream);
+int gemm_bf16_fused_ex(const void *A, const void *B, const void *bias, void *C, int64_t M, int64_t N,
+                       int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int epilogue, void *stream,
+                       int variant);
 
 /*
  * gemm_bf16_noalloc -- gemm_bf16 for callers that cannot allocate device

@@ -162,3 +162,19 @@ def test_k_zero_ignores_empty_inputs(g):
     # C-side checks are observable here)
     assert call_bf16(g, K=0, A=0, B=0, lda=1, ldb=3, ldc=5) == 3      # ldc still checked
     assert call_bf16(g, K=0, A=0, B=0, C=0) == 1
+
+
+def test_fused_epilogue_argument_errors():
+    # rejected before any device work: an unknown epilogue, a bias where none is
+    # used, no bias where one is required (GEMM_ERR_EPILOGUE = 11)
+    from dense_bit_weight_gb300 import gemm as g
+    p = 1 << 20   # never dereferenced
+    assert g.gemm_bf16_fused_ptr(p, p, 0, p, 8, 8, 8, 8, 8, 8, 7) == 11
+    assert g.gemm_bf16_fused_ptr(p, p, 0, p, 8, 8, 8, 8, 8, 8, 1) == 11
+    assert g.gemm_bf16_fused_ptr(p, p, p, p, 8, 8, 8, 8, 8, 8, 2) == 11
+    assert g.gemm_bf16_fused_ptr(p, p, p, p, 8, 8, 8, 8, 8, 8, 0) == 11
+    assert g.gemm_status_string(11) != g.gemm_status_string(99)
+    # the SiLU-mul plan is the plain plan on the 2N weight rows
+    sms = 152
+    for M in (1, 8, 128, 4096):
+        assert g.gemm_bf16_plan(M, 2 * 12288, 4096, num_sms=sms)["variant"] in (1, 2, 3)
