@@ -59,6 +59,8 @@ def _load():
             lib.oracle_round_to_bf16.restype = None
             lib.oracle_epilogue.argtypes = [ctypes.c_int, p, p, p, p, i64, i64]
             lib.oracle_epilogue.restype = ctypes.c_int
+            lib.oracle_gemm_grouped.argtypes = [p, p, p, p, i64, i64, i64, i64, ctypes.c_int]
+            lib.oracle_gemm_grouped.restype = ctypes.c_int
             lib.oracle_hardware_threads.argtypes = []
             lib.oracle_hardware_threads.restype = ctypes.c_int
             _lib = lib
@@ -163,6 +165,27 @@ def silu_mul(g: np.ndarray, u: np.ndarray) -> np.ndarray:
     rc = _load().oracle_epilogue(2, _ptr(G), _ptr(U), None, _ptr(R), 1, G.size)
     if rc != 0:
         raise RuntimeError(f"oracle_epilogue returned {rc}")
+    return R
+
+
+def gemm_grouped(A_bits: np.ndarray, B_bits: np.ndarray, ends: np.ndarray,
+                 threads: int | None = None) -> np.ndarray:
+    """The grouped (MoE) GEMM in fp64: A_bits uint16 [M,K] stacked token rows,
+    B_bits uint16 [G,N,K] per-expert weights, ends int32 [G] cumulative row
+    ends; R[m,n] = sum_k A[m,k]*B[g,n,k] for the expert g owning row m, 0 for
+    rows past ends[-1]."""
+    A = _as(A_bits, np.uint16, "A")
+    B = _as(B_bits, np.uint16, "B")
+    E = _as(ends, np.int32, "ends")
+    if A.ndim != 2 or B.ndim != 3 or A.shape[1] != B.shape[2] or E.shape != (B.shape[0],):
+        raise ValueError("shape mismatch for the grouped GEMM")
+    M, K = A.shape
+    G, N, _ = B.shape
+    R = np.empty((M, N), dtype=np.float64)
+    rc = _load().oracle_gemm_grouped(_ptr(A), _ptr(B), _ptr(E), _ptr(R), G, M, N, K,
+                                     threads or hardware_threads())
+    if rc != 0:
+        raise RuntimeError(f"oracle_gemm_grouped returned {rc}")
     return R
 
 

@@ -46,6 +46,15 @@
  *                 projection (hk-dsl PyPI page: the fused SiLU-mul kernel)
  *       exp is the C library's fp64 exp.
  *
+ *   oracle_gemm_grouped    the grouped (mixture-of-experts) GEMM: expert g
+ *       owns the token rows [end[g-1], end[g]) of the stacked activations
+ *       A [M,K] (end[-1] = 0, end = cumulative row ends) and multiplies them
+ *       by its own weights B_g [N,K] (B is [G,N,K]):
+ *       R[m,n] = sum_k A[m,k] * B_g[n,k] for every m of expert g; rows of
+ *       no expert are 0.  FlyDSL-in-PyTorch blog, section "Grouped GEMM: MoE
+ *       with uneven load" (concatenated activations, grouped weights,
+ *       offsets marking each expert's rows; empty experts own no rows).
+ *
  * Threads: outputs are split into contiguous ranges of the flattened (m,n)
  * index over POSIX threads; each output is computed by exactly one thread in
  * the same k order, so the result does not depend on the thread count.
@@ -260,6 +269,30 @@ int oracle_epilogue(int kind, const double *S, const double *U, const uint16_t *
                 return 2;
             }
         }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------ grouped GEMM */
+
+/* A [M,K], B [G,N,K] (expert g at B + g*N*K), R [M,N]; ends int32 [G],
+ * cumulative row ends (non-decreasing, <= M).  Returns 0, or 2 on bad sizes
+ * or offsets. */
+int oracle_gemm_grouped(const uint16_t *A, const uint16_t *B, const int32_t *ends, double *R,
+                        int64_t G, int64_t M, int64_t N, int64_t K, int nthreads)
+{
+    if (G < 1 || M < 0 || N < 0 || K < 0) return 2;
+    memset(R, 0, (size_t)(M * N) * sizeof(double));
+    int64_t start = 0;
+    for (int64_t g = 0; g < G; ++g) {
+        const int64_t end = ends[g];
+        if (end < start || end > M) return 2;
+        if (end > start) {
+            const int rc = oracle_gemm_bf16(A + start * K, B + g * N * K, R + start * N, end - start, N, K, K, K,
+                                            nthreads);
+            if (rc) return rc;
+        }
+        start = end;
     }
     return 0;
 }

@@ -318,6 +318,47 @@ def test_silu_mul_gate_up_layout(M, N, K):
     assert not np.allclose(got, swapped, rtol=1e-6, atol=1e-6)
 
 
+# ------------------------------------------------------------ grouped GEMM
+
+@pytest.mark.parametrize("sizes", [[5, 0, 17, 3], [0, 0, 9], [32], [1, 1, 1, 1, 1, 1, 1, 1]])
+def test_grouped_integer_exact_per_expert(sizes):
+    # every row against an int64 matmul with its own expert's weights; rows
+    # past the last expert stay 0
+    G, N, K = len(sizes), 24, 40
+    ends = np.cumsum(sizes).astype(np.int32)
+    M = int(ends[-1]) + 3
+    a, A = ints((M, K), 31)
+    b, B = ints((G, N, K), 32)
+    R = oracle.gemm_grouped(A, B, ends)
+    want = np.zeros((M, N))
+    start = 0
+    for g, e in enumerate(ends):
+        want[start:e] = a[start:e] @ b[g].T
+        start = e
+    assert np.array_equal(R, want)
+
+
+def test_grouped_one_expert_is_the_plain_gemm_and_order_matters():
+    a, A = ints((20, 32), 33)
+    b, B = ints((2, 16, 32), 34)
+    assert np.array_equal(oracle.gemm_grouped(A, B[:1], np.array([20], np.int32)), oracle.gemm_bf16(A, B[0]))
+    # moving the boundary moves rows between experts (an off-by-one in the
+    # row ranges fails this)
+    r1 = oracle.gemm_grouped(A, B, np.array([7, 20], np.int32))
+    r2 = oracle.gemm_grouped(A, B, np.array([8, 20], np.int32))
+    assert np.array_equal(r1[:7], r2[:7]) and np.array_equal(r1[8:], r2[8:])
+    assert np.array_equal(r1[7], (a[7] @ b[1].T).astype(np.float64))
+    assert np.array_equal(r2[7], (a[7] @ b[0].T).astype(np.float64))
+
+
+def test_grouped_rejects_bad_offsets():
+    _, A = ints((4, 8), 35)
+    _, B = ints((2, 8, 8), 36)
+    for bad in ([3, 2], [2, 5], [-1, 4]):
+        with pytest.raises(RuntimeError):
+            oracle.gemm_grouped(A, B, np.array(bad, np.int32))
+
+
 def test_tolerance_flags_planted_error():
     ref = synth.normal_f64(1000, 0, 9).reshape(10, 100)
     out = ref.copy()
