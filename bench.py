@@ -19,7 +19,7 @@ The JSON line also carries:
   cpu_baseline  the fp64 CPU oracle on this host, on a bounded sample
   sweeps        prefill (TFLOP/s), down-projection and W4A16 (GB/s) shapes, and the
                 fused gate/up projection with the SiLU-mul epilogue (decode GB/s,
-                prefill TFLOP/s)
+                prefill TFLOP/s), and the grouped (MoE) GEMM
   clocks        nvidia-smi samples taken during the timed region
 
 --impl reference times the oracle (the method's plain definition on the
@@ -50,6 +50,10 @@ W4 = [(M, N, K) for M in (1, 16, 64, 128)
 # fused gate/up projection with the SiLU-mul epilogue (C has N = 12288 columns, B 2N rows)
 GATE_UP_DECODE = [(M, 12288, 4096) for M in (1, 8, 32, 128)]
 GATE_UP_PREFILL = [(M, 12288, 4096) for M in (1024, 4096)]
+# grouped (MoE) GEMM: (name, expert token counts, N, K); ragged includes empty experts
+GROUPED = [("uniform 8 experts", [512] * 8, 4096, 4096),
+           ("ragged 16 experts", [1024, 0, 512, 37, 0, 800, 256, 1, 600, 0, 300, 64, 200, 150, 100, 52], 4096, 4096),
+           ("decode MoE 128 experts", [4] * 128, 1536, 2048)]
 WORKLOAD = ("decode projections, Qwen3-8B-like dims: bf16 A[M,4096], M in {1,8,32,128}, "
             "B in {qkv 6144x4096, o 4096x4096, gate/up 24576x4096}, fp32 accumulate, bf16 out")
 
@@ -294,6 +298,31 @@ def timed_sweep(g, torch, shapes, kind, reps=20):
     return out
 
 
+def grouped_sweep(g, torch, reps=20):
+    """The grouped GEMM: useful TFLOP/s (2 * rows * N * K) and GB/s (A, the
+    active experts' weights, C), graph-timed, weights rotated over copies."""
+    dev = torch.device("cuda")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(2)
+    out = []
+    for name, counts, N, K in GROUPED:
+        G, M = len(counts), sum(counts)
+        wbytes = G * N * K * 2
+        copies = max(1, min(8, -(-3 * 130_000_000 // wbytes)))
+        A = torch.randn((M, K), generator=gen, device=dev).to(torch.bfloat16)
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        Bs = [(torch.randn((G, N, K), generator=gen, device=dev) * K ** -0.5).to(torch.bfloat16)
+              for _ in range(copies)]
+        ends = torch.tensor(np.cumsum(counts), dtype=torch.int32, device=dev)
+        ms = graph_time_ms(torch, lambda i: g.gemm_bf16_grouped(A, Bs[i % copies], ends, C=C), reps)
+        active = sum(1 for c in counts if c)
+        fl = 2 * M * N * K
+        by = 2 * (M * K + active * N * K + M * N)
+        out.append([name, M, N, K, round(fl / (ms * 1e-3) / 1e12, 1), round(by / (ms * 1e-3) / 1e9, 1)])
+        del Bs, A, C
+    return {"unit": "[name, rows, N, K, TFLOP/s, GB/s]", "shapes": out}
+
+
 def cpu_oracle_sample(target_s=12.0):
     """Time the oracle on a fraction of every decode GEMM's output columns."""
     import oracle
@@ -494,6 +523,7 @@ def run_ours(args):
                 "unit": "TFLOP/s", "aggregate": tot_f / (tot_ms * 1e-3) / 1e12, "frac_of_peak": tot_f / (tot_ms * 1e-3) / 1e12 / tf,
                 "shapes": [[r["M"], r["N"], r["K"], round(r["work"] / (r["ms"] * 1e-3) / 1e12, 1), r["variant"]]
                            for r in rs]}
+        sweeps["grouped"] = grouped_sweep(g, torch)
         # each decode shape alone, graph-timed back to back (no events between launches)
         dec = timed_sweep(g, torch, DECODE, "bf16")
         sweeps["decode_per_shape"] = {"unit": "GB/s", "shapes": [

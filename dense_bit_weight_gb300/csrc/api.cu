@@ -305,6 +305,25 @@ bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan 
     }
 }
 
+void plan_grouped(int64_t G, int64_t M, int64_t N, int64_t K, int sm_count, Plan *p)
+{
+    *p = Plan{};
+    p->variant = GEMM_VARIANT_PREFILL;
+    p->kernels = 1;
+    p->bn = 256;
+    p->tile_m = kUmmaBM;
+    p->tile_n = 256;
+    p->mode = 0;
+    p->split = 1;
+    p->ctas_per_sm = 1;
+    p->stages = umma_stages(256, false, true);
+    // at most one partial m-tile per expert beyond the M / BM full ones
+    const int64_t tiles = ((M + kUmmaBM - 1) / kUmmaBM + G) * ((N + 255) / 256);
+    p->grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, sm_count));
+    p->group_r = 1;
+    (void)K;
+}
+
 // W4A16 routing (AUTO), from GB300 timings over the four decode shapes
 // (N, K) in {(7168, 5120), (5120, 5120), (34816, 5120), (5120, 17408)}:
 //   M <= 8       TMA-fed fragment kernel (w4frag.cu): 31.7 / 11.4 / 10.8 /
@@ -482,6 +501,32 @@ int gemm_bf16_fused_ex(const void *A, const void *B, const void *bias, void *C, 
     Plan p;
     if (!plan_bf16(M, NB, K, variant, s->sm_count, &p, true, pairs)) return GEMM_ERR_VARIANT;
     GemmArgs a{A, B, nullptr, nullptr, C, M, N, K, lda, ldb, ldc, 0, bias, epilogue};
+    return run(a, p, (cudaStream_t)stream, false);
+}
+
+int gemm_bf16_grouped(const void *A, const void *B, void *C, const void *ends, int64_t G, int64_t M,
+                      int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, void *stream)
+{
+    int rc = check_sizes(M, N, K);
+    if (rc) return rc;
+    if (G < 1 || G > kMaxExperts || K == 0 || G * N > kMaxDim) return GEMM_ERR_SHAPE;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (!A || !B || !C || !ends) return GEMM_ERR_NULL;
+    if (ldc < N || ldc % 8 || lda < K || ldb < K || lda % 8 || ldb % 8) return GEMM_ERR_LD;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || ((uintptr_t)ends & 3u)) return GEMM_ERR_ALIGN;
+    const int64_t cb = extent(M, N, ldc, 2);
+    if (overlaps(C, cb, A, extent(M, K, lda, 2)) || overlaps(C, cb, B, extent(G * N, K, ldb, 2)) ||
+        overlaps(C, cb, ends, G * 4))
+        return GEMM_ERR_ALIAS;
+    DeviceState *s = nullptr;
+    int dev = 0;
+    rc = device_state(&s, &dev);
+    if (rc) return rc;
+    Plan p;
+    plan_grouped(G, M, N, K, s->sm_count, &p);
+    GemmArgs a{A, B, nullptr, nullptr, C, M, N, K, lda, ldb, ldc, 0};
+    a.gends = (const int *)ends;
+    a.groups = G;
     return run(a, p, (cudaStream_t)stream, false);
 }
 

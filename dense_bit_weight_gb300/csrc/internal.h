@@ -29,7 +29,12 @@ struct GemmArgs {
     int64_t M, N, K, lda, ldb, ldc, group;
     const void *bias = nullptr;   // bf16 [N] for GEMM_EPI_BIAS
     int epi = GEMM_EPI_NONE;      // bf16 only; for GEMM_EPI_SILU_MUL, N counts the columns of C and B has 2N rows
+    const int *gends = nullptr;   // grouped GEMM: int32 cumulative token-row ends per expert (device)
+    int64_t groups = 0;           //   experts; B is [groups, N, K]
 };
+
+// Grouped GEMM: experts the prefill kernel's shared-memory table holds.
+constexpr int kMaxExperts = 1024;
 
 // Host-side plan (pure function of the sizes and the SM count).
 struct Plan {
@@ -56,6 +61,9 @@ bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan 
                bool pairs = false);
 bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int sm_count, Plan *p,
                 bool query = true);
+// Grouped GEMM over G experts sharing M stacked token rows (prefill kernel,
+// persistent whole tiles; the tile count is found on the device).
+void plan_grouped(int64_t G, int64_t M, int64_t N, int64_t K, int sm_count, Plan *p);
 
 // Workspace need (floats, counters) for a plan; 0 when it needs none.  The
 // permuted activation copy of a W4A16 tcgen05 plan sits after the split-K

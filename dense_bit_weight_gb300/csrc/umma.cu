@@ -96,7 +96,11 @@ struct Sched {
     int epi;                     // fused epilogue (GEMM_EPI_*)
     int pairs;                   // the weight operand's map interleaves (gate, up) rows: 3-D copies
     const uint16_t *bias;        // GEMM_EPI_BIAS: bf16 per weight row (output column)
+    const int *gends;            // grouped GEMM (prefill kernel, mode 0): cumulative token-row ends per expert
+    int groups;                  //   experts
+    int gN;                      //   weight rows per expert (columns of C)
 };
+
 
 struct Segment {
     int tile, kb0, kb1, slot;
@@ -275,16 +279,20 @@ struct Layout {
     static constexpr int BAR_OFF = SZ_OFF;
     static constexpr int NBARS = 2 * STAGES + 6 + (W4 ? 2 * kNX + 2 * AST : 0);
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
-    static constexpr int SMEM = MISC_OFF + 16 + 1024;   // + slack to align the base to 1024
+    // grouped GEMM (prefill kernel only): expert row ends [kMaxExperts], m-tile prefix [kMaxExperts + 1]
+    static constexpr int GRP_OFF = MISC_OFF + 16;
+    static constexpr int GRP_BYTES = (!W4 && BN == 256) ? (2 * kMaxExperts + 4) * 4 : 0;
+    static constexpr int SMEM = GRP_OFF + GRP_BYTES + 1024;   // + slack to align the base to 1024
 };
 
 template <int BN, int STAGES, bool SWAP, int MINB, bool W4>
 __global__ void __launch_bounds__(threads_for(W4), MINB)
 k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
-       uint16_t *__restrict__ C, int R, int Q, int64_t ldc, const Sched sched,
+       uint16_t *__restrict__ C, int R, int Q, int64_t ldc, const Sched sched_in,
        float *__restrict__ ws, int *__restrict__ counters, int *__restrict__ d_error, const W4Args w4)
 {
     using L = Layout<BN, STAGES, W4>;
+    Sched sched = sched_in;   // (the grouped GEMM sets its tile count on the device)
     // W4A16 takes all 512 columns: two accumulators below kXCol, the
     // dequantised tiles above.  Its shared memory admits one CTA per SM, so
     // the allocation never waits on a CTA of the same cluster.
@@ -350,6 +358,81 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = misc[0];
+
+    // Grouped GEMM (prefill kernel, whole tiles): expert g owns the token rows
+    // [end[g-1], end[g]) of A and C and multiplies them by its weight rows
+    // g*gN .. g*gN + gN - 1 of B.  The row ends come from the previous kernel
+    // (a router), so every thread waits for it; warp 0 clamps them into a
+    // non-decreasing sequence within [0, R] and writes the exclusive prefix of
+    // the experts' m-tile counts; tile t is then (m-tile t / tiles_q, n-tile
+    // t % tiles_q), and an expert with no rows owns no tile.
+    int *gend = reinterpret_cast<int *>(smem + L::GRP_OFF);
+    int *gpre = gend + kMaxExperts;
+    if constexpr (L::GRP_BYTES > 0) {
+        if (sched.gends) {
+            ptx::pdl_wait();
+            if (warp == 0) {
+                const int G = sched.groups;
+                const int per = (G + 31) / 32;   // consecutive experts per lane
+                const int g0 = min(G, lane * per), g1 = min(G, g0 + per);
+                int run = 0;                     // prefix max of the raw ends within this lane's run
+                for (int g = g0; g < g1; ++g) run = max(run, __ldg(sched.gends + g));
+                int before = run;                // inclusive max-scan over lanes, then shifted to exclusive
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, before, o);
+                    if (lane >= o) before = max(before, v);
+                }
+                before = __shfl_up_sync(0xffffffffu, before, 1);
+                if (lane == 0) before = 0;
+                int prev = min(before, R), mt = 0;
+                run = before;
+                for (int g = g0; g < g1; ++g) {
+                    run = max(run, __ldg(sched.gends + g));
+                    const int e = min(run, R);
+                    gend[g] = e;
+                    mt += (e - prev + BM - 1) / BM;
+                    prev = e;
+                }
+                int base = mt;                   // exclusive sum-scan of the m-tile counts
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, base, o);
+                    if (lane >= o) base += v;
+                }
+                if (lane == 31) gpre[G] = base;
+                base -= mt;
+                prev = before < R ? before : R;
+                for (int g = g0; g < g1; ++g) {
+                    gpre[g] = base;
+                    base += (gend[g] - (g == g0 ? prev : gend[g - 1]) + BM - 1) / BM;
+                }
+            }
+            __syncthreads();
+            sched.tiles = gpre[sched.groups] * sched.tiles_q;
+        }
+    }
+    // tile t -> X rows from xrow, Y rows from yrow, C rows below rlim, C columns from qb
+    auto geo = [&](int t, int &xrow, int &yrow, int &rlim, int &qb) {
+        if (L::GRP_BYTES > 0 && sched.gends) {
+            const int mt = t / sched.tiles_q, tq = t - mt * sched.tiles_q;
+            int lo = 0, hi = sched.groups;   // the expert: largest lo < G with gpre[lo] <= mt
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (gpre[mid] <= mt) lo = mid;
+                else hi = mid;
+            }
+            xrow = (lo > 0 ? gend[lo - 1] : 0) + (mt - gpre[lo]) * BM;
+            rlim = gend[lo];
+            yrow = lo * sched.gN + tq * BN;
+            qb = tq * BN;
+        } else {
+            int tr, tq;
+            tile_coords(sched, t, tr, tq);
+            xrow = tr * BM;
+            yrow = tq * BN;
+            rlim = R;
+            qb = tq * BN;
+        }
+    };
     // Programmatic dependent launch: let the next kernel start its prologue now;
     // each role waits for the previous kernel (griddepcontrol.wait) just before
     // its first global-memory access.  The MMA role touches only shared and
@@ -441,14 +524,14 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                 SegIter pre(sched, blockIdx.x);
                 Segment s0;
                 if (pre.next(sched, s0) && !sched.stall) {
-                    int tr, tq;
-                    tile_coords(sched, s0.tile, tr, tq);
+                    int xrow, yrow, rlim, qb;
+                    geo(s0.tile, xrow, yrow, rlim, qb);
                     const int kend = min(s0.kb1, s0.kb0 + STAGES);
                     for (int kb = s0.kb0; kb < kend; ++kb) {
-                        if (SWAP && sched.pairs) ptx::tma_prefetch_l2_3d(&tmX, kb * BK, 0, tr * (BM / 2));
-                        else ptx::tma_prefetch_l2_2d(&tmX, kb * BK, tr * BM);
-                        if (!SWAP && sched.pairs) ptx::tma_prefetch_l2_3d(&tmY, kb * BK, 0, tq * (BN / 2));
-                        else ptx::tma_prefetch_l2_2d(&tmY, kb * BK, tq * BN);
+                        if (SWAP && sched.pairs) ptx::tma_prefetch_l2_3d(&tmX, kb * BK, 0, xrow / 2);
+                        else ptx::tma_prefetch_l2_2d(&tmX, kb * BK, xrow);
+                        if (!SWAP && sched.pairs) ptx::tma_prefetch_l2_3d(&tmY, kb * BK, 0, yrow / 2);
+                        else ptx::tma_prefetch_l2_2d(&tmY, kb * BK, yrow);
                     }
                 }
                 ptx::pdl_wait();
@@ -457,8 +540,8 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
             Segment seg;
             bool ok = true;
             while (ok && it.next(sched, seg)) {
-                int tr, tq;
-                tile_coords(sched, seg.tile, tr, tq);
+                int xrow, yrow, rlim, qb;
+                geo(seg.tile, xrow, yrow, rlim, qb);
                 for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
                     if (!wait_bar(EMPTY(stage), phase ^ 1u, abort_flag, d_error)) {
                         ok = false;
@@ -469,11 +552,11 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                         const uint32_t xs = sbase + stage * L::STAGE_BYTES;
                         // (gate, up) pairs: the 3-D view [row / 2][gate or up][k] puts the
                         // pair's rows next to each other in the tile
-                        if (SWAP && sched.pairs) ptx::tma_load_3d(xs, &tmX, FULL(stage), kb * BK, 0, tr * (BM / 2), pol_x);
-                        else ptx::tma_load_2d(xs, &tmX, FULL(stage), kb * BK, tr * BM, pol_x);
+                        if (SWAP && sched.pairs) ptx::tma_load_3d(xs, &tmX, FULL(stage), kb * BK, 0, xrow / 2, pol_x);
+                        else ptx::tma_load_2d(xs, &tmX, FULL(stage), kb * BK, xrow, pol_x);
                         if (!SWAP && sched.pairs)
-                            ptx::tma_load_3d(xs + L::X_BYTES, &tmY, FULL(stage), kb * BK, 0, tq * (BN / 2), pol_y);
-                        else ptx::tma_load_2d(xs + L::X_BYTES, &tmY, FULL(stage), kb * BK, tq * BN, pol_y);
+                            ptx::tma_load_3d(xs + L::X_BYTES, &tmY, FULL(stage), kb * BK, 0, yrow / 2, pol_y);
+                        else ptx::tma_load_2d(xs + L::X_BYTES, &tmY, FULL(stage), kb * BK, yrow, pol_y);
                         ++issued;
                     }
                     if (++stage == STAGES) {
@@ -714,10 +797,9 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
         while (it.next(sched, seg)) {
             if (!wait_bar_warp(TFULL(acc), acc_phase, abort_flag, d_error)) break;
             ptx::tc_fence_after();
-            int tr, tq;
-            tile_coords(sched, seg.tile, tr, tq);
-            const int r = tr * BM + row;
-            const int qb = tq * BN;
+            int xrow, yrow, rlim, qb;
+            geo(seg.tile, xrow, yrow, rlim, qb);
+            const int r = xrow + row;
             const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(acc * BN);
             const bool whole = seg.kb0 == 0 && seg.kb1 == sched.nk;
             // stream-K partial: float4 columns, [column/4][row], so a warp's store is 512 contiguous bytes
@@ -732,7 +814,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
 #pragma unroll
                 for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(v[j]);
                 if (whole) {
-                    store_chunk_epi<SWAP>(C, ldc, R, Q, r, qb + c, f, sched);
+                    store_chunk_epi<SWAP>(C, ldc, rlim, Q, r, qb + c, f, sched);
                 } else if (cluster_split) {
                     float4 *prow = reinterpret_cast<float4 *>(smem + row * PSTRIDE + c * 4);
 #pragma unroll
@@ -816,7 +898,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                         f[4 * u + 2] = a4[4 * j16 + u].z;
                         f[4 * u + 3] = a4[4 * j16 + u].w;
                     }
-                    store_chunk_epi<SWAP>(C, ldc, R, Q, r, qb + cb * 4 + j16 * 16, f, sched);
+                    store_chunk_epi<SWAP>(C, ldc, rlim, Q, r, qb + cb * 4 + j16 * 16, f, sched);
                 }
             }
         }
@@ -1209,8 +1291,9 @@ cudaError_t launch_umma_bf16(const GemmArgs &a, const Plan &p, const LaunchCtx &
     const int64_t R = swap ? NW : a.M, Q = swap ? a.M : NW;
     const int64_t ldx = swap ? a.ldb : a.lda, ldy = swap ? a.lda : a.ldb;
     CUtensorMap mx, my;
+    const int64_t QY = a.gends ? a.groups * a.N : Q;   // grouped: B stacks the experts' weights
     const bool okx = swap && pairs ? make_map_pairs(&mx, X, a.N, a.K, ldx, BM / 2) : make_map(&mx, X, R, a.K, ldx, BM);
-    const bool oky = !swap && pairs ? make_map_pairs(&my, Y, a.N, a.K, ldy, p.bn / 2) : make_map(&my, Y, Q, a.K, ldy, p.bn);
+    const bool oky = !swap && pairs ? make_map_pairs(&my, Y, a.N, a.K, ldy, p.bn / 2) : make_map(&my, Y, QY, a.K, ldy, p.bn);
     if (!okx || !oky) return cudaErrorInvalidValue;
     Sched s{};
     s.mode = p.mode;
@@ -1225,6 +1308,10 @@ cudaError_t launch_umma_bf16(const GemmArgs &a, const Plan &p, const LaunchCtx &
     s.epi = a.epi;
     s.pairs = pairs ? 1 : 0;
     s.bias = (const uint16_t *)a.bias;
+    s.gends = a.gends;
+    s.groups = (int)a.groups;
+    s.gN = (int)a.N;
+    if (a.gends && (swap || p.mode != 0 || p.bn != 256)) return cudaErrorInvalidValue;
     uint16_t *C = (uint16_t *)a.C;
     const int r = (int)R, q = (int)Q;
     s.split = p.split;

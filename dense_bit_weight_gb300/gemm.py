@@ -26,7 +26,8 @@ VARIANT_NAME = {v: k for k, v in VARIANT.items()}
 
 EXPORTS = ["gemm_bf16", "gemm_w4a16", "gemm_bf16_ex", "gemm_w4a16_ex", "gemm_bf16_plan",
            "gemm_w4a16_plan", "gemm_last_device_error", "gemm_status_string", "gemm_shutdown",
-           "gemm_debug_inject_timeout", "gemm_bf16_noalloc", "gemm_bf16_fused", "gemm_bf16_fused_ex"]
+           "gemm_debug_inject_timeout", "gemm_bf16_noalloc", "gemm_bf16_fused", "gemm_bf16_fused_ex",
+           "gemm_bf16_grouped"]
 
 
 class gemm_plan(ctypes.Structure):
@@ -45,6 +46,8 @@ lib.gemm_bf16.argtypes = [_p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _p]
 lib.gemm_bf16_ex.argtypes = lib.gemm_bf16.argtypes + [_i]
 lib.gemm_bf16_fused_ex.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _i, _p, _i]
 lib.gemm_bf16_fused_ex.restype = _i
+lib.gemm_bf16_grouped.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _p]
+lib.gemm_bf16_grouped.restype = _i
 lib.gemm_bf16_noalloc.argtypes = lib.gemm_bf16.argtypes
 lib.gemm_bf16_noalloc.restype = _i
 lib.gemm_w4a16.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _p]
@@ -185,6 +188,31 @@ def gemm_bf16_fused(A, B, bias=None, C=None, epilogue="bias", stream=None, varia
                                 C.data_ptr(), M, N, K, lda, ldb, ldc, epi, _stream_handle(stream),
                                 _variant(variant))
     _check(rc, "gemm_bf16_fused")
+    return C
+
+
+def gemm_bf16_grouped(A, B, ends, C=None, stream=None):
+    """The grouped (MoE) GEMM: expert g's token rows ends[g-1]..ends[g]-1 of A
+    [M,K] times its weights B[g] ([G,N,K]); C [M,N] rows past ends[-1] are not
+    written.  ends: CUDA int32 [G] cumulative row ends.  Returns C."""
+    import torch
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
+        raise TypeError("A and B must be bfloat16")
+    if B.dim() != 3 or not B.is_contiguous() or ends.dtype != torch.int32 or ends.dim() != 1 \
+            or not ends.is_cuda or not ends.is_contiguous():
+        raise ValueError("B must be a contiguous [G,N,K] tensor and ends a contiguous CUDA int32 [G] tensor")
+    M, K = A.shape
+    G, N, K2 = B.shape
+    if K != K2 or ends.shape[0] != G:
+        raise ValueError("shape mismatch")
+    if C is None:
+        C = torch.zeros((M, N), dtype=torch.bfloat16, device=A.device)
+    if C.dtype != torch.bfloat16 or tuple(C.shape) != (M, N):
+        raise ValueError("C must be bfloat16 [M,N]")
+    lda, ldc = _row_major_2d(A, "A"), _row_major_2d(C, "C")
+    rc = lib.gemm_bf16_grouped(A.data_ptr(), B.data_ptr(), C.data_ptr(), ends.data_ptr(), G, M, N, K,
+                               lda, K, ldc, _stream_handle(stream))
+    _check(rc, "gemm_bf16_grouped")
     return C
 
 

@@ -151,6 +151,34 @@ int gemm_bf16_fused_ex(const void *A, const void *B, const void *bias, void *C, 
                        int variant);
 
 /*
+ * gemm_bf16_grouped -- the grouped (mixture-of-experts) GEMM.  The FlyDSL
+ * PyTorch blog (section "Grouped GEMM: MoE with uneven load") stacks the
+ * tokens routed to G experts into one activation matrix, keeps the experts'
+ * weights grouped, and marks each expert's rows with offsets; one persistent
+ * launch walks the tiles of all experts, so an expert with no tokens costs
+ * nothing.
+ *
+ *   A     [M, K] bf16 (row m at A + m*lda): expert g's tokens are the rows
+ *         ends[g-1] .. ends[g]-1 (ends[-1] = 0).
+ *   B     [G, N, K] bf16: expert g's weights are the rows g*N .. g*N+N-1
+ *         (row j at B + j*ldb).  (The blog's B[G, K, N] is the logical shape;
+ *         here every expert is stored K-contiguous like gemm_bf16's B.)
+ *   C     [M, N] bf16 (row m at C + m*ldc): C[m,:] = A[m,:] . B_g^T for the
+ *         expert g owning row m; rows at or past ends[G-1] are not written.
+ *   ends  int32 [G] device memory, 4-byte aligned: cumulative row ends,
+ *         normally non-decreasing and <= M.  It may be written by the
+ *         previous kernel on the stream (a router); the kernel reads it after
+ *         that kernel completes.  Out-of-range values are clamped (each end to
+ *         at least the previous one and at most M), so they never address
+ *         outside A or C.
+ * 1 <= G <= 1024, K >= 8; other sizes, leading dimensions and alignment as
+ * gemm_bf16 (K == 0 returns GEMM_ERR_SHAPE).  Accumulation fp32, one bf16
+ * rounding.  Runs on `stream` with no host synchronisation.
+ */
+int gemm_bf16_grouped(const void *A, const void *B, void *C, const void *ends, int64_t G, int64_t M,
+                      int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, void *stream);
+
+/*
  * gemm_bf16_noalloc -- gemm_bf16 for callers that cannot allocate device
  * memory.  (The pages have no counterpart: this is a property of the
  * library, not of the method.)
