@@ -19,7 +19,8 @@ The JSON line also carries:
   cpu_baseline  the fp64 CPU oracle on this host, on a bounded sample
   sweeps        prefill (TFLOP/s), down-projection and W4A16 (GB/s) shapes, and the
                 fused gate/up projection with the SiLU-mul epilogue (decode GB/s,
-                prefill TFLOP/s), and the grouped (MoE) GEMM
+                prefill TFLOP/s), the grouped (MoE) GEMM, and W4A16 at
+                prefill-size token counts (TFLOP/s)
   clocks        nvidia-smi samples taken during the timed region
 
 --impl reference times the oracle (the method's plain definition on the
@@ -47,6 +48,8 @@ PREFILL = [(M, N, K) for M in (1024, 4096, 16384)
            for (N, K) in ((4096, 4096), (6144, 4096), (24576, 4096), (4096, 12288), (8192, 8192))]
 W4 = [(M, N, K) for M in (1, 16, 64, 128)
       for (N, K) in ((7168, 5120), (5120, 5120), (34816, 5120), (5120, 17408))]
+# W4A16 at prefill-size token counts (TFLOP/s)
+W4_PREFILL = [(1024, 34816, 5120), (4096, 34816, 5120), (4096, 5120, 17408)]
 # fused gate/up projection with the SiLU-mul epilogue (C has N = 12288 columns, B 2N rows)
 GATE_UP_DECODE = [(M, 12288, 4096) for M in (1, 8, 32, 128)]
 GATE_UP_PREFILL = [(M, 12288, 4096) for M in (1024, 4096)]
@@ -510,6 +513,14 @@ def run_ours(args):
                            "frac_of_peak": tot_b / (tot_ms * 1e-3) / 1e9 / hbm,
                            "shapes": [[r["M"], r["N"], r["K"], round(r["work"] / (r["ms"] * 1e-3) / 1e9, 1),
                                        r["variant"]] for r in rs]}
+        rs = timed_sweep(g, torch, W4_PREFILL, "w4", reps=10) if not args.quick else []
+        if rs:
+            tot_f = sum(flops(r["M"], r["N"], r["K"]) for r in rs)
+            tot_ms = sum(r["ms"] for r in rs)
+            sweeps["w4a16_prefill"] = {
+                "unit": "TFLOP/s", "aggregate": tot_f / (tot_ms * 1e-3) / 1e12, "frac_of_peak": tot_f / (tot_ms * 1e-3) / 1e12 / tf,
+                "shapes": [[r["M"], r["N"], r["K"], round(flops(r["M"], r["N"], r["K"]) / (r["ms"] * 1e-3) / 1e12, 1),
+                            r["variant"]] for r in rs]}
         # the fused gate/up projection with the SiLU-mul epilogue
         rs = timed_sweep(g, torch, GATE_UP_DECODE, "silu")
         tot_b, tot_ms = sum(r["work"] for r in rs), sum(r["ms"] for r in rs)

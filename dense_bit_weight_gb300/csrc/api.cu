@@ -329,18 +329,21 @@ void plan_grouped(int64_t G, int64_t M, int64_t N, int64_t K, int sm_count, Plan
 //   M <= 8       TMA-fed fragment kernel (w4frag.cu): 31.7 / 11.4 / 10.8 /
 //                30.8 us at M = 1 against 39.5 / 12.6 / 12.2 / 28.2 for the
 //                register-fragment kernel and 43 / 18 / 15 / 30 for tcgen05
-//   9..128       tcgen05 skinny kernel with in-kernel dequantisation into
-//                TMEM (stages of 256 k): cluster split-K (mode 2) when the
-//                weight tiles fit one wave, stream-K (mode 1) beyond; at
-//                M = 16 it leads the fragment kernel (44 vs 52 us on
-//                34816 x 5120), whose activation loads grow with M
-//   > 128        GEMV path (one pass per four rows)
+//   9 and up     tcgen05 kernel with in-kernel dequantisation into TMEM
+//                (stages of 256 k, tokens in tiles of up to 128): cluster
+//                split-K (mode 2) when the tiles fit one wave, stream-K
+//                (mode 1) beyond; at M = 16 it leads the fragment kernel (44
+//                vs 52 us on 34816 x 5120), whose activation loads grow with
+//                M.  Above 128 tokens every weight tile is dequantised once
+//                per token tile; the token tiles of a weight tile are
+//                neighbours in the tile order, so its packed weights come
+//                from L2 after the first.
 bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int sm_count, Plan *p, bool query)
 {
     *p = Plan{};
     if (K == 0) return false;
     if (variant == GEMM_VARIANT_AUTO)
-        variant = M > 128 ? GEMM_VARIANT_GEMV : M <= 8 ? GEMM_VARIANT_FRAGMENT : GEMM_VARIANT_SKINNY;
+        variant = M <= 8 ? GEMM_VARIANT_FRAGMENT : GEMM_VARIANT_SKINNY;
     if (variant == GEMM_VARIANT_REGISTER) {
         if (M > 32 || K / group > kW4RegisterMaxGroups) return false;
         p->variant = GEMM_VARIANT_REGISTER;
@@ -367,10 +370,10 @@ bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int
         return true;
     }
     if (variant == GEMM_VARIANT_SKINNY) {
-        if (M > 128) return false;
         int bn = 16;
-        while (bn < M) bn *= 2;
-        const int64_t tiles = (N + kUmmaBM - 1) / kUmmaBM;
+        while (bn < M && bn < 128) bn *= 2;
+        const int64_t tiles_r = (N + kUmmaBM - 1) / kUmmaBM, tiles_q = (M + bn - 1) / bn;
+        const int64_t tiles = tiles_r * tiles_q;
         const int64_t nk = (K + 4 * kUmmaBK - 1) / (4 * kUmmaBK);   // 256-k stages
         const int64_t G = sm_count;
         p->variant = GEMM_VARIANT_SKINNY;
@@ -379,7 +382,7 @@ bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int
         p->bn = bn;
         p->tile_m = bn;
         p->tile_n = kUmmaBM;
-        p->group_r = (int)tiles;
+        p->group_r = tiles_q > 1 ? 1 : (int)tiles_r;   // token tiles of a weight tile run next to each other
         p->ctas_per_sm = 1;
         p->stages = umma_w4_stages(bn);
         if (tiles <= G) {

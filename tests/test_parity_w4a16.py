@@ -55,7 +55,9 @@ SMALL = [(1, 8, 128, 32), (1, 64, 256, 64), (2, 136, 384, 128), (3, 520, 1024, 3
          (4, 1000, 2048, 128), (8, 264, 640, 128), (16, 136, 512, 64), (17, 4104, 256, 128),
          (64, 512, 1024, 128), (128, 392, 1280, 128), (129, 136, 512, 32),
          # K % 64 == 32: the last 64-k sub-tile is half past K (its second group is absent)
-         (16, 264, 608, 32), (40, 136, 4128, 32)]
+         (16, 264, 608, 32), (40, 136, 4128, 32),
+         # more than 128 tokens: several token tiles per weight tile
+         (300, 520, 1024, 128), (1000, 264, 2048, 64), (257, 4104, 256, 32)]
 
 
 @pytest.mark.parametrize("M,N,K,group", SMALL)
@@ -77,6 +79,8 @@ def test_deterministic(g):
 
 W4 = [(M, N, K) for M in (1, 16, 64, 128)
       for (N, K) in ((7168, 5120), (5120, 5120), (34816, 5120), (5120, 17408))]
+# prefill-size token counts (several 128-token tiles per weight tile)
+W4 += [(512, 7168, 5120), (2048, 5120, 17408), (4096, 34816, 5120)]
 
 
 @pytest.mark.parametrize("M,N,K", W4)
