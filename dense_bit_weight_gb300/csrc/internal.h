@@ -49,6 +49,8 @@ struct Plan {
     int bn;                // tcgen05: MMA N (columns of the Y operand per tile)
     int group_r;           // tcgen05: tile-rows per raster group
     int ctas_per_sm;       // tcgen05 skinny: 1 = deep pipeline, 2 = shallow (two CTAs per SM)
+    int whole = 0;         // tcgen05 mode 1: leading tiles done whole (the full waves), then stream-K
+    int sk_grid = 0;       // tcgen05 mode 1: CTAs sharing the stream-K units (0 = all)
     int act_copy;          // W4A16: activations are first copied into the kernels' k order
     int64_t ws_extra;      // W4A16 register variant: fp32 group sums after the copy (floats)
 };

@@ -57,6 +57,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -92,7 +93,9 @@ struct Sched {
     int group_r;                 // raster: tile-rows per group
     int stall;                   // test hook: producer issues nothing (forces the watchdog)
     int split;                   // mode 2: CTAs per tile (cluster size)
-    long long units;             // tiles * nk
+    long long units;             // mode 1: stream-K units, (tiles - whole) * nk
+    int whole;                   // mode 1: leading tiles done whole, round-robin over the grid (the full waves)
+    int sk_grid;                 // mode 1: CTAs sharing the stream-K units (<= grid)
     int epi;                     // fused epilogue (GEMM_EPI_*)
     int pairs;                   // the weight operand's map interleaves (gate, up) rows: 3-D copies
     const uint16_t *bias;        // GEMM_EPI_BIAS: bf16 per weight row (output column)
@@ -117,26 +120,32 @@ __device__ __forceinline__ void tile_coords(const Sched &s, int t, int &tr, int 
     tq = local / rows_in;
 }
 
+// Mode 1: first unit of CTA c's stream-K range (units of tiles >= whole; CTAs
+// c >= sk_grid have an empty range).
 __device__ __forceinline__ long long range_begin(const Sched &s, int c)
 {
-    return (long long)c * s.units / s.grid;
+    const int cc = c < s.sk_grid ? c : s.sk_grid;
+    return (long long)s.whole * s.nk + (long long)cc * s.units / s.sk_grid;
 }
 
-// CTA whose unit range contains unit u (mode 1).
+// CTA whose stream-K range contains unit u (mode 1).
 __device__ __forceinline__ int cta_of_unit(const Sched &s, long long u)
 {
-    return (int)(((u + 1) * s.grid + s.units - 1) / s.units) - 1;
+    const long long v = u - (long long)s.whole * s.nk;
+    return (int)(((v + 1) * s.sk_grid + s.units - 1) / s.units) - 1;
 }
 
 struct SegIter {
     long long u, u_end;
-    int next_tile, count;
-    __device__ SegIter(const Sched &s, int cta)
+    int next_tile, count, sk;   // sk: stream-K segments so far (their workspace slot)
+    int tiles;                  // mode 0: tiles to walk
+    __device__ SegIter(const Sched &s, int cta, int ntiles) : tiles(ntiles)
     {
         count = 0;
         next_tile = cta;
         u = s.mode == 1 ? range_begin(s, cta) : 0;
         u_end = s.mode == 1 ? range_begin(s, cta + 1) : 0;
+        sk = 0;
     }
     __device__ bool next(const Sched &s, Segment &seg)
     {
@@ -149,7 +158,13 @@ struct SegIter {
             seg.kb1 = (int)((long long)(r + 1) * s.nk / s.split);
             seg.slot = 0;
         } else if (s.mode == 0) {
-            if (next_tile >= s.tiles) return false;
+            if (next_tile >= tiles) return false;
+            seg.tile = next_tile;
+            seg.kb0 = 0;
+            seg.kb1 = s.nk;
+            seg.slot = 0;
+            next_tile += s.grid;
+        } else if (next_tile < s.whole) {   // mode 1: this CTA's whole tiles of the full waves first
             seg.tile = next_tile;
             seg.kb0 = 0;
             seg.kb1 = s.nk;
@@ -161,7 +176,8 @@ struct SegIter {
             seg.kb0 = (int)(u % s.nk);
             const long long left = u_end - u;
             seg.kb1 = (int)min((long long)s.nk, seg.kb0 + left);
-            seg.slot = count == 0 ? 0 : 1;
+            seg.slot = sk == 0 ? 0 : 1;
+            ++sk;
             u += seg.kb1 - seg.kb0;
         }
         ++count;
@@ -200,14 +216,19 @@ __device__ __forceinline__ void store_chunk(uint16_t *__restrict__ C, int64_t ld
     }
 }
 
-// store_chunk with the fused epilogue.  Rows of X (SWAP) or columns of Y hold
-// weight rows; with GEMM_EPI_SILU_MUL they come as (gate, up) pairs 2j, 2j + 1
-// for output column j.  SWAP: a thread owns one weight row and its pair
-// partner is the neighbouring lane (every lane of the warp must call this).
+// store_chunk with a fused epilogue (GEMM_EPI_BIAS or GEMM_EPI_SILU_MUL).
+// Rows of X (SWAP) or columns of Y hold weight rows; with GEMM_EPI_SILU_MUL
+// they come as (gate, up) pairs 2j, 2j + 1 for output column j.  SWAP: a
+// thread owns one weight row and its pair partner is the neighbouring lane
+// (every lane of the warp must call this).  Kept out of line so the plain
+// store path keeps its own register allocation.
 template <bool SWAP>
-__device__ __forceinline__ void store_chunk_epi(uint16_t *__restrict__ C, int64_t ldc, int R, int Q, int r,
-                                                int q0, float (&f)[16], const Sched &s)
+__device__ __noinline__ void store_chunk_fused(uint16_t *__restrict__ C, int64_t ldc, int R, int Q, int r, int q0,
+                                               const float *fin, const Sched &s)
 {
+    float f[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) f[j] = fin[j];
     if (s.epi == GEMM_EPI_SILU_MUL) {
         if (SWAP) {
             float u[16];
@@ -252,6 +273,57 @@ __device__ __forceinline__ void store_chunk_epi(uint16_t *__restrict__ C, int64_
     store_chunk<SWAP>(C, ldc, R, Q, r, q0, f);
 }
 
+template <bool SWAP, bool FUSED>
+__device__ __forceinline__ void store_chunk_epi(uint16_t *__restrict__ C, int64_t ldc, int R, int Q, int r, int q0,
+                                                const float (&f)[16], const Sched &s)
+{
+    if (!FUSED || s.epi == GEMM_EPI_NONE) store_chunk<SWAP>(C, ldc, R, Q, r, q0, f);
+    else store_chunk_fused<SWAP>(C, ldc, R, Q, r, q0, f, s);
+}
+
+// The cluster split-K reduction's store of one summed float4 (tokens q0 .. q0 + 3
+// of row r) with a fused epilogue; paired: lanes rl, rl ^ 1 hold rows re, re + 1
+// (every lane of the warp calls this).
+template <bool SWAP>
+__device__ __noinline__ void cluster_store_fused(uint16_t *__restrict__ C, int64_t ldc, int R, int Q, int r, int q0,
+                                                 bool paired, bool odd, const float *ain, const Sched &s)
+{
+    float a[4] = {ain[0], ain[1], ain[2], ain[3]};
+    if (paired) {
+        float x[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) x[j] = __shfl_xor_sync(0xffffffffu, a[j], 1);
+        const int re = r - (odd ? 1 : 0);   // the pair's even row
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {    // even lane: tokens 0, 1; odd lane: tokens 2, 3
+            const int j = odd ? 2 + jj : jj;
+            float lo = odd ? x[j] : a[j], hi = odd ? a[j] : x[j];
+            const int q = q0 + j;
+            if (q < Q && re < R) {
+                if (s.epi == GEMM_EPI_SILU_MUL) {   // rows re, re + 1: gate and up of column re / 2
+                    C[(int64_t)q * ldc + (re >> 1)] = f32_to_bf16_rn(silu_mul(lo, hi));
+                    continue;
+                }
+                lo += bf16lo(s.bias[re]);
+                if (re + 1 < R) hi += bf16lo(s.bias[re + 1]);
+                uint16_t *dst = C + (int64_t)q * ldc + re;
+                if (re + 1 < R) *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2_rn(lo, hi);
+                else *dst = f32_to_bf16_rn(lo);
+            }
+        }
+    } else if (r < R && s.epi == GEMM_EPI_BIAS) {   // (pairs are only split in twos)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int q = q0 + j;
+            if (q < Q) {
+                const float b = bf16lo(s.bias[SWAP ? r : q]);
+                if (SWAP) C[(int64_t)q * ldc + r] = f32_to_bf16_rn(a[j] + b);
+                else C[(int64_t)r * ldc + q] = f32_to_bf16_rn(a[j] + b);
+            }
+        }
+    }
+}
+
 constexpr uint32_t tmem_cols_for(int n)
 {
     return n <= 32 ? 32u : n <= 64 ? 64u : n <= 128 ? 128u : n <= 256 ? 256u : 512u;
@@ -285,14 +357,15 @@ struct Layout {
     static constexpr int SMEM = GRP_OFF + GRP_BYTES + 1024;   // + slack to align the base to 1024
 };
 
-template <int BN, int STAGES, bool SWAP, int MINB, bool W4>
+// FUSED: the instance serves gemm_bf16_fused (epilogues, gate/up pair maps);
+// plain calls run the FUSED = false instances, which carry none of that code.
+template <int BN, int STAGES, bool SWAP, int MINB, bool W4, bool FUSED>
 __global__ void __launch_bounds__(threads_for(W4), MINB)
 k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
-       uint16_t *__restrict__ C, int R, int Q, int64_t ldc, const Sched sched_in,
+       uint16_t *__restrict__ C, int R, int Q, int64_t ldc, const Sched sched,
        float *__restrict__ ws, int *__restrict__ counters, int *__restrict__ d_error, const W4Args w4)
 {
     using L = Layout<BN, STAGES, W4>;
-    Sched sched = sched_in;   // (the grouped GEMM sets its tile count on the device)
     // W4A16 takes all 512 columns: two accumulators below kXCol, the
     // dequantised tiles above.  Its shared memory admits one CTA per SM, so
     // the allocation never waits on a CTA of the same cluster.
@@ -368,6 +441,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
     // t % tiles_q), and an expert with no rows owns no tile.
     int *gend = reinterpret_cast<int *>(smem + L::GRP_OFF);
     int *gpre = gend + kMaxExperts;
+    int ntiles = sched.tiles;   // mode 0 tile count (the grouped GEMM finds its own here)
     if constexpr (L::GRP_BYTES > 0) {
         if (sched.gends) {
             ptx::pdl_wait();
@@ -407,7 +481,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                 }
             }
             __syncthreads();
-            sched.tiles = gpre[sched.groups] * sched.tiles_q;
+            ntiles = gpre[sched.groups] * sched.tiles_q;
         }
     }
     // tile t -> X rows from xrow, Y rows from yrow, C rows below rlim, C columns from qb
@@ -460,7 +534,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
             uint32_t phase = 0;
             long long issued = 0;
             {
-                SegIter pre(sched, blockIdx.x);
+                SegIter pre(sched, blockIdx.x, ntiles);
                 Segment s0;
                 if (packed && pre.next(sched, s0) && !sched.stall) {
                     int tr, tq;
@@ -470,7 +544,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                 }
                 ptx::pdl_wait();
             }
-            SegIter it(sched, blockIdx.x);
+            SegIter it(sched, blockIdx.x, ntiles);
             Segment seg;
             bool ok = true;
             while (ok && it.next(sched, seg)) {
@@ -521,22 +595,22 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
             {
                 // warm L2 with the first stages of this CTA's work while the
                 // previous kernel drains, then wait for it
-                SegIter pre(sched, blockIdx.x);
+                SegIter pre(sched, blockIdx.x, ntiles);
                 Segment s0;
                 if (pre.next(sched, s0) && !sched.stall) {
                     int xrow, yrow, rlim, qb;
                     geo(s0.tile, xrow, yrow, rlim, qb);
                     const int kend = min(s0.kb1, s0.kb0 + STAGES);
                     for (int kb = s0.kb0; kb < kend; ++kb) {
-                        if (SWAP && sched.pairs) ptx::tma_prefetch_l2_3d(&tmX, kb * BK, 0, xrow / 2);
+                        if (FUSED && SWAP && sched.pairs) ptx::tma_prefetch_l2_3d(&tmX, kb * BK, 0, xrow / 2);
                         else ptx::tma_prefetch_l2_2d(&tmX, kb * BK, xrow);
-                        if (!SWAP && sched.pairs) ptx::tma_prefetch_l2_3d(&tmY, kb * BK, 0, yrow / 2);
+                        if (FUSED && !SWAP && sched.pairs) ptx::tma_prefetch_l2_3d(&tmY, kb * BK, 0, yrow / 2);
                         else ptx::tma_prefetch_l2_2d(&tmY, kb * BK, yrow);
                     }
                 }
                 ptx::pdl_wait();
             }
-            SegIter it(sched, blockIdx.x);
+            SegIter it(sched, blockIdx.x, ntiles);
             Segment seg;
             bool ok = true;
             while (ok && it.next(sched, seg)) {
@@ -552,9 +626,9 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                         const uint32_t xs = sbase + stage * L::STAGE_BYTES;
                         // (gate, up) pairs: the 3-D view [row / 2][gate or up][k] puts the
                         // pair's rows next to each other in the tile
-                        if (SWAP && sched.pairs) ptx::tma_load_3d(xs, &tmX, FULL(stage), kb * BK, 0, xrow / 2, pol_x);
+                        if (FUSED && SWAP && sched.pairs) ptx::tma_load_3d(xs, &tmX, FULL(stage), kb * BK, 0, xrow / 2, pol_x);
                         else ptx::tma_load_2d(xs, &tmX, FULL(stage), kb * BK, xrow, pol_x);
-                        if (!SWAP && sched.pairs)
+                        if (FUSED && !SWAP && sched.pairs)
                             ptx::tma_load_3d(xs + L::X_BYTES, &tmY, FULL(stage), kb * BK, 0, yrow / 2, pol_y);
                         else ptx::tma_load_2d(xs + L::X_BYTES, &tmY, FULL(stage), kb * BK, yrow, pol_y);
                         ++issued;
@@ -580,7 +654,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
         // commit (see mma_bf16_warp).
         int stage = 0, acc = 0, xb = 0;
         uint32_t phase = 0, acc_phase = 0, xphase = 0;
-        SegIter it(sched, blockIdx.x);
+        SegIter it(sched, blockIdx.x, ntiles);
         Segment seg;
         bool ok = true;
         while (ok && it.next(sched, seg)) {
@@ -684,7 +758,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
         ptx::pdl_wait();                           // scales and zeros come from global memory
         int stage = 0, xsel = 0, astage = 0;
         uint32_t phase = 0, xphase = 0, aphase = 0;
-        SegIter it(sched, blockIdx.x);
+        SegIter it(sched, blockIdx.x, ntiles);
         Segment seg;
         bool ok = true;
         while (ok && it.next(sched, seg)) {
@@ -792,7 +866,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
         ptx::pdl_wait();                    // C, workspace and counters may be in use by the previous kernel
         int acc = 0;
         uint32_t acc_phase = 0;
-        SegIter it(sched, blockIdx.x);
+        SegIter it(sched, blockIdx.x, ntiles);
         Segment seg;
         while (it.next(sched, seg)) {
             if (!wait_bar_warp(TFULL(acc), acc_phase, abort_flag, d_error)) break;
@@ -814,7 +888,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
 #pragma unroll
                 for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(v[j]);
                 if (whole) {
-                    store_chunk_epi<SWAP>(C, ldc, rlim, Q, r, qb + c, f, sched);
+                    store_chunk_epi<SWAP, FUSED>(C, ldc, rlim, Q, r, qb + c, f, sched);
                 } else if (cluster_split) {
                     float4 *prow = reinterpret_cast<float4 *>(smem + row * PSTRIDE + c * 4);
 #pragma unroll
@@ -898,7 +972,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                         f[4 * u + 2] = a4[4 * j16 + u].z;
                         f[4 * u + 3] = a4[4 * j16 + u].w;
                     }
-                    store_chunk_epi<SWAP>(C, ldc, rlim, Q, r, qb + cb * 4 + j16 * 16, f, sched);
+                    store_chunk_epi<SWAP, FUSED>(C, ldc, rlim, Q, r, qb + cb * 4 + j16 * 16, f, sched);
                 }
             }
         }
@@ -957,7 +1031,9 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                     }
                 }
                 const int r = tr * BM + r0 + rl;
-                if (paired) {
+                if (FUSED && sched.epi != GEMM_EPI_NONE) {
+                    cluster_store_fused<SWAP>(C, ldc, R, Q, r, qb + c4 * 4, paired, rl & 1, a, sched);
+                } else if (paired) {
                     float x[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) x[j] = __shfl_xor_sync(0xffffffffu, a[j], 1);
@@ -966,30 +1042,21 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
 #pragma unroll
                     for (int jj = 0; jj < 2; ++jj) {    // even lane: tokens 0, 1; odd lane: tokens 2, 3
                         const int j = odd ? 2 + jj : jj;
-                        float lo = odd ? x[j] : a[j], hi = odd ? a[j] : x[j];
+                        const float lo = odd ? x[j] : a[j], hi = odd ? a[j] : x[j];
                         const int q = qb + c4 * 4 + j;
                         if (q < Q && re < R) {
-                            if (sched.epi == GEMM_EPI_SILU_MUL) {   // rows re, re + 1: gate and up of column re / 2
-                                C[(int64_t)q * ldc + (re >> 1)] = f32_to_bf16_rn(silu_mul(lo, hi));
-                                continue;
-                            }
-                            if (sched.epi == GEMM_EPI_BIAS) {
-                                lo += bf16lo(sched.bias[re]);
-                                if (re + 1 < R) hi += bf16lo(sched.bias[re + 1]);
-                            }
                             uint16_t *dst = C + (int64_t)q * ldc + re;
                             if (re + 1 < R) *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2_rn(lo, hi);
                             else *dst = f32_to_bf16_rn(lo);
                         }
                     }
-                } else if (r < R && sched.epi != GEMM_EPI_SILU_MUL) {   // (pairs are only split in twos)
+                } else if (r < R) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const int q = qb + c4 * 4 + j;
                         if (q < Q) {
-                            const float b = sched.epi == GEMM_EPI_BIAS ? bf16lo(sched.bias[SWAP ? r : q]) : 0.f;
-                            if (SWAP) C[(int64_t)q * ldc + r] = f32_to_bf16_rn(a[j] + b);
-                            else C[(int64_t)r * ldc + q] = f32_to_bf16_rn(a[j] + b);
+                            if (SWAP) C[(int64_t)q * ldc + r] = f32_to_bf16_rn(a[j]);
+                            else C[(int64_t)r * ldc + q] = f32_to_bf16_rn(a[j]);
                         }
                     }
                 }
@@ -1065,12 +1132,12 @@ bool make_map_packed(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K)
     return make_map_words(m, ptr, rows, K, BM);
 }
 
-template <int BN, int STAGES, bool SWAP, int MINB, bool W4 = false>
+template <int BN, int STAGES, bool SWAP, int MINB, bool W4 = false, bool FUSED = false>
 cudaError_t launch_t(const CUtensorMap &mx, const CUtensorMap &my, uint16_t *C, int R, int Q, int64_t ldc,
                      const Sched &s, const LaunchCtx &c, const W4Args &w4 = W4Args{})
 {
     using L = Layout<BN, STAGES, W4>;
-    auto kern = k_umma<BN, STAGES, SWAP, MINB, W4>;
+    auto kern = k_umma<BN, STAGES, SWAP, MINB, W4, FUSED>;
     static std::once_flag once[64];
     static cudaError_t attr_err[64];
     int dev = 0;
@@ -1139,7 +1206,7 @@ template <int BN, int STAGES, bool SWAP, int MINB, bool W4 = false>
 int cluster_capacity_t(int cluster)
 {
     using L = Layout<BN, STAGES, W4>;
-    auto kern = k_umma<BN, STAGES, SWAP, MINB, W4>;
+    auto kern = k_umma<BN, STAGES, SWAP, MINB, W4, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM) != cudaSuccess)
         return -1;
     cudaLaunchConfig_t cfg = {};
@@ -1265,6 +1332,8 @@ cudaError_t launch_umma_w4a16(const GemmArgs &a, const Plan &p, const LaunchCtx 
     s.nk = (int)((a.K + 4 * BK - 1) / (4 * BK));   // 256-k stages
     s.grid = p.grid;
     s.group_r = p.group_r > 0 ? p.group_r : s.tiles_r;
+    s.whole = 0;
+    s.sk_grid = p.grid;
     s.units = (long long)s.tiles * s.nk;
     s.stall = g_debug_stall;
     s.split = p.split;
@@ -1280,6 +1349,36 @@ cudaError_t launch_umma_w4a16(const GemmArgs &a, const Plan &p, const LaunchCtx 
     default: return cudaErrorInvalidValue;
     }
 }
+
+namespace {
+template <bool FUSED>
+cudaError_t launch_bf16_t(const CUtensorMap &mx, const CUtensorMap &my, uint16_t *C, int r, int q, int64_t ldc,
+                          const Sched &s, const Plan &p, const LaunchCtx &c, bool swap)
+{
+    if (swap && p.ctas_per_sm == 1) {
+        switch (p.bn) {
+        case 16: return launch_t<16, 8, true, 1, false, FUSED>(mx, my, C, r, q, ldc, s, c);
+        case 32: return launch_t<32, 8, true, 1, false, FUSED>(mx, my, C, r, q, ldc, s, c);
+        case 64: return launch_t<64, 8, true, 1, false, FUSED>(mx, my, C, r, q, ldc, s, c);
+        case 128: return launch_t<128, 6, true, 1, false, FUSED>(mx, my, C, r, q, ldc, s, c);
+        default: return cudaErrorInvalidValue;
+        }
+    }
+    if (swap) {
+        switch (p.bn) {
+        case 16: return launch_t<16, 6, true, 2, false, FUSED>(mx, my, C, r, q, ldc, s, c);
+        case 32: return launch_t<32, 5, true, 2, false, FUSED>(mx, my, C, r, q, ldc, s, c);
+        case 64: return launch_t<64, 4, true, 2, false, FUSED>(mx, my, C, r, q, ldc, s, c);
+        case 128: return launch_t<128, 3, true, 2, false, FUSED>(mx, my, C, r, q, ldc, s, c);
+        default: return cudaErrorInvalidValue;
+        }
+    }
+    switch (p.bn) {
+    case 256: return launch_t<256, 4, false, 1, false, FUSED>(mx, my, C, r, q, ldc, s, c);
+    default: return cudaErrorInvalidValue;
+    }
+}
+}  // namespace
 
 cudaError_t launch_umma_bf16(const GemmArgs &a, const Plan &p, const LaunchCtx &c)
 {
@@ -1303,7 +1402,11 @@ cudaError_t launch_umma_bf16(const GemmArgs &a, const Plan &p, const LaunchCtx &
     s.nk = (int)((a.K + BK - 1) / BK);
     s.grid = p.grid;
     s.group_r = p.group_r > 0 ? p.group_r : s.tiles_r;
-    s.units = (long long)s.tiles * s.nk;
+    s.whole = p.mode == 1 ? p.whole : 0;
+    // (a caller may shrink the grid to fit a fixed workspace: every CTA sharing
+    // the stream-K units must exist)
+    s.sk_grid = p.mode == 1 && p.sk_grid > 0 ? std::min(p.sk_grid, p.grid) : p.grid;
+    s.units = (long long)(s.tiles - s.whole) * s.nk;
     s.stall = g_debug_stall;
     s.epi = a.epi;
     s.pairs = pairs ? 1 : 0;
@@ -1313,30 +1416,9 @@ cudaError_t launch_umma_bf16(const GemmArgs &a, const Plan &p, const LaunchCtx &
     s.gN = (int)a.N;
     if (a.gends && (swap || p.mode != 0 || p.bn != 256)) return cudaErrorInvalidValue;
     uint16_t *C = (uint16_t *)a.C;
-    const int r = (int)R, q = (int)Q;
     s.split = p.split;
-    if (swap && p.ctas_per_sm == 1) {
-        switch (p.bn) {
-        case 16: return launch_t<16, 8, true, 1>(mx, my, C, r, q, a.ldc, s, c);
-        case 32: return launch_t<32, 8, true, 1>(mx, my, C, r, q, a.ldc, s, c);
-        case 64: return launch_t<64, 8, true, 1>(mx, my, C, r, q, a.ldc, s, c);
-        case 128: return launch_t<128, 6, true, 1>(mx, my, C, r, q, a.ldc, s, c);
-        default: return cudaErrorInvalidValue;
-        }
-    }
-    if (swap) {
-        switch (p.bn) {
-        case 16: return launch_t<16, 6, true, 2>(mx, my, C, r, q, a.ldc, s, c);
-        case 32: return launch_t<32, 5, true, 2>(mx, my, C, r, q, a.ldc, s, c);
-        case 64: return launch_t<64, 4, true, 2>(mx, my, C, r, q, a.ldc, s, c);
-        case 128: return launch_t<128, 3, true, 2>(mx, my, C, r, q, a.ldc, s, c);
-        default: return cudaErrorInvalidValue;
-        }
-    }
-    switch (p.bn) {
-    case 256: return launch_t<256, 4, false, 1>(mx, my, C, r, q, a.ldc, s, c);
-    default: return cudaErrorInvalidValue;
-    }
+    return a.epi != GEMM_EPI_NONE ? launch_bf16_t<true>(mx, my, C, (int)R, (int)Q, a.ldc, s, p, c, swap)
+                                  : launch_bf16_t<false>(mx, my, C, (int)R, (int)Q, a.ldc, s, p, c, swap);
 }
 
 }  // namespace dbw

@@ -181,3 +181,13 @@ def test_fused_epilogue_argument_errors():
     sms = 152
     for M in (1, 8, 128, 4096):
         assert g.gemm_bf16_plan(M, 2 * 12288, 4096, num_sms=sms)["variant"] in (1, 2, 3)
+
+
+def test_prefill_last_wave_split():
+    # a last wave a quarter to half full is split along K (2 or 3 CTAs per
+    # leftover tile, whole tiles before); a smaller leftover stays whole tiles
+    from dense_bit_weight_gb300 import gemm as g
+    sms = 152
+    assert g.gemm_bf16_plan(1024, 6144, 4096, num_sms=sms)["split"] == 3      # 192 tiles: 152 + 40
+    assert g.gemm_bf16_plan(4096, 4096, 4096, num_sms=sms)["split"] == 2      # 512 tiles: 456 + 56
+    assert g.gemm_bf16_plan(4096, 24576, 4096, num_sms=sms)["split"] == 1     # 3072 tiles: 3040 + 32
