@@ -1,7 +1,11 @@
 """Run one GEMM shape repeatedly on the GPU (for profiling and quick timing).
 
     python -m dense_bit_weight_gb300.run_case --M 1 --N 24576 --K 4096 \
-        [--kind bf16|w4a16] [--variant auto|gemv|skinny|prefill] [--reps 4] [--copies 0]
+        [--kind bf16|w4a16|silu_mul|grouped] [--variant auto|gemv|skinny|prefill]
+        [--groups G] [--reps 4] [--copies 0]
+
+--kind silu_mul runs the fused gate/up projection (C [M,N], weights 2N rows);
+--kind grouped runs the grouped GEMM with M tokens split evenly over G experts.
 
 Weights are drawn on the device with torch's seeded generator; `--copies`
 weight copies (0 = enough to exceed three L2 sizes) are used round robin so
@@ -21,7 +25,8 @@ def main(argv=None):
     ap.add_argument("--M", type=int, required=True)
     ap.add_argument("--N", type=int, required=True)
     ap.add_argument("--K", type=int, required=True)
-    ap.add_argument("--kind", choices=["bf16", "w4a16"], default="bf16")
+    ap.add_argument("--kind", choices=["bf16", "w4a16", "silu_mul", "grouped"], default="bf16")
+    ap.add_argument("--groups", type=int, default=8)
     ap.add_argument("--variant", default="auto")
     ap.add_argument("--group", type=int, default=128)
     ap.add_argument("--reps", type=int, default=4)
@@ -36,11 +41,25 @@ def main(argv=None):
     gen = torch.Generator(device=dev)
     gen.manual_seed(0)
     M, N, K = a.M, a.N, a.K
-    wbytes = N * K * 2 if a.kind == "bf16" else N * K // 2
+    NB = 2 * N if a.kind == "silu_mul" else a.groups * N if a.kind == "grouped" else N   # weight rows
+    wbytes = NB * K * 2 if a.kind != "w4a16" else N * K // 2
     copies = a.copies or max(1, min(16, math.ceil(3 * 130e6 / wbytes)))
     A = torch.randn((M, K), generator=gen, device=dev).to(torch.bfloat16)
     C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    if a.kind == "bf16":
+    if a.kind == "silu_mul":
+        Bs = [(torch.randn((NB, K), generator=gen, device=dev) * K ** -0.5).to(torch.bfloat16)
+              for _ in range(copies)]
+        plan = g.gemm_bf16_plan(M, NB, K, a.variant)
+        fn = lambda i: g.gemm_bf16_fused(A, Bs[i % copies], C=C, epilogue="silu_mul", variant=a.variant)
+        work = {"GB": 2 * (M * K + NB * K + M * N) / 1e9, "TFLOP": 2 * M * NB * K / 1e12}
+    elif a.kind == "grouped":
+        Bs = [(torch.randn((a.groups, N, K), generator=gen, device=dev) * K ** -0.5).to(torch.bfloat16)
+              for _ in range(copies)]
+        ends = torch.tensor([M * (e + 1) // a.groups for e in range(a.groups)], dtype=torch.int32, device=dev)
+        plan = {"variant_name": "prefill (grouped)", "groups": a.groups}
+        fn = lambda i: g.gemm_bf16_grouped(A, Bs[i % copies], ends, C=C)
+        work = {"GB": 2 * (M * K + NB * K + M * N) / 1e9, "TFLOP": 2 * M * N * K / 1e12}
+    elif a.kind == "bf16":
         Bs = [(torch.randn((N, K), generator=gen, device=dev) * K ** -0.5).to(torch.bfloat16)
               for _ in range(copies)]
         plan = g.gemm_bf16_plan(M, N, K, a.variant)
