@@ -437,8 +437,8 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
     // g*gN .. g*gN + gN - 1 of B.  The row ends come from the previous kernel
     // (a router), so every thread waits for it; warp 0 clamps them into a
     // non-decreasing sequence within [0, R] and writes the exclusive prefix of
-    // the experts' m-tile counts; tile t is then (m-tile t / tiles_q, n-tile
-    // t % tiles_q), and an expert with no rows owns no tile.
+    // the experts' m-tile counts; expert g then owns the tiles from
+    // gpre[g] * tiles_q, m-tile fastest, and an expert with no rows owns none.
     int *gend = reinterpret_cast<int *>(smem + L::GRP_OFF);
     int *gpre = gend + kMaxExperts;
     int ntiles = sched.tiles;   // mode 0 tile count (the grouped GEMM finds its own here)
@@ -487,17 +487,22 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
     // tile t -> X rows from xrow, Y rows from yrow, C rows below rlim, C columns from qb
     auto geo = [&](int t, int &xrow, int &yrow, int &rlim, int &qb) {
         if (L::GRP_BYTES > 0 && sched.gends) {
-            const int mt = t / sched.tiles_q, tq = t - mt * sched.tiles_q;
+            const int mt = t / sched.tiles_q;   // expert g owns tiles [gpre[g], gpre[g + 1]) * tiles_q
             int lo = 0, hi = sched.groups;   // the expert: largest lo < G with gpre[lo] <= mt
             while (hi - lo > 1) {
                 const int mid = (lo + hi) >> 1;
                 if (gpre[mid] <= mt) lo = mid;
                 else hi = mid;
             }
-            xrow = (lo > 0 ? gend[lo - 1] : 0) + (mt - gpre[lo]) * BM;
+            // within the expert, m-tiles vary fastest: the CTAs that read one
+            // weight tile run side by side, so it comes from DRAM once
+            const int nm = gpre[lo + 1] - gpre[lo];               // m-tiles of the expert
+            const int local = t - gpre[lo] * sched.tiles_q;
+            const int tqe = local / nm, mte = local - tqe * nm;
+            xrow = (lo > 0 ? gend[lo - 1] : 0) + mte * BM;
             rlim = gend[lo];
-            yrow = lo * sched.gN + tq * BN;
-            qb = tq * BN;
+            yrow = lo * sched.gN + tqe * BN;
+            qb = tqe * BN;
         } else {
             int tr, tq;
             tile_coords(sched, t, tr, tq);
