@@ -294,6 +294,42 @@ __device__ __forceinline__ void cluster_sync()
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
+// The two halves of the cluster barrier: arrive and wait (acquire).  Each
+// thread alternates them; work placed between them overlaps the barrier.  The
+// arrive is relaxed: it orders control only, and publishes none of this
+// thread's memory writes (a release would first wait for every write in
+// flight, remote ones included).
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+
+// 16-byte store into a (possibly other) CTA's shared memory of this cluster,
+// counted in bytes on that CTA's mbarrier; both addresses are shared::cluster.
+__device__ __forceinline__ void st_async_v4(uint32_t caddr, uint4 v, uint32_t mbar_cluster)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1,%2,%3,%4}, [%5];" ::"r"(
+                     caddr),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(mbar_cluster)
+                 : "memory");
+}
+
+// 2-D tiled store shared -> global (c0 innermost, in elements); out-of-range
+// elements of the box are not written.  Completion through the bulk group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, uint32_t src, int32_t c0, int32_t c1)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(src), "r"(c0), "r"(c1)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// every committed bulk store has finished reading shared memory
+__device__ __forceinline__ void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+__device__ __forceinline__ void sts16(uint32_t saddr, uint16_t v)
+{
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(saddr), "h"(v) : "memory");
+}
+
 // Address of the same shared-memory location in CTA `rank` of this cluster.
 __device__ __forceinline__ uint32_t map_cluster(uint32_t saddr, uint32_t rank)
 {

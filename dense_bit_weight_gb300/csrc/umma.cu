@@ -102,6 +102,7 @@ struct Sched {
     const int *gends;            // grouped GEMM (prefill kernel, mode 0): cumulative token-row ends per expert
     int groups;                  //   experts
     int gN;                      //   weight rows per expert (columns of C)
+    int tma_c;                   // mode 2: each CTA's block of the tile leaves through a TMA store (tmC)
 };
 
 
@@ -338,7 +339,14 @@ constexpr uint32_t tmem_cols_for(int n)
 // tiles, released by the MMA.  The dequantised weights live in tensor memory
 // (kNX stages of 128 x 256 bf16 from column kXCol), where the MMA reads its A
 // operand.
-template <int BN, int STAGES, bool W4 = false>
+// Cluster split-K (CS: the deep skinny instances): the S CTAs of a cluster
+// exchange fp32 partial rows in a region of S slices of up to BM / S + 1 rows
+// (slice s holds CTA s's rows for this CTA's block of the tile), followed by
+// a bf16 staging tile for the TMA store of the block.  The region has its own
+// shared memory when that fits beside the ring (RED_OWN: partials may arrive
+// while this CTA is still in its main loop), otherwise it reuses the ring once
+// every CTA of the cluster has drained its pipeline.
+template <int BN, int STAGES, bool W4 = false, bool CS = false>
 struct Layout {
     static constexpr int KSTAGE = W4 ? 4 * BK : BK;                 // k per ring stage
     static constexpr int X_BYTES = W4 ? BM * KSTAGE / 2 : BM * BK * 2;
@@ -354,7 +362,15 @@ struct Layout {
     // grouped GEMM (prefill kernel only): expert row ends [kMaxExperts], m-tile prefix [kMaxExperts + 1]
     static constexpr int GRP_OFF = MISC_OFF + 16;
     static constexpr int GRP_BYTES = (!W4 && BN == 256) ? (2 * kMaxExperts + 4) * 4 : 0;
-    static constexpr int SMEM = GRP_OFF + GRP_BYTES + 1024;   // + slack to align the base to 1024
+    static constexpr int RSTRIDE = BN * 4 + 16;         // bytes per partial row (conflict-free 16-byte reads)
+    static constexpr int RED_BYTES = CS ? (BM + 8) * RSTRIDE : 0;
+    static constexpr int STG_BYTES = CS ? 64 * BN * 2 : 0;   // bf16 [BN][BM / S], S >= 2
+    static constexpr int OWN_OFF = (GRP_OFF + GRP_BYTES + 127) / 128 * 128;
+    static constexpr bool RED_OWN = CS && OWN_OFF + RED_BYTES + STG_BYTES + 1024 <= 227 * 1024;
+    static constexpr int RED_OFF = RED_OWN ? OWN_OFF : 0;
+    static constexpr int STG_OFF = RED_OFF + (RED_BYTES + 127) / 128 * 128;
+    static constexpr int SMEM = (RED_OWN ? STG_OFF + STG_BYTES : GRP_OFF + GRP_BYTES) + 1024;   // + slack to align the base
+    static_assert(!CS || RED_OWN || STG_OFF + STG_BYTES <= SZ_OFF, "the split-K region must fit the ring");
 };
 
 // FUSED: the instance serves gemm_bf16_fused (epilogues, gate/up pair maps);
@@ -362,10 +378,10 @@ struct Layout {
 template <int BN, int STAGES, bool SWAP, int MINB, bool W4, bool FUSED>
 __global__ void __launch_bounds__(threads_for(W4), MINB)
 k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
-       uint16_t *__restrict__ C, int R, int Q, int64_t ldc, const Sched sched,
+       const __grid_constant__ CUtensorMap tmC, uint16_t *__restrict__ C, int R, int Q, int64_t ldc, const Sched sched,
        float *__restrict__ ws, int *__restrict__ counters, int *__restrict__ d_error, const W4Args w4)
 {
-    using L = Layout<BN, STAGES, W4>;
+    using L = Layout<BN, STAGES, W4, SWAP && MINB == 1>;
     // W4A16 takes all 512 columns: two accumulators below kXCol, the
     // dequantised tiles above.  Its shared memory admits one CTA per SM, so
     // the allocation never waits on a CTA of the same cluster.
@@ -393,6 +409,10 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile uint32_t *abort_flag = misc + 1;
+    // cluster split-K runs only in the deep skinny kernels (the planner never
+    // asks another instance for it; they lack the shared memory for it)
+    constexpr bool kCanClusterSplit = SWAP && MINB == 1;
+    const bool cluster_split = kCanClusterSplit && sched.mode == 2 && sched.split > 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -417,6 +437,11 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
         }
         misc[1] = 0;
         misc[2] = 0;
+        if (cluster_split) {   // this CTA's block receives S - 1 slices of BN fp32 per row
+            const uint32_t rank = ptx::cluster_ctarank(), S = (uint32_t)sched.split;
+            const uint32_t nrows = (rank + 1) * BM / S - rank * BM / S;
+            ptx::mbar_arrive_expect_tx(REDUCE, (S - 1) * nrows * BN * 4);
+        }
         ptx::fence_mbar_init();
     }
     if (warp == 1) {
@@ -426,11 +451,15 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&tmX);
         ptx::prefetch_tmap(&tmY);
+        if (sched.tma_c) ptx::prefetch_tmap(&tmC);
     }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = misc[0];
+    // phase A of the cluster barrier: with its own region, a CTA may receive
+    // partials as soon as every CTA's barriers are initialised
+    if (L::RED_OWN && cluster_split) ptx::cluster_arrive();
 
     // Grouped GEMM (prefill kernel, whole tiles): expert g owns the token rows
     // [end[g-1], end[g]) of A and C and multiplies them by its weight rows
@@ -517,16 +546,8 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
     // its first global-memory access.  The MMA role touches only shared and
     // tensor memory and does not wait.
     ptx::pdl_launch_dependents();
-    // cluster split-K runs only in the deep skinny kernels (the planner never
-    // asks another instance for it; they lack the shared memory for it)
-    constexpr bool kCanClusterSplit = SWAP && MINB == 1;
-    const bool cluster_split = kCanClusterSplit && sched.mode == 2 && sched.split > 1;
-    constexpr int PSTRIDE = BN * 4 + 16;   // bytes per row of the mode-2 partial tile in smem
-    // mode-2 partial [128][PSTRIDE] at ring offset 0, incoming slices after it
-    constexpr int IN_OFF = BM * PSTRIDE;
-    // (the rings are free by then)
-    static_assert(!kCanClusterSplit || (BM + 8 + BM) * PSTRIDE <= L::SZ_OFF, "partials must fit the ring");
 
+    bool have_acc = false;   // cluster split: this epilogue warp holds the tile's accumulator
     if (W4 && (warp == 0 || warp == kActWarp)) {
         // ------------------------------------------------------------ W4A16 producers
         // warp 0 streams the packed weights, warp kActWarp the activation tiles;
@@ -876,6 +897,10 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
         while (it.next(sched, seg)) {
             if (!wait_bar_warp(TFULL(acc), acc_phase, abort_flag, d_error)) break;
             ptx::tc_fence_after();
+            if (cluster_split) {   // one tile per CTA: its partial leaves from TMEM in the cluster tail
+                have_acc = true;
+                break;
+            }
             int xrow, yrow, rlim, qb;
             geo(seg.tile, xrow, yrow, rlim, qb);
             const int r = xrow + row;
@@ -894,12 +919,6 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                 for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(v[j]);
                 if (whole) {
                     store_chunk_epi<SWAP, FUSED>(C, ldc, rlim, Q, r, qb + c, f, sched);
-                } else if (cluster_split) {
-                    float4 *prow = reinterpret_cast<float4 *>(smem + row * PSTRIDE + c * 4);
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        prow[u] = make_float4(f[4 * u], f[4 * u + 1], f[4 * u + 2], f[4 * u + 3]);
-                    if (c + 16 >= BN) ptx::fence_proxy_async_smem();   // the bulk copies read these rows
                 } else {
 #pragma unroll
                     for (int u = 0; u < 4; ++u)
@@ -913,7 +932,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                 acc = 0;
                 acc_phase ^= 1u;
             }
-            if (whole || cluster_split) continue;
+            if (whole) continue;
 
             // ---- stream-K fixup: the last contributor of this tile sums the partials
             const int t = seg.tile;
@@ -984,25 +1003,59 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
     }
 
     if (cluster_split) {
+        // Cluster split-K reduction.  CTA `rank` owns rows [r0, r1) of the tile:
+        // every CTA sends those rows of its partial to the owner (slice `rank`
+        // of the owner's region), the owner sums the S slices in rank order
+        // (increasing k) and stores its block of C.
         const int S = sched.split;
         const int rank = (int)ptx::cluster_ctarank();
         const int nmax = (BM + S - 1) / S;                    // rows per owner, at most
         const int r0 = rank * BM / S, r1 = (rank + 1) * BM / S, nrows = r1 - r0;
-        if (threadIdx.x == 64)   // this CTA receives S-1 slices of its nrows rows
-            ptx::mbar_arrive_expect_tx(REDUCE, (uint32_t)((S - 1) * nrows * PSTRIDE));
-        // every CTA's pipeline has drained and its partial is in shared memory
-        ptx::cluster_sync();
-        if (threadIdx.x == 64) {
-            for (int o = 0; o < S; ++o) {
-                if (o == rank) continue;
-                const int o0 = o * BM / S, o1 = (o + 1) * BM / S;
-                const uint32_t src = sbase + (uint32_t)(o0 * PSTRIDE);
-                const uint32_t dst = ptx::map_cluster(sbase + (uint32_t)(IN_OFF + rank * nmax * PSTRIDE), (uint32_t)o);
-                ptx::bulk_copy_to_cluster(dst, src, (uint32_t)((o1 - o0) * PSTRIDE), ptx::map_cluster(REDUCE, (uint32_t)o));
+        const bool epi = warp >= 2 && warp < 6;
+        // phase A: every CTA's barriers are initialised (own region) or every
+        // CTA's pipeline has drained, so the ring may take the partials
+        if (!L::RED_OWN) ptx::cluster_arrive();
+        ptx::cluster_wait();
+        __syncwarp();   // (the cluster barrier's wait is per thread)
+        const uint32_t red = sbase + (uint32_t)L::RED_OFF;
+        if (epi && have_acc) {
+            const int q4 = warp & 3;
+            const int row = q4 * 32 + lane;                   // accumulator row (TMEM lane)
+            const int o = ((row + 1) * S - 1) / BM;           // its owner: o * BM / S <= row < (o + 1) * BM / S
+            const int o0 = o * BM / S;
+            const uint32_t dst_local = red + (uint32_t)((rank * nmax + row - o0) * L::RSTRIDE);
+            const uint32_t dst = o == rank ? dst_local : ptx::map_cluster(dst_local, (uint32_t)o);
+            const uint32_t bar = ptx::map_cluster(REDUCE, (uint32_t)o);
+            const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16);
+            constexpr int CH = BN >= 32 ? 2 : 1;   // 16-column TMEM loads in flight together
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 16 * CH) {
+                uint32_t v[CH][16];
+                __syncwarp();
+#pragma unroll
+                for (int h = 0; h < CH; ++h) ptx::tmem_ld16(taddr + (uint32_t)(c + 16 * h), v[h]);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int h = 0; h < CH; ++h)
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const uint4 w = make_uint4(v[h][4 * u], v[h][4 * u + 1], v[h][4 * u + 2], v[h][4 * u + 3]);
+                        const uint32_t off = (uint32_t)((c + 16 * h + 4 * u) * 4);
+                        if (o == rank) ptx::sts128(dst + off, w);
+                        else ptx::st_async_v4(dst + off, w, bar);
+                    }
             }
+            ptx::tc_fence_before();
         }
-        if (warp >= 2 && warp < 6) {
-            const bool ok = wait_bar_warp(REDUCE, 0, abort_flag, d_error);   // warp-uniform: shuffles below
+        bool ok = true;
+        if (epi) {
+            ok = wait_bar_warp(REDUCE, 0, abort_flag, d_error) && have_acc;   // warp-uniform: shuffles below
+            ptx::named_bar_sync(1, kEpiThreads);                               // this CTA's own slice is written
+        }
+        // phase B: this CTA has received every byte sent to it, so no CTA leaves
+        // while another still writes into its shared memory
+        ptx::cluster_arrive();
+        if (epi) {
             int tr, tq;
             tile_coords(sched, (int)blockIdx.x / S, tr, tq);
             const int qb = tq * BN;
@@ -1012,8 +1065,9 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
             const int lg = nrows <= 16 ? 4 : nrows <= 32 ? 5 : nrows <= 64 ? 6 : 7;
             const int rl = etid & ((1 << lg) - 1);   // neighbouring threads: neighbouring rows
             const int cstep = kEpiThreads >> lg;
-            const uint32_t own = sbase + (uint32_t)((r0 + rl) * PSTRIDE);
-            const uint32_t inb = sbase + (uint32_t)(IN_OFF + rl * PSTRIDE);
+            const uint32_t src = red + (uint32_t)(rl * L::RSTRIDE);
+            const uint32_t stg = sbase + (uint32_t)L::STG_OFF;
+            const bool tma = sched.tma_c != 0;
             // S in {2, 4, 8}: the owner's rows are a power of two and start even, every
             // lane of a warp runs the same iterations, and neighbouring lanes (rows r,
             // r + 1) pair their values into 4-byte stores of C
@@ -1022,9 +1076,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                 uint4 u[8];
 #pragma unroll
                 for (int q = 0; q < 8; ++q)   // all slices' loads in flight before the sums
-                    if (q < S)
-                        u[q] = ptx::lds128((q == rank ? own : inb + (uint32_t)(q * nmax * PSTRIDE)) +
-                                           (uint32_t)(c4 * 16));
+                    if (q < S) u[q] = ptx::lds128(src + (uint32_t)(q * nmax * L::RSTRIDE + c4 * 16));
                 float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {   // rank order
@@ -1036,7 +1088,11 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                     }
                 }
                 const int r = tr * BM + r0 + rl;
-                if (FUSED && sched.epi != GEMM_EPI_NONE) {
+                if (tma) {   // bf16 [token][row] staging tile of the TMA store
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        ptx::sts16(stg + (uint32_t)(((c4 * 4 + j) * nrows + rl) * 2), f32_to_bf16_rn(a[j]));
+                } else if (FUSED && sched.epi != GEMM_EPI_NONE) {
                     cluster_store_fused<SWAP>(C, ldc, R, Q, r, qb + c4 * 4, paired, rl & 1, a, sched);
                 } else if (paired) {
                     float x[4];
@@ -1066,12 +1122,24 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                     }
                 }
             }
+            if (tma) {   // (every epilogue warp reaches the barrier, whatever its `ok`)
+                ptx::fence_proxy_async_smem();   // the staging tile is read by the TMA engine
+                __syncwarp();
+                ptx::named_bar_sync(1, kEpiThreads);
+                if (etid == 0 && ok) {            // box: nrows rows of C's columns x BN tokens (clipped)
+                    ptx::tma_store_2d(&tmC, stg, tr * BM + r0, qb);
+                    ptx::bulk_commit_group();
+                    ptx::bulk_wait_group_read0();
+                }
+            }
         }
-        // every incoming copy has landed (each owner waited for its bytes), so no
-        // CTA leaves while a copy still reads its shared memory
-        ptx::cluster_sync();
+        ptx::cluster_wait();
     }
 
+    // every warp converged before the CTA barrier (bar.sync counts warps; a
+    // warp split by the per-thread cluster wait or an elected branch would
+    // otherwise arrive in pieces)
+    __syncwarp();
     __syncthreads();
     if (warp == 1) {
         __syncwarp();
@@ -1131,6 +1199,30 @@ bool make_map_pairs(CUtensorMap *m, const void *ptr, int64_t N, int64_t K, int64
     return r == CUDA_SUCCESS;
 }
 
+// C of the skinny kernels ([Q tokens][R columns] bf16, row pitch ldc) for the
+// cluster split-K's TMA store: a box of BM / S columns x bn tokens, no swizzle.
+// Used only when the box is a whole number of 16-byte units and C's address
+// and pitch are multiples of 16 bytes; otherwise the kernel stores directly.
+bool cluster_store_map(CUtensorMap *m, Sched &s, const Plan &p, void *C, int64_t R, int64_t Q, int64_t ldc)
+{
+    s.tma_c = 0;
+    const int S = p.split;
+    if (p.variant != GEMM_VARIANT_SKINNY || p.mode != 2 || p.ctas_per_sm != 1 || s.epi != GEMM_EPI_NONE) return false;
+    if ((S != 2 && S != 4 && S != 8) || (reinterpret_cast<uintptr_t>(C) & 15) || (ldc * 2) % 16) return false;
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)R, (cuuint64_t)Q};
+    cuuint64_t strides[1] = {(cuuint64_t)ldc * 2};
+    cuuint32_t box[2] = {(cuuint32_t)(BM / S), (cuuint32_t)p.bn};
+    cuuint32_t estr[2] = {1, 1};
+    if (fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+        CUDA_SUCCESS)
+        return false;
+    s.tma_c = 1;
+    return true;
+}
+
 // Packed 4-bit weights for the tcgen05 kernel: boxes of 32 words x 128 rows.
 bool make_map_packed(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K)
 {
@@ -1138,10 +1230,10 @@ bool make_map_packed(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K)
 }
 
 template <int BN, int STAGES, bool SWAP, int MINB, bool W4 = false, bool FUSED = false>
-cudaError_t launch_t(const CUtensorMap &mx, const CUtensorMap &my, uint16_t *C, int R, int Q, int64_t ldc,
-                     const Sched &s, const LaunchCtx &c, const W4Args &w4 = W4Args{})
+cudaError_t launch_t(const CUtensorMap &mx, const CUtensorMap &my, const CUtensorMap &mc, uint16_t *C, int R, int Q,
+                     int64_t ldc, const Sched &s, const LaunchCtx &c, const W4Args &w4 = W4Args{})
 {
-    using L = Layout<BN, STAGES, W4>;
+    using L = Layout<BN, STAGES, W4, SWAP && MINB == 1>;
     auto kern = k_umma<BN, STAGES, SWAP, MINB, W4, FUSED>;
     static std::once_flag once[64];
     static cudaError_t attr_err[64];
@@ -1170,7 +1262,7 @@ cudaError_t launch_t(const CUtensorMap &mx, const CUtensorMap &my, uint16_t *C, 
     }
     cfg.attrs = at;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, kern, mx, my, C, R, Q, ldc, s, c.workspace, c.counters, c.d_error, w4);
+    return cudaLaunchKernelEx(&cfg, kern, mx, my, mc, C, R, Q, ldc, s, c.workspace, c.counters, c.d_error, w4);
 }
 
 }  // namespace
@@ -1210,7 +1302,7 @@ namespace {
 template <int BN, int STAGES, bool SWAP, int MINB, bool W4 = false>
 int cluster_capacity_t(int cluster)
 {
-    using L = Layout<BN, STAGES, W4>;
+    using L = Layout<BN, STAGES, W4, SWAP && MINB == 1>;
     auto kern = k_umma<BN, STAGES, SWAP, MINB, W4, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM) != cudaSuccess)
         return -1;
@@ -1346,40 +1438,43 @@ cudaError_t launch_umma_w4a16(const GemmArgs &a, const Plan &p, const LaunchCtx 
               a.group == 32 ? 5 : a.group == 64 ? 6 : 7};
     uint16_t *C = (uint16_t *)a.C;
     const int r = (int)a.N, q = (int)a.M;
+    s.epi = GEMM_EPI_NONE;
+    CUtensorMap mc;
+    if (!cluster_store_map(&mc, s, p, C, a.N, a.M, a.ldc)) mc = mx;   // (then unused)
     switch (p.bn) {
-    case 16: return launch_t<16, 8, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
-    case 32: return launch_t<32, 8, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
-    case 64: return launch_t<64, 6, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
-    case 128: return launch_t<128, 5, true, 1, true>(mx, my, C, r, q, a.ldc, s, c, w4);
+    case 16: return launch_t<16, 8, true, 1, true>(mx, my, mc, C, r, q, a.ldc, s, c, w4);
+    case 32: return launch_t<32, 8, true, 1, true>(mx, my, mc, C, r, q, a.ldc, s, c, w4);
+    case 64: return launch_t<64, 6, true, 1, true>(mx, my, mc, C, r, q, a.ldc, s, c, w4);
+    case 128: return launch_t<128, 5, true, 1, true>(mx, my, mc, C, r, q, a.ldc, s, c, w4);
     default: return cudaErrorInvalidValue;
     }
 }
 
 namespace {
 template <bool FUSED>
-cudaError_t launch_bf16_t(const CUtensorMap &mx, const CUtensorMap &my, uint16_t *C, int r, int q, int64_t ldc,
-                          const Sched &s, const Plan &p, const LaunchCtx &c, bool swap)
+cudaError_t launch_bf16_t(const CUtensorMap &mx, const CUtensorMap &my, const CUtensorMap &mc, uint16_t *C, int r,
+                          int q, int64_t ldc, const Sched &s, const Plan &p, const LaunchCtx &c, bool swap)
 {
     if (swap && p.ctas_per_sm == 1) {
         switch (p.bn) {
-        case 16: return launch_t<16, 8, true, 1, false, FUSED>(mx, my, C, r, q, ldc, s, c);
-        case 32: return launch_t<32, 8, true, 1, false, FUSED>(mx, my, C, r, q, ldc, s, c);
-        case 64: return launch_t<64, 8, true, 1, false, FUSED>(mx, my, C, r, q, ldc, s, c);
-        case 128: return launch_t<128, 6, true, 1, false, FUSED>(mx, my, C, r, q, ldc, s, c);
+        case 16: return launch_t<16, 8, true, 1, false, FUSED>(mx, my, mc, C, r, q, ldc, s, c);
+        case 32: return launch_t<32, 8, true, 1, false, FUSED>(mx, my, mc, C, r, q, ldc, s, c);
+        case 64: return launch_t<64, 8, true, 1, false, FUSED>(mx, my, mc, C, r, q, ldc, s, c);
+        case 128: return launch_t<128, 6, true, 1, false, FUSED>(mx, my, mc, C, r, q, ldc, s, c);
         default: return cudaErrorInvalidValue;
         }
     }
     if (swap) {
         switch (p.bn) {
-        case 16: return launch_t<16, 6, true, 2, false, FUSED>(mx, my, C, r, q, ldc, s, c);
-        case 32: return launch_t<32, 5, true, 2, false, FUSED>(mx, my, C, r, q, ldc, s, c);
-        case 64: return launch_t<64, 4, true, 2, false, FUSED>(mx, my, C, r, q, ldc, s, c);
-        case 128: return launch_t<128, 3, true, 2, false, FUSED>(mx, my, C, r, q, ldc, s, c);
+        case 16: return launch_t<16, 6, true, 2, false, FUSED>(mx, my, mc, C, r, q, ldc, s, c);
+        case 32: return launch_t<32, 5, true, 2, false, FUSED>(mx, my, mc, C, r, q, ldc, s, c);
+        case 64: return launch_t<64, 4, true, 2, false, FUSED>(mx, my, mc, C, r, q, ldc, s, c);
+        case 128: return launch_t<128, 3, true, 2, false, FUSED>(mx, my, mc, C, r, q, ldc, s, c);
         default: return cudaErrorInvalidValue;
         }
     }
     switch (p.bn) {
-    case 256: return launch_t<256, 4, false, 1, false, FUSED>(mx, my, C, r, q, ldc, s, c);
+    case 256: return launch_t<256, 4, false, 1, false, FUSED>(mx, my, mc, C, r, q, ldc, s, c);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -1422,8 +1517,10 @@ cudaError_t launch_umma_bf16(const GemmArgs &a, const Plan &p, const LaunchCtx &
     if (a.gends && (swap || p.mode != 0 || p.bn != 256)) return cudaErrorInvalidValue;
     uint16_t *C = (uint16_t *)a.C;
     s.split = p.split;
-    return a.epi != GEMM_EPI_NONE ? launch_bf16_t<true>(mx, my, C, (int)R, (int)Q, a.ldc, s, p, c, swap)
-                                  : launch_bf16_t<false>(mx, my, C, (int)R, (int)Q, a.ldc, s, p, c, swap);
+    CUtensorMap mc;
+    if (!cluster_store_map(&mc, s, p, C, R, Q, a.ldc)) mc = mx;   // (then unused)
+    return a.epi != GEMM_EPI_NONE ? launch_bf16_t<true>(mx, my, mc, C, (int)R, (int)Q, a.ldc, s, p, c, swap)
+                                  : launch_bf16_t<false>(mx, my, mc, C, (int)R, (int)Q, a.ldc, s, p, c, swap);
 }
 
 }  // namespace dbw
