@@ -64,11 +64,11 @@ WORKLOAD = ("decode projections, Qwen3-8B-like dims: bf16 A[M,4096], M in {1,8,3
 # DRAM bytes (read + write) per launch of each decode GEMM, from one ncu pass
 # (profiles/decode_step_dram_traffic.md) over the kernel sources with this
 # SHA-256; reported only while the sources are unchanged.
-TRAFFIC_SOURCES_SHA256 = "44722ebcbb5d02837410f7bc0cfd5aa96f9c0ff36d001ac487c267328e8f2de4"
-TRAFFIC_BYTES = {(1, 4096, 4096): 33.57e6, (1, 6144, 4096): 50.35e6, (1, 24576, 4096): 201.45e6,
-                 (8, 4096, 4096): 33.71e6, (8, 6144, 4096): 50.48e6, (8, 24576, 4096): 201.52e6,
-                 (32, 4096, 4096): 33.91e6, (32, 6144, 4096): 50.68e6, (32, 24576, 4096): 201.78e6,
-                 (128, 4096, 4096): 34.70e6, (128, 6144, 4096): 51.47e6, (128, 24576, 4096): 203.04e6}
+TRAFFIC_SOURCES_SHA256 = "cfc7aa04407f07fceb86e81a54c43183fb51ed37eee3d408b24510a70a075d39"
+TRAFFIC_BYTES = {(1, 4096, 4096): 33.57e6, (1, 6144, 4096): 50.35e6, (1, 24576, 4096): 201.46e6,
+                 (8, 4096, 4096): 33.70e6, (8, 6144, 4096): 50.48e6, (8, 24576, 4096): 201.59e6,
+                 (32, 4096, 4096): 33.90e6, (32, 6144, 4096): 50.68e6, (32, 24576, 4096): 201.81e6,
+                 (128, 4096, 4096): 34.69e6, (128, 6144, 4096): 51.47e6, (128, 24576, 4096): 202.66e6}
 
 
 def kernel_sources_sha256():

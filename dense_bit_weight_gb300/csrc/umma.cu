@@ -613,8 +613,10 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
     } else if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
+            // weights stream (evict first) unless several token tiles read them
+            const bool y_once = !SWAP && sched.tiles_r == 1;
             const uint64_t pol_x = SWAP ? ptx::policy_evict_first() : ptx::policy_evict_last();
-            const uint64_t pol_y = ptx::policy_evict_last();
+            const uint64_t pol_y = y_once ? ptx::policy_evict_first() : ptx::policy_evict_last();
             int stage = 0;
             uint32_t phase = 0;
             long long issued = 0;
@@ -1201,8 +1203,8 @@ bool make_map_pairs(CUtensorMap *m, const void *ptr, int64_t N, int64_t K, int64
 
 // C of the skinny kernels ([Q tokens][R columns] bf16, row pitch ldc) for the
 // cluster split-K's TMA store: a box of BM / S columns x bn tokens, no swizzle.
-// Used only when the box is a whole number of 16-byte units and C's address
-// and pitch are multiples of 16 bytes; otherwise the kernel stores directly.
+// Used when the box is a whole number of 16-byte units (S = 2, 4 or 8) and the
+// result needs no epilogue; otherwise the kernel stores directly.
 bool cluster_store_map(CUtensorMap *m, Sched &s, const Plan &p, void *C, int64_t R, int64_t Q, int64_t ldc)
 {
     s.tma_c = 0;
@@ -1290,7 +1292,7 @@ bool make_map_words(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, in
 // of up to two CTAs per SM.  Prefill uses one CTA per SM.
 int umma_stages(int bn, bool skinny, bool deep)
 {
-    if (!skinny) return 4;
+    if (!skinny) return bn <= 192 ? 5 : 4;
     if (deep) return bn <= 64 ? 8 : 6;
     return bn <= 16 ? 6 : bn <= 32 ? 5 : bn <= 64 ? 4 : 3;
 }
@@ -1475,6 +1477,9 @@ cudaError_t launch_bf16_t(const CUtensorMap &mx, const CUtensorMap &my, const CU
     }
     switch (p.bn) {
     case 256: return launch_t<256, 4, false, 1, false, FUSED>(mx, my, mc, C, r, q, ldc, s, c);
+    case 224: return launch_t<224, 4, false, 1, false, FUSED>(mx, my, mc, C, r, q, ldc, s, c);
+    case 192: return launch_t<192, 5, false, 1, false, FUSED>(mx, my, mc, C, r, q, ldc, s, c);
+    case 176: return launch_t<176, 5, false, 1, false, FUSED>(mx, my, mc, C, r, q, ldc, s, c);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -63,6 +63,23 @@ def test_small_shapes_integer_exact(g, M, N, K, variant):
     assert_exact(host_bits(C), oracle.gemm_bf16(A, B), what=f"{variant} {M}x{N}x{K}")
 
 
+# Prefill kernel with one token tile and the wide weight tiles the planner picks
+# for it (176, 192 or 224 rows, a single wave): ragged N, K and M.
+WIDE = [(100, 24536, 72, 176), (17, 24576, 136, 176), (64, 28000, 40, 192), (128, 32760, 64, 224)]
+
+
+@pytest.mark.parametrize("M,N,K,bn", WIDE)
+@pytest.mark.parametrize("kind", ["normal", "int"])
+def test_wide_single_token_tile(g, M, N, K, bn, kind):
+    p = g.gemm_bf16_plan(M, N, K)
+    if p["grid"] * 100 < 85 * 152 or p["tile_n"] != bn:
+        pytest.skip(f"plan on this device: {p}")
+    A, B = bf16_inputs(M, N, K, seed=M + K, kind=kind)
+    C = g.gemm_bf16(dev_bf16(A), dev_bf16(B))
+    ref = oracle.gemm_bf16(A, B)
+    (assert_exact if kind == "int" else assert_close)(host_bits(C), ref, what=f"wide {bn} {M}x{N}x{K}")
+
+
 def test_leading_dimensions_and_views(g):
     import torch
     M, N, K = 37, 200, 96

@@ -84,6 +84,25 @@ def test_silu_mul_splits_keep_pairs(g, variant, M):
     assert_close(host_bits(C), oracle.gemm_bf16_silu_mul(A, B), what=f"split {variant} {p}")
 
 
+@pytest.mark.parametrize("epilogue", ["bias", "silu_mul"])
+def test_wide_single_token_tile(g, epilogue):
+    # one token tile: the planner takes 176-row weight tiles (88 gate/up pairs)
+    M, N, K = 48, 12280 if epilogue == "silu_mul" else 24560, 64
+    NB = 2 * N if epilogue == "silu_mul" else N
+    p = g.gemm_bf16_plan(M, NB, K)
+    if p["tile_n"] != 176:
+        pytest.skip(f"plan on this device: {p}")
+    A, B = bf16_inputs(M, NB, K, seed=5)
+    if epilogue == "bias":
+        bias = synth.bf16_normal((N,), 1.0, 5, synth.STREAM_B)
+        C = g.gemm_bf16_fused(dev_bf16(A), dev_bf16(B), dev_bf16(bias), epilogue="bias")
+        ref = oracle.gemm_bf16_bias(A, B, bias)
+    else:
+        C = g.gemm_bf16_fused(dev_bf16(A), dev_bf16(B), epilogue="silu_mul")
+        ref = oracle.gemm_bf16_silu_mul(A, B)
+    assert_close(host_bits(C), ref, what=f"wide {epilogue}")
+
+
 def test_strided_operands_and_padding(g):
     import torch
     M, N, K = 40, 264, 512
