@@ -292,11 +292,14 @@ static void plan_umma(int64_t M, int64_t N, int64_t K, bool swap, int bn, int sm
 // Measured on GB300 at N = 24576, K = 4096 against the skinny kernel's 192
 // tiles of 128 weight rows, two CTAs on some SMs: 176-row tiles on 140 SMs
 // take 34.2 us instead of 40.5 at M = 128, 32.7 instead of 35.7 at M = 64 and
-// 32.2 instead of 33.9 at M = 32.  Below 16 tokens the activation boxes are
-// almost all out of range and the plan loses (42.5 us against 33.4 at M = 8).
-static int wide_bn(int64_t M, int64_t N, int sm_count)
+// 32.2 instead of 33.9 at M = 32, 32.7 instead of 33.0 at M = 8 (the
+// activation copies then cover the token rows only) and 32.6 against the
+// GEMV's 33.6 at M = 1.  The fused gate/up pairs gain only from M = 64 on
+// (M = 128: 4.95 TB/s against the skinny kernel's 4.0; M = 32: 4.98 against
+// 5.5, M = 8: 4.95 against 5.9).
+static int wide_bn(int64_t M, int64_t N, int sm_count, bool pairs)
 {
-    if (M < 16 || M > kUmmaBM) return 0;
+    if (M > kUmmaBM || (pairs && M < 64)) return 0;
     for (int bn : {176, 192, 224, 256}) {
         const int64_t tiles = (N + bn - 1) / bn;
         if (tiles > sm_count) continue;
@@ -317,9 +320,9 @@ bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan 
         return true;
     }
     if (variant == GEMM_VARIANT_AUTO)
-        variant = M <= 4                              ? GEMM_VARIANT_GEMV
-                  : M > 128 || wide_bn(M, N, sm_count) ? GEMM_VARIANT_PREFILL
-                                                      : GEMM_VARIANT_SKINNY;
+        variant = M > 128 || wide_bn(M, N, sm_count, pairs) ? GEMM_VARIANT_PREFILL
+                  : M <= 4                                   ? GEMM_VARIANT_GEMV
+                                                             : GEMM_VARIANT_SKINNY;
     switch (variant) {
     case GEMM_VARIANT_GEMV:
         p->variant = GEMM_VARIANT_GEMV;
@@ -338,7 +341,7 @@ bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan 
         return true;
     }
     case GEMM_VARIANT_PREFILL: {
-        const int bn = wide_bn(M, N, sm_count);
+        const int bn = wide_bn(M, N, sm_count, pairs);
         plan_umma(M, N, K, false, bn ? bn : 256, sm_count, query, p, pairs);
         return true;
     }

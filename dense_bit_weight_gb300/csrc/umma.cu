@@ -103,6 +103,7 @@ struct Sched {
     int groups;                  //   experts
     int gN;                      //   weight rows per expert (columns of C)
     int tma_c;                   // mode 2: each CTA's block of the tile leaves through a TMA store (tmC)
+    int x_bytes;                 // bytes one stage's X copy delivers (its box may be short: one token tile)
 };
 
 
@@ -650,7 +651,7 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
                         break;
                     }
                     if (!sched.stall) {
-                        ptx::mbar_arrive_expect_tx(FULL(stage), L::STAGE_BYTES);
+                        ptx::mbar_arrive_expect_tx(FULL(stage), (uint32_t)(sched.x_bytes + L::Y_BYTES));
                         const uint32_t xs = sbase + stage * L::STAGE_BYTES;
                         // (gate, up) pairs: the 3-D view [row / 2][gate or up][k] puts the
                         // pair's rows next to each other in the tile
@@ -953,7 +954,9 @@ k_umma(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensor
             __threadfence();
             // many float4 loads in flight: CB4 float4 columns of BATCH contributors at a time,
             // summed per column in increasing contributor (= increasing k) order
-            constexpr int CB4 = (BN / 4) < (W4 ? 4 : 16) ? (BN / 4) : (W4 ? 4 : 16);
+            // (a divisor of BN / 4, a multiple of 4 since BN is a multiple of 16)
+            constexpr int CB4 = W4 || (BN / 4) % 8 ? 4 : (BN / 4) % 16 ? 8 : 16;
+            static_assert((BN / 4) % CB4 == 0 && CB4 % 4 == 0, "fixup column batches tile BN");
             constexpr int INFL = W4 ? 4 : (MINB == 1 ? 32 : 16);
             constexpr int BATCH = INFL / CB4 > 0 ? INFL / CB4 : 1;
             const float4 *wsv = reinterpret_cast<const float4 *>(ws);
@@ -1496,7 +1499,13 @@ cudaError_t launch_umma_bf16(const GemmArgs &a, const Plan &p, const LaunchCtx &
     const int64_t ldx = swap ? a.ldb : a.lda, ldy = swap ? a.lda : a.ldb;
     CUtensorMap mx, my;
     const int64_t QY = a.gends ? a.groups * a.N : Q;   // grouped: B stacks the experts' weights
-    const bool okx = swap && pairs ? make_map_pairs(&mx, X, a.N, a.K, ldx, BM / 2) : make_map(&mx, X, R, a.K, ldx, BM);
+    // One token tile (prefill kernel, M <= 128): the X box covers the token rows
+    // only, rounded up to 16.  Boxes that are mostly out of range were slow
+    // (M = 8, 176-row weight tiles: 42.5 us with 128-row boxes, 31.9 with 16);
+    // the MMA's remaining A rows hold stale shared memory and produce C rows
+    // that are never stored (row m of C depends on row m of A alone).
+    const int xbox = !swap && !a.gends && R <= BM ? (int)((R + 15) / 16 * 16) : BM;
+    const bool okx = swap && pairs ? make_map_pairs(&mx, X, a.N, a.K, ldx, BM / 2) : make_map(&mx, X, R, a.K, ldx, xbox);
     const bool oky = !swap && pairs ? make_map_pairs(&my, Y, a.N, a.K, ldy, p.bn / 2) : make_map(&my, Y, QY, a.K, ldy, p.bn);
     if (!okx || !oky) return cudaErrorInvalidValue;
     Sched s{};
@@ -1522,6 +1531,7 @@ cudaError_t launch_umma_bf16(const GemmArgs &a, const Plan &p, const LaunchCtx &
     if (a.gends && (swap || p.mode != 0 || p.bn != 256)) return cudaErrorInvalidValue;
     uint16_t *C = (uint16_t *)a.C;
     s.split = p.split;
+    s.x_bytes = xbox * BK * 2;
     CUtensorMap mc;
     if (!cluster_store_map(&mc, s, p, C, R, Q, a.ldc)) mc = mx;   // (then unused)
     return a.epi != GEMM_EPI_NONE ? launch_bf16_t<true>(mx, my, mc, C, (int)R, (int)Q, a.ldc, s, p, c, swap)

@@ -194,20 +194,19 @@ def test_prefill_last_wave_split():
 
 
 def test_wide_tiles_for_one_token_tile():
-    # 16 <= M <= 128 and a weight count that fills one wave of 176-256-row tiles:
+    # M <= 128 and a weight count that fills one wave of 176-256-row tiles:
     # the prefill kernel, weights read once each; otherwise the skinny split-K
     from dense_bit_weight_gb300 import gemm as g
     sms = 152
-    for M in (16, 32, 128):
+    for M in (1, 4, 5, 8, 16, 32, 128):
         p = g.gemm_bf16_plan(M, 24576, 4096, num_sms=sms)
         assert (p["variant"], p["tile_n"], p["grid"], p["split"]) == (3, 176, 140, 1)
-    assert g.gemm_bf16_plan(8, 24576, 4096, num_sms=sms)["variant"] == 2        # below 16 tokens
     assert g.gemm_bf16_plan(64, 28000, 4096, num_sms=sms)["tile_n"] == 192      # 146 tiles
     assert g.gemm_bf16_plan(64, 32768, 4096, num_sms=sms)["tile_n"] == 224      # 147 tiles
     assert g.gemm_bf16_plan(128, 16384, 4096, num_sms=sms)["variant"] == 2      # 176 rows: 94 tiles, too few
     assert g.gemm_bf16_plan(128, 4096, 4096, num_sms=sms)["variant"] == 2
     assert g.gemm_bf16_plan(129, 24576, 4096, num_sms=sms)["tile_n"] == 256     # two token tiles
-    assert g.gemm_bf16_plan(4, 24576, 4096, num_sms=sms)["variant"] == 1        # GEMV below 5 rows
+    assert g.gemm_bf16_plan(4, 4096, 4096, num_sms=sms)["variant"] == 1         # GEMV below 5 rows
     # forced variants keep their kernels; the fused gate/up pairs take the same tiles
     assert g.gemm_bf16_plan(128, 24576, 4096, "skinny", num_sms=sms)["variant"] == 2
     assert g.gemm_bf16_plan(128, 2 * 12288, 4096, num_sms=sms)["tile_n"] == 176

@@ -64,8 +64,10 @@ def test_small_shapes_integer_exact(g, M, N, K, variant):
 
 
 # Prefill kernel with one token tile and the wide weight tiles the planner picks
-# for it (176, 192 or 224 rows, a single wave): ragged N, K and M.
-WIDE = [(100, 24536, 72, 176), (17, 24576, 136, 176), (64, 28000, 40, 192), (128, 32760, 64, 224)]
+# for it (176, 192 or 224 rows, a single wave): ragged N, K and M.  The token
+# copies cover only M rows rounded up to 16; the MMA rows beyond hold stale data.
+WIDE = [(100, 24536, 72, 176), (17, 24576, 136, 176), (5, 24576, 64, 176), (64, 28000, 40, 192),
+        (128, 32760, 64, 224)]
 
 
 @pytest.mark.parametrize("M,N,K,bn", WIDE)

@@ -86,8 +86,9 @@ def test_silu_mul_splits_keep_pairs(g, variant, M):
 
 @pytest.mark.parametrize("epilogue", ["bias", "silu_mul"])
 def test_wide_single_token_tile(g, epilogue):
-    # one token tile: the planner takes 176-row weight tiles (88 gate/up pairs)
-    M, N, K = 48, 12280 if epilogue == "silu_mul" else 24560, 64
+    # one token tile: the planner takes 176-row weight tiles (88 gate/up pairs,
+    # from 64 tokens on)
+    M, N, K = (64, 12280, 64) if epilogue == "silu_mul" else (48, 24560, 64)
     NB = 2 * N if epilogue == "silu_mul" else N
     p = g.gemm_bf16_plan(M, NB, K)
     if p["tile_n"] != 176:
