@@ -269,7 +269,8 @@ def timed_sweep(g, torch, shapes, kind, reps=20):
     for (M, N, K) in shapes:
         silu = kind.startswith("silu")
         NB = 2 * N if silu else N   # weight rows
-        plan = (g.gemm_w4a16_plan(M, N, K, 128) if kind == "w4" else g.gemm_bf16_plan(M, NB, K))
+        plan = (g.gemm_w4a16_plan(M, N, K, 128) if kind == "w4"
+                else g.gemm_bf16_fused_plan(M, N, K, "silu_mul") if silu else g.gemm_bf16_plan(M, NB, K))
         if plan["variant"] == 1 and M > 64:
             continue            # no tensor-core plan for this shape
         # enough weight copies that consecutive launches miss L2

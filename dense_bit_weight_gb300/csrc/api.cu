@@ -630,6 +630,27 @@ int gemm_bf16_plan(int64_t M, int64_t N, int64_t K, int variant, int num_sms, ge
     return GEMM_OK;
 }
 
+int gemm_bf16_fused_plan(int64_t M, int64_t N, int64_t K, int epilogue, int variant, int num_sms,
+                         gemm_plan *out)
+{
+    if (epilogue != GEMM_EPI_NONE && epilogue != GEMM_EPI_BIAS && epilogue != GEMM_EPI_SILU_MUL)
+        return GEMM_ERR_EPILOGUE;
+    if (epilogue == GEMM_EPI_NONE) return gemm_bf16_plan(M, N, K, variant, num_sms, out);
+    if (!out) return GEMM_ERR_NULL;
+    int rc = check_sizes(M, N, K);
+    if (rc) return rc;
+    const bool pairs = epilogue == GEMM_EPI_SILU_MUL;
+    const int64_t NB = pairs ? 2 * N : N;   // rows of B
+    if (NB > kMaxDim) return GEMM_ERR_SHAPE;
+    int sms = 0;
+    rc = sm_count_for_plan(num_sms, &sms);
+    if (rc) return rc;
+    Plan p;
+    if (!plan_bf16(M, NB, K, variant, sms, &p, num_sms == 0, pairs)) return GEMM_ERR_VARIANT;
+    to_public(p, out);
+    return GEMM_OK;
+}
+
 int gemm_w4a16_plan(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int num_sms,
                     gemm_plan *out)
 {

@@ -27,7 +27,7 @@ VARIANT_NAME = {v: k for k, v in VARIANT.items()}
 EXPORTS = ["gemm_bf16", "gemm_w4a16", "gemm_bf16_ex", "gemm_w4a16_ex", "gemm_bf16_plan",
            "gemm_w4a16_plan", "gemm_last_device_error", "gemm_status_string", "gemm_shutdown",
            "gemm_debug_inject_timeout", "gemm_bf16_noalloc", "gemm_bf16_fused", "gemm_bf16_fused_ex",
-           "gemm_bf16_grouped"]
+           "gemm_bf16_grouped", "gemm_bf16_fused_plan"]
 
 
 class gemm_plan(ctypes.Structure):
@@ -54,6 +54,7 @@ lib.gemm_w4a16.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _p]
 lib.gemm_w4a16_ex.argtypes = lib.gemm_w4a16.argtypes + [_i]
 lib.gemm_bf16_plan.argtypes = [_i64, _i64, _i64, _i, _i, ctypes.POINTER(gemm_plan)]
 lib.gemm_w4a16_plan.argtypes = [_i64, _i64, _i64, _i64, _i, _i, ctypes.POINTER(gemm_plan)]
+lib.gemm_bf16_fused_plan.argtypes = [_i64, _i64, _i64, _i, _i, _i, ctypes.POINTER(gemm_plan)]
 lib.gemm_last_device_error.argtypes = []
 lib.gemm_status_string.argtypes = [_i]
 lib.gemm_status_string.restype = ctypes.c_char_p
@@ -62,7 +63,7 @@ lib.gemm_debug_inject_timeout.restype = _i
 lib.gemm_shutdown.argtypes = []
 lib.gemm_shutdown.restype = None
 for _f in ("gemm_bf16", "gemm_bf16_ex", "gemm_w4a16", "gemm_w4a16_ex", "gemm_bf16_plan",
-           "gemm_w4a16_plan", "gemm_last_device_error"):
+           "gemm_w4a16_plan", "gemm_bf16_fused_plan", "gemm_last_device_error"):
     getattr(lib, _f).restype = _i
 
 
@@ -101,6 +102,15 @@ def _variant(v) -> int:
 def gemm_bf16_plan(M: int, N: int, K: int, variant="auto", num_sms: int = 0) -> dict:
     out = gemm_plan()
     _check(lib.gemm_bf16_plan(M, N, K, _variant(variant), num_sms, ctypes.byref(out)), "gemm_bf16_plan")
+    return out.as_dict()
+
+
+def gemm_bf16_fused_plan(M: int, N: int, K: int, epilogue="silu_mul", variant="auto", num_sms: int = 0) -> dict:
+    """Plan of gemm_bf16_fused (N = columns of C)."""
+    epi = EPILOGUE[epilogue] if isinstance(epilogue, str) else int(epilogue)
+    out = gemm_plan()
+    _check(lib.gemm_bf16_fused_plan(M, N, K, epi, _variant(variant), num_sms, ctypes.byref(out)),
+           "gemm_bf16_fused_plan")
     return out.as_dict()
 
 

@@ -234,6 +234,11 @@ int gemm_w4a16_ex(const void *A, const void *Bq, const void *scales, const void 
  * Returns a gemm_status for the sizes (pointers are not checked).
  */
 int gemm_bf16_plan(int64_t M, int64_t N, int64_t K, int variant, int num_sms, gemm_plan *out);
+/* The plan of gemm_bf16_fused_ex with these sizes (N = columns of C; the
+ * SiLU-mul epilogue multiplies 2N weight rows); GEMM_ERR_EPILOGUE for an
+ * unknown epilogue. */
+int gemm_bf16_fused_plan(int64_t M, int64_t N, int64_t K, int epilogue, int variant, int num_sms,
+                         gemm_plan *out);
 int gemm_w4a16_plan(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int num_sms,
                     gemm_plan *out);
 

@@ -210,3 +210,10 @@ def test_wide_tiles_for_one_token_tile():
     # forced variants keep their kernels; the fused gate/up pairs take the same tiles
     assert g.gemm_bf16_plan(128, 24576, 4096, "skinny", num_sms=sms)["variant"] == 2
     assert g.gemm_bf16_plan(128, 2 * 12288, 4096, num_sms=sms)["tile_n"] == 176
+    # the fused gate/up pairs (C 12288 columns) take them from 64 tokens on
+    for M, variant in ((1, 1), (8, 2), (32, 2), (64, 3), (128, 3)):
+        assert g.gemm_bf16_fused_plan(M, 12288, 4096, "silu_mul", num_sms=sms)["variant"] == variant
+    assert g.gemm_bf16_fused_plan(8, 24576, 4096, "bias", num_sms=sms)["tile_n"] == 176
+    assert g.gemm_bf16_fused_plan(8, 24576, 4096, "none", num_sms=sms) == g.gemm_bf16_plan(8, 24576, 4096, num_sms=sms)
+    with pytest.raises(g.GemmError):
+        g.gemm_bf16_fused_plan(8, 24576, 4096, 7, num_sms=sms)
