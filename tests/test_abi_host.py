@@ -217,3 +217,29 @@ def test_wide_tiles_for_one_token_tile():
     assert g.gemm_bf16_fused_plan(8, 24576, 4096, "none", num_sms=sms) == g.gemm_bf16_plan(8, 24576, 4096, num_sms=sms)
     with pytest.raises(g.GemmError):
         g.gemm_bf16_fused_plan(8, 24576, 4096, 7, num_sms=sms)
+
+
+def test_planner_invariants_over_shapes():
+    # every AUTO plan over a spread of decode and prefill shapes is one the
+    # kernels accept: a known family, a grid within the SM count (persistent
+    # kernels) or a positive GEMV grid, wide weight tiles in one wave filling
+    # at least 85% of the SMs, and split plans that leave every CTA work
+    from dense_bit_weight_gb300 import gemm as g
+    import random
+    rnd = random.Random(7)
+    for sms in (152, 148, 132):
+        for _ in range(400):
+            M = rnd.choice([1, 2, 3, 4, 5, 8, 15, 16, 17, 31, 32, 64, 100, 128, 129, 512, 4096])
+            N = rnd.randrange(8, 40000, 8)
+            K = rnd.randrange(8, 16384, 8)
+            p = g.gemm_bf16_plan(M, N, K, num_sms=sms)
+            assert p["variant"] in (1, 2, 3), p
+            assert p["grid"] >= 1 and p["split"] >= 1
+            if p["variant"] in (2, 3):
+                assert p["grid"] <= 2 * sms, (M, N, K, p)
+            if p["variant"] == 3 and M <= 128 and p["tile_n"] != 256:
+                tiles = -(-N // p["tile_n"])
+                assert p["tile_n"] in (176, 192, 224) and p["tile_n"] >= M
+                assert tiles == p["grid"] and 0.85 * sms <= tiles <= sms, (M, N, K, p)
+            if p["variant"] == 2 and -(-N // 128) <= sms:   # one wave of weight tiles: cluster split-K
+                assert p["grid"] == -(-N // 128) * p["split"] and p["split"] <= 8 and p["grid"] <= sms
