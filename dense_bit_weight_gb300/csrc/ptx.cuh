@@ -288,12 +288,6 @@ __device__ __forceinline__ uint32_t cluster_ctarank()
     return r;
 }
 
-// Full-cluster barrier (every non-exited thread of every CTA of the cluster).
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-
 // The two halves of the cluster barrier: arrive and wait (acquire).  Each
 // thread alternates them; work placed between them overlaps the barrier.  The
 // arrive is relaxed: it orders control only, and publishes none of this
@@ -336,29 +330,6 @@ __device__ __forceinline__ uint32_t map_cluster(uint32_t saddr, uint32_t rank)
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
     return r;
-}
-
-// Plain load from distributed shared memory (ordering comes from the cluster
-// barriers around it, so the compiler may keep several in flight).
-__device__ __forceinline__ float4 ld_cluster_v4(uint32_t caddr)
-{
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(caddr));
-    return v;
-}
-
-// Bulk copy from this CTA's shared memory into another CTA's shared memory in
-// the cluster; completion (bytes) is counted on the destination's mbarrier.
-// Addresses 16-byte aligned, size a multiple of 16.
-__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
-                                                     uint32_t mbar_cluster)
-{
-    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     dst_cluster),
-                 "r"(src_cta), "r"(bytes), "r"(mbar_cluster)
-                 : "memory");
 }
 
 // Make this thread's generic-proxy shared-memory writes visible to the async
