@@ -216,7 +216,14 @@ def test_wide_tiles_for_one_token_tile():
     assert g.gemm_bf16_fused_plan(8, 24576, 4096, "bias", num_sms=sms)["tile_n"] == 176
     assert g.gemm_bf16_fused_plan(8, 24576, 4096, "none", num_sms=sms) == g.gemm_bf16_plan(8, 24576, 4096, num_sms=sms)
     with pytest.raises(g.GemmError):
-        g.gemm_bf16_fused_plan(8, 24576, 4096, 7, num_sms=sms)
+        g.gemm_bf16_fused_plan(8, 24576, 4096, 7, num_sms=sms)              # unknown epilogue
+    with pytest.raises(g.GemmError):
+        g.gemm_bf16_fused_plan(8, 2 ** 30 + 8, 4096, "silu_mul", num_sms=sms)  # 2N weight rows too many
+    with pytest.raises(g.GemmError):
+        g.gemm_bf16_fused_plan(200, 24576, 4096, "silu_mul", "skinny", num_sms=sms)
+    with pytest.raises(g.GemmError):
+        g.gemm_bf16_fused_plan(8, 24576, 12, "bias", num_sms=sms)            # K % 8
+    assert g.gemm_bf16_fused_plan(8, 24576, 4096, "bias", "gemv", num_sms=sms)["variant"] == 1
 
 
 def test_planner_invariants_over_shapes():
