@@ -85,9 +85,14 @@ int stream_workspace(DeviceState &s, cudaStream_t st, int64_t floats, int64_t co
         // round up so neighbouring shapes reuse the allocation
         int64_t f = std::max<int64_t>(floats, int64_t(1) << 20);
         int64_t c = std::max<int64_t>(counters, 4096);
-        if (cudaMalloc(&w.partials, (size_t)f * sizeof(float)) != cudaSuccess) return GEMM_ERR_CUDA;
-        if (cudaMalloc(&w.counters, (size_t)c * sizeof(int)) != cudaSuccess) return GEMM_ERR_CUDA;
-        if (cudaMemset(w.counters, 0, (size_t)c * sizeof(int)) != cudaSuccess) return GEMM_ERR_CUDA;
+        if (cudaMalloc(&w.partials, (size_t)f * sizeof(float)) != cudaSuccess ||
+            cudaMalloc(&w.counters, (size_t)c * sizeof(int)) != cudaSuccess ||
+            cudaMemset(w.counters, 0, (size_t)c * sizeof(int)) != cudaSuccess) {
+            cudaFree(w.partials);   // (either may be null)
+            cudaFree(w.counters);
+            w = StreamWorkspace();
+            return GEMM_ERR_CUDA;
+        }
         w.floats = f;
         w.n_counters = c;
     }
