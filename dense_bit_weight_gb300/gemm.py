@@ -129,6 +129,14 @@ def _stream_handle(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def _same_cuda_device(ref, *tensors):
+    """Every tensor (None skipped) must be a CUDA tensor on ref's device: the C
+    calls take raw device addresses and cannot tell host memory apart."""
+    for name, t in tensors:
+        if t is not None and (not t.is_cuda or t.device != ref.device):
+            raise ValueError(f"{name} must be a CUDA tensor on {ref.device}")
+
+
 def _row_major_2d(t, name):
     if t.dim() != 2 or t.stride(1) != 1:
         raise ValueError(f"{name} must be a 2-D tensor with unit stride along its last dimension")
@@ -155,6 +163,7 @@ def gemm_bf16(A, B, C=None, stream=None, variant="auto"):
         C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
     if C.dtype != torch.bfloat16 or tuple(C.shape) != (M, N):
         raise ValueError("C must be bfloat16 [M,N]")
+    _same_cuda_device(A, ("B", B), ("C", C))
     lda, ldb, ldc = _row_major_2d(A, "A"), _row_major_2d(B, "B"), _row_major_2d(C, "C")
     rc = lib.gemm_bf16_ex(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, lda, ldb, ldc,
                           _stream_handle(stream), _variant(variant))
@@ -193,6 +202,7 @@ def gemm_bf16_fused(A, B, bias=None, C=None, epilogue="bias", stream=None, varia
         C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
     if C.dtype != torch.bfloat16 or tuple(C.shape) != (M, N):
         raise ValueError("C must be bfloat16 [M,N]")
+    _same_cuda_device(A, ("B", B), ("C", C), ("bias", bias))
     lda, ldb, ldc = _row_major_2d(A, "A"), _row_major_2d(B, "B"), _row_major_2d(C, "C")
     rc = lib.gemm_bf16_fused_ex(A.data_ptr(), B.data_ptr(), bias.data_ptr() if bias is not None else None,
                                 C.data_ptr(), M, N, K, lda, ldb, ldc, epi, _stream_handle(stream),
@@ -219,6 +229,7 @@ def gemm_bf16_grouped(A, B, ends, C=None, stream=None):
         C = torch.zeros((M, N), dtype=torch.bfloat16, device=A.device)
     if C.dtype != torch.bfloat16 or tuple(C.shape) != (M, N):
         raise ValueError("C must be bfloat16 [M,N]")
+    _same_cuda_device(A, ("A", A), ("B", B), ("C", C), ("ends", ends))
     lda, ldc = _row_major_2d(A, "A"), _row_major_2d(C, "C")
     rc = lib.gemm_bf16_grouped(A.data_ptr(), B.data_ptr(), C.data_ptr(), ends.data_ptr(), G, M, N, K,
                                lda, K, ldc, _stream_handle(stream))
@@ -246,6 +257,7 @@ def gemm_w4a16(A, Bq, scales, zeros, group: int, C=None, stream=None, variant="a
         C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
     if C.dtype != torch.bfloat16 or tuple(C.shape) != (M, N) or not C.is_contiguous():
         raise ValueError("C must be a contiguous bfloat16 [M,N] tensor")
+    _same_cuda_device(A, ("Bq", Bq), ("scales", scales), ("zeros", zeros), ("C", C))
     rc = lib.gemm_w4a16_ex(A.data_ptr(), Bq.data_ptr(), scales.data_ptr(), zeros.data_ptr(),
                            C.data_ptr(), M, N, K, group, _stream_handle(stream), _variant(variant))
     _check(rc, "gemm_w4a16")

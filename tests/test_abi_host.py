@@ -250,3 +250,42 @@ def test_planner_invariants_over_shapes():
                 assert tiles == p["grid"] and 0.85 * sms <= tiles <= sms, (M, N, K, p)
             if p["variant"] == 2 and -(-N // 128) <= sms:   # one wave of weight tiles: cluster split-K
                 assert p["grid"] == -(-N // 128) * p["split"] and p["split"] <= 8 and p["grid"] <= sms
+
+
+class _FakeCudaTensor:
+    """Stands in for a CUDA bf16 tensor (no GPU here): only the attributes the
+    binding reads before it reaches the C call."""
+
+    def __init__(self, shape, dtype=None, device_index=0):
+        import torch
+        self.shape = tuple(shape)
+        self.dtype = dtype or torch.bfloat16
+        self.is_cuda = True
+        self.device = torch.device("cuda", device_index)
+
+    def dim(self):
+        return len(self.shape)
+
+    def stride(self, i=None):
+        st = (self.shape[1], 1) if len(self.shape) == 2 else (1,)
+        return st if i is None else st[i]
+
+    def is_contiguous(self):
+        return True
+
+    def data_ptr(self):
+        raise AssertionError("the binding must reject the call before reading pointers")
+
+
+def test_binding_rejects_host_and_cross_device_tensors():
+    import torch
+    from dense_bit_weight_gb300 import gemm as g
+    A, B = _FakeCudaTensor((4, 64)), _FakeCudaTensor((32, 64))
+    with pytest.raises(ValueError):
+        g.gemm_bf16(A, B, C=torch.empty((4, 32), dtype=torch.bfloat16))            # C in host memory
+    with pytest.raises(ValueError):
+        g.gemm_bf16(A, _FakeCudaTensor((32, 64), device_index=1), C=_FakeCudaTensor((4, 32)))
+    with pytest.raises(ValueError):
+        g.gemm_bf16_fused(A, B, bias=torch.zeros(32, dtype=torch.bfloat16), C=_FakeCudaTensor((4, 32)))
+    with pytest.raises(ValueError):
+        g.gemm_bf16(torch.empty((4, 64), dtype=torch.bfloat16), B)                 # A in host memory
