@@ -112,7 +112,9 @@ class Clocks:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        # raw samples in the system temporary directory (the JSON line carries the summary)
+        import tempfile
+        self.path = os.path.join(tempfile.gettempdir(), f"dbw_clocks_bench_{os.getpid()}.csv")
 
     def start(self):
         try:
