@@ -61,6 +61,8 @@ typedef enum {
     GEMM_VARIANT_GEMV = 1,       /* CUDA-core weight streaming, small M            */
     GEMM_VARIANT_SKINNY = 2,     /* tcgen05, weights as the MMA M side (swap AB)   */
     GEMM_VARIANT_PREFILL = 3,    /* tcgen05, persistent warp-specialised tiles     */
+                                 /* (also decode whose weight rows fill one wave   */
+                                 /* of 176-256-row tiles: no K split)              */
     GEMM_VARIANT_ZERO = 4,       /* K == 0: C is the empty sum, written as zeros   */
     GEMM_VARIANT_REGISTER = 5,   /* W4A16, M <= 32: weights dequantised into       */
                                  /* registers for warp-level MMAs (mma.sync)       */
