@@ -94,6 +94,21 @@ def flops(M, N, K):
     return 2 * M * N * K
 
 
+def roof_frac(M, N, K, ms, kind, hbm, tf):
+    """t_roof / t_measured with t_roof = max(flops / P_tc, bytes / BW): the
+    per-shape fraction of the roofline (a shape is graded on whichever side
+    bounds it).  kind: "bf16" (bytes 2(MK + NK + MN)), "w4" (the W4A16 bytes)
+    or "silu" (2N weight rows, C of N columns)."""
+    if kind == "w4":
+        fl, by = flops(M, N, K), bytes_w4(M, N, K)
+    elif kind == "silu":
+        fl, by = flops(M, 2 * N, K), 2 * (M * K + 2 * N * K + M * N)
+    else:
+        fl, by = flops(M, N, K), bytes_bf16(M, N, K)
+    t_roof = max(fl / (tf * 1e12), by / (hbm * 1e9))
+    return t_roof / (ms * 1e-3), t_roof
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -383,6 +398,56 @@ def cpu_oracle_sample(target_s=12.0):
                       f"({work / 1e6:.1f} MB algorithmic, {secs:.1f} s)"}, secs
 
 
+def cpu_oracle_configs(seconds_each=4.0):
+    """The oracle on a bounded sample of each other config (down projection,
+    prefill sweep, W4A16 decode): every shape of the config on its first rows
+    of C (rows of A for prefill, weight rows for the decode-like configs),
+    sized for about `seconds_each` seconds per config.  Rates are of the
+    sampled work: GFLOP/s (2 * MACs) and algorithmic GB/s of the sampled
+    operands."""
+    import oracle
+    from dense_bit_weight_gb300 import synth
+    # calibration: MACs per second of each oracle routine on this host
+    A = synth.bf16_normal((4, 4096), 1.0, 0, synth.STREAM_A)
+    B = synth.bf16_normal((256, 4096), 4096 ** -0.5, 0, synth.STREAM_B)
+    t = time.perf_counter()
+    oracle.gemm_bf16(A, B)
+    bf16_mac_s = 4 * 256 * 4096 / (time.perf_counter() - t)
+    Bq, S, Z = synth.w4a16_operands(256, 4096, 128, 0)
+    t = time.perf_counter()
+    oracle.gemm_w4a16(A, Bq, S, Z, 128)
+    w4_mac_s = 4 * 256 * 4096 / (time.perf_counter() - t)
+    out = {}
+    for name, shapes, kind in (("down", DOWN, "bf16"), ("prefill", PREFILL, "bf16"), ("w4a16", W4, "w4")):
+        rate = w4_mac_s if kind == "w4" else bf16_mac_s
+        total = sum(M * N * K for (M, N, K) in shapes)
+        frac = min(1.0, seconds_each * rate / total)
+        macs, by, secs = 0, 0, 0.0
+        for (M, N, K) in shapes:
+            if name == "prefill":       # the first m token rows against all weights
+                m, n = max(1, int(M * frac)), N
+            else:                       # all tokens against the first n weight rows
+                m, n = M, max(8, int(N * frac) // 8 * 8)
+            A = synth.bf16_normal((m, K), 1.0, 0, synth.STREAM_A)
+            if kind == "w4":
+                Bq, S, Z = synth.w4a16_operands(n, K, 128, 0)
+                t = time.perf_counter()
+                oracle.gemm_w4a16(A, Bq, S, Z, 128)
+                by += bytes_w4(m, n, K)
+            else:
+                B = synth.bf16_normal((n, K), K ** -0.5, 0, synth.STREAM_B)
+                t = time.perf_counter()
+                oracle.gemm_bf16(A, B)
+                by += bytes_bf16(m, n, K)
+            secs += time.perf_counter() - t
+            macs += m * n * K
+        out[name] = {"GFLOP/s": round(2 * macs / secs / 1e9, 3), "GB/s": round(by / secs / 1e9, 4),
+                     "sample": f"every shape on {'the first' if name == 'prefill' else 'all tokens x the first'} "
+                               f"{frac:.3%} of its {'token rows' if name == 'prefill' else 'weight rows'} "
+                               f"({2 * macs / 1e9:.1f} GFLOP, {secs:.1f} s)"}
+    return out
+
+
 def run_ours(args):
     import torch
     ws, rank, local = dist_init(args)
@@ -527,6 +592,16 @@ def run_ours(args):
     sweeps = None
     if rank == 0 and not args.no_sweeps:
         sweeps = {}
+
+        def graded(rs, kind):
+            # per shape: [M, N, K, rate, variant, t_roof / t_measured]; aggregate: sum t_roof / sum t
+            shapes, t_roof, t_meas = [], 0.0, 0.0
+            for r in rs:
+                f, tr = roof_frac(r["M"], r["N"], r["K"], r["ms"], kind, hbm, tf)
+                t_roof += tr
+                t_meas += r["ms"] * 1e-3
+                shapes.append(round(f, 3))
+            return shapes, (t_roof / t_meas if t_meas else None)
         pre = timed_sweep(g, torch, PREFILL, "prefill") if not args.quick else []
         if pre:
             tot_f = sum(r["work"] for r in pre)
@@ -535,6 +610,8 @@ def run_ours(args):
                                  "frac_of_peak": tot_f / (tot_ms * 1e-3) / 1e12 / tf,
                                  "shapes": [[r["M"], r["N"], r["K"], round(r["work"] / (r["ms"] * 1e-3) / 1e12, 1),
                                              r["variant"]] for r in pre]}
+            fr, agg = graded(pre, "bf16")
+            sweeps["prefill"]["roofline_frac"] = {"per_shape": fr, "aggregate": agg}
         for key, shapes, kind in (("down", DOWN, "bf16"), ("w4a16", W4, "w4")):
             rs = timed_sweep(g, torch, shapes, kind)
             tot_b = sum(r["work"] for r in rs)
@@ -543,6 +620,8 @@ def run_ours(args):
                            "frac_of_peak": tot_b / (tot_ms * 1e-3) / 1e9 / hbm,
                            "shapes": [[r["M"], r["N"], r["K"], round(r["work"] / (r["ms"] * 1e-3) / 1e9, 1),
                                        r["variant"]] for r in rs]}
+            fr, agg = graded(rs, kind)
+            sweeps[key]["roofline_frac"] = {"per_shape": fr, "aggregate": agg}
         rs = timed_sweep(g, torch, W4_PREFILL, "w4", reps=10) if not args.quick else []
         if rs:
             tot_f = sum(flops(r["M"], r["N"], r["K"]) for r in rs)
@@ -551,12 +630,16 @@ def run_ours(args):
                 "unit": "TFLOP/s", "aggregate": tot_f / (tot_ms * 1e-3) / 1e12, "frac_of_peak": tot_f / (tot_ms * 1e-3) / 1e12 / tf,
                 "shapes": [[r["M"], r["N"], r["K"], round(flops(r["M"], r["N"], r["K"]) / (r["ms"] * 1e-3) / 1e12, 1),
                             r["variant"]] for r in rs]}
+            fr, agg = graded(rs, "w4")
+            sweeps["w4a16_prefill"]["roofline_frac"] = {"per_shape": fr, "aggregate": agg}
         # the fused gate/up projection with the SiLU-mul epilogue
         rs = timed_sweep(g, torch, GATE_UP_DECODE, "silu")
         tot_b, tot_ms = sum(r["work"] for r in rs), sum(r["ms"] for r in rs)
         sweeps["gate_up_silu_decode"] = {
             "unit": "GB/s", "aggregate": tot_b / (tot_ms * 1e-3) / 1e9, "frac_of_peak": tot_b / (tot_ms * 1e-3) / 1e9 / hbm,
             "shapes": [[r["M"], r["N"], r["K"], round(r["work"] / (r["ms"] * 1e-3) / 1e9, 1), r["variant"]] for r in rs]}
+        fr, agg = graded(rs, "silu")
+        sweeps["gate_up_silu_decode"]["roofline_frac"] = {"per_shape": fr, "aggregate": agg}
         rs = timed_sweep(g, torch, GATE_UP_PREFILL, "silu_prefill") if not args.quick else []
         if rs:
             tot_f, tot_ms = sum(r["work"] for r in rs), sum(r["ms"] for r in rs)
@@ -564,16 +647,24 @@ def run_ours(args):
                 "unit": "TFLOP/s", "aggregate": tot_f / (tot_ms * 1e-3) / 1e12, "frac_of_peak": tot_f / (tot_ms * 1e-3) / 1e12 / tf,
                 "shapes": [[r["M"], r["N"], r["K"], round(r["work"] / (r["ms"] * 1e-3) / 1e12, 1), r["variant"]]
                            for r in rs]}
+            fr, agg = graded(rs, "silu")
+            sweeps["gate_up_silu_prefill"]["roofline_frac"] = {"per_shape": fr, "aggregate": agg}
         sweeps["grouped"] = grouped_sweep(g, torch)
         # each decode shape alone, graph-timed back to back (no events between launches)
         dec = timed_sweep(g, torch, DECODE, "bf16")
         sweeps["decode_per_shape"] = {"unit": "GB/s", "shapes": [
             [r["M"], r["N"], r["K"], round(r["work"] / (r["ms"] * 1e-3) / 1e9, 1), r["variant"]]
             for r in dec]}
+        fr, agg = graded(dec, "bf16")
+        sweeps["decode_per_shape"]["roofline_frac"] = {"per_shape": fr, "aggregate": agg}
+        sweeps["roofline_peaks"] = {"hbm_gbs": hbm, "bf16_tflops": tf, "source": src,
+                                    "t_roof": "max(2MNK / bf16_tflops, algorithmic bytes / hbm_gbs)"}
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
         cpu, _ = cpu_oracle_sample(args.cpu_seconds)
+        if not args.no_sweeps:
+            cpu["other_configs"] = cpu_oracle_configs()
 
     err = g.gemm_last_device_error()
     if err:

@@ -467,10 +467,18 @@ bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int
     return true;
 }
 
+// CTAs of a stream-K plan that write fp32 partial tiles: those sharing the
+// stream-K units (CTA c keeps two partial slots at 2c and 2c + 1).  When full
+// waves of whole tiles come first, only the first sk_grid CTAs share units.
+static int64_t partial_writers(const Plan &p)
+{
+    return p.whole > 0 && p.sk_grid > 0 ? std::min(p.sk_grid, p.grid) : p.grid;
+}
+
 int64_t act_copy_offset(const Plan &p)
 {
     const bool split = (p.variant == GEMM_VARIANT_SKINNY || p.variant == GEMM_VARIANT_PREFILL) && p.mode == 1;
-    const int64_t partials = split ? (int64_t)p.grid * 2 * kUmmaBM * p.bn : 0;
+    const int64_t partials = split ? partial_writers(p) * 2 * kUmmaBM * p.bn : 0;
     return (partials + 63) / 64 * 64;   // 256-byte aligned
 }
 
@@ -479,7 +487,7 @@ void workspace_need(const Plan &p, int64_t M, int64_t N, int64_t K, int64_t *flo
     *floats = 0;
     *counters = 0;
     if ((p.variant == GEMM_VARIANT_SKINNY || p.variant == GEMM_VARIANT_PREFILL) && p.mode == 1) {
-        *floats = (int64_t)p.grid * 2 * kUmmaBM * p.bn;
+        *floats = partial_writers(p) * 2 * kUmmaBM * p.bn;
         *counters = ((M + p.tile_m - 1) / p.tile_m) * ((N + p.tile_n - 1) / p.tile_n);
     }
     if (p.variant == GEMM_VARIANT_FRAGMENT) {

@@ -4,19 +4,18 @@
 // gemm_bf16 lazily cudaMalloc's a device error word and, for split-K
 // (stream-K) launches, a per-stream workspace of fp32 partial tiles and
 // per-tile arrival counters.  Some callers cannot let a library do that:
-// code being captured into a CUDA graph in global capture mode (cudaMalloc is
-// refused while the stream captures), programs whose caching allocator has
-// already reserved the device's memory budget, and latency-critical loops
-// where the implicit device synchronisation of cudaMalloc/cudaFree would
-// stall other streams.  This entry point runs the same kernels with the
-// split-K scratch taken from fixed arrays in this file instead.
+// programs whose caching allocator has already reserved the device's memory
+// budget, and latency-critical loops where the implicit device
+// synchronisation of cudaMalloc/cudaFree would stall other streams.  This
+// entry point runs the same kernels with the split-K scratch taken from fixed
+// arrays in this file instead.
 //
 // The arrays are file-scope __device__ objects, so every GPU that loads the
 // library holds them (16 MiB of partials, 64 KiB of counters, one error
 // word) until the process exits.  In host code their names are host-side
 // stand-ins, not device addresses; the device addresses come from
 // cudaGetSymbolAddress, once per device, on the first call with that device
-// current.  That first call should therefore come before any stream capture.
+// current.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -117,10 +116,18 @@ extern "C" int gemm_bf16_noalloc(const void *A, const void *B, void *C, int64_t 
 
     const bool umma = p.variant == GEMM_VARIANT_SKINNY || p.variant == GEMM_VARIANT_PREFILL;
     if (umma && p.mode == 1) {
-        // fit the split-K partials in the fixed array: fewer CTAs share the units
+        // fit the split-K partials in the fixed array.  Only the CTAs that
+        // share the stream-K units write partials (two tiles' worth each):
+        // when full waves of whole tiles come first, only those sharing CTAs
+        // are capped and every SM still takes whole tiles; a plan that is
+        // stream-K throughout runs on fewer CTAs instead.
         const int64_t per_cta = 2 * (int64_t)kUmmaBM * p.bn;
-        const int64_t max_grid = kScratchFloats / per_cta;
-        if (p.grid > max_grid) p.grid = (int)max_grid;
+        const int64_t max_writers = kScratchFloats / per_cta;
+        if (p.whole > 0 && p.sk_grid > 0) {
+            if (p.sk_grid > max_writers) p.sk_grid = (int)max_writers;
+        } else if (p.grid > max_writers) {
+            p.grid = (int)max_writers;
+        }
         int64_t R = p.variant == GEMM_VARIANT_SKINNY ? N : M, Q = p.variant == GEMM_VARIANT_SKINNY ? M : N;
         const int64_t tiles = ((R + kUmmaBM - 1) / kUmmaBM) * ((Q + p.bn - 1) / p.bn);
         if (tiles > kScratchCounters) return GEMM_ERR_SHAPE;
@@ -135,4 +142,22 @@ extern "C" int gemm_bf16_noalloc(const void *A, const void *B, void *C, int64_t 
     default: e = launch_umma_bf16(a, p, c); break;
     }
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+extern "C" int gemm_bf16_noalloc_last_error(void)
+{
+    // the word gemm_bf16_noalloc's kernels write on a bounded-wait expiry;
+    // read and cleared with symbol copies, which allocate nothing
+    ScratchPtrs *s = nullptr;
+    int rc = scratch_for_device(&s);
+    if (rc) return rc;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_scratch_error, sizeof v, 0, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_scratch_error, &zero, sizeof zero, 0, cudaMemcpyHostToDevice) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+    }
+    return v;
 }

@@ -38,13 +38,14 @@
 //           last one adds all partials in increasing-k order (deterministic,
 //           no float atomics) and resets the counter to zero.
 //   mode 2  cluster split-K (decode): the S CTAs that split one tile's K
-//           form a thread-block cluster.  Each writes its fp32 partial to its
-//           own shared memory; after a cluster barrier it sends row slice o
-//           of that partial to CTA o with one bulk shared-to-shared copy
-//           (completion counted on CTA o's mbarrier), and each CTA sums the S
-//           slices it owns from its own shared memory in rank order
-//           (deterministic, no global scratch).  One tile per CTA; the grid is
-//           small enough for every CTA to be resident at once.
+//           form a thread-block cluster, and CTA o owns row block o of the
+//           tile.  Each CTA reads its fp32 partial from TMEM and sends every
+//           row to the row's owner with 16-byte st.async remote stores into
+//           slice `rank` of the owner's exchange region (bytes counted on the
+//           owner's mbarrier); the owner sums its S slices in rank order
+//           (deterministic, no global scratch), rounds to bf16 into a staging
+//           tile and writes its block of C with one TMA store.  One tile per
+//           CTA; the grid is small enough for every CTA to be resident at once.
 //
 // Launches use programmatic dependent launch: a kernel's prologue (barrier
 // set-up, TMEM allocation, descriptor prefetch) overlaps the tail of the

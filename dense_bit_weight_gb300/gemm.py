@@ -26,7 +26,7 @@ VARIANT_NAME = {v: k for k, v in VARIANT.items()}
 
 EXPORTS = ["gemm_bf16", "gemm_w4a16", "gemm_bf16_ex", "gemm_w4a16_ex", "gemm_bf16_plan",
            "gemm_w4a16_plan", "gemm_last_device_error", "gemm_status_string", "gemm_shutdown",
-           "gemm_debug_inject_timeout", "gemm_bf16_noalloc", "gemm_bf16_fused", "gemm_bf16_fused_ex",
+           "gemm_debug_inject_timeout", "gemm_bf16_noalloc", "gemm_bf16_noalloc_last_error", "gemm_bf16_fused", "gemm_bf16_fused_ex",
            "gemm_bf16_grouped", "gemm_bf16_fused_plan"]
 
 
@@ -50,6 +50,8 @@ lib.gemm_bf16_grouped.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, 
 lib.gemm_bf16_grouped.restype = _i
 lib.gemm_bf16_noalloc.argtypes = lib.gemm_bf16.argtypes
 lib.gemm_bf16_noalloc.restype = _i
+lib.gemm_bf16_noalloc_last_error.argtypes = []
+lib.gemm_bf16_noalloc_last_error.restype = _i
 lib.gemm_w4a16.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _p]
 lib.gemm_w4a16_ex.argtypes = lib.gemm_w4a16.argtypes + [_i]
 lib.gemm_bf16_plan.argtypes = [_i64, _i64, _i64, _i, _i, ctypes.POINTER(gemm_plan)]
@@ -84,6 +86,11 @@ def gemm_status_string(status: int) -> str:
 
 def gemm_last_device_error() -> int:
     return int(lib.gemm_last_device_error())
+
+
+def gemm_bf16_noalloc_last_error() -> int:
+    """The watchdog word of gemm_bf16_noalloc (read and cleared)."""
+    return int(lib.gemm_bf16_noalloc_last_error())
 
 
 def gemm_debug_inject_timeout(enable: bool) -> bool:

@@ -186,36 +186,46 @@ int gemm_bf16_grouped(const void *A, const void *B, void *C, const void *ends, i
  * library, not of the method.)
  *
  * gemm_bf16 lazily allocates its device error word and, for split-K
- * launches, a per-stream workspace.  Code that cannot let a library call
- * cudaMalloc -- a stream being captured into a CUDA graph in global capture
- * mode (allocation is refused there), a program whose own caching allocator
- * already holds the device memory budget, or a latency-critical loop that
- * cannot afford the implicit device synchronisation of cudaMalloc/cudaFree --
- * calls this instead.  Arguments, layouts, preconditions and results are
- * those of gemm_bf16; it allocates nothing.
+ * launches, a per-stream workspace.  Some callers cannot let a library call
+ * cudaMalloc: a program whose own caching allocator already holds the device
+ * memory budget (a library allocation would fail or fragment it), or a
+ * latency-critical loop that cannot afford the implicit device
+ * synchronisation of cudaMalloc/cudaFree.  They call this instead.
+ * Arguments, layouts, preconditions and results are those of gemm_bf16; it
+ * allocates nothing.
  *
  *   - Scratch: split-K partial tiles and per-tile counters live in fixed
  *     file-scope device arrays of the library: 16 MiB of fp32 partials and
  *     16384 counters.  Every GPU that loads the library holds them until the
  *     process exits.  When a split-K plan would need more partials than fit,
- *     fewer CTAs share the work instead; a split plan with more than 16384
- *     output tiles is rejected with GEMM_ERR_SHAPE (the current planner never
- *     splits that many tiles).
+ *     fewer CTAs share the split work (full waves of whole tiles still run on
+ *     every SM); a split plan with more than 16384 output tiles is rejected
+ *     with GEMM_ERR_SHAPE (the current planner never splits that many tiles).
  *   - Set-up: the first call on a device, with that device current, looks up
- *     the arrays' device addresses (cudaGetSymbolAddress); make that first
- *     call before any stream capture.
+ *     the arrays' device addresses (cudaGetSymbolAddress).
  *   - Sharing: all calls on a device share the arrays, which keep the last
  *     call's contents.  The counters are cleared on the stream at the start
  *     of each split-K call.  Calls that overlap on the GPU (different streams
  *     without ordering between them) race on the scratch and give undefined
  *     results; order them.
- *   - Watchdog: its kernels' bounded waits still end them cleanly, but an
- *     expiry is recorded in a word of this entry point's own, not in the word
- *     gemm_last_device_error() reads.
+ *   - Watchdog: its kernels' bounded waits end them cleanly; an expiry is
+ *     recorded in a word of this entry point's own, which
+ *     gemm_bf16_noalloc_last_error() reads (not gemm_last_device_error()).
  * Returns gemm_status.
  */
 int gemm_bf16_noalloc(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
                       int64_t lda, int64_t ldb, int64_t ldc, void *stream);
+
+/*
+ * gemm_bf16_noalloc_last_error -- the watchdog word of gemm_bf16_noalloc on
+ * the current device: GEMM_ERR_DEVICE_TIMEOUT when one of its kernels' bounded
+ * waits expired since the last read (C of that call is then unspecified),
+ * GEMM_OK otherwise.  Reading clears it.  Call after synchronising the
+ * stream; it copies one int each way (cudaMemcpyFromSymbol/ToSymbol, which
+ * allocate nothing and synchronise with the legacy default stream).  After a
+ * timeout the next split-K call clears the counters itself.
+ */
+int gemm_bf16_noalloc_last_error(void);
 
 /*
  * gemm_bf16_ex / gemm_w4a16_ex -- as above, but `variant` may force a kernel

@@ -1,6 +1,6 @@
 """Run one GEMM shape repeatedly on the GPU (for profiling and quick timing).
 
-    python -m dense_bit_weight_gb300.run_case --M 1 --N 24576 --K 4096 \
+    python run_case.py --M 1 --N 24576 --K 4096 \
         [--kind bf16|w4a16|silu_mul|grouped] [--variant auto|gemv|skinny|prefill]
         [--groups G] [--reps 4] [--copies 0]
 

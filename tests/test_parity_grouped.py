@@ -2,7 +2,10 @@
 
 Uniform, ragged, empty and skewed expert loads, offsets that end before M
 (rows past the last expert are not written) and out-of-range offsets (which
-the kernel clamps), compared element by element; integer-valued inputs must
+the kernel clamps), compared element by element, and the three loads the
+bench times at full size (8 experts x 512 tokens and a ragged 16-expert load
+with empty experts, N = K = 4096; 128 experts x 4 tokens, N = 1536, K = 2048),
+also every element; integer-valued inputs must
 match bit for bit, N(0,1) inputs satisfy |out - ref| <= 1e-2*|ref| + 1e-2*rms(ref).
 """
 import numpy as np
@@ -48,6 +51,10 @@ CASES = [  # (expert token counts, N, K, spare rows past the last expert)
     ([0, 0, 0, 1000], 264, 1024, 3),                # all tokens on one expert
     ([3] * 64, 256, 128, 0),                        # many small experts (decode-like)
     ([130], 4104, 72, 0),                           # one expert = the plain GEMM, ragged N
+    # the bench's loads, full size
+    ([512] * 8, 4096, 4096, 0),
+    ([1024, 0, 512, 37, 0, 800, 256, 1, 600, 0, 300, 64, 200, 150, 100, 52], 4096, 4096, 0),
+    ([4] * 128, 1536, 2048, 0),
 ]
 
 
