@@ -156,6 +156,10 @@ int run(const GemmArgs &a, const Plan &p, cudaStream_t st, bool w4)
         if (!w4) return GEMM_ERR_VARIANT;
         e = launch_w4_frag(a, p, c);
         break;
+    case GEMM_VARIANT_GROUPWISE:
+        if (!w4) return GEMM_ERR_VARIANT;
+        e = launch_w4tc(a, p, c);
+        break;
     case GEMM_VARIANT_SKINNY:
     case GEMM_VARIANT_PREFILL:
         if (w4 && p.variant != GEMM_VARIANT_SKINNY) return GEMM_ERR_VARIANT;
@@ -406,6 +410,29 @@ bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int
         p->grid = w4_register_grid(N);
         return true;
     }
+    if (variant == GEMM_VARIANT_GROUPWISE) {
+        // tokens in tiles of 16, 32 or 64; 128-k stages; stream-K over every SM
+        int bn = 16;
+        while (bn < M && bn < 64) bn *= 2;
+        const int64_t tiles_r = (N + kUmmaBM - 1) / kUmmaBM, tiles_q = (M + bn - 1) / bn;
+        const int64_t nk = (K + 127) / 128;
+        const int64_t units = tiles_r * tiles_q * nk;
+        p->variant = GEMM_VARIANT_GROUPWISE;
+        p->kernels = 2;                      // activation copy and group sums, then the GEMM
+        p->act_copy = 1;
+        p->bn = bn;
+        p->tile_m = bn;
+        p->tile_n = kUmmaBM;
+        p->group_r = tiles_q > 1 ? 1 : (int)tiles_r;   // token tiles of a weight tile run next to each other
+        p->ctas_per_sm = 1;
+        p->stages = w4tc_stages(bn);
+        p->mode = 1;
+        p->grid = (int)std::min<int64_t>(sm_count, units);
+        const int64_t per_cta = units / p->grid;
+        p->split = (int)std::min<int64_t>(p->grid, (nk + per_cta - 1) / per_cta + 1);
+        p->ws_extra = tiles_q * bn * (K / group);   // group sums [K / group][tokens padded to whole tiles]
+        return true;
+    }
     if (variant == GEMM_VARIANT_FRAGMENT) {
         if (M > 16) return false;
         p->variant = GEMM_VARIANT_FRAGMENT;
@@ -475,9 +502,17 @@ static int64_t partial_writers(const Plan &p)
     return p.whole > 0 && p.sk_grid > 0 ? std::min(p.sk_grid, p.grid) : p.grid;
 }
 
+// Plans whose kernel keeps stream-K partials (and tile counters) in the workspace.
+static bool streamk_partials(const Plan &p)
+{
+    return (p.variant == GEMM_VARIANT_SKINNY || p.variant == GEMM_VARIANT_PREFILL ||
+            p.variant == GEMM_VARIANT_GROUPWISE) &&
+           p.mode == 1;
+}
+
 int64_t act_copy_offset(const Plan &p)
 {
-    const bool split = (p.variant == GEMM_VARIANT_SKINNY || p.variant == GEMM_VARIANT_PREFILL) && p.mode == 1;
+    const bool split = streamk_partials(p);
     const int64_t partials = split ? partial_writers(p) * 2 * kUmmaBM * p.bn : 0;
     return (partials + 63) / 64 * 64;   // 256-byte aligned
 }
@@ -486,7 +521,7 @@ void workspace_need(const Plan &p, int64_t M, int64_t N, int64_t K, int64_t *flo
 {
     *floats = 0;
     *counters = 0;
-    if ((p.variant == GEMM_VARIANT_SKINNY || p.variant == GEMM_VARIANT_PREFILL) && p.mode == 1) {
+    if (streamk_partials(p)) {
         *floats = partial_writers(p) * 2 * kUmmaBM * p.bn;
         *counters = ((M + p.tile_m - 1) / p.tile_m) * ((N + p.tile_n - 1) / p.tile_n);
     }

@@ -95,6 +95,20 @@ cudaError_t launch_w4_frag(const GemmArgs &a, const Plan &p, const LaunchCtx &c)
 int w4_frag_split(int64_t N, int64_t K, int sm_count, int tile_m);
 int w4_frag_grid(int64_t N, int P);
 int64_t w4_frag_workspace_floats(int64_t M, int64_t TP, int64_t K, int64_t group);
+// The W4A16 activation pre-pass (w4frag.cu): Ap = A with every 8-k block in
+// the order 0,4,1,5,2,6,3,7, and S[g][m] = sum of A[m, k] over group g for
+// tokens m < TP (zero for m >= M).  TP * K / 8 threads.
+cudaError_t launch_w4_prep(const GemmArgs &a, const LaunchCtx &c, uint16_t *Ap, float *S, int TP);
+// W4A16 on tcgen05 with per-group accumulators (w4tc.cu): token tiles of bn
+// (16, 32 or 64), 128-k stages, stream-K over (weight tile, stage) units.
+int w4tc_stages(int bn);
+cudaError_t launch_w4tc(const GemmArgs &a, const Plan &p, const LaunchCtx &c);
+// bf16 [rows, K] K-major (leading dimension ld, elements): TMA boxes of 64 k x
+// box_rows rows, 128-byte swizzle, out-of-range elements read as zero.
+bool make_map_bf16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int64_t ld, int box_rows);
+// Packed 4-bit weights [rows, K/8] (uint32): boxes of 16 words (128 k) x
+// box_rows rows, 64-byte swizzle.
+bool make_map_words16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int box_rows);
 
 // tcgen05 kernel geometry (umma.cu)
 constexpr int kUmmaBM = 128;

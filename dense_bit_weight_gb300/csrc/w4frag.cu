@@ -457,6 +457,13 @@ int64_t w4_frag_workspace_floats(int64_t M, int64_t TP, int64_t K, int64_t group
     return (M * K + 127) / 128 * 64 + TP * (K / group);
 }
 
+cudaError_t launch_w4_prep(const GemmArgs &a, const LaunchCtx &c, uint16_t *Ap, float *S, int TP)
+{
+    const int64_t items = (int64_t)TP * (a.K / 8);
+    return launch_pdl(k_w4_frag_prep, (int)((items + 255) / 256), 256, 0, c.stream, (const uint16_t *)a.A, Ap, S,
+                      (int)a.M, TP, (int)a.K, (int)a.group);
+}
+
 cudaError_t launch_w4_frag(const GemmArgs &a, const Plan &p, const LaunchCtx &c)
 {
     if (!c.act_copy) return cudaErrorInvalidValue;
@@ -465,9 +472,7 @@ cudaError_t launch_w4_frag(const GemmArgs &a, const Plan &p, const LaunchCtx &c)
     float *S = reinterpret_cast<float *>(Ap + (a.M * a.K + 127) / 128 * 128);
     CUtensorMap m;
     if (!make_map_words(&m, a.B, a.N, a.K, kW4FragRows)) return cudaErrorInvalidValue;
-    const int items = TP * (int)(a.K / 8);
-    cudaError_t e = launch_pdl(k_w4_frag_prep, (items + 255) / 256, 256, 0, c.stream, (const uint16_t *)a.A, Ap, S,
-                               (int)a.M, TP, (int)a.K, (int)a.group);
+    cudaError_t e = launch_w4_prep(a, c, Ap, S, TP);
     if (e != cudaSuccess) return e;
     return TP <= 8 ? launch_frag_nt<1>(m, a, c, Ap, S, p.grid, p.split)
                    : launch_frag_nt<2>(m, a, c, Ap, S, p.grid, p.split);

@@ -66,8 +66,11 @@ typedef enum {
     GEMM_VARIANT_ZERO = 4,       /* K == 0: C is the empty sum, written as zeros   */
     GEMM_VARIANT_REGISTER = 5,   /* W4A16, M <= 32: weights dequantised into       */
                                  /* registers for warp-level MMAs (mma.sync)       */
-    GEMM_VARIANT_FRAGMENT = 6    /* W4A16, M <= 16: weights streamed by TMA and    */
+    GEMM_VARIANT_FRAGMENT = 6,   /* W4A16, M <= 16: weights streamed by TMA and    */
                                  /* dequantised into mma.sync fragments            */
+    GEMM_VARIANT_GROUPWISE = 7   /* W4A16: exact 128 + q weights in tensor memory, */
+                                 /* one tcgen05 accumulator per quantisation       */
+                                 /* group, scale and zero applied per group        */
 } gemm_variant;
 
 typedef struct {
