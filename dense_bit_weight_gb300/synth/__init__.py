@@ -28,6 +28,7 @@ _lib = None
 # stream ids: one per operand so operands are independent
 STREAM_A, STREAM_B, STREAM_Q, STREAM_Z, STREAM_S = 1, 2, 3, 4, 5
 STREAM_A_INT, STREAM_B_INT = 11, 12
+STREAM_MX_A, STREAM_MX_B, STREAM_MX_SA, STREAM_MX_SB = 21, 22, 23, 24
 
 
 def build(force: bool = False) -> str:
@@ -129,3 +130,72 @@ def w4a16_operands(n_rows: int, k: int, group: int = 128, seed: int = 0,
     return (packed_int4(n_rows, k, seed, STREAM_Q),
             bf16_uniform((n_rows, g), scale_lo, scale_hi, seed, STREAM_S),
             zeros_uint4(n_rows, g, seed, STREAM_Z))
+
+
+# ------------------------------------------------------------ MX (microscaling) operands
+# Codes are drawn field by field (sign, exponent, mantissa), so no value is
+# computed here; the formats are the OCP ones (E4M3 "fn": s eeee mmm, bias 7;
+# E2M1: s ee m, bias 1; E8M0: a biased exponent).
+
+# E4M3 / E2M1 codes of the integers 0..4 (for exactly representable cases)
+_E4M3_INT = {0: 0x00, 1: 0x38, 2: 0x40, 3: 0x44, 4: 0x48}
+_E2M1_INT = {0: 0x0, 1: 0x2, 2: 0x4, 3: 0x5, 4: 0x6}
+
+
+def e4m3_codes(shape, seed: int = 0, stream: int = STREAM_MX_A, exp_lo: int = 4, exp_hi: int = 10) -> np.ndarray:
+    """E4M3 codes with a uniform sign, an exponent field uniform in
+    [exp_lo, exp_hi] (the default spans 2^-3 .. 2^3 x 1.m) and a uniform
+    3-bit mantissa; exp_hi <= 14 never draws the NaN code.  uint8 of shape."""
+    if not 0 <= exp_lo <= exp_hi <= 14:
+        raise ValueError("exponent field range must lie in [0, 14]")
+    n = _n(shape)
+    sgn = int_uniform((n,), 0, 1, seed, stream)
+    ex = int_uniform((n,), exp_lo, exp_hi, seed, stream + 100)
+    man = int_uniform((n,), 0, 7, seed, stream + 200)
+    return ((sgn << 7) | (ex << 3) | man).astype(np.uint8).reshape(shape)
+
+
+def e2m1_packed(rows: int, k: int, seed: int = 0, stream: int = STREAM_MX_B) -> np.ndarray:
+    """Packed E2M1 operand [rows, k/2]: every nibble a uniform 4-bit code
+    (all sixteen codes are finite values)."""
+    if k % 8:
+        raise ValueError("k must be a multiple of 8")
+    out = np.empty(rows * (k // 8), dtype=np.uint32)
+    _load().synth_u32(seed, stream, 0, out.size, out.ctypes.data)
+    return out.view(np.uint8).reshape(rows, k // 2)
+
+
+def e8m0_codes(shape, lo: int = 124, hi: int = 130, seed: int = 0, stream: int = STREAM_MX_SA) -> np.ndarray:
+    """E8M0 scale codes uniform in [lo, hi] (default 2^-3 .. 2^3), uint8."""
+    if not 0 <= lo <= hi <= 254:
+        raise ValueError("scale codes must lie in [0, 254]")
+    return int_uniform(shape, lo, hi, seed, stream).astype(np.uint8)
+
+
+def mx_int_operand(rows: int, k: int, fmt: str, lo: int = -4, hi: int = 4, seed: int = 0,
+                   stream: int = STREAM_MX_A) -> np.ndarray:
+    """Integers uniform in [lo, hi] (|v| <= 4) as MX element codes: E4M3 bytes
+    [rows, k], or packed E2M1 [rows, k/2] (element k in the low nibble for
+    even k)."""
+    if not -4 <= lo <= hi <= 4:
+        raise ValueError("|v| <= 4")
+    v = int_uniform((rows, k), lo, hi, seed, stream)
+    table = _E4M3_INT if fmt == "e4m3" else _E2M1_INT
+    sign = 0x80 if fmt == "e4m3" else 0x8
+    mag = np.vectorize(table.get, otypes=[np.int64])(np.abs(v))
+    codes = (mag | np.where(v < 0, sign, 0)).astype(np.uint8)
+    if fmt == "e4m3":
+        return codes
+    return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+
+
+def mx_operands(rows: int, k: int, fmt: str, seed: int = 0, role: str = "a", kind: str = "random"):
+    """(elements, scales) of one MX operand: random codes with scales in
+    2^-3 .. 2^3, or (kind "int") integers in [-4, 4] with unit scales (code
+    127), so every product and partial sum is exact."""
+    es = STREAM_MX_A if role == "a" else STREAM_MX_B
+    ss = STREAM_MX_SA if role == "a" else STREAM_MX_SB
+    if kind == "int":
+        return mx_int_operand(rows, k, fmt, seed=seed, stream=es), np.full((rows, k // 32), 127, np.uint8)
+    el = e4m3_codes((rows, k), seed, es) if fmt == "e4m3" else e2m1_packed(rows, k, seed, es)
+    return el, e8m0_codes((rows, k // 32), seed=seed, stream=ss)

@@ -61,6 +61,10 @@ def _load():
             lib.oracle_epilogue.restype = ctypes.c_int
             lib.oracle_gemm_grouped.argtypes = [p, p, p, p, i64, i64, i64, i64, ctypes.c_int]
             lib.oracle_gemm_grouped.restype = ctypes.c_int
+            lib.oracle_gemm_mx.argtypes = [ctypes.c_int, p, p, ctypes.c_int, p, p, p, i64, i64, i64, ctypes.c_int]
+            lib.oracle_gemm_mx.restype = ctypes.c_int
+            lib.oracle_mx_decode.argtypes = [ctypes.c_int, p, p, i64]
+            lib.oracle_mx_decode.restype = ctypes.c_int
             lib.oracle_hardware_threads.argtypes = []
             lib.oracle_hardware_threads.restype = ctypes.c_int
             _lib = lib
@@ -187,6 +191,45 @@ def gemm_grouped(A_bits: np.ndarray, B_bits: np.ndarray, ends: np.ndarray,
     if rc != 0:
         raise RuntimeError(f"oracle_gemm_grouped returned {rc}")
     return R
+
+
+MX_FORMATS = {"e4m3": 0, "e2m1": 1}
+
+
+def gemm_mx(A: np.ndarray, SA: np.ndarray, B: np.ndarray, SB: np.ndarray, fmt_a: str = "e4m3",
+            fmt_b: str = "e4m3", threads: int | None = None) -> np.ndarray:
+    """The block-scaled (MX) GEMM in fp64 (unrounded):
+    R[m,n] = sum_k a[m,k] 2^(SA[m,k/32]-127) * b[n,k] 2^(SB[n,k/32]-127).
+
+    A: uint8 E4M3 codes [M,K] or packed E2M1 [M,K/2] (element k in bits
+    4*(k%2)..); B likewise [N,K] / [N,K/2]; SA uint8 [M,K/32], SB uint8
+    [N,K/32] E8M0 codes.
+    """
+    fa, fb = MX_FORMATS[fmt_a], MX_FORMATS[fmt_b]
+    A = _as(A, np.uint8, "A")
+    B = _as(B, np.uint8, "B")
+    SA = _as(SA, np.uint8, "SA")
+    SB = _as(SB, np.uint8, "SB")
+    M, N = A.shape[0], B.shape[0]
+    K = A.shape[1] * (2 if fa else 1)
+    if B.shape[1] * (2 if fb else 1) != K or K % 32 or SA.shape != (M, K // 32) or SB.shape != (N, K // 32):
+        raise ValueError("MX operand shapes do not match")
+    R = np.empty((M, N), dtype=np.float64)
+    rc = _load().oracle_gemm_mx(fa, _ptr(A), _ptr(SA), fb, _ptr(B), _ptr(SB), _ptr(R), M, N, K,
+                                threads or hardware_threads())
+    if rc != 0:
+        raise RuntimeError(f"oracle_gemm_mx returned {rc}")
+    return R
+
+
+def mx_decode(codes: np.ndarray, kind: str) -> np.ndarray:
+    """Values of MX codes (one per byte): kind "e4m3", "e2m1" (low nibble) or "e8m0"."""
+    c = _as(codes, np.uint8, "codes")
+    out = np.empty(c.shape, dtype=np.float64)
+    rc = _load().oracle_mx_decode({"e4m3": 0, "e2m1": 1, "e8m0": 2}[kind], _ptr(c), _ptr(out), c.size)
+    if rc != 0:
+        raise RuntimeError(f"oracle_mx_decode returned {rc}")
+    return out
 
 
 def dequant_w4(Bq: np.ndarray, scales_bits: np.ndarray, zeros: np.ndarray, group: int) -> np.ndarray:

@@ -55,6 +55,24 @@
  *       with uneven load" (concatenated activations, grouped weights,
  *       offsets marking each expert's rows; empty experts own no rows).
  *
+ *   oracle_gemm_mx         the block-scaled (microscaling, "MX") GEMM:
+ *       R[m,n] = sum_k (a[m,k] * 2^(sa[m,k/32] - 127)) * (b[n,k] * 2^(sb[n,k/32] - 127))
+ *       FlyDSL-in-PyTorch blog, section "MXFP": operands FP8 E4M3 or packed
+ *       FP4 E2M1, one E8M0 scale per 32 values along the reduction axis
+ *       (BlockWise1x32), fp32 accumulation, fp16/bf16 output, K a multiple of
+ *       128, unit stride along K for A and B; FlyDSL prebuilt kernels guide
+ *       §3.1, the MX GEMM note (per-32 E8M0 scales).  The element codes follow
+ *       the OCP microscaling formats the pages name:
+ *         E4M3  s eeee mmm, bias 7: (1 + m/8) 2^(e-7), subnormal (m/8) 2^-6,
+ *               no infinities, s 1111 111 is NaN (the "e4m3fn" of the pages)
+ *         E2M1  s ee m, bias 1: (1 + m/2) 2^(e-1), subnormal m/2
+ *         E8M0  unsigned exponent: 2^(e-127), 0xFF is NaN
+ *       Layouts (the pages say "packed FP4" only; this is the library's
+ *       stated format): E4M3 one byte per element, [rows, K]; E2M1 two per
+ *       byte along K, [rows, K/2], element k in bits 4*(k%2) .. 4*(k%2)+3
+ *       (low nibble first); scales uint8 [rows, K/32].  Every product is
+ *       exact in fp64.
+ *
  * Threads: outputs are split into contiguous ranges of the flattened (m,n)
  * index over POSIX threads; each output is computed by exactly one thread in
  * the same k order, so the result does not depend on the thread count.
@@ -294,5 +312,103 @@ int oracle_gemm_grouped(const uint16_t *A, const uint16_t *B, const int32_t *end
         }
         start = end;
     }
+    return 0;
+}
+
+/* ------------------------------------------------------------ MX GEMM */
+
+/* OCP E4M3 ("fn": no infinities): s eeee mmm, exponent bias 7. */
+static double e4m3_to_f64(uint8_t c)
+{
+    const int sgn = c >> 7, e = (c >> 3) & 0xF, m = c & 7;
+    if (e == 0xF && m == 7) return NAN;
+    /* normal (1 + m/8) 2^(e-7) = (8 + m) 2^(e-10); subnormal (m/8) 2^-6 = m 2^-9 */
+    const double v = e == 0 ? ldexp((double)m, -9) : ldexp(8.0 + m, e - 10);
+    return sgn ? -v : v;
+}
+
+/* OCP E2M1: s ee m, exponent bias 1. */
+static double e2m1_to_f64(uint8_t c)
+{
+    const int sgn = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+    /* normal (1 + m/2) 2^(e-1) = (2 + m) 2^(e-2); subnormal m/2 */
+    const double v = e == 0 ? 0.5 * m : ldexp(2.0 + m, e - 2);
+    return sgn ? -v : v;
+}
+
+/* OCP E8M0 scale: 2^(e-127); 0xFF is NaN. */
+static double e8m0_to_f64(uint8_t c) { return c == 0xFF ? NAN : ldexp(1.0, (int)c - 127); }
+
+/* Element k of row `row` of an MX operand (fmt 0: E4M3 [rows, ld] bytes;
+ * fmt 1: E2M1 packed two per byte, [rows, ld/2] bytes). */
+static double mx_elem(int fmt, const uint8_t *X, int64_t ld, int64_t row, int64_t k)
+{
+    if (fmt == 0) return e4m3_to_f64(X[row * ld + k]);
+    const uint8_t byte = X[row * (ld / 2) + k / 2];
+    return e2m1_to_f64((uint8_t)((byte >> (4 * (k % 2))) & 0xF));
+}
+
+typedef struct {
+    int fa, fb;
+    const uint8_t *A, *SA, *B, *SB;
+    double *R;
+    int64_t M, N, K;
+    int64_t begin, end;
+} mx_job;
+
+static void *mx_worker(void *arg)
+{
+    const mx_job *j = (const mx_job *)arg;
+    const int64_t nb = j->K / 32;
+    for (int64_t idx = j->begin; idx < j->end; ++idx) {
+        const int64_t m = idx / j->N, n = idx % j->N;
+        double acc = 0.0;
+        for (int64_t k = 0; k < j->K; ++k) {
+            const double a = mx_elem(j->fa, j->A, j->K, m, k) * e8m0_to_f64(j->SA[m * nb + k / 32]);
+            const double b = mx_elem(j->fb, j->B, j->K, n, k) * e8m0_to_f64(j->SB[n * nb + k / 32]);
+            acc += a * b;
+        }
+        j->R[idx] = acc;
+    }
+    return NULL;
+}
+
+/* fmt_a, fmt_b: 0 = E4M3, 1 = E2M1 (packed).  A: [M, K] elements, B: [N, K]
+ * elements, SA: [M, K/32], SB: [N, K/32] E8M0 codes; R [M, N] row-major.
+ * Returns 0, or 2 on a bad format or size (K must be a multiple of 32). */
+int oracle_gemm_mx(int fmt_a, const uint8_t *A, const uint8_t *SA, int fmt_b, const uint8_t *B,
+                   const uint8_t *SB, double *R, int64_t M, int64_t N, int64_t K, int nthreads)
+{
+    if ((fmt_a != 0 && fmt_a != 1) || (fmt_b != 0 && fmt_b != 1) || M < 0 || N < 0 || K < 0 || K % 32)
+        return 2;
+    const int64_t total = M * N;
+    if (total == 0) return 0;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > total) nthreads = (int)total;
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof *th);
+    mx_job *jobs = (mx_job *)calloc((size_t)nthreads, sizeof *jobs);
+    if (!th || !jobs) { free(th); free(jobs); return 3; }
+    for (int t = 0; t < nthreads; ++t) {
+        mx_job j = {fmt_a, fmt_b, A, SA, B, SB, R, M, N, K, total * t / nthreads, total * (t + 1) / nthreads};
+        jobs[t] = j;
+        if (pthread_create(&th[t], NULL, mx_worker, &jobs[t]) != 0) {
+            mx_worker(&jobs[t]);
+            th[t] = 0;
+        }
+    }
+    for (int t = 0; t < nthreads; ++t)
+        if (th[t]) pthread_join(th[t], NULL);
+    free(th);
+    free(jobs);
+    return 0;
+}
+
+/* Decoded values of MX codes, for pins: kind 0 = E4M3, 1 = E2M1 (one code
+ * per byte, low nibble), 2 = E8M0. */
+int oracle_mx_decode(int kind, const uint8_t *codes, double *out, int64_t n)
+{
+    if (kind < 0 || kind > 2 || n < 0) return 2;
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = kind == 0 ? e4m3_to_f64(codes[i]) : kind == 1 ? e2m1_to_f64(codes[i] & 0xF) : e8m0_to_f64(codes[i]);
     return 0;
 }
