@@ -29,15 +29,19 @@
 //   warps 7-14  dequantisation: two warpgroups take the stages alternately;
 //               a warp handles its 32 weight rows (its tensor-memory lane
 //               quarter) for the whole 128-k stage, so it meets the other
-//               roles once per two stages.  Each warpgroup alternates between
-//               two tensor-memory stage buffers of 64 columns.
-// The packed-weight and activation rings have multiples of four slots, so a
-// slot is only ever used by the stages of one warpgroup (its mbarrier phases
-// are never skipped by a waiter).
+//               roles once per two stages.  The NXB tensor-memory stage
+//               buffers (6 for token tiles up to 32, else 4) are used in turn,
+//               so each warpgroup can run NXB / 2 stages ahead of the MMAs.
+// The packed-weight and activation rings and the stage buffers have even
+// counts, so a slot is only ever used by the stages of one warpgroup (its
+// mbarrier phases are never skipped by a waiter).
 //
-// Tensor memory (512 columns): dequantised stage buffers b = 0..3 at columns
-// 64 b (128 k each: column c of a buffer holds k pair c in the permuted
-// order, bf16x2), accumulators d = 0..ND-1 at 256 + BN d.
+// Tensor memory (512 columns): dequantised stage buffers b = 0..NXB-1 at
+// columns 64 b (128 k each: column c of a buffer holds k pair c in the
+// permuted order, bf16x2), accumulators d = 0..ND-1 after them, BN columns
+// each.  The MMA issue is unrolled over the stage's eight k-steps (the group
+// size is a template parameter), and the warps probe the barriers they will
+// need next before their work and settle them after it.
 //
 // Schedule: stream-K over (weight tile, stage) units (sched.cuh), the
 // deterministic last-arriver fixup summing the fp32 partials in k order.
@@ -61,17 +65,17 @@ namespace {
 
 constexpr int BM = kTileRows;   // weight rows per tile
 constexpr int KST = 128;        // k per stage
-constexpr int NXB = 4;          // dequantised stage buffers in tensor memory
 constexpr int NWG = 2;          // dequantising warpgroups (stages alternate between them)
 constexpr int ND = 4;           // per-group accumulators in tensor memory (ring)
 constexpr uint32_t kXCols = KST / 2;          // tensor-memory columns of one dequantised stage
-constexpr uint32_t kDCol = NXB * kXCols;      // first accumulator column
 constexpr int kEpiWarp0 = 2, kActWarp = 6, kDqWarp0 = 7;
 constexpr int kThreads = (kDqWarp0 + 4 * NWG) * 32;
 constexpr int kEpiThreads = 128;
 
 template <int BN>
 struct TcLayout {
+    static constexpr int NXB = BN <= 32 ? 6 : 4;            // dequantised stage buffers in tensor memory
+    static constexpr uint32_t DCOL = NXB * kXCols;          // first accumulator column
     static constexpr int STAGES = BN <= 32 ? 12 : 8;        // packed-weight ring (8 KB per slot)
     static constexpr int AST = BN <= 32 ? 8 : 4;            // activation ring
     static constexpr int PK_BYTES = BM * KST / 2;           // 8 KB of packed words per stage
@@ -81,8 +85,8 @@ struct TcLayout {
     static constexpr int NBARS = 2 * STAGES + 2 * AST + 2 * NXB + 2 * ND + 1;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int SMEM = MISC_OFF + 16 + 1024;       // + slack to align the base
-    static_assert(STAGES % NXB == 0 && AST % NXB == 0, "ring slots must map to one warpgroup");
-    static_assert(kDCol + ND * BN <= 512, "tensor-memory map");
+    static_assert(STAGES % NWG == 0 && AST % NWG == 0 && NXB % NWG == 0, "ring slots must map to one warpgroup");
+    static_assert(DCOL + ND * BN <= 512, "tensor-memory map");
     static_assert(A_BYTES % 1024 == 0, "activation boxes keep the 1024-byte swizzle alignment");
 };
 
@@ -91,7 +95,6 @@ struct TcArgs {
     const uint8_t *zeros;     // uint8 [N, G]
     const float *gsum;        // fp32 [G][TP]: S_g per token (the pre-pass)
     int G, TP;                // groups per row; tokens of the group sums (whole token tiles)
-    int lg_group;             // log2(group): 5, 6 or 7
 };
 
 // The last contributor's sum of a split tile, stored as bf16.  Out of line:
@@ -106,7 +109,8 @@ __device__ __noinline__ void fixup_store(const Sched &sched, const float *__rest
     });
 }
 
-template <int BN>
+// LG: log2 of the quantisation group (5, 6 or 7).
+template <int BN, int LG>
 __global__ void __launch_bounds__(kThreads, 1)
 k_w4tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmA, uint16_t *__restrict__ C,
        int R, int Q, int64_t ldc, const __grid_constant__ Sched sched, const TcArgs w, float *__restrict__ ws,
@@ -114,7 +118,10 @@ k_w4tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensor
        int *__restrict__ d_error)
 {
     using L = TcLayout<BN>;
-    constexpr int STAGES = L::STAGES, AST = L::AST;
+    constexpr int STAGES = L::STAGES, AST = L::AST, NXB = L::NXB;
+    constexpr uint32_t kDCol = L::DCOL;
+    constexpr int GROUP = 1 << LG;
+    constexpr int NGS = KST >> LG;   // groups per stage: 1, 2 or 4
     constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN);
     extern __shared__ uint8_t tc_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~uintptr_t(1023));
@@ -132,8 +139,6 @@ k_w4tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensor
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + L::MISC_OFF);   // [0] tmem, [1] abort, [2] last flag
     volatile uint32_t *abort_flag = misc + 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int group = 1 << w.lg_group;
-    const int ngs = KST >> w.lg_group;   // groups per stage: 1, 2 or 4
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -222,38 +227,49 @@ k_w4tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensor
         // Per stage: one wait for the dequantised buffer (its warpgroup also
         // waited for the stage's activations before signalling), then per
         // group one wait for a free accumulator and g / 16 MMAs.
+        // The next stage's buffer is probed (non-blocking) before this
+        // stage's MMAs and settled after them, so the barrier's latency
+        // overlaps MMA issue.
         long long gs = 0, gc = 0;
         SegIter it(sched, blockIdx.x, sched.tiles);
         Segment seg;
-        bool ok = true;
+        bool ok = true, probe = false;
         while (ok && it.next(sched, seg)) {
-            for (int kb = seg.kb0; ok && kb < seg.kb1; ++kb, ++gs) {
+            for (int kb = seg.kb0; kb < seg.kb1; ++kb, ++gs, gc += NGS) {
                 const int b = (int)(gs % NXB);
                 const int a = (int)(gs % AST);
-                if (!wait_bar_warp(XFULL(b), (uint32_t)((gs / NXB) & 1), abort_flag, d_error)) {
+                if (!settle_warp(probe, XFULL(b), (uint32_t)((gs / NXB) & 1), abort_flag, d_error)) {
                     ok = false;
                     break;
                 }
+                uint32_t dt[NGS];
+#pragma unroll
+                for (int i = 0; i < NGS; ++i) {
+                    const int d = (int)((gc + i) % ND);
+                    dt[i] = tmem + kDCol + (uint32_t)(d * BN);
+                    if (!wait_bar_warp(DEMPTY(d), (uint32_t)((((gc + i) / ND) & 1) ^ 1), abort_flag, d_error))
+                        ok = false;
+                }
+                if (!ok) break;
                 ptx::tc_fence_after();
                 const uint32_t xa = tmem + (uint32_t)b * kXCols;
                 const uint32_t ab = sbase + L::A_OFF + a * L::A_BYTES;
-                for (int i = 0; i < ngs; ++i, ++gc) {
-                    const int d = (int)(gc % ND);
-                    if (!wait_bar_warp(DEMPTY(d), (uint32_t)(((gc / ND) & 1) ^ 1), abort_flag, d_error)) {
-                        ok = false;
-                        break;
+                const uint64_t bd0 = ptx::sdesc_kmajor_sw128(ab), bd1 = ptx::sdesc_kmajor_sw128(ab + BN * 128);
+                const long long gn = gs + 1;
+                const int bn_ = (int)(gn % NXB);
+#pragma unroll
+                for (int kk = 0; kk < KST / 16; ++kk) {   // 16 k per MMA; group kk * 16 >> LG
+                    const int kp = 16 * kk;
+                    const int i = kp >> LG;
+                    if (kk == KST / 16 - 1)   // (a stage past this segment's end is the next segment's first)
+                        probe = ptx::mbar_test_wait(XFULL(bn_), (uint32_t)((gn / NXB) & 1));
+                    ptx::mma_bf16_ts_warp(dt[i], xa + (uint32_t)(kp >> 1), (kp < 64 ? bd0 : bd1) + (uint64_t)(2 * ((kp & 63) >> 4)),
+                                          IDESC, (kp & (GROUP - 1)) ? 1u : 0u);
+                    if (((kp + 16) & (GROUP - 1)) == 0) {
+                        const int d = (int)((gc + i) % ND);
+                        ptx::mma_commit_warp(DFULL(d));
                     }
-                    ptx::tc_fence_after();
-                    const uint32_t dt = tmem + kDCol + (uint32_t)(d * BN);
-                    for (int kk = 0; kk < (group >> 4); ++kk) {
-                        const int kp = i * group + 16 * kk;   // k within the stage
-                        const uint64_t bd = ptx::sdesc_kmajor_sw128(ab + (uint32_t)((kp >> 6) * BN * 128)) +
-                                            (uint64_t)(2 * ((kp & 63) >> 4));
-                        ptx::mma_bf16_ts_warp(dt, xa + (uint32_t)(kp >> 1), bd, IDESC, kk > 0 ? 1u : 0u);
-                    }
-                    ptx::mma_commit_warp(DFULL(d));
                 }
-                if (!ok) break;
                 ptx::mma_commit_warp(XEMPTY(b));
                 ptx::mma_commit_warp(AEMPTY(a));
             }
@@ -294,12 +310,9 @@ k_w4tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensor
 #pragma unroll
                 for (int c = 0; c < 4; ++c) wv[c] = ptx::lds128(sp + ((((uint32_t)c) ^ sw) << 4));
                 arrive_warp(EMPTY(slot));   // the slot may be refilled
-                // the buffer's previous stage (four stages back) was consumed long ago in steady state
-                if (!wait_bar_warp(XEMPTY(b), (uint32_t)(((gs / NXB) & 1) ^ 1), abort_flag, d_error)) {
-                    ok = false;
-                    break;
-                }
-                ptx::tc_fence_after();
+                const uint32_t xpar = (uint32_t)(((gs / NXB) & 1) ^ 1);
+                const bool pxe = ptx::mbar_test_wait(XEMPTY(b), xpar);
+                const bool pact = ptx::mbar_test_wait(AFULL(a), (uint32_t)((gs / AST) & 1));
                 const uint32_t xa = trow + (uint32_t)b * kXCols;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {   // words 8h .. 8h + 7 -> columns 32h .. 32h + 31
@@ -314,10 +327,19 @@ k_w4tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensor
                             for (int j = 0; j < 4; ++j)
                                 v[16 * c + 4 * e + j] = ((words[e] >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
                     }
+                    if (h == 0) {
+                        // the buffer's previous stage was consumed NXB stages ago
+                        if (!settle_warp(pxe, XEMPTY(b), xpar, abort_flag, d_error)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                    }
                     ptx::tmem_st32(xa + 32u * (uint32_t)h, v);
                 }
+                if (!ok) break;
                 ptx::tmem_wait_st();
-                if (!wait_bar_warp(AFULL(a), (uint32_t)((gs / AST) & 1), abort_flag, d_error)) {
+                if (!settle_warp(pact, AFULL(a), (uint32_t)((gs / AST) & 1), abort_flag, d_error)) {
                     ok = false;
                     break;
                 }
@@ -347,7 +369,7 @@ k_w4tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensor
             float acc[BN];
 #pragma unroll
             for (int j = 0; j < BN; ++j) acc[j] = 0.f;
-            const int g0 = seg.kb0 * ngs, g1 = seg.kb1 * ngs;
+            const int g0 = seg.kb0 * NGS, g1 = seg.kb1 * NGS;
             // scale and zero of the next group, loaded one group ahead
             float sn = 0.f, cn = 0.f;
             auto load_sc = [&](int gi, float &sv, float &cv) {
@@ -436,12 +458,12 @@ k_w4tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensor
     }
 }
 
-template <int BN>
+template <int BN, int LG>
 cudaError_t launch_tc_t(const CUtensorMap &mq, const CUtensorMap &ma, uint16_t *C, int R, int Q, int64_t ldc,
                         const Sched &s, const TcArgs &w, const LaunchCtx &c)
 {
     using L = TcLayout<BN>;
-    auto kern = k_w4tc<BN>;
+    auto kern = k_w4tc<BN, LG>;
     static std::once_flag once[64];
     static cudaError_t attr_err[64];
     int dev = 0;
@@ -493,15 +515,16 @@ cudaError_t launch_w4tc(const GemmArgs &a, const Plan &p, const LaunchCtx &c)
     s.units = (long long)s.tiles * s.nk;
     s.stall = g_debug_stall;
     s.split = p.split;
-    TcArgs w{(const uint16_t *)a.scales, (const uint8_t *)a.zeros, S, (int)(a.K / a.group), TP,
-             a.group == 32 ? 5 : a.group == 64 ? 6 : 7};
+    TcArgs w{(const uint16_t *)a.scales, (const uint8_t *)a.zeros, S, (int)(a.K / a.group), TP};
     uint16_t *C = (uint16_t *)a.C;
-    switch (bn) {
-    case 16: return launch_tc_t<16>(mq, ma, C, (int)a.N, (int)a.M, a.ldc, s, w, c);
-    case 32: return launch_tc_t<32>(mq, ma, C, (int)a.N, (int)a.M, a.ldc, s, w, c);
-    case 64: return launch_tc_t<64>(mq, ma, C, (int)a.N, (int)a.M, a.ldc, s, w, c);
-    default: return cudaErrorInvalidValue;
-    }
+    const int lg = a.group == 32 ? 5 : a.group == 64 ? 6 : 7;
+#define W4TC_CASE(BNV, LGV) \
+    if (bn == BNV && lg == LGV) return launch_tc_t<BNV, LGV>(mq, ma, C, (int)a.N, (int)a.M, a.ldc, s, w, c);
+    W4TC_CASE(16, 7) W4TC_CASE(16, 6) W4TC_CASE(16, 5)
+    W4TC_CASE(32, 7) W4TC_CASE(32, 6) W4TC_CASE(32, 5)
+    W4TC_CASE(64, 7) W4TC_CASE(64, 6) W4TC_CASE(64, 5)
+#undef W4TC_CASE
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace dbw
