@@ -122,7 +122,9 @@ int check_sizes(int64_t M, int64_t N, int64_t K)
     return GEMM_OK;
 }
 
-int run(const GemmArgs &a, const Plan &p, cudaStream_t st, bool w4)
+// w4: the W4A16 entry point; mx_fmt: the block-scaled entry points (0 E4M3,
+// 1 E2M1), -1 otherwise.
+int run(const GemmArgs &a, const Plan &p, cudaStream_t st, bool w4, int mx_fmt = -1)
 {
     DeviceState *s = nullptr;
     int dev = 0;
@@ -159,6 +161,10 @@ int run(const GemmArgs &a, const Plan &p, cudaStream_t st, bool w4)
     case GEMM_VARIANT_GROUPWISE:
         if (!w4) return GEMM_ERR_VARIANT;
         e = launch_w4tc(a, p, c);
+        break;
+    case GEMM_VARIANT_BLOCK_SCALED:
+        if (mx_fmt < 0) return GEMM_ERR_VARIANT;
+        e = launch_mx(a, p, c, mx_fmt);
         break;
     case GEMM_VARIANT_SKINNY:
     case GEMM_VARIANT_PREFILL:
@@ -494,6 +500,47 @@ bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int
     return true;
 }
 
+// Block-scaled GEMM: tiles of 128 rows of A x 256 rows of B (128 when N <=
+// 128), stages of 128 bytes of every row.  Whole tiles round-robin when they
+// fill at least half the SMs, stream-K over every SM below that.
+void plan_mx(int64_t M, int64_t N, int64_t K, int fmt, int sm_count, Plan *p)
+{
+    *p = Plan{};
+    if (K == 0) {
+        p->variant = GEMM_VARIANT_ZERO;
+        p->kernels = 1;
+        p->split = 1;
+        return;
+    }
+    const int bn = N <= 128 ? 128 : 256;
+    const int64_t tiles_r = (M + kUmmaBM - 1) / kUmmaBM, tiles_q = (N + bn - 1) / bn;
+    const int64_t tiles = tiles_r * tiles_q;
+    const int64_t kst = mx_stage_k(fmt);
+    const int64_t nk = (K + kst - 1) / kst;
+    const int64_t G = sm_count;
+    p->variant = GEMM_VARIANT_BLOCK_SCALED;
+    p->kernels = 2;                          // scale rearrangement, then the GEMM
+    p->act_copy = 1;
+    p->bn = bn;
+    p->tile_m = kUmmaBM;
+    p->tile_n = bn;
+    p->stages = 4;
+    p->ctas_per_sm = 1;
+    p->group_r = (int)std::min<int64_t>(tiles_r, 16);
+    p->ws_extra = (mx_sf_workspace_bytes(M, N, K, fmt, bn) + 3) / 4;
+    if (2 * tiles >= G) {
+        p->mode = 0;
+        p->grid = (int)std::min<int64_t>(tiles, G);
+        p->split = 1;
+    } else {
+        const int64_t units = tiles * nk;
+        p->mode = 1;
+        p->grid = (int)std::min<int64_t>(G, units);
+        const int64_t per_cta = units / p->grid;
+        p->split = (int)std::min<int64_t>(p->grid, (nk + per_cta - 1) / per_cta + 1);
+    }
+}
+
 // CTAs of a stream-K plan that write fp32 partial tiles: those sharing the
 // stream-K units (CTA c keeps two partial slots at 2c and 2c + 1).  When full
 // waves of whole tiles come first, only the first sk_grid CTAs share units.
@@ -506,7 +553,7 @@ static int64_t partial_writers(const Plan &p)
 static bool streamk_partials(const Plan &p)
 {
     return (p.variant == GEMM_VARIANT_SKINNY || p.variant == GEMM_VARIANT_PREFILL ||
-            p.variant == GEMM_VARIANT_GROUPWISE) &&
+            p.variant == GEMM_VARIANT_GROUPWISE || p.variant == GEMM_VARIANT_BLOCK_SCALED) &&
            p.mode == 1;
 }
 
@@ -527,6 +574,10 @@ void workspace_need(const Plan &p, int64_t M, int64_t N, int64_t K, int64_t *flo
     }
     if (p.variant == GEMM_VARIANT_FRAGMENT) {
         *floats = p.ws_extra;
+        return;
+    }
+    if (p.variant == GEMM_VARIANT_BLOCK_SCALED) {   // rearranged scale chunks after the partials
+        *floats = act_copy_offset(p) + p.ws_extra;
         return;
     }
     else if (p.act_copy) *floats = act_copy_offset(p) + (M * K + 127) / 128 * 64 + p.ws_extra;   // bf16 [M, K] (+ sums)
@@ -662,6 +713,59 @@ int gemm_w4a16(const void *A, const void *Bq, const void *scales, const void *ze
                int64_t M, int64_t N, int64_t K, int64_t group, void *stream)
 {
     return gemm_w4a16_ex(A, Bq, scales, zeros, C, M, N, K, group, stream, GEMM_VARIANT_AUTO);
+}
+
+static int gemm_mx_checked(const void *A, const void *SA, const void *B, const void *SB, void *C, int64_t M,
+                           int64_t N, int64_t K, void *stream, int fmt)
+{
+    int rc = check_sizes(M, N, K);
+    if (rc) return rc;
+    if (K % 128 || N % 8) return GEMM_ERR_SHAPE;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (!C || (K > 0 && (!A || !B || !SA || !SB))) return GEMM_ERR_NULL;
+    if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B) || ((uintptr_t)SA & 3u) || ((uintptr_t)SB & 3u))))
+        return GEMM_ERR_ALIGN;
+    const int64_t cb = M * N * 2, eb = fmt == 0 ? K : K / 2;
+    if (K > 0 && (overlaps(C, cb, A, M * eb) || overlaps(C, cb, B, N * eb) || overlaps(C, cb, SA, M * (K / 32)) ||
+                  overlaps(C, cb, SB, N * (K / 32))))
+        return GEMM_ERR_ALIAS;
+    DeviceState *s = nullptr;
+    int dev = 0;
+    rc = device_state(&s, &dev);
+    if (rc) return rc;
+    Plan p;
+    plan_mx(M, N, K, fmt, s->sm_count, &p);
+    GemmArgs a{A, B, nullptr, nullptr, C, M, N, K, K, K, N, 0};
+    a.sfa = SA;
+    a.sfb = SB;
+    return run(a, p, (cudaStream_t)stream, false, fmt);
+}
+
+int gemm_mxfp8(const void *A, const void *SA, const void *B, const void *SB, void *C, int64_t M, int64_t N, int64_t K,
+               void *stream)
+{
+    return gemm_mx_checked(A, SA, B, SB, C, M, N, K, stream, 0);
+}
+
+int gemm_mxfp4(const void *A, const void *SA, const void *B, const void *SB, void *C, int64_t M, int64_t N, int64_t K,
+               void *stream)
+{
+    return gemm_mx_checked(A, SA, B, SB, C, M, N, K, stream, 1);
+}
+
+int gemm_mx_plan(int64_t M, int64_t N, int64_t K, int fmt, int num_sms, gemm_plan *out)
+{
+    if (!out) return GEMM_ERR_NULL;
+    int rc = check_sizes(M, N, K);
+    if (rc) return rc;
+    if (K % 128 || N % 8 || (fmt != 0 && fmt != 1)) return GEMM_ERR_SHAPE;
+    int sms = 0;
+    rc = sm_count_for_plan(num_sms, &sms);
+    if (rc) return rc;
+    Plan p;
+    plan_mx(M, N, K, fmt, sms, &p);
+    to_public(p, out);
+    return GEMM_OK;
 }
 
 int gemm_bf16_plan(int64_t M, int64_t N, int64_t K, int variant, int num_sms, gemm_plan *out)

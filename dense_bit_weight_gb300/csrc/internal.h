@@ -31,6 +31,8 @@ struct GemmArgs {
     int epi = GEMM_EPI_NONE;      // bf16 only; for GEMM_EPI_SILU_MUL, N counts the columns of C and B has 2N rows
     const int *gends = nullptr;   // grouped GEMM: int32 cumulative token-row ends per expert (device)
     int64_t groups = 0;           //   experts; B is [groups, N, K]
+    const void *sfa = nullptr;    // block-scaled GEMM: E8M0 scales of A [M, K/32] and B [N, K/32]
+    const void *sfb = nullptr;
 };
 
 // Grouped GEMM: experts the prefill kernel's shared-memory table holds.
@@ -103,9 +105,19 @@ cudaError_t launch_w4_prep(const GemmArgs &a, const LaunchCtx &c, uint16_t *Ap, 
 // (16, 32 or 64), 128-k stages, stream-K over (weight tile, stage) units.
 int w4tc_stages(int bn);
 cudaError_t launch_w4tc(const GemmArgs &a, const Plan &p, const LaunchCtx &c);
+// Block-scaled (MX) GEMM (mxgemm.cu): fmt 0 = E4M3 x E4M3, 1 = packed E2M1 x
+// E2M1; k per stage (128 bytes of every row) and the workspace bytes of the
+// rearranged scale chunks; the launch runs the scale pre-pass, then the GEMM.
+int mx_stage_k(int fmt);
+int64_t mx_sf_workspace_bytes(int64_t M, int64_t N, int64_t K, int fmt, int bn);
+cudaError_t launch_mx(const GemmArgs &a, const Plan &p, const LaunchCtx &c, int fmt);
+void plan_mx(int64_t M, int64_t N, int64_t K, int fmt, int sm_count, Plan *p);
 // bf16 [rows, K] K-major (leading dimension ld, elements): TMA boxes of 64 k x
 // box_rows rows, 128-byte swizzle, out-of-range elements read as zero.
 bool make_map_bf16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int64_t ld, int box_rows);
+// Bytes [rows, width] (fp8 / packed fp4 codes): boxes of 128 bytes x box_rows
+// rows, 128-byte swizzle.
+bool make_map_u8(CUtensorMap *m, const void *ptr, int64_t rows, int64_t width, int box_rows);
 // Packed 4-bit weights [rows, K/8] (uint32): boxes of 16 words (128 k) x
 // box_rows rows, 64-byte swizzle.
 bool make_map_words16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int box_rows);

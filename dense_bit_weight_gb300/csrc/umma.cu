@@ -1098,6 +1098,21 @@ bool make_map_bf16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int
     return make_map(m, ptr, rows, K, ld, box_rows);
 }
 
+// Bytes [rows, width] row-major (fp8 or packed fp4 codes): boxes of 128 bytes
+// x box_rows rows, 128-byte swizzle, out-of-range bytes read as zero.
+bool make_map_u8(CUtensorMap *m, const void *ptr, int64_t rows, int64_t width, int box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)width, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)width};
+    cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Packed 4-bit weights as uint32 words [rows, K/8]; box 16 words (128 k) x
 // box_rows rows with the 64-byte swizzle (16-byte piece c of row r lands at
 // piece c ^ ((r / 2) % 4)), out-of-range words read as zero.

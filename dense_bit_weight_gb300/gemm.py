@@ -22,13 +22,13 @@ STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_NULL", 2: "GEMM_ERR_SHAPE", 3: "GEMM_ERR_LD
           7: "GEMM_ERR_DEVICE_TIMEOUT", 8: "GEMM_ERR_ARCH", 9: "GEMM_ERR_ALIAS",
           10: "GEMM_ERR_VARIANT", 11: "GEMM_ERR_EPILOGUE"}
 VARIANT = {"auto": 0, "gemv": 1, "skinny": 2, "prefill": 3, "zero": 4, "register": 5, "fragment": 6,
-           "groupwise": 7}
+           "groupwise": 7, "block_scaled": 8}
 VARIANT_NAME = {v: k for k, v in VARIANT.items()}
 
 EXPORTS = ["gemm_bf16", "gemm_w4a16", "gemm_bf16_ex", "gemm_w4a16_ex", "gemm_bf16_plan",
            "gemm_w4a16_plan", "gemm_last_device_error", "gemm_status_string", "gemm_shutdown",
            "gemm_debug_inject_timeout", "gemm_bf16_noalloc", "gemm_bf16_noalloc_last_error", "gemm_bf16_fused", "gemm_bf16_fused_ex",
-           "gemm_bf16_grouped", "gemm_bf16_fused_plan"]
+           "gemm_bf16_grouped", "gemm_bf16_fused_plan", "gemm_mxfp8", "gemm_mxfp4", "gemm_mx_plan"]
 
 
 class gemm_plan(ctypes.Structure):
@@ -53,6 +53,12 @@ lib.gemm_bf16_noalloc.argtypes = lib.gemm_bf16.argtypes
 lib.gemm_bf16_noalloc.restype = _i
 lib.gemm_bf16_noalloc_last_error.argtypes = []
 lib.gemm_bf16_noalloc_last_error.restype = _i
+lib.gemm_mxfp8.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p]
+lib.gemm_mxfp8.restype = _i
+lib.gemm_mxfp4.argtypes = lib.gemm_mxfp8.argtypes
+lib.gemm_mxfp4.restype = _i
+lib.gemm_mx_plan.argtypes = [_i64, _i64, _i64, _i, _i, ctypes.POINTER(gemm_plan)]
+lib.gemm_mx_plan.restype = _i
 lib.gemm_w4a16.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _p]
 lib.gemm_w4a16_ex.argtypes = lib.gemm_w4a16.argtypes + [_i]
 lib.gemm_bf16_plan.argtypes = [_i64, _i64, _i64, _i, _i, ctypes.POINTER(gemm_plan)]
@@ -272,6 +278,43 @@ def gemm_w4a16(A, Bq, scales, zeros, group: int, C=None, stream=None, variant="a
     return C
 
 
+MX_FMT = {"e4m3": 0, "e2m1": 1}
+
+
+def gemm_mx_plan(M: int, N: int, K: int, fmt="e4m3", num_sms: int = 0) -> dict:
+    out = gemm_plan()
+    _check(lib.gemm_mx_plan(M, N, K, MX_FMT[fmt] if isinstance(fmt, str) else int(fmt), num_sms,
+                            ctypes.byref(out)), "gemm_mx_plan")
+    return out.as_dict()
+
+
+def gemm_mx(A, SA, B, SB, fmt="e4m3", C=None, stream=None):
+    """The block-scaled (MX) GEMM: C[M,N] bf16 = sum_k a 2^(SA-127) * b 2^(SB-127).
+
+    fmt "e4m3": A uint8 [M,K], B uint8 [N,K] (E4M3 codes); fmt "e2m1": A
+    uint8 [M,K/2], B uint8 [N,K/2] (packed, low nibble first).  SA uint8
+    [M,K/32], SB uint8 [N,K/32] (E8M0 codes).  All contiguous CUDA tensors.
+    """
+    import torch
+    f = MX_FMT[fmt]
+    M, N = A.shape[0], B.shape[0]
+    K = A.shape[1] * (2 if f else 1)
+    for t, name in ((A, "A"), (SA, "SA"), (B, "B"), (SB, "SB")):
+        if t.dtype != torch.uint8 or not t.is_cuda or not t.is_contiguous() or t.dim() != 2:
+            raise ValueError(f"{name} must be a contiguous 2-D CUDA uint8 tensor")
+    if B.shape[1] * (2 if f else 1) != K or tuple(SA.shape) != (M, K // 32) or tuple(SB.shape) != (N, K // 32):
+        raise ValueError("MX operand shapes do not match")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    if C.dtype != torch.bfloat16 or tuple(C.shape) != (M, N) or not C.is_contiguous():
+        raise ValueError("C must be a contiguous bfloat16 [M,N] tensor")
+    _same_cuda_device(A, ("SA", SA), ("B", B), ("SB", SB), ("C", C))
+    fn = lib.gemm_mxfp8 if f == 0 else lib.gemm_mxfp4
+    _check(fn(A.data_ptr(), SA.data_ptr(), B.data_ptr(), SB.data_ptr(), C.data_ptr(), M, N, K,
+              _stream_handle(stream)), "gemm_mx" + ("fp8" if f == 0 else "fp4"))
+    return C
+
+
 # --------------------------------------------------------------- raw pointers
 
 def gemm_bf16_ptr(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
@@ -298,3 +341,10 @@ def gemm_w4a16_ptr(A: int, Bq: int, scales: int, zeros: int, C: int, M: int, N: 
                    group: int, stream: int = 0, variant="auto") -> int:
     return int(lib.gemm_w4a16_ex(A, Bq, scales, zeros, C, M, N, K, group, ctypes.c_void_p(stream),
                                  _variant(variant)))
+
+
+def gemm_mx_ptr(fmt: str, A: int, SA: int, B: int, SB: int, C: int, M: int, N: int, K: int,
+                stream: int = 0) -> int:
+    """gemm_mxfp8 / gemm_mxfp4 on raw device addresses; returns the gemm_status."""
+    fn = lib.gemm_mxfp8 if MX_FMT[fmt] == 0 else lib.gemm_mxfp4
+    return int(fn(A, SA, B, SB, C, M, N, K, ctypes.c_void_p(stream)))

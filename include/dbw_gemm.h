@@ -68,9 +68,10 @@ typedef enum {
                                  /* registers for warp-level MMAs (mma.sync)       */
     GEMM_VARIANT_FRAGMENT = 6,   /* W4A16, M <= 16: weights streamed by TMA and    */
                                  /* dequantised into mma.sync fragments            */
-    GEMM_VARIANT_GROUPWISE = 7   /* W4A16: exact 128 + q weights in tensor memory, */
+    GEMM_VARIANT_GROUPWISE = 7,  /* W4A16: exact 128 + q weights in tensor memory, */
                                  /* one tcgen05 accumulator per quantisation       */
                                  /* group, scale and zero applied per group        */
+    GEMM_VARIANT_BLOCK_SCALED = 8 /* MX: block-scaled tcgen05 MMAs (gemm_mxfp*)    */
 } gemm_variant;
 
 typedef struct {
@@ -229,6 +230,40 @@ int gemm_bf16_noalloc(const void *A, const void *B, void *C, int64_t M, int64_t 
  * timeout the next split-K call clears the counters itself.
  */
 int gemm_bf16_noalloc_last_error(void);
+
+/*
+ * gemm_mxfp8 / gemm_mxfp4 -- the block-scaled ("microscaling", MX) GEMM
+ *
+ *     C[m,n] = sum_k (a[m,k] * 2^(SA[m,k/32] - 127)) * (b[n,k] * 2^(SB[n,k/32] - 127))
+ *
+ * FlyDSL-in-PyTorch blog, section "MXFP": FP8 E4M3 or packed FP4 E2M1
+ * operands, one E8M0 scale per 32 values along the reduction axis, fp32
+ * accumulation, bf16 output, K a multiple of 128, unit stride along K for A
+ * and B ("NT"); FlyDSL prebuilt kernels guide §3.1, the MX GEMM note.  The
+ * element formats are the OCP microscaling ones: E4M3 (s eeee mmm, bias 7, no
+ * infinities, 0x7F/0xFF NaN), E2M1 (s ee m, bias 1), E8M0 (2^(e - 127),
+ * 0xFF NaN).  The scales are applied inside the tensor-core MMA.
+ *
+ *   A    gemm_mxfp8: E4M3 codes uint8 [M, K], dense.
+ *        gemm_mxfp4: packed E2M1 uint8 [M, K/2], dense; element k is bits
+ *        4*(k%2) .. 4*(k%2)+3 of byte k/2 (low nibble first).
+ *   SA   E8M0 codes uint8 [M, K/32], dense (row m's block j at SA + m*(K/32) + j)
+ *   B    as A, [N, K] or [N, K/2] (the weights)
+ *   SB   E8M0 codes uint8 [N, K/32], dense
+ *   C    [M, N] bf16, dense (row m at C + m*N); must not overlap any input
+ *   M, N, K >= 0, K % 128 == 0, N % 8 == 0, each < 2^31.  M == 0 or N == 0:
+ *   nothing to do.  K == 0: C is set to zero.
+ *   A, B, C 16-byte aligned; SA, SB 4-byte aligned.  Device memory.
+ * Inputs are finite (NaN codes are out of scope).  The library keeps a
+ * rearranged copy of the scales in its per-stream workspace, so the call
+ * allocates on first use like gemm_bf16.  Returns gemm_status.
+ */
+int gemm_mxfp8(const void *A, const void *SA, const void *B, const void *SB, void *C, int64_t M, int64_t N,
+               int64_t K, void *stream);
+int gemm_mxfp4(const void *A, const void *SA, const void *B, const void *SB, void *C, int64_t M, int64_t N,
+               int64_t K, void *stream);
+/* The plan of gemm_mxfp8 (fmt 0) or gemm_mxfp4 (fmt 1) with these sizes. */
+int gemm_mx_plan(int64_t M, int64_t N, int64_t K, int fmt, int num_sms, gemm_plan *out);
 
 /*
  * gemm_bf16_ex / gemm_w4a16_ex -- as above, but `variant` may force a kernel
