@@ -289,3 +289,24 @@ def test_binding_rejects_host_and_cross_device_tensors():
         g.gemm_bf16_fused(A, B, bias=torch.zeros(32, dtype=torch.bfloat16), C=_FakeCudaTensor((4, 32)))
     with pytest.raises(ValueError):
         g.gemm_bf16(torch.empty((4, 64), dtype=torch.bfloat16), B)                 # A in host memory
+
+
+def test_mx_plans_cover_both_schedules(g):
+    p = g.gemm_mx_plan(4096, 8192, 1024, num_sms=152)               # 1024 tiles: whole tiles on every SM
+    assert p["grid"] == 152 and p["split"] == 1 and p["kernels"] == 2
+    p = g.gemm_mx_plan(1024, 1024, 1024, num_sms=152)               # 32 tiles: stream-K over the SMs
+    assert p["grid"] == 152 and p["split"] > 1 and p["tile_n"] == 256
+    assert g.gemm_mx_plan(37, 120, 384, num_sms=152)["tile_n"] == 128
+    assert g.gemm_mx_plan(32, 64, 0, num_sms=152)["variant_name"] == "zero"
+
+
+def test_mx_rejects_bad_arguments_before_launch(g):
+    a = 1 << 20
+    assert g.gemm_mx_ptr("e4m3", a, a, a, a, a * 64, 4, 16, 96) == 2          # K % 128
+    assert g.gemm_mx_ptr("e4m3", a, a, a, a, a * 64, 4, 12, 128) == 2         # N % 8
+    assert g.gemm_mx_ptr("e4m3", a, a, a, a, a * 64, -1, 16, 128) == 2
+    assert g.gemm_mx_ptr("e4m3", a + 8, a, a, a, a * 64, 4, 16, 128) == 4     # A alignment
+    assert g.gemm_mx_ptr("e2m1", a, a + 2, a, a, a * 64, 4, 16, 128) == 4     # SA alignment
+    assert g.gemm_mx_ptr("e4m3", 0, a, a, a, a * 64, 4, 16, 128) == 1
+    assert g.gemm_mx_ptr("e4m3", a, a, a, a, a + 64, 4, 16, 128) == 9         # C overlaps A
+    assert g.gemm_mx_ptr("e4m3", a, a, a, a, a * 64, 0, 16, 128) == 0         # empty: nothing to do
