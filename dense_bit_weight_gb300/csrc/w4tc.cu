@@ -19,19 +19,23 @@
 // Roles (one CTA per SM, 15 warps):
 //   warp 0      TMA producer of the packed weights: one 128-row x 128-k stage
 //               (16 words per row, 8 KB, 64-byte swizzle) per slot of a ring
-//   warp 1      MMA issuer: per stage and group, g / 16 MMAs of K = 16 into
-//               that group's accumulator (a ring of ND in tensor memory)
+//   warp 1      allocates (and at exit frees) the tensor memory
 //   warps 2-5   epilogue: per group, read D_g (tcgen05.ld), release it, add
 //               s D_g + c S_g to fp32 registers; at a segment's end store the
 //               tile or its stream-K partial (deterministic fixup)
 //   warp 6      TMA producer of the activations (the pre-pass's copy in the
 //               0,4,1,5,2,6,3,7 order of each 8-k block): BN x 128 k per stage
-//   warps 7-14  dequantisation: two warpgroups take the stages alternately;
-//               a warp handles its 32 weight rows (its tensor-memory lane
-//               quarter) for the whole 128-k stage, so it meets the other
-//               roles once per two stages.  The NXB tensor-memory stage
-//               buffers (6 for token tiles up to 32, else 4) are used in turn,
-//               so each warpgroup can run NXB / 2 stages ahead of the MMAs.
+//   warps 7-14  dequantisation and MMA issue: two warpgroups take the stages
+//               alternately; a warp handles its 32 weight rows (its
+//               tensor-memory lane quarter) for the whole 128-k stage, and one
+//               warp of the group issues the stage's eight MMAs (K = 16) into
+//               the accumulators of the stage's groups (a ring of ND).
+//               The NXB tensor-memory stage buffers (6 for token tiles up to
+//               32, else 4) are used in turn, so each warpgroup can run NXB / 2
+//               stages ahead.  Issuing from the warpgroups instead of a
+//               dedicated MMA warp (measured: ~1000 cycles per stage there,
+//               sharing its SMSP with dequantising warps, and a wake-up per
+//               stage) keeps the MMA issue next to the data it waits for.
 // The packed-weight and activation rings and the stage buffers have even
 // counts, so a slot is only ever used by the stages of one warpgroup (its
 // mbarrier phases are never skipped by a waiter).
@@ -40,8 +44,7 @@
 // columns 64 b (128 k each: column c of a buffer holds k pair c in the
 // permuted order, bf16x2), accumulators d = 0..ND-1 after them, BN columns
 // each.  The MMA issue is unrolled over the stage's eight k-steps (the group
-// size is a template parameter), and the warps probe the barriers they will
-// need next before their work and settle them after it.
+// size is a template parameter).
 //
 // Schedule: stream-K over (weight tile, stage) units (sched.cuh), the
 // deterministic last-arriver fixup summing the fp32 partials in k order.
@@ -82,12 +85,28 @@ struct TcLayout {
     static constexpr int A_BYTES = BN * KST * 2;            // two 64-k boxes of BN rows
     static constexpr int A_OFF = STAGES * PK_BYTES;
     static constexpr int BAR_OFF = A_OFF + AST * A_BYTES;
-    static constexpr int NBARS = 2 * STAGES + 2 * AST + 2 * NXB + 2 * ND + 1;
+    static constexpr int NBARS = 2 * STAGES + 2 * AST + 2 * NXB + 2 * ND + NWG;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int SMEM = MISC_OFF + 16 + 1024;       // + slack to align the base
     static_assert(STAGES % NWG == 0 && AST % NWG == 0 && NXB % NWG == 0, "ring slots must map to one warpgroup");
     static_assert(DCOL + ND * BN <= 512, "tensor-memory map");
     static_assert(A_BYTES % 1024 == 0, "activation boxes keep the 1024-byte swizzle alignment");
+};
+
+// A ring of n slots walked in steps of k <= n: slot and the parity of the
+// slot's current use.
+struct Ring {
+    int slot;
+    uint32_t phase;
+    int n;
+    __device__ __forceinline__ void adv(int k)
+    {
+        slot += k;
+        if (slot >= n) {
+            slot -= n;
+            phase ^= 1u;
+        }
+    }
 };
 
 struct TcArgs {
@@ -135,7 +154,7 @@ k_w4tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensor
     auto XEMPTY = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 * AST + NXB + b); };
     auto DFULL = [&](int d) { return bar0 + 8u * (2 * STAGES + 2 * AST + 2 * NXB + d); };
     auto DEMPTY = [&](int d) { return bar0 + 8u * (2 * STAGES + 2 * AST + 2 * NXB + ND + d); };
-    const uint32_t DONE = bar0 + 8u * (2 * STAGES + 2 * AST + 2 * NXB + 2 * ND);
+    auto DONE = [&](int u) { return bar0 + 8u * (2 * STAGES + 2 * AST + 2 * NXB + 2 * ND + u); };
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + L::MISC_OFF);   // [0] tmem, [1] abort, [2] last flag
     volatile uint32_t *abort_flag = misc + 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -157,7 +176,7 @@ k_w4tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensor
             ptx::mbar_init(DFULL(d), 1);
             ptx::mbar_init(DEMPTY(d), kEpiThreads / 32);
         }
-        ptx::mbar_init(DONE, 1);
+        for (int u = 0; u < NWG; ++u) ptx::mbar_init(DONE(u), 1);
         misc[1] = 0;
         misc[2] = 0;
         ptx::fence_mbar_init();
@@ -185,29 +204,27 @@ k_w4tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensor
             const bool packed = warp == 0;
             if (!packed) ptx::pdl_wait();   // the activation copy
             const uint64_t pol = packed ? ptx::policy_evict_first() : ptx::policy_evict_last();
-            const int nslots = packed ? STAGES : AST;
-            long long gs = 0, issued = 0;
+            Ring ring{0, 0u, packed ? STAGES : AST};
+            int issued = 0;
             SegIter it(sched, blockIdx.x, sched.tiles);
             Segment seg;
             bool ok = true;
             while (ok && it.next(sched, seg)) {
                 int tr, tq;
                 tile_coords(sched, seg.tile, tr, tq);
-                for (int kb = seg.kb0; kb < seg.kb1; ++kb, ++gs) {
-                    const int slot = (int)(gs % nslots);
-                    const uint32_t par = (uint32_t)((gs / nslots) & 1);
-                    const uint32_t full = packed ? FULL(slot) : AFULL(slot);
-                    if (!wait_bar(packed ? EMPTY(slot) : AEMPTY(slot), par ^ 1u, abort_flag, d_error)) {
+                for (int kb = seg.kb0; kb < seg.kb1; ++kb, ring.adv(1)) {
+                    const uint32_t full = packed ? FULL(ring.slot) : AFULL(ring.slot);
+                    if (!wait_bar(packed ? EMPTY(ring.slot) : AEMPTY(ring.slot), ring.phase ^ 1u, abort_flag, d_error)) {
                         ok = false;
                         break;
                     }
                     if (sched.stall) continue;
                     if (packed) {
                         ptx::mbar_arrive_expect_tx(full, L::PK_BYTES);
-                        ptx::tma_load_2d(sbase + slot * L::PK_BYTES, &tmQ, full, kb * (KST / 8), tr * BM, pol);
+                        ptx::tma_load_2d(sbase + ring.slot * L::PK_BYTES, &tmQ, full, kb * (KST / 8), tr * BM, pol);
                     } else {
                         ptx::mbar_arrive_expect_tx(full, L::A_BYTES);
-                        const uint32_t dst = sbase + L::A_OFF + slot * L::A_BYTES;
+                        const uint32_t dst = sbase + L::A_OFF + ring.slot * L::A_BYTES;
                         ptx::tma_load_2d(dst, &tmA, full, kb * KST, tq * BN, pol);
                         ptx::tma_load_2d(dst + BN * 128, &tmA, full, kb * KST + 64, tq * BN, pol);
                     }
@@ -215,105 +232,58 @@ k_w4tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensor
                 }
             }
             if (!ok) {   // every slot's most recent copy lands before exit
-                for (int s = 0; s < nslots; ++s) {
-                    if (issued <= s) continue;
-                    const long long last = issued - 1 - ((issued - 1 - s) % nslots);
-                    wait_bar_drain(packed ? FULL(s) : AFULL(s), (uint32_t)((last / nslots) & 1));
+                for (int s2 = 0; s2 < ring.n; ++s2) {
+                    if (issued <= s2) continue;
+                    const int last = issued - 1 - ((issued - 1 - s2) % ring.n);
+                    wait_bar_drain(packed ? FULL(s2) : AFULL(s2), (uint32_t)((last / ring.n) & 1));
                 }
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        // Per stage: one wait for the dequantised buffer (its warpgroup also
-        // waited for the stage's activations before signalling), then per
-        // group one wait for a free accumulator and g / 16 MMAs.
-        // The next stage's buffer is probed (non-blocking) before this
-        // stage's MMAs and settled after them, so the barrier's latency
-        // overlaps MMA issue.
-        long long gs = 0, gc = 0;
-        SegIter it(sched, blockIdx.x, sched.tiles);
-        Segment seg;
-        bool ok = true, probe = false;
-        while (ok && it.next(sched, seg)) {
-            for (int kb = seg.kb0; kb < seg.kb1; ++kb, ++gs, gc += NGS) {
-                const int b = (int)(gs % NXB);
-                const int a = (int)(gs % AST);
-                if (!settle_warp(probe, XFULL(b), (uint32_t)((gs / NXB) & 1), abort_flag, d_error)) {
-                    ok = false;
-                    break;
-                }
-                uint32_t dt[NGS];
-#pragma unroll
-                for (int i = 0; i < NGS; ++i) {
-                    const int d = (int)((gc + i) % ND);
-                    dt[i] = tmem + kDCol + (uint32_t)(d * BN);
-                    if (!wait_bar_warp(DEMPTY(d), (uint32_t)((((gc + i) / ND) & 1) ^ 1), abort_flag, d_error))
-                        ok = false;
-                }
-                if (!ok) break;
-                ptx::tc_fence_after();
-                const uint32_t xa = tmem + (uint32_t)b * kXCols;
-                const uint32_t ab = sbase + L::A_OFF + a * L::A_BYTES;
-                const uint64_t bd0 = ptx::sdesc_kmajor_sw128(ab), bd1 = ptx::sdesc_kmajor_sw128(ab + BN * 128);
-                const long long gn = gs + 1;
-                const int bn_ = (int)(gn % NXB);
-#pragma unroll
-                for (int kk = 0; kk < KST / 16; ++kk) {   // 16 k per MMA; group kk * 16 >> LG
-                    const int kp = 16 * kk;
-                    const int i = kp >> LG;
-                    if (kk == KST / 16 - 1)   // (a stage past this segment's end is the next segment's first)
-                        probe = ptx::mbar_test_wait(XFULL(bn_), (uint32_t)((gn / NXB) & 1));
-                    ptx::mma_bf16_ts_warp(dt[i], xa + (uint32_t)(kp >> 1), (kp < 64 ? bd0 : bd1) + (uint64_t)(2 * ((kp & 63) >> 4)),
-                                          IDESC, (kp & (GROUP - 1)) ? 1u : 0u);
-                    if (((kp + 16) & (GROUP - 1)) == 0) {
-                        const int d = (int)((gc + i) % ND);
-                        ptx::mma_commit_warp(DFULL(d));
-                    }
-                }
-                ptx::mma_commit_warp(XEMPTY(b));
-                ptx::mma_commit_warp(AEMPTY(a));
-            }
-        }
-        ptx::mma_commit_warp(DONE);          // every issued MMA retires before tensor memory is freed
-        wait_bar_drain(DONE, 0);
     } else if (warp >= kDqWarp0) {
-        // ------------------------------------------------------------ dequantisation
-        // Warpgroup u takes the stages gs = u, u + NWG, ...; warp q4 (its
+        // ------------------------------------------------------------ dequantisation and MMA issue
+        // Warpgroup u takes the stages u, u + NWG, ...; warp q4 (its
         // tensor-memory lane quarter) handles weight rows 32 q4 .. 32 q4 + 31,
         // lane l row r = 32 q4 + l.  A thread reads its row's 16 packed words
         // (four 16-byte pieces, conflict-free under the 64-byte swizzle),
         // releases the slot, forms the 64 bf16x2 columns 128 + q (column 4w + j
         // of word w holds nibbles j and j + 4: k pair j of the permuted 8-k
-        // block) and stores them into its stage buffer.
+        // block) and stores them into the stage's buffer; every warp then
+        // arrives on XFULL.  One warp of the group (the issuer; the two groups'
+        // issuers sit on different SMSPs) waits for the other three, the
+        // stage's activations and free accumulators, and issues the stage's
+        // eight MMAs itself: a group's MMAs write accumulators no other group
+        // writes, so no ordering between issuing warps is needed, and no
+        // separate MMA warp has to be woken per stage.
         const int u = (warp - kDqWarp0) >> 2;
         const int q4 = warp & 3;
+        const bool issuer = q4 == (u == 0 ? 1 : 3);
         const int r = 32 * q4 + lane;
         const uint32_t row_off = (uint32_t)(r * 64);
         const uint32_t sw = (uint32_t)((r >> 1) & 3);
         const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
-        long long gs = 0;
+        // rings at this group's first stage; every own stage advances them by NWG
+        Ring pk{u, 0u, STAGES}, act{u, 0u, AST}, xb{u, 0u, NXB};
+        uint32_t gc = (uint32_t)(u * NGS);   // this stage's first group (accumulator gc % ND)
+        int cyc = 0;
         SegIter it(sched, blockIdx.x, sched.tiles);
         Segment seg;
         bool ok = true;
         while (ok && it.next(sched, seg)) {
-            for (int kb = seg.kb0; kb < seg.kb1; ++kb, ++gs) {
-                if ((int)(gs % NWG) != u) continue;
-                const int slot = (int)(gs % STAGES);
-                const int b = (int)(gs % NXB);
-                const int a = (int)(gs % AST);
-                if (!wait_bar_warp(FULL(slot), (uint32_t)((gs / STAGES) & 1), abort_flag, d_error)) {
+            for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
+                const bool own = cyc == u;
+                cyc = cyc + 1 == NWG ? 0 : cyc + 1;
+                if (!own) continue;
+                if (!wait_bar_warp(FULL(pk.slot), pk.phase, abort_flag, d_error)) {
                     ok = false;
                     break;
                 }
-                const uint32_t sp = sbase + slot * L::PK_BYTES + row_off;
+                const uint32_t sp = sbase + pk.slot * L::PK_BYTES + row_off;
                 uint4 wv[4];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) wv[c] = ptx::lds128(sp + ((((uint32_t)c) ^ sw) << 4));
-                arrive_warp(EMPTY(slot));   // the slot may be refilled
-                const uint32_t xpar = (uint32_t)(((gs / NXB) & 1) ^ 1);
-                const bool pxe = ptx::mbar_test_wait(XEMPTY(b), xpar);
-                const bool pact = ptx::mbar_test_wait(AFULL(a), (uint32_t)((gs / AST) & 1));
-                const uint32_t xa = trow + (uint32_t)b * kXCols;
+                arrive_warp(EMPTY(pk.slot));   // the slot may be refilled
+                const bool pxe = ptx::mbar_test_wait(XEMPTY(xb.slot), xb.phase ^ 1u);
+                const uint32_t xa = trow + (uint32_t)xb.slot * kXCols;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {   // words 8h .. 8h + 7 -> columns 32h .. 32h + 31
                     uint32_t v[32];
@@ -328,8 +298,8 @@ k_w4tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensor
                                 v[16 * c + 4 * e + j] = ((words[e] >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
                     }
                     if (h == 0) {
-                        // the buffer's previous stage was consumed NXB stages ago
-                        if (!settle_warp(pxe, XEMPTY(b), xpar, abort_flag, d_error)) {
+                        // the buffer's previous stage was issued NXB stages ago
+                        if (!settle_warp(pxe, XEMPTY(xb.slot), xb.phase ^ 1u, abort_flag, d_error)) {
                             ok = false;
                             break;
                         }
@@ -339,13 +309,43 @@ k_w4tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensor
                 }
                 if (!ok) break;
                 ptx::tmem_wait_st();
-                if (!settle_warp(pact, AFULL(a), (uint32_t)((gs / AST) & 1), abort_flag, d_error)) {
-                    ok = false;
-                    break;
+                ptx::tc_fence_before();   // the MMAs read these columns after XFULL
+                arrive_warp(XFULL(xb.slot));
+                if (issuer) {
+                    bool go = wait_bar_warp(XFULL(xb.slot), xb.phase, abort_flag, d_error) &&
+                              wait_bar_warp(AFULL(act.slot), act.phase, abort_flag, d_error);
+#pragma unroll
+                    for (int i = 0; i < NGS; ++i)
+                        go = go && wait_bar_warp(DEMPTY((gc + i) % ND), (((gc + i) / ND) & 1u) ^ 1u, abort_flag, d_error);
+                    if (!go) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t xm = tmem + (uint32_t)xb.slot * kXCols;
+                    const uint32_t ab = sbase + L::A_OFF + act.slot * L::A_BYTES;
+                    const uint64_t bd0 = ptx::sdesc_kmajor_sw128(ab), bd1 = ptx::sdesc_kmajor_sw128(ab + BN * 128);
+#pragma unroll
+                    for (int kk = 0; kk < KST / 16; ++kk) {   // 16 k per MMA; group kk * 16 >> LG of the stage
+                        const int kp = 16 * kk;
+                        const uint32_t d = (gc + (uint32_t)(kp >> LG)) % ND;
+                        ptx::mma_bf16_ts_warp(tmem + kDCol + d * BN, xm + (uint32_t)(kp >> 1),
+                                              (kp < 64 ? bd0 : bd1) + (uint64_t)(2 * ((kp & 63) >> 4)), IDESC,
+                                              (kp & (GROUP - 1)) ? 1u : 0u);
+                        if (((kp + 16) & (GROUP - 1)) == 0) ptx::mma_commit_warp(DFULL(d));
+                    }
+                    ptx::mma_commit_warp(XEMPTY(xb.slot));
+                    ptx::mma_commit_warp(AEMPTY(act.slot));
                 }
-                ptx::tc_fence_before();   // the MMA reads these columns after XFULL
-                arrive_warp(XFULL(b));
+                pk.adv(NWG);
+                act.adv(NWG);
+                xb.adv(NWG);
+                gc += (uint32_t)(NWG * NGS);
             }
+        }
+        if (issuer) {   // every MMA this warp issued retires before tensor memory is freed
+            ptx::mma_commit_warp(DONE(u));
+            wait_bar_drain(DONE(u), 0);
         }
     } else {
         // ------------------------------------------------------------ epilogue (warps 2-5)
@@ -354,7 +354,7 @@ k_w4tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensor
         const int etid = threadIdx.x - 32 * kEpiWarp0;
         const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16) + kDCol;
         ptx::pdl_wait();                    // the group sums; C, workspace and counters may be in use before
-        long long gc = 0;
+        uint32_t gc = 0;
         SegIter it(sched, blockIdx.x, sched.tiles);
         Segment seg;
         bool ok = true;
@@ -384,7 +384,7 @@ k_w4tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensor
                 const int d = (int)(gc % ND);
                 const float sv = sn, cv = cn;
                 if (gi + 1 < g1) load_sc(gi + 1, sn, cn);
-                if (!wait_bar_warp(DFULL(d), (uint32_t)((gc / ND) & 1), abort_flag, d_error)) {
+                if (!wait_bar_warp(DFULL(d), (gc / ND) & 1u, abort_flag, d_error)) {
                     ok = false;
                     break;
                 }
