@@ -21,6 +21,7 @@ The JSON line also carries:
                 fused gate/up projection with the SiLU-mul epilogue (decode GB/s,
                 prefill TFLOP/s), the grouped (MoE) GEMM, and W4A16 at
                 prefill-size token counts (TFLOP/s)
+                and the block-scaled (MX) GEMMs, E4M3 and E2M1 (TFLOP/s)
   clocks        nvidia-smi samples taken during the timed region
 
 --impl reference times the oracle (the method's plain definition on the
@@ -57,6 +58,12 @@ GATE_UP_PREFILL = [(M, 12288, 4096) for M in (1024, 4096)]
 GROUPED = [("uniform 8 experts", [512] * 8, 4096, 4096),
            ("ragged 16 experts", [1024, 0, 512, 37, 0, 800, 256, 1, 600, 0, 300, 64, 200, 150, 100, 52], 4096, 4096),
            ("decode MoE 128 experts", [4] * 128, 1536, 2048)]
+# block-scaled (MX) GEMMs: the prefill shapes, plus the pages' MXFP shapes
+# (32 x 4096 x 4096 for MXFP8, 32 x 14336 x 4096 for MXFP4)
+MX_SHAPES = [(32, 4096, 4096), (32, 14336, 4096)] + PREFILL
+# dense tensor peaks per format relative to bf16 (nominal GB300 figures:
+# bf16 2.25, fp8 4.5, fp4 13.5 PFLOP/s); the bench scales the measured bf16 peak
+MX_PEAK_RATIO = {"e4m3": 2.0, "e2m1": 6.0}
 WORKLOAD = ("decode projections, Qwen3-8B-like dims: bf16 A[M,4096], M in {1,8,32,128}, "
             "B in {qkv 6144x4096, o 4096x4096, gate/up 24576x4096}, fp32 accumulate, bf16 out")
 
@@ -92,6 +99,47 @@ def bytes_w4(M, N, K, g=128):
 
 def flops(M, N, K):
     return 2 * M * N * K
+
+
+def bytes_mx(M, N, K, fmt):
+    el = 1 if fmt == "e4m3" else 0.5
+    return int(el * (M * K + N * K) + (M * K + N * K) // 32 + 2 * M * N)
+
+
+def mx_sweep(g, torch, reps=10):
+    """Block-scaled GEMMs: TFLOP/s per shape (graph-timed, random codes drawn on
+    the device; operands rotated over copies larger than L2) and the
+    fraction of max(flops / P_fmt, bytes / BW), P_fmt = the measured bf16
+    peak times the nominal format ratio."""
+    hbm, tf, _, _ = peaks()
+    dev = torch.device("cuda")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3)
+    out = {}
+    for fmt in ("e4m3", "e2m1"):
+        p_fmt = tf * MX_PEAK_RATIO[fmt]
+        rows, t_roof, t_meas = [], 0.0, 0.0
+        for (M, N, K) in MX_SHAPES:
+            w = K if fmt == "e4m3" else K // 2
+            copies = max(1, min(6, int(np.ceil(3 * 126e6 / (N * w + M * w)))))
+            def codes(r):   # E4M3: exponent fields 4..10 (no NaN); E2M1: any byte
+                x = torch.randint(0, 256, (r, w), generator=gen, device=dev, dtype=torch.uint8)
+                return (x & 0xB7) | 0x20 if fmt == "e4m3" else x
+            ops = [(codes(M), torch.randint(124, 131, (M, K // 32), generator=gen, device=dev, dtype=torch.uint8),
+                    codes(N), torch.randint(124, 131, (N, K // 32), generator=gen, device=dev, dtype=torch.uint8))
+                   for _ in range(copies)]
+            C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            ms = graph_time_ms(torch, lambda i: g.gemm_mx(*ops[i % copies], fmt, C=C), reps)
+            fl, by = flops(M, N, K), bytes_mx(M, N, K, fmt)
+            tr = max(fl / (p_fmt * 1e12), by / (hbm * 1e9))
+            t_roof += tr
+            t_meas += ms * 1e-3
+            rows.append([M, N, K, round(fl / (ms * 1e-3) / 1e12, 1), round(tr / (ms * 1e-3), 3)])
+            del ops, C
+        out[fmt] = {"unit": "[M, N, K, TFLOP/s, t_roof / t]", "peak_tflops": round(p_fmt, 1),
+                    "peak_source": "measured bf16 x nominal ratio", "roofline_frac_aggregate": t_roof / t_meas,
+                    "shapes": rows}
+    return out
 
 
 def roof_frac(M, N, K, ms, kind, hbm, tf):
@@ -650,6 +698,8 @@ def run_ours(args):
             fr, agg = graded(rs, "silu")
             sweeps["gate_up_silu_prefill"]["roofline_frac"] = {"per_shape": fr, "aggregate": agg}
         sweeps["grouped"] = grouped_sweep(g, torch)
+        if not args.quick:
+            sweeps["mx"] = mx_sweep(g, torch)
         # each decode shape alone, graph-timed back to back (no events between launches)
         dec = timed_sweep(g, torch, DECODE, "bf16")
         sweeps["decode_per_shape"] = {"unit": "GB/s", "shapes": [

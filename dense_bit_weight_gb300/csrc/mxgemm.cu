@@ -139,7 +139,7 @@ struct MxLayout {
     static constexpr int SF_STAGE = SFA_BYTES + SFB_BYTES;
     static constexpr int BAR_OFF = SF_OFF + STAGES * SF_STAGE;
     static constexpr int NACC = BN == 128 ? 2 : 1;
-    static constexpr int NBARS = 2 * STAGES + 2 * NACC + 1;
+    static constexpr int NBARS = 2 * STAGES + 2 * NACC + 2;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int SMEM = MISC_OFF + 16 + 1024;
     static_assert(STAGE_BYTES % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
@@ -170,6 +170,7 @@ k_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMa
     auto TFULL = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
     auto TEMPTY = [&](int a) { return bar0 + 8u * (2 * STAGES + NACC + a); };
     const uint32_t DONE = bar0 + 8u * (2 * STAGES + 2 * NACC);
+    const uint32_t FIXB = bar0 + 8u * (2 * STAGES + 2 * NACC + 1);   // epilogue warps' barrier
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + L::MISC_OFF);   // [0] tmem, [1] abort, [2] last flag
     volatile uint32_t *abort_flag = misc + 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -184,6 +185,7 @@ k_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMa
             ptx::mbar_init(TEMPTY(a), kEpiThreads / 32);
         }
         ptx::mbar_init(DONE, 1);
+        ptx::mbar_init(FIXB, kEpiThreads / 32);
         misc[1] = 0;
         misc[2] = 0;
         ptx::fence_mbar_init();
@@ -302,7 +304,7 @@ k_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMa
         const int etid = threadIdx.x - 64;
         ptx::pdl_wait();
         int acc = 0;
-        uint32_t acc_phase = 0;
+        uint32_t acc_phase = 0, fphase = 0;
         SegIter it(sched, blockIdx.x, sched.tiles);
         Segment seg;
         while (it.next(sched, seg)) {
@@ -342,14 +344,14 @@ k_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMa
             const int c_first = cta_of_unit(sched, (long long)t * sched.nk);
             const int c_last = cta_of_unit(sched, (long long)(t + 1) * sched.nk - 1);
             __threadfence();
-            ptx::named_bar_sync(1, kEpiThreads);
+            if (!group_sync_warp(FIXB, fphase, abort_flag, d_error)) break;
             if (etid == 0) {
                 const int old = atomicAdd(counters + t, 1);
                 const bool last = old == c_last - c_first;
                 if (last) counters[t] = 0;
                 misc[2] = last ? 1u : 0u;
             }
-            ptx::named_bar_sync(1, kEpiThreads);
+            if (!group_sync_warp(FIXB, fphase, abort_flag, d_error)) break;
             if (!misc[2]) continue;
             __threadfence();
             streamk_fixup<BN, 16>(sched, ws, t, row, [&](int c0, const float(&f)[16]) {

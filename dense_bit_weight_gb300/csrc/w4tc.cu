@@ -85,7 +85,7 @@ struct TcLayout {
     static constexpr int A_BYTES = BN * KST * 2;            // two 64-k boxes of BN rows
     static constexpr int A_OFF = STAGES * PK_BYTES;
     static constexpr int BAR_OFF = A_OFF + AST * A_BYTES;
-    static constexpr int NBARS = 2 * STAGES + 2 * AST + 2 * NXB + 2 * ND + NWG;
+    static constexpr int NBARS = 2 * STAGES + 2 * AST + 2 * NXB + 2 * ND + NWG + 1;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int SMEM = MISC_OFF + 16 + 1024;       // + slack to align the base
     static_assert(STAGES % NWG == 0 && AST % NWG == 0 && NXB % NWG == 0, "ring slots must map to one warpgroup");
@@ -155,6 +155,7 @@ k_w4tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensor
     auto DFULL = [&](int d) { return bar0 + 8u * (2 * STAGES + 2 * AST + 2 * NXB + d); };
     auto DEMPTY = [&](int d) { return bar0 + 8u * (2 * STAGES + 2 * AST + 2 * NXB + ND + d); };
     auto DONE = [&](int u) { return bar0 + 8u * (2 * STAGES + 2 * AST + 2 * NXB + 2 * ND + u); };
+    const uint32_t FIXB = bar0 + 8u * (2 * STAGES + 2 * AST + 2 * NXB + 2 * ND + NWG);   // epilogue warps' barrier
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + L::MISC_OFF);   // [0] tmem, [1] abort, [2] last flag
     volatile uint32_t *abort_flag = misc + 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -177,6 +178,7 @@ k_w4tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensor
             ptx::mbar_init(DEMPTY(d), kEpiThreads / 32);
         }
         for (int u = 0; u < NWG; ++u) ptx::mbar_init(DONE(u), 1);
+        ptx::mbar_init(FIXB, kEpiThreads / 32);
         misc[1] = 0;
         misc[2] = 0;
         ptx::fence_mbar_init();
@@ -347,14 +349,14 @@ k_w4tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensor
             ptx::mma_commit_warp(DONE(u));
             wait_bar_drain(DONE(u), 0);
         }
-    } else {
+    } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
         // ------------------------------------------------------------ epilogue (warps 2-5)
         const int q4 = warp & 3;            // tensor-memory lane quarter this warp may read
         const int row = q4 * 32 + lane;     // accumulator row = weight row within the tile
         const int etid = threadIdx.x - 32 * kEpiWarp0;
         const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16) + kDCol;
         ptx::pdl_wait();                    // the group sums; C, workspace and counters may be in use before
-        uint32_t gc = 0;
+        uint32_t gc = 0, fphase = 0;
         SegIter it(sched, blockIdx.x, sched.tiles);
         Segment seg;
         bool ok = true;
@@ -434,14 +436,14 @@ k_w4tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensor
             const int c_first = cta_of_unit(sched, (long long)t * sched.nk);
             const int c_last = cta_of_unit(sched, (long long)(t + 1) * sched.nk - 1);
             __threadfence();
-            ptx::named_bar_sync(1, kEpiThreads);
+            if (!group_sync_warp(FIXB, fphase, abort_flag, d_error)) break;
             if (etid == 0) {
                 const int old = atomicAdd(counters + t, 1);
                 const bool last = old == c_last - c_first;
                 if (last) counters[t] = 0;
                 misc[2] = last ? 1u : 0u;
             }
-            ptx::named_bar_sync(1, kEpiThreads);
+            if (!group_sync_warp(FIXB, fphase, abort_flag, d_error)) break;
             if (!misc[2]) continue;
             __threadfence();
             fixup_store<BN>(sched, ws, t, row, C, ldc, R, Q, n, qb);

@@ -63,6 +63,20 @@ __device__ __forceinline__ void arrive_warp(uint32_t bar)
     if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(bar);
 }
 
+// A barrier among several warps built on an mbarrier whose count is the
+// number of warps: every warp arrives once, then waits for the phase with the
+// bounded wait, so a warp that gave up elsewhere can never leave the others
+// stuck (a named barrier, bar.sync, has no time limit).  `phase` is the
+// caller's running parity of this barrier.  Returns false on expiry or abort.
+__device__ __forceinline__ bool group_sync_warp(uint32_t bar, uint32_t &phase, volatile uint32_t *abort_flag,
+                                                int *d_error)
+{
+    arrive_warp(bar);
+    const bool ok = wait_bar_warp(bar, phase, abort_flag, d_error);
+    phase ^= 1u;
+    return ok;
+}
+
 // Wait without looking at the abort flag (used when draining before exit).
 __device__ __forceinline__ void wait_bar_drain(uint32_t bar, uint32_t parity)
 {
