@@ -417,9 +417,11 @@ bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int
         return true;
     }
     if (variant == GEMM_VARIANT_GROUPWISE) {
-        // tokens in tiles of 16, 32 or 64; 128-k stages; stream-K over every SM
+        // tokens in tiles of 16, 32 or 64 (group 32: at most 32, the kernel's
+        // eight per-group accumulators must fit beside its stage buffers);
+        // 128-k stages; stream-K over every SM
         int bn = 16;
-        while (bn < M && bn < 64) bn *= 2;
+        while (bn < M && bn < (group == 32 ? 32 : 64)) bn *= 2;
         const int64_t tiles_r = (N + kUmmaBM - 1) / kUmmaBM, tiles_q = (M + bn - 1) / bn;
         const int64_t nk = (K + 127) / 128;
         const int64_t units = tiles_r * tiles_q * nk;

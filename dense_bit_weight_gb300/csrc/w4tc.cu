@@ -30,15 +30,17 @@
 //               tensor-memory lane quarter) for the whole 128-k stage, and one
 //               warp of the group issues the stage's eight MMAs (K = 16) into
 //               the accumulators of the stage's groups (a ring of ND).
-//               The NXB tensor-memory stage buffers (6 for token tiles up to
-//               32, else 4) are used in turn, so each warpgroup can run NXB / 2
-//               stages ahead.  Issuing from the warpgroups instead of a
+//               The NXB tensor-memory stage buffers (6 or 4) are used in
+//               turn, so each warpgroup can run NXB / 2 stages ahead.  Issuing from the warpgroups instead of a
 //               dedicated MMA warp (measured: ~1000 cycles per stage there,
 //               sharing its SMSP with dequantising warps, and a wake-up per
 //               stage) keeps the MMA issue next to the data it waits for.
-// The packed-weight and activation rings and the stage buffers have even
-// counts, so a slot is only ever used by the stages of one warpgroup (its
-// mbarrier phases are never skipped by a waiter).
+// The packed-weight and activation rings, the stage buffers and the
+// accumulators are sized so that a slot is only ever used by the stages of
+// one warpgroup: a waiter's previous use of a slot is then its own, and a
+// parity wait can never mistake a phase two steps behind for a completed one.
+// (Group 32 puts four groups in a stage, so it takes eight accumulators and
+// token tiles of at most 32.)
 //
 // Tensor memory (512 columns): dequantised stage buffers b = 0..NXB-1 at
 // columns 64 b (128 k each: column c of a buffer holds k pair c in the
@@ -69,15 +71,19 @@ namespace {
 constexpr int BM = kTileRows;   // weight rows per tile
 constexpr int KST = 128;        // k per stage
 constexpr int NWG = 2;          // dequantising warpgroups (stages alternate between them)
-constexpr int ND = 4;           // per-group accumulators in tensor memory (ring)
 constexpr uint32_t kXCols = KST / 2;          // tensor-memory columns of one dequantised stage
 constexpr int kEpiWarp0 = 2, kActWarp = 6, kDqWarp0 = 7;
 constexpr int kThreads = (kDqWarp0 + 4 * NWG) * 32;
 constexpr int kEpiThreads = 128;
 
-template <int BN>
+// BN: token tile; LG: log2 of the quantisation group.
+template <int BN, int LG>
 struct TcLayout {
-    static constexpr int NXB = BN <= 32 ? 6 : 4;            // dequantised stage buffers in tensor memory
+    static constexpr int NGS = KST >> LG;                   // groups per stage
+    // per-group accumulators (a ring): a multiple of NWG x NGS, so stage gs's
+    // accumulators are used only by the stages of its own warpgroup
+    static constexpr int ND = LG == 5 ? 8 : 4;
+    static constexpr int NXB = BN <= 16 || (BN == 32 && LG > 5) ? 6 : 4;   // dequantised stage buffers
     static constexpr uint32_t DCOL = NXB * kXCols;          // first accumulator column
     static constexpr int STAGES = BN <= 32 ? 12 : 8;        // packed-weight ring (8 KB per slot)
     static constexpr int AST = BN <= 32 ? 8 : 4;            // activation ring
@@ -90,6 +96,7 @@ struct TcLayout {
     static constexpr int SMEM = MISC_OFF + 16 + 1024;       // + slack to align the base
     static_assert(STAGES % NWG == 0 && AST % NWG == 0 && NXB % NWG == 0, "ring slots must map to one warpgroup");
     static_assert(DCOL + ND * BN <= 512, "tensor-memory map");
+    static_assert(ND % (NWG * NGS) == 0, "a warpgroup's accumulators are its own");
     static_assert(A_BYTES % 1024 == 0, "activation boxes keep the 1024-byte swizzle alignment");
 };
 
@@ -136,11 +143,11 @@ k_w4tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensor
        int *__restrict__ counters,
        int *__restrict__ d_error)
 {
-    using L = TcLayout<BN>;
-    constexpr int STAGES = L::STAGES, AST = L::AST, NXB = L::NXB;
+    using L = TcLayout<BN, LG>;
+    constexpr int STAGES = L::STAGES, AST = L::AST, NXB = L::NXB, ND = L::ND;
     constexpr uint32_t kDCol = L::DCOL;
     constexpr int GROUP = 1 << LG;
-    constexpr int NGS = KST >> LG;   // groups per stage: 1, 2 or 4
+    constexpr int NGS = L::NGS;      // groups per stage: 1, 2 or 4
     constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN);
     extern __shared__ uint8_t tc_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~uintptr_t(1023));
@@ -464,7 +471,7 @@ template <int BN, int LG>
 cudaError_t launch_tc_t(const CUtensorMap &mq, const CUtensorMap &ma, uint16_t *C, int R, int Q, int64_t ldc,
                         const Sched &s, const TcArgs &w, const LaunchCtx &c)
 {
-    using L = TcLayout<BN>;
+    using L = TcLayout<BN, LG>;
     auto kern = k_w4tc<BN, LG>;
     static std::once_flag once[64];
     static cudaError_t attr_err[64];
@@ -489,7 +496,7 @@ cudaError_t launch_tc_t(const CUtensorMap &mq, const CUtensorMap &ma, uint16_t *
 
 }  // namespace
 
-int w4tc_stages(int bn) { return bn <= 32 ? TcLayout<16>::STAGES : TcLayout<64>::STAGES; }
+int w4tc_stages(int bn) { return bn <= 32 ? TcLayout<16, 7>::STAGES : TcLayout<64, 7>::STAGES; }
 
 cudaError_t launch_w4tc(const GemmArgs &a, const Plan &p, const LaunchCtx &c)
 {
@@ -524,7 +531,7 @@ cudaError_t launch_w4tc(const GemmArgs &a, const Plan &p, const LaunchCtx &c)
     if (bn == BNV && lg == LGV) return launch_tc_t<BNV, LGV>(mq, ma, C, (int)a.N, (int)a.M, a.ldc, s, w, c);
     W4TC_CASE(16, 7) W4TC_CASE(16, 6) W4TC_CASE(16, 5)
     W4TC_CASE(32, 7) W4TC_CASE(32, 6) W4TC_CASE(32, 5)
-    W4TC_CASE(64, 7) W4TC_CASE(64, 6) W4TC_CASE(64, 5)
+    W4TC_CASE(64, 7) W4TC_CASE(64, 6)
 #undef W4TC_CASE
     return cudaErrorInvalidValue;
 }
