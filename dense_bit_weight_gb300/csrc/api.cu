@@ -166,6 +166,10 @@ int run(const GemmArgs &a, const Plan &p, cudaStream_t st, bool w4, int mx_fmt =
         if (mx_fmt < 0) return GEMM_ERR_VARIANT;
         e = launch_mx(a, p, c, mx_fmt);
         break;
+    case GEMM_VARIANT_PAIR:
+        if (w4 || mx_fmt >= 0 || a.epi != GEMM_EPI_NONE || a.gends) return GEMM_ERR_VARIANT;
+        e = launch_umma_pair(a, p, c);
+        break;
     case GEMM_VARIANT_SKINNY:
     case GEMM_VARIANT_PREFILL:
         if (w4 && p.variant != GEMM_VARIANT_SKINNY) return GEMM_ERR_VARIANT;
@@ -358,6 +362,20 @@ bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan 
     case GEMM_VARIANT_PREFILL: {
         const int bn = wide_bn(M, N, sm_count, pairs);
         plan_umma(M, N, K, false, bn ? bn : 256, sm_count, query, p, pairs);
+        return true;
+    }
+    case GEMM_VARIANT_PAIR: {
+        if (pairs) return false;   // plain C = A B^T only
+        p->variant = GEMM_VARIANT_PAIR;
+        p->kernels = 1;
+        p->split = 1;
+        p->mode = 0;
+        p->bn = 256;
+        p->tile_m = 256;
+        p->tile_n = 256;
+        p->stages = 6;
+        p->ctas_per_sm = 1;
+        p->grid = umma_pair_grid(M, N, sm_count);
         return true;
     }
     default: return false;

@@ -105,6 +105,10 @@ cudaError_t launch_w4_prep(const GemmArgs &a, const LaunchCtx &c, uint16_t *Ap, 
 // (16, 32 or 64), 128-k stages, stream-K over (weight tile, stage) units.
 int w4tc_stages(int bn);
 cudaError_t launch_w4tc(const GemmArgs &a, const Plan &p, const LaunchCtx &c);
+// Prefill on CTA pairs (umma2.cu): 256 x 256 tiles, tcgen05.mma.cta_group::2;
+// the grid is twice the number of pairs.
+int umma_pair_grid(int64_t M, int64_t N, int sm_count);
+cudaError_t launch_umma_pair(const GemmArgs &a, const Plan &p, const LaunchCtx &c);
 // Block-scaled (MX) GEMM (mxgemm.cu): fmt 0 = E4M3 x E4M3, 1 = packed E2M1 x
 // E2M1; k per stage (128 bytes of every row) and the workspace bytes of the
 // rearranged scale chunks; the launch runs the scale pre-pass, then the GEMM.

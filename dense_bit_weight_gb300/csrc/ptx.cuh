@@ -308,6 +308,9 @@ __device__ __forceinline__ uint32_t cluster_ctarank()
 // thread's memory writes (a release would first wait for every write in
 // flight, remote ones included).
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory"); }
+// The arrive with release semantics: this thread's earlier writes (barrier
+// initialisation included) are visible to the cluster after the wait.
+__device__ __forceinline__ void cluster_arrive_release() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
 
 // 16-byte store into a (possibly other) CTA's shared memory of this cluster,

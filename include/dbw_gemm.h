@@ -71,7 +71,9 @@ typedef enum {
     GEMM_VARIANT_GROUPWISE = 7,  /* W4A16: exact 128 + q weights in tensor memory, */
                                  /* one tcgen05 accumulator per quantisation       */
                                  /* group, scale and zero applied per group        */
-    GEMM_VARIANT_BLOCK_SCALED = 8 /* MX: block-scaled tcgen05 MMAs (gemm_mxfp*)    */
+    GEMM_VARIANT_BLOCK_SCALED = 8, /* MX: block-scaled tcgen05 MMAs (gemm_mxfp*)   */
+    GEMM_VARIANT_PAIR = 9        /* bf16 prefill on CTA pairs: 256 x 256 tiles,    */
+                                 /* tcgen05.mma.cta_group::2 (plain epilogue only) */
 } gemm_variant;
 
 typedef struct {
