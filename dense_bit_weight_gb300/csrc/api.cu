@@ -338,10 +338,18 @@ bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan 
         p->split = 1;
         return true;
     }
-    if (variant == GEMM_VARIANT_AUTO)
-        variant = M > 128 || wide_bn(M, N, sm_count, pairs) ? GEMM_VARIANT_PREFILL
-                  : M <= 4                                   ? GEMM_VARIANT_GEMV
-                                                             : GEMM_VARIANT_SKINNY;
+    if (variant == GEMM_VARIANT_AUTO) {
+        // CTA pairs (256 x 256 tiles, cta_group::2) whenever their tiles keep
+        // at least half the SM pairs busy: measured on the fifteen prefill
+        // shapes at 1185-1961 TFLOP/s against 1039-1683 for single-CTA
+        // 128 x 256 tiles (every shape faster); below that the single-CTA
+        // kernel's stream-K spreads the work over every SM
+        const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
+        variant = !pairs && M > 128 && 4 * pair_tiles >= sm_count           ? GEMM_VARIANT_PAIR
+                  : M > 128 || wide_bn(M, N, sm_count, pairs)               ? GEMM_VARIANT_PREFILL
+                  : M <= 4                                                  ? GEMM_VARIANT_GEMV
+                                                                            : GEMM_VARIANT_SKINNY;
+    }
     switch (variant) {
     case GEMM_VARIANT_GEMV:
         p->variant = GEMM_VARIANT_GEMV;

@@ -108,7 +108,7 @@ def test_plans_are_host_only_and_cover_the_workloads(g):
             assert p["variant"] in (1, 2, 3) and p["kernels"] >= 1 and p["grid"] >= 1
     for M in (1024, 4096, 16384):
         p = g.gemm_bf16_plan(M, 8192, 8192, num_sms=sms)
-        assert p["variant"] in (1, 2, 3)
+        assert p["variant"] == 9 and p["tile_m"] == p["tile_n"] == 256
     assert g.gemm_bf16_plan(5, 7, 0, num_sms=sms)["variant"] == 4
     for M in (1, 16, 64, 128):
         p = g.gemm_w4a16_plan(M, 7168, 5120, 128, num_sms=sms)
@@ -177,10 +177,10 @@ def test_fused_epilogue_argument_errors():
     assert g.gemm_bf16_fused_ptr(p, p, p, p, 8, 8, 8, 8, 8, 8, 2) == 11
     assert g.gemm_bf16_fused_ptr(p, p, p, p, 8, 8, 8, 8, 8, 8, 0) == 11
     assert g.gemm_status_string(11) != g.gemm_status_string(99)
-    # the SiLU-mul plan is the plain plan on the 2N weight rows
+    # the SiLU-mul plans are plans on the 2N weight rows, on single-CTA kernels
     sms = 152
     for M in (1, 8, 128, 4096):
-        assert g.gemm_bf16_plan(M, 2 * 12288, 4096, num_sms=sms)["variant"] in (1, 2, 3)
+        assert g.gemm_bf16_fused_plan(M, 12288, 4096, "silu_mul", num_sms=sms)["variant"] in (1, 2, 3)
 
 
 def test_prefill_last_wave_split():
@@ -188,9 +188,25 @@ def test_prefill_last_wave_split():
     # leftover tile, whole tiles before); a smaller leftover stays whole tiles
     from dense_bit_weight_gb300 import gemm as g
     sms = 152
-    assert g.gemm_bf16_plan(1024, 6144, 4096, num_sms=sms)["split"] == 3      # 192 tiles: 152 + 40
-    assert g.gemm_bf16_plan(4096, 4096, 4096, num_sms=sms)["split"] == 2      # 512 tiles: 456 + 56
-    assert g.gemm_bf16_plan(4096, 24576, 4096, num_sms=sms)["split"] == 1     # 3072 tiles: 3040 + 32
+    pf = lambda M, N, K: g.gemm_bf16_plan(M, N, K, "prefill", num_sms=sms)   # the single-CTA kernel
+    assert pf(1024, 6144, 4096)["split"] == 3      # 192 tiles: 152 + 40
+    assert pf(4096, 4096, 4096)["split"] == 2      # 512 tiles: 456 + 56
+    assert pf(4096, 24576, 4096)["split"] == 1     # 3072 tiles: 3040 + 32
+
+
+def test_prefill_on_cta_pairs():
+    # 256 x 256 pair tiles whenever they keep at least half the SM pairs busy;
+    # the grid is two CTAs per pair, at most one pair per two SMs
+    from dense_bit_weight_gb300 import gemm as g
+    sms = 152
+    p = g.gemm_bf16_plan(1024, 4096, 4096, num_sms=sms)          # 4 x 16 = 64 pair tiles
+    assert (p["variant"], p["grid"], p["tile_m"], p["tile_n"]) == (9, 128, 256, 256)
+    assert g.gemm_bf16_plan(4096, 24576, 4096, num_sms=sms)["grid"] == sms
+    assert g.gemm_bf16_plan(512, 4096, 12288, num_sms=sms)["variant"] == 3    # 32 pair tiles: stream-K instead
+    assert g.gemm_bf16_plan(300, 1200, 4096, num_sms=sms)["variant"] == 3
+    # fused epilogues stay on the single-CTA kernel; the pair kernel can be forced
+    assert g.gemm_bf16_fused_plan(4096, 12288, 4096, "silu_mul", num_sms=sms)["variant"] == 3
+    assert g.gemm_bf16_plan(8, 64, 64, "pair", num_sms=sms)["grid"] == 2
 
 
 def test_wide_tiles_for_one_token_tile():
@@ -240,10 +256,12 @@ def test_planner_invariants_over_shapes():
             N = rnd.randrange(8, 40000, 8)
             K = rnd.randrange(8, 16384, 8)
             p = g.gemm_bf16_plan(M, N, K, num_sms=sms)
-            assert p["variant"] in (1, 2, 3), p
+            assert p["variant"] in (1, 2, 3, 9), p
             assert p["grid"] >= 1 and p["split"] >= 1
             if p["variant"] in (2, 3):
                 assert p["grid"] <= 2 * sms, (M, N, K, p)
+            if p["variant"] == 9:
+                assert M > 128 and p["grid"] % 2 == 0 and p["grid"] <= sms, (M, N, K, p)
             if p["variant"] == 3 and M <= 128 and p["tile_n"] != 256:
                 tiles = -(-N // p["tile_n"])
                 assert p["tile_n"] in (176, 192, 224) and p["tile_n"] >= M

@@ -18,7 +18,7 @@ from gpu_helpers import assert_close, assert_exact, bf16_inputs, dev_bf16, host_
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = ["gemv", "skinny", "prefill"]
+VARIANTS = ["gemv", "skinny", "prefill", "pair"]
 
 
 @pytest.fixture(scope="module")

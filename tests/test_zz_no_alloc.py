@@ -8,9 +8,8 @@ and checks both results against the fp64 oracle (bit for bit on integer
 inputs, |out - ref| <= 1e-2*|ref| + 1e-2*rms(ref) on N(0,1) inputs) and
 against the allocating entry point gemm_bf16 within the same tolerance.
 Shapes cover the GEMV path, cluster split-K (skinny), the skinny kernel's
-stream-K schedule with more CTAs than the fixed partials allow, whole-tile
-prefill, stream-K prefill that must run on fewer CTAs, and prefill whose full
-waves of whole tiles keep every SM while fewer CTAs share the split last wave.
+stream-K schedule with more CTAs than the fixed partials allow, prefill on
+CTA pairs, and stream-K prefill that must run on fewer CTAs.
 
 This file is collected last so that a failure here stops a run only after
 every other test has run.
@@ -27,9 +26,8 @@ pytestmark = pytest.mark.gpu
 
 # (M, N, K): GEMV, cluster split-K, skinny stream-K over 320 weight tiles of 128
 # columns (its 152 partial writers need more than the fixed 16 MiB: 128 share
-# the units), whole-tile prefill, stream-K prefill on 15 tiles (64 CTAs),
-# 4096^3 (full waves of whole tiles on all 152 SMs, the last wave split among
-# at most 64 CTAs).
+# the units), prefill on CTA pairs (no scratch), stream-K prefill on 15 tiles
+# (64 CTAs), and 4096^3 on CTA pairs.
 SHAPES = [(1, 4096, 4096), (16, 4096, 4096), (128, 40960, 512), (1024, 4096, 4096),
           (300, 1200, 2056), (4096, 4096, 4096)]
 
