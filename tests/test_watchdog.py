@@ -15,7 +15,7 @@ from gpu_helpers import assert_close, bf16_inputs, dev_bf16, host_bits
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("variant,M", [("skinny", 16), ("prefill", 256)])
+@pytest.mark.parametrize("variant,M", [("skinny", 16), ("prefill", 256), ("pair", 512)])
 def test_forced_timeout_is_reported_and_recoverable(variant, M):
     import torch
     from dense_bit_weight_gb300 import gemm as g
@@ -38,7 +38,7 @@ def test_forced_timeout_is_reported_and_recoverable(variant, M):
     assert g.gemm_last_device_error() == 0
 
 
-@pytest.mark.parametrize("variant", ["skinny", "fragment"])
+@pytest.mark.parametrize("variant", ["skinny", "fragment", "groupwise"])
 def test_forced_timeout_w4a16(variant):
     import torch
     from dense_bit_weight_gb300 import gemm as g, synth
@@ -58,4 +58,26 @@ def test_forced_timeout_w4a16(variant):
     C = g.gemm_w4a16(*args, variant=variant)
     torch.cuda.synchronize()
     assert_close(host_bits(C), oracle.gemm_w4a16(A, Bq, S, Z, group), what="w4a16 after timeout")
+    assert g.gemm_last_device_error() == 0
+
+
+def test_forced_timeout_mx():
+    import torch
+    from dense_bit_weight_gb300 import gemm as g, synth
+    M, N, K = 256, 512, 512
+    A, SA = synth.mx_operands(M, K, "e4m3", seed=1, role="a")
+    B, SB = synth.mx_operands(N, K, "e4m3", seed=2, role="b")
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    args = (dev(A), dev(SA), dev(B), dev(SB))
+    g.gemm_debug_inject_timeout(True)
+    try:
+        g.gemm_mx(*args, "e4m3")
+        torch.cuda.synchronize()
+    finally:
+        g.gemm_debug_inject_timeout(False)
+    assert g.gemm_last_device_error() == 7
+    g.gemm_shutdown()
+    C = g.gemm_mx(*args, "e4m3")
+    torch.cuda.synchronize()
+    assert_close(host_bits(C), oracle.gemm_mx(A, SA, B, SB), what="mx after timeout")
     assert g.gemm_last_device_error() == 0
