@@ -424,12 +424,13 @@ def cpu_oracle_sample(target_s=12.0):
     import oracle
     from dense_bit_weight_gb300 import synth
     cores = oracle.hardware_threads()
-    # calibrate on a small piece, then size the sample for about target_s seconds
-    A = synth.bf16_normal((1, 4096), 1.0, 0, synth.STREAM_A)
-    B = synth.bf16_normal((512, 4096), 4096 ** -0.5, 0, synth.STREAM_B)
+    # calibrate on a piece large enough that thread start-up does not count,
+    # then size the sample for about target_s seconds
+    A = synth.bf16_normal((8, 4096), 1.0, 0, synth.STREAM_A)
+    B = synth.bf16_normal((4096, 4096), 4096 ** -0.5, 0, synth.STREAM_B)
     t = time.perf_counter()
     oracle.gemm_bf16(A, B)
-    per_mac = (time.perf_counter() - t) / (512 * 4096)
+    per_mac = (time.perf_counter() - t) / (8 * 4096 * 4096)
     total_macs = sum(M * N * K for (M, N, K) in DECODE)
     frac = min(1.0, target_s / max(per_mac * total_macs, 1e-9))
     work, secs = 0, 0.0
@@ -456,15 +457,15 @@ def cpu_oracle_configs(seconds_each=4.0):
     import oracle
     from dense_bit_weight_gb300 import synth
     # calibration: MACs per second of each oracle routine on this host
-    A = synth.bf16_normal((4, 4096), 1.0, 0, synth.STREAM_A)
-    B = synth.bf16_normal((256, 4096), 4096 ** -0.5, 0, synth.STREAM_B)
+    A = synth.bf16_normal((8, 4096), 1.0, 0, synth.STREAM_A)
+    B = synth.bf16_normal((2048, 4096), 4096 ** -0.5, 0, synth.STREAM_B)
     t = time.perf_counter()
     oracle.gemm_bf16(A, B)
-    bf16_mac_s = 4 * 256 * 4096 / (time.perf_counter() - t)
-    Bq, S, Z = synth.w4a16_operands(256, 4096, 128, 0)
+    bf16_mac_s = 8 * 2048 * 4096 / (time.perf_counter() - t)
+    Bq, S, Z = synth.w4a16_operands(2048, 4096, 128, 0)
     t = time.perf_counter()
     oracle.gemm_w4a16(A, Bq, S, Z, 128)
-    w4_mac_s = 4 * 256 * 4096 / (time.perf_counter() - t)
+    w4_mac_s = 8 * 2048 * 4096 / (time.perf_counter() - t)
     out = {}
     for name, shapes, kind in (("down", DOWN, "bf16"), ("prefill", PREFILL, "bf16"), ("w4a16", W4, "w4")):
         rate = w4_mac_s if kind == "w4" else bf16_mac_s
@@ -762,11 +763,11 @@ def run_reference(args):
     from dense_bit_weight_gb300 import synth
     cores = oracle.hardware_threads()
     # each step: every decode GEMM on a slice of its weight rows, about 1 s of CPU work
-    A = synth.bf16_normal((1, 4096), 1.0, 0, synth.STREAM_A)
-    Bc = synth.bf16_normal((512, 4096), 4096 ** -0.5, 0, synth.STREAM_B)
+    A = synth.bf16_normal((8, 4096), 1.0, 0, synth.STREAM_A)
+    Bc = synth.bf16_normal((4096, 4096), 4096 ** -0.5, 0, synth.STREAM_B)
     t = time.perf_counter()
     oracle.gemm_bf16(A, Bc)
-    per_mac = (time.perf_counter() - t) / (512 * 4096)
+    per_mac = (time.perf_counter() - t) / (8 * 4096 * 4096)
     total = sum(M * N * K for (M, N, K) in DECODE)
     frac = min(1.0, args.ref_step_seconds / max(per_mac * total, 1e-9))
     ops = []
