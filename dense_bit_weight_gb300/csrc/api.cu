@@ -167,8 +167,8 @@ int run(const GemmArgs &a, const Plan &p, cudaStream_t st, bool w4, int mx_fmt =
         e = launch_mx(a, p, c, mx_fmt);
         break;
     case GEMM_VARIANT_PAIR:
-        if (w4 || mx_fmt >= 0 || a.epi != GEMM_EPI_NONE || a.gends) return GEMM_ERR_VARIANT;
-        e = launch_umma_pair(a, p, c);
+        if (mx_fmt >= 0 || a.epi != GEMM_EPI_NONE || a.gends) return GEMM_ERR_VARIANT;
+        e = w4 ? launch_w4_pair(a, p, c) : launch_umma_pair(a, p, c);
         break;
     case GEMM_VARIANT_SKINNY:
     case GEMM_VARIANT_PREFILL:
@@ -427,8 +427,29 @@ bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int
 {
     *p = Plan{};
     if (K == 0) return false;
-    if (variant == GEMM_VARIANT_AUTO)
-        variant = M <= 8 ? GEMM_VARIANT_FRAGMENT : GEMM_VARIANT_SKINNY;
+    if (variant == GEMM_VARIANT_AUTO) {
+        // from 1024 tokens on, and when pair tiles keep half the SM pairs
+        // busy: dequantise the weights once and run the pair GEMM
+        const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
+        variant = M >= 1024 && 4 * pair_tiles >= sm_count ? GEMM_VARIANT_PAIR
+                  : M <= 8                                ? GEMM_VARIANT_FRAGMENT
+                                                          : GEMM_VARIANT_SKINNY;
+    }
+    if (variant == GEMM_VARIANT_PAIR) {
+        p->variant = GEMM_VARIANT_PAIR;
+        p->kernels = 2;                      // dequantisation, then the pair GEMM
+        p->act_copy = 1;
+        p->ws_extra = N * K / 2;             // bf16 [N, K] as floats
+        p->split = 1;
+        p->mode = 0;
+        p->bn = 256;
+        p->tile_m = 256;
+        p->tile_n = 256;
+        p->stages = 6;
+        p->ctas_per_sm = 1;
+        p->grid = umma_pair_grid(M, N, sm_count);
+        return true;
+    }
     if (variant == GEMM_VARIANT_REGISTER) {
         if (M > 32 || K / group > kW4RegisterMaxGroups) return false;
         p->variant = GEMM_VARIANT_REGISTER;
@@ -606,6 +627,10 @@ void workspace_need(const Plan &p, int64_t M, int64_t N, int64_t K, int64_t *flo
     }
     if (p.variant == GEMM_VARIANT_BLOCK_SCALED) {   // rearranged scale chunks after the partials
         *floats = act_copy_offset(p) + p.ws_extra;
+        return;
+    }
+    if (p.variant == GEMM_VARIANT_PAIR) {   // W4A16: the dequantised weights only
+        *floats = p.ws_extra;
         return;
     }
     else if (p.act_copy) *floats = act_copy_offset(p) + (M * K + 127) / 128 * 64 + p.ws_extra;   // bf16 [M, K] (+ sums)

@@ -109,6 +109,9 @@ cudaError_t launch_w4tc(const GemmArgs &a, const Plan &p, const LaunchCtx &c);
 // the grid is twice the number of pairs.
 int umma_pair_grid(int64_t M, int64_t N, int sm_count);
 cudaError_t launch_umma_pair(const GemmArgs &a, const Plan &p, const LaunchCtx &c);
+// W4A16 with many tokens: weights dequantised to bf16 into the workspace
+// (act_copy, N * K bf16), then the pair GEMM.
+cudaError_t launch_w4_pair(const GemmArgs &a, const Plan &p, const LaunchCtx &c);
 // Block-scaled (MX) GEMM (mxgemm.cu): fmt 0 = E4M3 x E4M3, 1 = packed E2M1 x
 // E2M1; k per stage (128 bytes of every row) and the workspace bytes of the
 // rearranged scale chunks; the launch runs the scale pre-pass, then the GEMM.

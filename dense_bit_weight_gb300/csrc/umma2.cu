@@ -295,7 +295,70 @@ k_umma_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     }
 }
 
+// W4A16 weights dequantised to bf16: W[n,k] = (q[n,k] - z[n,k/g]) * s[n,k/g],
+// the product exact in fp32 and rounded once to bf16 (nearest even).  One
+// thread per 16 bytes of packed words (32 weights of one group, since g is a
+// multiple of 32): a 16-byte streaming load, four 16-byte stores.
+__global__ void __launch_bounds__(256) k_w4_dequant(const uint4 *__restrict__ bq, const uint16_t *__restrict__ scales,
+                                                    const uint8_t *__restrict__ zeros, uint4 *__restrict__ w,
+                                                    int64_t chunks, int cpr, int G, int lg_group)
+{
+    ptx::pdl_wait();   // the previous kernel may still read the buffer
+    ptx::pdl_launch_dependents();
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < chunks; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t n = i / cpr;
+        const int k0 = (int)(i - n * cpr) * 32;
+        const int grp = k0 >> lg_group;
+        const float s = bf16lo(__ldg(scales + n * G + grp));
+        const float z = (float)__ldg(zeros + n * G + grp);
+        const uint4 q = ld_stream_v4(bq + i);
+        const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {   // word j: weights k0 + 8j .. k0 + 8j + 7
+            uint4 o;
+            uint32_t *op = reinterpret_cast<uint32_t *>(&o);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float lo = ((float)((words[j] >> (8 * e)) & 0xFu) - z) * s;
+                const float hi = ((float)((words[j] >> (8 * e + 4)) & 0xFu) - z) * s;
+                op[e] = pack_bf16x2_rn(lo, hi);
+            }
+            w[i * 4 + j] = o;
+        }
+    }
+}
+
 }  // namespace
+
+// W4A16 at prefill sizes: dequantise the weights once into the workspace
+// (bf16 [N, K]), then the pair GEMM on them.
+cudaError_t launch_w4_pair(const GemmArgs &a, const Plan &p, const LaunchCtx &c)
+{
+    if (!c.act_copy) return cudaErrorInvalidValue;
+    uint16_t *W = (uint16_t *)c.act_copy;
+    const int64_t chunks = a.N * (a.K / 32);
+    int64_t grid = (chunks + 255) / 256;
+    if (grid > (int64_t)c.sm_count * 16) grid = (int64_t)c.sm_count * 16;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = c.stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_w4_dequant, (const uint4 *)a.B, (const uint16_t *)a.scales,
+                                       (const uint8_t *)a.zeros, (uint4 *)W, chunks, (int)(a.K / 32),
+                                       (int)(a.K / a.group), a.group == 32 ? 5 : a.group == 64 ? 6 : 7);
+    if (e != cudaSuccess) return e;
+    GemmArgs b = a;
+    b.B = W;
+    b.ldb = a.K;
+    b.lda = a.K;
+    b.ldc = a.N;
+    return launch_umma_pair(b, p, c);
+}
 
 // Pair tiles for the prefill shapes: 256 x 256 tiles in a grouped raster,
 // whole tiles round-robin over the pairs (two CTAs per pair, at most one pair

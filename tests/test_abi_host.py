@@ -117,11 +117,15 @@ def test_plans_are_host_only_and_cover_the_workloads(g):
     for M in (1, 2, 4, 5, 8):
         p = g.gemm_w4a16_plan(M, 34816, 5120, 128, num_sms=sms)
         assert p["variant"] == 6 and p["tile_m"] == 8 and p["kernels"] == 2
-    for M in (9, 16, 128, 129, 4096):
+    for M in (9, 16, 128, 129, 1023):
         assert g.gemm_w4a16_plan(M, 34816, 5120, 128, num_sms=sms)["variant"] == 2
-    # more than 128 tokens: 128-token tiles, the token tiles of a weight tile adjacent
-    p = g.gemm_w4a16_plan(4096, 34816, 5120, 128, num_sms=sms)
+    # more than 128 tokens on the tcgen05 W4A16 kernel: 128-token tiles
+    p = g.gemm_w4a16_plan(1000, 34816, 5120, 128, num_sms=sms)
     assert p["tile_m"] == 128 and p["grid"] <= sms
+    # from 1024 tokens: weights dequantised once, then the pair GEMM
+    for M in (1024, 4096):
+        p = g.gemm_w4a16_plan(M, 34816, 5120, 128, num_sms=sms)
+        assert (p["variant"], p["kernels"], p["tile_m"]) == (9, 2, 256) and p["grid"] <= sms
     # the fragment kernel stages scales per stage: any number of groups plans
     assert g.gemm_w4a16_plan(1, 4096, 32 * 545, 32, num_sms=sms)["variant"] == 6
     # beyond the staged-scale limit (K / group > 544 groups) the register kernel does not plan

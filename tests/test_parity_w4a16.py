@@ -17,7 +17,7 @@ from gpu_helpers import assert_close, assert_exact, dev_bf16, dev_raw, host_bits
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = ["gemv", "skinny", "prefill", "register", "fragment", "groupwise"]
+VARIANTS = ["gemv", "skinny", "prefill", "register", "fragment", "groupwise", "pair"]
 
 
 @pytest.fixture(scope="module")
