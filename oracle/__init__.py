@@ -142,6 +142,30 @@ def gemm_bf16_bias(A_bits: np.ndarray, B_bits: np.ndarray, bias_bits: np.ndarray
     return R
 
 
+def gemm_bf16_bias_act(A_bits: np.ndarray, B_bits: np.ndarray, bias_bits: np.ndarray, act: str,
+                       threads: int | None = None) -> np.ndarray:
+    """R[m,n] = act(sum_k A[m,k]*B[n,k] + bias[n]) in fp64 (unrounded), act
+    "relu" (max(x, 0)), "silu" (x / (1 + e^-x)) or "gelu" (x/2 (1 + erf(x/sqrt 2)))."""
+    S = gemm_bf16(A_bits, B_bits, threads)
+    return bias_act(S, bias_bits, act)
+
+
+def bias_act(S: np.ndarray, bias_bits: np.ndarray, act: str) -> np.ndarray:
+    """act(S[m,n] + bias[n]) in fp64, S [M,N] fp64 (the epilogue alone, for pins)."""
+    S = np.ascontiguousarray(S, dtype=np.float64)
+    if S.ndim == 1:
+        S = S.reshape(1, -1)
+    b = _as(bias_bits, np.uint16, "bias")
+    if b.shape != (S.shape[1],):
+        raise ValueError("bias must have one entry per column")
+    R = np.empty_like(S)
+    rc = _load().oracle_epilogue({"relu": 3, "silu": 4, "gelu": 5}[act], _ptr(S), None, _ptr(b), _ptr(R),
+                                 S.shape[0], S.shape[1])
+    if rc != 0:
+        raise RuntimeError(f"oracle_epilogue returned {rc}")
+    return R
+
+
 def gemm_bf16_silu_mul(A_bits: np.ndarray, B_bits: np.ndarray, threads: int | None = None) -> np.ndarray:
     """The fused gate/up projection: B_bits uint16 [2N,K] holds the gate rows
     0..N-1 and the up rows N..2N-1; R[m,n] = silu(g)*u in fp64 (unrounded)

@@ -44,7 +44,12 @@
  *       silu_mul  R[m,n] = silu(G[m,n]) * U[m,n], silu(x) = x / (1 + e^-x),
  *                 with G and U the gate and up halves of a fused gate/up
  *                 projection (hk-dsl PyPI page: the fused SiLU-mul kernel)
- *       exp is the C library's fp64 exp.
+ *       bias_relu / bias_silu / bias_gelu   R[m,n] = act(S[m,n] + bias[n]) with
+ *                 relu(x) = max(x, 0), silu(x) = x / (1 + e^-x) and
+ *                 gelu(x) = x * Phi(x) = x / 2 * (1 + erf(x / sqrt 2)) (the
+ *                 exact form; the guide's epilogue list, same section, names
+ *                 "bias_relu", "bias_silu", "bias_gelu" without a formula)
+ *       exp and erf are the C library's fp64 functions.
  *
  *   oracle_gemm_grouped    the grouped (mixture-of-experts) GEMM: expert g
  *       owns the token rows [end[g-1], end[g]) of the stacked activations
@@ -271,6 +276,7 @@ void oracle_round_to_bf16(const double *x, uint16_t *out, int64_t n)
 
 /* kind 1: R[m,n] = S[m,n] + bias[n] (bias bf16 bits [N]); S is [M,N].
  * kind 2: R[m,n] = silu(S[m,n]) * U[m,n], both [M,N].
+ * kind 3, 4, 5: R[m,n] = relu / silu / gelu (S[m,n] + bias[n]).
  * R may alias S.  Returns 0 on success, 2 on a bad kind or size. */
 int oracle_epilogue(int kind, const double *S, const double *U, const uint16_t *bias, double *R,
                     int64_t M, int64_t N)
@@ -283,6 +289,11 @@ int oracle_epilogue(int kind, const double *S, const double *U, const uint16_t *
                 R[m * N + n] = s + bf16_to_f64(bias[n]);
             } else if (kind == 2) {
                 R[m * N + n] = s / (1.0 + exp(-s)) * U[m * N + n];
+            } else if (kind >= 3 && kind <= 5) {
+                const double x = s + bf16_to_f64(bias[n]);
+                R[m * N + n] = kind == 3 ? (x > 0.0 ? x : 0.0)
+                               : kind == 4 ? x / (1.0 + exp(-x))
+                                           : 0.5 * x * (1.0 + erf(x / sqrt(2.0)));
             } else {
                 return 2;
             }

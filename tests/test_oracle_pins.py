@@ -359,6 +359,47 @@ def test_grouped_rejects_bad_offsets():
             oracle.gemm_grouped(A, B, np.array(bad, np.int32))
 
 
+# ------------------------------------------------------------ bias + activation epilogues
+
+def test_bias_relu_integer_exact():
+    M, N, K = 5, 33, 64
+    A = synth.bf16_int_uniform((M, K), -4, 4, 1, synth.STREAM_A_INT)
+    B = synth.bf16_int_uniform((N, K), -4, 4, 1, synth.STREAM_B_INT)
+    bias = synth.bf16_int_uniform((N,), -40, 40, 2, synth.STREAM_B_INT)
+    ia = oracle.bf16_bits_to_f64(A).astype(np.int64)
+    ib = oracle.bf16_bits_to_f64(B).astype(np.int64)
+    pre = ia @ ib.T + oracle.bf16_bits_to_f64(bias).astype(np.int64)
+    got = oracle.gemm_bf16_bias_act(A, B, bias, "relu")
+    assert np.array_equal(got, np.maximum(pre, 0).astype(np.float64))
+    assert (got == 0).any() and (got > 0).any()
+
+
+def test_bias_silu_tanh_form():
+    x = np.linspace(-30.0, 30.0, 601).reshape(1, -1)
+    bias = synth.bf16_from_small_ints(np.arange(601) % 7 - 3)
+    xb = x + oracle.bf16_bits_to_f64(bias)
+    got = oracle.bias_act(x, bias, "silu")
+    assert np.allclose(got, xb / 2 * (1 + np.tanh(xb / 2)), rtol=1e-12, atol=1e-12)
+    neg = xb < 0   # the stable form for negative x, exact relative agreement
+    assert np.allclose(got[neg], (xb * np.exp(xb) / (1 + np.exp(xb)))[neg], rtol=1e-13, atol=0)
+
+
+def test_bias_gelu_against_library_and_invariants():
+    x = np.linspace(-12.0, 12.0, 481).reshape(1, -1)
+    zero = np.zeros(x.shape[1], np.uint16)
+    got = oracle.bias_act(x, zero, "gelu")
+    ref = torch.nn.functional.gelu(torch.from_numpy(x), approximate="none").numpy()
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-15)
+    # x Phi(x) - (-x) Phi(-x) = x, and the textbook value at 1
+    neg = oracle.bias_act(-x, zero, "gelu")
+    assert np.allclose(got - neg, x, rtol=1e-13, atol=1e-13)
+    one = oracle.bias_act(np.array([[1.0]]), np.zeros(1, np.uint16), "gelu")
+    assert abs(one[0, 0] - 0.8413447460685429) < 1e-15
+    # the bias is added before the activation
+    b = synth.bf16_from_small_ints(np.full(x.shape[1], 2))
+    assert np.allclose(oracle.bias_act(x, b, "gelu"), oracle.bias_act(x + 2.0, zero, "gelu"), rtol=1e-15, atol=0)
+
+
 def test_tolerance_flags_planted_error():
     ref = synth.normal_f64(1000, 0, 9).reshape(10, 100)
     out = ref.copy()
