@@ -102,6 +102,11 @@ int stream_workspace(DeviceState &s, cudaStream_t st, int64_t floats, int64_t co
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+bool epi_needs_bias(int epi)
+{
+    return epi == GEMM_EPI_BIAS || epi == GEMM_EPI_BIAS_RELU || epi == GEMM_EPI_BIAS_SILU || epi == GEMM_EPI_BIAS_GELU;
+}
+
 bool overlaps(const void *a, int64_t abytes, const void *b, int64_t bbytes)
 {
     uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
@@ -328,7 +333,8 @@ static int wide_bn(int64_t M, int64_t N, int sm_count, bool pairs)
     return 0;
 }
 
-bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan *p, bool query, bool pairs)
+bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan *p, bool query, bool pairs,
+               bool fused)
 {
     *p = Plan{};
     if (K == 0) {
@@ -345,7 +351,7 @@ bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan 
         // 128 x 256 tiles (every shape faster); below that the single-CTA
         // kernel's stream-K spreads the work over every SM
         const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
-        variant = !pairs && M > 128 && 4 * pair_tiles >= sm_count           ? GEMM_VARIANT_PAIR
+        variant = !fused && M > 128 && 4 * pair_tiles >= sm_count           ? GEMM_VARIANT_PAIR
                   : M > 128 || wide_bn(M, N, sm_count, pairs)               ? GEMM_VARIANT_PREFILL
                   : M <= 4                                                  ? GEMM_VARIANT_GEMV
                                                                             : GEMM_VARIANT_SKINNY;
@@ -373,7 +379,7 @@ bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan 
         return true;
     }
     case GEMM_VARIANT_PAIR: {
-        if (pairs) return false;   // plain C = A B^T only
+        if (pairs || fused) return false;   // plain C = A B^T only
         p->variant = GEMM_VARIANT_PAIR;
         p->kernels = 1;
         p->split = 1;
@@ -428,12 +434,20 @@ bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int
     *p = Plan{};
     if (K == 0) return false;
     if (variant == GEMM_VARIANT_AUTO) {
-        // from 1024 tokens on, and when pair tiles keep half the SM pairs
-        // busy: dequantise the weights once and run the pair GEMM
+        // From 1024 tokens on, dequantise the weights once (2.5 bytes per
+        // weight) and run the pair GEMM, when its waves of pair tiles are at
+        // least three quarters full.  Measured on GB300 (fraction of the bf16
+        // roofline, pair against the in-kernel dequantisation): 4096 x 34816
+        // x 5120 0.875 against 0.546, 4096 x 5120 x 17408 0.779 against 0.466,
+        // 2048 x 7168 x 5120 0.773 against 0.483, 1024 x 34816 x 5120 0.582
+        // against 0.547; 1024 x 5120 x 17408 (80 pair tiles on 76 pairs: two
+        // waves, the second almost empty) 0.439 against 0.477.
         const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
-        variant = M >= 1024 && 4 * pair_tiles >= sm_count ? GEMM_VARIANT_PAIR
-                  : M <= 8                                ? GEMM_VARIANT_FRAGMENT
-                                                          : GEMM_VARIANT_SKINNY;
+        const int64_t pairs_n = std::max<int64_t>(1, sm_count / 2);
+        const int64_t waves = (pair_tiles + pairs_n - 1) / pairs_n;
+        variant = M >= 1024 && 4 * pair_tiles >= 3 * waves * pairs_n ? GEMM_VARIANT_PAIR
+                  : M <= 8                                              ? GEMM_VARIANT_FRAGMENT
+                                                                        : GEMM_VARIANT_SKINNY;
     }
     if (variant == GEMM_VARIANT_PAIR) {
         p->variant = GEMM_VARIANT_PAIR;
@@ -675,9 +689,8 @@ int gemm_bf16_fused_ex(const void *A, const void *B, const void *bias, void *C, 
                        int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int epilogue, void *stream,
                        int variant)
 {
-    if (epilogue != GEMM_EPI_NONE && epilogue != GEMM_EPI_BIAS && epilogue != GEMM_EPI_SILU_MUL)
-        return GEMM_ERR_EPILOGUE;
-    if ((epilogue == GEMM_EPI_BIAS) != (bias != nullptr)) return GEMM_ERR_EPILOGUE;
+    if (epilogue < GEMM_EPI_NONE || epilogue > GEMM_EPI_BIAS_GELU) return GEMM_ERR_EPILOGUE;
+    if (epi_needs_bias(epilogue) != (bias != nullptr)) return GEMM_ERR_EPILOGUE;
     if (epilogue == GEMM_EPI_NONE) return gemm_bf16_ex(A, B, C, M, N, K, lda, ldb, ldc, stream, variant);
     int rc = check_sizes(M, N, K);
     if (rc) return rc;
@@ -698,7 +711,7 @@ int gemm_bf16_fused_ex(const void *A, const void *B, const void *bias, void *C, 
     rc = device_state(&s, &dev);
     if (rc) return rc;
     Plan p;
-    if (!plan_bf16(M, NB, K, variant, s->sm_count, &p, true, pairs)) return GEMM_ERR_VARIANT;
+    if (!plan_bf16(M, NB, K, variant, s->sm_count, &p, true, pairs, true)) return GEMM_ERR_VARIANT;
     GemmArgs a{A, B, nullptr, nullptr, C, M, N, K, lda, ldb, ldc, 0, bias, epilogue};
     return run(a, p, (cudaStream_t)stream, false);
 }
@@ -838,8 +851,7 @@ int gemm_bf16_plan(int64_t M, int64_t N, int64_t K, int variant, int num_sms, ge
 int gemm_bf16_fused_plan(int64_t M, int64_t N, int64_t K, int epilogue, int variant, int num_sms,
                          gemm_plan *out)
 {
-    if (epilogue != GEMM_EPI_NONE && epilogue != GEMM_EPI_BIAS && epilogue != GEMM_EPI_SILU_MUL)
-        return GEMM_ERR_EPILOGUE;
+    if (epilogue < GEMM_EPI_NONE || epilogue > GEMM_EPI_BIAS_GELU) return GEMM_ERR_EPILOGUE;
     if (epilogue == GEMM_EPI_NONE) return gemm_bf16_plan(M, N, K, variant, num_sms, out);
     if (!out) return GEMM_ERR_NULL;
     int rc = check_sizes(M, N, K);
@@ -851,7 +863,7 @@ int gemm_bf16_fused_plan(int64_t M, int64_t N, int64_t K, int epilogue, int vari
     rc = sm_count_for_plan(num_sms, &sms);
     if (rc) return rc;
     Plan p;
-    if (!plan_bf16(M, NB, K, variant, sms, &p, num_sms == 0, pairs)) return GEMM_ERR_VARIANT;
+    if (!plan_bf16(M, NB, K, variant, sms, &p, num_sms == 0, pairs, true)) return GEMM_ERR_VARIANT;
     to_public(p, out);
     return GEMM_OK;
 }

@@ -4,6 +4,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "../../include/dbw_gemm.h"
+
 namespace dbw {
 
 // bf16 pair (packed in one 32-bit word, element 0 in the low half) -> two fp32.
@@ -43,6 +45,23 @@ __device__ __forceinline__ uint4 ld_ro_v4(const void *p)
 // The gated-MLP epilogue: silu(g) * u with silu(x) = x / (1 + e^-x), in fp32
 // (IEEE division, so a huge negative g gives -0, not NaN).
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + __expf(-g)) * u; }
+
+// The bias epilogues: x + b, then the epilogue's activation (relu, silu, or
+// the exact erf form of gelu), in fp32.
+__device__ __forceinline__ float bias_act(float x, float b, int epi)
+{
+    x += b;
+    if (epi == GEMM_EPI_BIAS_RELU) return fmaxf(x, 0.f);
+    if (epi == GEMM_EPI_BIAS_SILU) return x / (1.f + __expf(-x));
+    if (epi == GEMM_EPI_BIAS_GELU) return 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
+    return x;
+}
+
+// Whether an epilogue adds a bias (plain or with an activation).
+__host__ __device__ constexpr bool epi_has_bias(int epi)
+{
+    return epi == GEMM_EPI_BIAS || (epi >= GEMM_EPI_BIAS_RELU && epi <= GEMM_EPI_BIAS_GELU);
+}
 
 __device__ __forceinline__ float warp_sum(float v)
 {

@@ -11,9 +11,9 @@
 //
 // For M larger than the per-pass row count the kernel makes one pass over the
 // weight row per group of rows (the tcgen05 kernels serve those shapes).
-// Fused epilogues: EPI = 1 adds bias[n] to the fp32 sum; EPI = 2 has the warp
-// take the weight rows n (gate) and N + n (up) together and store
-// silu(gate) * up.
+// Fused epilogues: EPI = 1 adds bias[n] to the fp32 sum and applies the
+// epilogue's activation (none, relu, silu or gelu); EPI = 2 has the warp take
+// the weight rows n (gate) and N + n (up) together and store silu(gate) * up.
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
@@ -27,7 +27,7 @@ template <int MT, int U, int EPI>
 __global__ void __launch_bounds__(kWarps * 32)
 k_gemv_bf16(const uint16_t *__restrict__ A, const uint16_t *__restrict__ B,
             uint16_t *__restrict__ C, int M, int N, int K, int64_t lda, int64_t ldb, int64_t ldc,
-            const uint16_t *__restrict__ bias)
+            const uint16_t *__restrict__ bias, int epi)
 {
     ptx::pdl_wait();
     ptx::pdl_launch_dependents();
@@ -79,7 +79,7 @@ k_gemv_bf16(const uint16_t *__restrict__ A, const uint16_t *__restrict__ B,
 #pragma unroll
             for (int i = 0; i < MT; ++i) {
                 float v = warp_sum(acc[0][i]);
-                if (EPI == 1) v += bf16lo(bias[n]);
+                if (EPI == 1) v = bias_act(v, bf16lo(bias[n]), epi);
                 if (EPI == 2) v = silu_mul(v, warp_sum(acc[NR - 1][i]));
                 if (lane == 0 && m0 + i < M) C[(int64_t)(m0 + i) * ldc + n] = f32_to_bf16_rn(v);
             }
@@ -158,11 +158,14 @@ k_gemv_w4a16(const uint16_t *__restrict__ A, const uint32_t *__restrict__ Bq,
 }
 
 // K == 0: the empty sum (plus the bias, if one is fused; silu(0) * 0 = 0).
-__global__ void k_zero_fill(uint16_t *C, int M, int N, int64_t ldc, const uint16_t *bias)
+// K == 0: the empty sum, plus the bias epilogues' bias and activation.
+__global__ void k_zero_fill(uint16_t *C, int M, int N, int64_t ldc, const uint16_t *bias, int epi)
 {
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < (int64_t)M * N;
          i += (int64_t)gridDim.x * blockDim.x)
-        C[(i / N) * ldc + (i % N)] = bias ? bias[i % N] : (uint16_t)0;
+        C[(i / N) * ldc + (i % N)] =
+            bias ? (epi == GEMM_EPI_BIAS ? bias[i % N] : f32_to_bf16_rn(bias_act(0.f, bf16lo(bias[i % N]), epi)))
+                 : (uint16_t)0;
 }
 
 template <typename Kern, typename... Args>
@@ -197,7 +200,7 @@ cudaError_t launch_zero_fill(const GemmArgs &a, const LaunchCtx &c)
     if (grid > c.sm_count * 8) grid = c.sm_count * 8;
     if (grid < 1) grid = 1;
     k_zero_fill<<<grid, 256, 0, c.stream>>>((uint16_t *)a.C, (int)a.M, (int)a.N, a.ldc,
-                                           a.epi == GEMM_EPI_BIAS ? (const uint16_t *)a.bias : nullptr);
+                                           epi_has_bias(a.epi) ? (const uint16_t *)a.bias : nullptr, a.epi);
     return cudaGetLastError();
 }
 
@@ -208,10 +211,10 @@ cudaError_t launch_gemv_mt(const GemmArgs &a, const Plan &p, const LaunchCtx &c,
     const int M = (int)a.M, N = (int)a.N, K = (int)a.K;
     const uint16_t *bias = (const uint16_t *)a.bias;
     switch (p.m_per_pass) {
-    case 1: return launch_pdl(k_gemv_bf16<1, 8, EPI>, p.grid, c.stream, A, B, C, M, N, K, a.lda, a.ldb, a.ldc, bias);
-    case 2: return launch_pdl(k_gemv_bf16<2, 8, EPI>, p.grid, c.stream, A, B, C, M, N, K, a.lda, a.ldb, a.ldc, bias);
-    case 3: return launch_pdl(k_gemv_bf16<3, 4, EPI>, p.grid, c.stream, A, B, C, M, N, K, a.lda, a.ldb, a.ldc, bias);
-    default: return launch_pdl(k_gemv_bf16<4, 4, EPI>, p.grid, c.stream, A, B, C, M, N, K, a.lda, a.ldb, a.ldc, bias);
+    case 1: return launch_pdl(k_gemv_bf16<1, 8, EPI>, p.grid, c.stream, A, B, C, M, N, K, a.lda, a.ldb, a.ldc, bias, a.epi);
+    case 2: return launch_pdl(k_gemv_bf16<2, 8, EPI>, p.grid, c.stream, A, B, C, M, N, K, a.lda, a.ldb, a.ldc, bias, a.epi);
+    case 3: return launch_pdl(k_gemv_bf16<3, 4, EPI>, p.grid, c.stream, A, B, C, M, N, K, a.lda, a.ldb, a.ldc, bias, a.epi);
+    default: return launch_pdl(k_gemv_bf16<4, 4, EPI>, p.grid, c.stream, A, B, C, M, N, K, a.lda, a.ldb, a.ldc, bias, a.epi);
     }
 }
 
@@ -220,7 +223,10 @@ cudaError_t launch_gemv_bf16(const GemmArgs &a, const Plan &p, const LaunchCtx &
     const uint16_t *A = (const uint16_t *)a.A, *B = (const uint16_t *)a.B;
     uint16_t *C = (uint16_t *)a.C;
     switch (a.epi) {
-    case GEMM_EPI_BIAS: return launch_gemv_mt<1>(a, p, c, A, B, C);
+    case GEMM_EPI_BIAS:
+    case GEMM_EPI_BIAS_RELU:
+    case GEMM_EPI_BIAS_SILU:
+    case GEMM_EPI_BIAS_GELU: return launch_gemv_mt<1>(a, p, c, A, B, C);
     case GEMM_EPI_SILU_MUL: return launch_gemv_mt<2>(a, p, c, A, B, C);
     default: return launch_gemv_mt<0>(a, p, c, A, B, C);
     }

@@ -61,8 +61,9 @@ struct Plan {
 // false: host-only model of a device with sm_count SMs.
 // pairs: the weight rows come in (gate, up) pairs (GEMM_EPI_SILU_MUL; N is
 // then the kernel's row count 2 * columns of C): splits keep pairs together.
+// fused: any epilogue (the pair kernel stores the plain product only).
 bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan *p, bool query = true,
-               bool pairs = false);
+               bool pairs = false, bool fused = false);
 bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int sm_count, Plan *p,
                 bool query = true);
 // Grouped GEMM over G experts sharing M stacked token rows (prefill kernel,

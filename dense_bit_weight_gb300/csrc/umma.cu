@@ -87,7 +87,7 @@ struct W4Args {
     int lg_group;                // log2(group); group is 32, 64 or 128
 };
 
-// store_chunk with a fused epilogue (GEMM_EPI_BIAS or GEMM_EPI_SILU_MUL).
+// store_chunk with a fused epilogue (a bias epilogue or GEMM_EPI_SILU_MUL).
 // Rows of X (SWAP) or columns of Y hold weight rows; with GEMM_EPI_SILU_MUL
 // they come as (gate, up) pairs 2j, 2j + 1 for output column j.  SWAP: a
 // thread owns one weight row and its pair partner is the neighbouring lane
@@ -130,15 +130,15 @@ __device__ __noinline__ void store_chunk_fused(uint16_t *__restrict__ C, int64_t
         }
         return;
     }
-    if (s.epi == GEMM_EPI_BIAS) {
+    if (epi_has_bias(s.epi)) {
         if (SWAP) {
             const float b = r < R ? bf16lo(s.bias[r]) : 0.f;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) f[j] += b;
+            for (int j = 0; j < 16; ++j) f[j] = bias_act(f[j], b, s.epi);
         } else {
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-                if (q0 + j < Q) f[j] += bf16lo(s.bias[q0 + j]);
+                if (q0 + j < Q) f[j] = bias_act(f[j], bf16lo(s.bias[q0 + j]), s.epi);
         }
     }
     store_chunk<SWAP>(C, ldc, R, Q, r, q0, f);
@@ -175,21 +175,21 @@ __device__ __noinline__ void cluster_store_fused(uint16_t *__restrict__ C, int64
                     C[(int64_t)q * ldc + (re >> 1)] = f32_to_bf16_rn(silu_mul(lo, hi));
                     continue;
                 }
-                lo += bf16lo(s.bias[re]);
-                if (re + 1 < R) hi += bf16lo(s.bias[re + 1]);
+                lo = bias_act(lo, bf16lo(s.bias[re]), s.epi);
+                if (re + 1 < R) hi = bias_act(hi, bf16lo(s.bias[re + 1]), s.epi);
                 uint16_t *dst = C + (int64_t)q * ldc + re;
                 if (re + 1 < R) *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2_rn(lo, hi);
                 else *dst = f32_to_bf16_rn(lo);
             }
         }
-    } else if (r < R && s.epi == GEMM_EPI_BIAS) {   // (pairs are only split in twos)
+    } else if (r < R && epi_has_bias(s.epi)) {   // (pairs are only split in twos)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int q = q0 + j;
             if (q < Q) {
-                const float b = bf16lo(s.bias[SWAP ? r : q]);
-                if (SWAP) C[(int64_t)q * ldc + r] = f32_to_bf16_rn(a[j] + b);
-                else C[(int64_t)r * ldc + q] = f32_to_bf16_rn(a[j] + b);
+                const float v = bias_act(a[j], bf16lo(s.bias[SWAP ? r : q]), s.epi);
+                if (SWAP) C[(int64_t)q * ldc + r] = f32_to_bf16_rn(v);
+                else C[(int64_t)r * ldc + q] = f32_to_bf16_rn(v);
             }
         }
     }

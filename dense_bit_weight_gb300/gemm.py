@@ -185,13 +185,14 @@ def gemm_bf16(A, B, C=None, stream=None, variant="auto"):
     return C
 
 
-EPILOGUE = {"none": 0, "bias": 1, "silu_mul": 2}
+EPILOGUE = {"none": 0, "bias": 1, "silu_mul": 2, "bias_relu": 3, "bias_silu": 4, "bias_gelu": 5}
 
 
 def gemm_bf16_fused(A, B, bias=None, C=None, epilogue="bias", stream=None, variant="auto"):
     """gemm_bf16 with a fused epilogue (applied in fp32 to the full K sum).
 
-    epilogue "bias": C[m,n] = (A @ B^T)[m,n] + bias[n] (bias bf16 [N]).
+    epilogue "bias": C[m,n] = (A @ B^T)[m,n] + bias[n] (bias bf16 [N]);
+    "bias_relu" / "bias_silu" / "bias_gelu": the activation of that sum.
     epilogue "silu_mul": B is the fused gate/up weight [2N,K] (gate rows, then
     up rows) and C[m,n] = silu(g) * u with g, u the two halves of A @ B^T.
     Returns C bf16 [M,N].

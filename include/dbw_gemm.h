@@ -139,17 +139,25 @@ int gemm_w4a16(const void *A, const void *Bq, const void *scales, const void *ze
  *                      g = sum_k A[m,k] B[n,k], u = sum_k A[m,k] B[N+n,k],
  *                      C[m,n] = silu(g) * u, silu(x) = x / (1 + exp(-x)).
  *                      C is [M, N]; bias must be NULL.
+ *   GEMM_EPI_BIAS_RELU C[m,n] = relu(x), x = sum_k A[m,k] B[n,k] + bias[n],
+ *   GEMM_EPI_BIAS_SILU relu(x) = max(x, 0), silu(x) = x / (1 + exp(-x)),
+ *   GEMM_EPI_BIAS_GELU gelu(x) = x/2 (1 + erf(x / sqrt 2)) (the exact form);
+ *                      bias as for GEMM_EPI_BIAS (the guide's "bias_relu",
+ *                      "bias_silu", "bias_gelu").
  *
  * Sizes, leading dimensions, alignment and errors as for gemm_bf16 (N counts
  * the columns of C; B spans 2N rows for GEMM_EPI_SILU_MUL).  An unknown
- * epilogue, or a bias that is NULL for GEMM_EPI_BIAS or not NULL otherwise,
+ * epilogue, or a bias that is NULL for a bias epilogue or not NULL otherwise,
  * returns GEMM_ERR_EPILOGUE; C overlapping bias returns GEMM_ERR_ALIAS.
  * gemm_bf16_fused_ex forces a kernel family like gemm_bf16_ex.
  */
 typedef enum {
     GEMM_EPI_NONE = 0,
     GEMM_EPI_BIAS = 1,
-    GEMM_EPI_SILU_MUL = 2
+    GEMM_EPI_SILU_MUL = 2,
+    GEMM_EPI_BIAS_RELU = 3,
+    GEMM_EPI_BIAS_SILU = 4,
+    GEMM_EPI_BIAS_GELU = 5
 } gemm_epilogue;
 
 int gemm_bf16_fused(const void *A, const void *B, const void *bias, void *C, int64_t M, int64_t N,

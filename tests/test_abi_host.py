@@ -122,10 +122,13 @@ def test_plans_are_host_only_and_cover_the_workloads(g):
     # more than 128 tokens on the tcgen05 W4A16 kernel: 128-token tiles
     p = g.gemm_w4a16_plan(1000, 34816, 5120, 128, num_sms=sms)
     assert p["tile_m"] == 128 and p["grid"] <= sms
-    # from 1024 tokens: weights dequantised once, then the pair GEMM
+    # from 1024 tokens, waves of pair tiles at least 3/4 full: weights
+    # dequantised once, then the pair GEMM
     for M in (1024, 4096):
         p = g.gemm_w4a16_plan(M, 34816, 5120, 128, num_sms=sms)
         assert (p["variant"], p["kernels"], p["tile_m"]) == (9, 2, 256) and p["grid"] <= sms
+    assert g.gemm_w4a16_plan(4096, 5120, 17408, 128, num_sms=sms)["variant"] == 9     # 320 pair tiles: 0.84
+    assert g.gemm_w4a16_plan(1024, 5120, 17408, 128, num_sms=sms)["variant"] == 2     # 80 pair tiles: 0.53
     # the fragment kernel stages scales per stage: any number of groups plans
     assert g.gemm_w4a16_plan(1, 4096, 32 * 545, 32, num_sms=sms)["variant"] == 6
     # beyond the staged-scale limit (K / group > 544 groups) the register kernel does not plan
@@ -180,7 +183,13 @@ def test_fused_epilogue_argument_errors():
     assert g.gemm_bf16_fused_ptr(p, p, 0, p, 8, 8, 8, 8, 8, 8, 1) == 11
     assert g.gemm_bf16_fused_ptr(p, p, p, p, 8, 8, 8, 8, 8, 8, 2) == 11
     assert g.gemm_bf16_fused_ptr(p, p, p, p, 8, 8, 8, 8, 8, 8, 0) == 11
+    for epi in (3, 4, 5):                        # the bias + activation epilogues need a bias
+        assert g.gemm_bf16_fused_ptr(p, p, 0, p, 8, 8, 8, 8, 8, 8, epi) == 11
+    assert g.gemm_bf16_fused_ptr(p, p, 0, p, 8, 8, 8, 8, 8, 8, -1) == 11
     assert g.gemm_status_string(11) != g.gemm_status_string(99)
+    # every fused epilogue stays on the single-CTA kernels (the pair kernel stores the plain product)
+    for epi in ("bias", "bias_relu", "bias_silu", "bias_gelu"):
+        assert g.gemm_bf16_fused_plan(4096, 8192, 8192, epi, num_sms=152)["variant"] == 3
     # the SiLU-mul plans are plans on the 2N weight rows, on single-CTA kernels
     sms = 152
     for M in (1, 8, 128, 4096):

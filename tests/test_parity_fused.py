@@ -63,6 +63,41 @@ def test_bias(g, M, N, K, variant, kind):
     (assert_exact if kind == "int" else assert_close)(host_bits(C), ref, what=f"bias {variant} {M}x{N}x{K}")
 
 
+# bias + activation (the guide's bias_relu, bias_silu, bias_gelu) on every
+# store path: GEMV, skinny whole tiles / cluster split-K / stream-K, prefill
+# stream-K and whole tiles, and K = 0
+ACT_SHAPES = [(3, 72, 264), (16, 520, 1032), (128, 200, 4096), (8, 20480, 512), (300, 1200, 4096),
+              (2048, 2048, 1024)]
+
+
+@pytest.mark.parametrize("M,N,K", ACT_SHAPES)
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("act", ["relu", "silu", "gelu"])
+def test_bias_activation(g, M, N, K, variant, act):
+    if not runnable(g, M, N, K, variant):
+        pytest.skip(f"{variant} does not run {M}x{N}x{K}")
+    kind = "int" if act == "relu" else "normal"
+    A, B = bf16_inputs(M, N, K, seed=M + 5 * N + K, kind=kind)
+    if kind == "int":
+        bias = synth.bf16_int_uniform((N,), -40, 40, 6, synth.STREAM_B_INT)
+    else:
+        bias = synth.bf16_normal((N,), 1.0, 6, synth.STREAM_B)
+    C = g.gemm_bf16_fused(dev_bf16(A), dev_bf16(B), dev_bf16(bias), epilogue="bias_" + act, variant=variant)
+    ref = oracle.gemm_bf16_bias_act(A, B, bias, act)
+    (assert_exact if kind == "int" else assert_close)(host_bits(C), ref, what=f"bias_{act} {variant} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("act", ["relu", "silu", "gelu"])
+def test_bias_activation_k_zero(g, act):
+    import torch
+    bias = synth.bf16_normal((24,), 1.0, 2, synth.STREAM_B)
+    A = torch.empty((5, 0), dtype=torch.bfloat16, device="cuda")
+    C = g.gemm_bf16_fused(A, torch.empty((24, 0), dtype=torch.bfloat16, device="cuda"), dev_bf16(bias),
+                          epilogue="bias_" + act)
+    ref = oracle.bias_act(np.zeros((5, 24)), bias, act)
+    assert_close(host_bits(C), ref, what=f"bias_{act} K=0")
+
+
 @pytest.mark.parametrize("M,N,K", SMALL)
 @pytest.mark.parametrize("variant", VARIANTS)
 def test_silu_mul(g, M, N, K, variant):
