@@ -382,14 +382,12 @@ bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan 
         if (pairs || fused) return false;   // plain C = A B^T only
         p->variant = GEMM_VARIANT_PAIR;
         p->kernels = 1;
-        p->split = 1;
-        p->mode = 0;
         p->bn = 256;
         p->tile_m = 256;
         p->tile_n = 256;
         p->stages = 6;
         p->ctas_per_sm = 1;
-        p->grid = umma_pair_grid(M, N, sm_count);
+        plan_pair(M, N, K, sm_count, p);
         return true;
     }
     default: return false;
@@ -454,14 +452,12 @@ bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int
         p->kernels = 2;                      // dequantisation, then the pair GEMM
         p->act_copy = 1;
         p->ws_extra = N * K / 2;             // bf16 [N, K] as floats
-        p->split = 1;
-        p->mode = 0;
         p->bn = 256;
         p->tile_m = 256;
         p->tile_n = 256;
         p->stages = 6;
         p->ctas_per_sm = 1;
-        p->grid = umma_pair_grid(M, N, sm_count);
+        plan_pair(M, N, K, sm_count, p);
         return true;
     }
     if (variant == GEMM_VARIANT_REGISTER) {
@@ -609,6 +605,7 @@ void plan_mx(int64_t M, int64_t N, int64_t K, int fmt, int sm_count, Plan *p)
 // waves of whole tiles come first, only the first sk_grid CTAs share units.
 static int64_t partial_writers(const Plan &p)
 {
+    if (p.variant == GEMM_VARIANT_PAIR) return 2 * (int64_t)p.sk_grid;   // both CTAs of each sharing pair
     return p.whole > 0 && p.sk_grid > 0 ? std::min(p.sk_grid, p.grid) : p.grid;
 }
 
@@ -616,14 +613,22 @@ static int64_t partial_writers(const Plan &p)
 static bool streamk_partials(const Plan &p)
 {
     return (p.variant == GEMM_VARIANT_SKINNY || p.variant == GEMM_VARIANT_PREFILL ||
-            p.variant == GEMM_VARIANT_GROUPWISE || p.variant == GEMM_VARIANT_BLOCK_SCALED) &&
+            p.variant == GEMM_VARIANT_GROUPWISE || p.variant == GEMM_VARIANT_BLOCK_SCALED ||
+            p.variant == GEMM_VARIANT_PAIR) &&
            p.mode == 1;
+}
+
+// fp32 partial floats of a stream-K plan: two tile slots per writer; the pair
+// kernel's writers are its CTAs (each keeps its 128 rows of a 256-row tile).
+static int64_t partial_floats(const Plan &p)
+{
+    return partial_writers(p) * 2 * kUmmaBM * p.bn;
 }
 
 int64_t act_copy_offset(const Plan &p)
 {
     const bool split = streamk_partials(p);
-    const int64_t partials = split ? partial_writers(p) * 2 * kUmmaBM * p.bn : 0;
+    const int64_t partials = split ? partial_floats(p) : 0;
     return (partials + 63) / 64 * 64;   // 256-byte aligned
 }
 
@@ -632,8 +637,9 @@ void workspace_need(const Plan &p, int64_t M, int64_t N, int64_t K, int64_t *flo
     *floats = 0;
     *counters = 0;
     if (streamk_partials(p)) {
-        *floats = partial_writers(p) * 2 * kUmmaBM * p.bn;
+        *floats = partial_floats(p);
         *counters = ((M + p.tile_m - 1) / p.tile_m) * ((N + p.tile_n - 1) / p.tile_n);
+        if (p.variant == GEMM_VARIANT_PAIR) *counters *= 2;   // one per CTA half of a tile
     }
     if (p.variant == GEMM_VARIANT_FRAGMENT) {
         *floats = p.ws_extra;
@@ -643,8 +649,8 @@ void workspace_need(const Plan &p, int64_t M, int64_t N, int64_t K, int64_t *flo
         *floats = act_copy_offset(p) + p.ws_extra;
         return;
     }
-    if (p.variant == GEMM_VARIANT_PAIR) {   // W4A16: the dequantised weights only
-        *floats = p.ws_extra;
+    if (p.variant == GEMM_VARIANT_PAIR) {   // W4A16: the dequantised weights after the partials
+        *floats = act_copy_offset(p) + p.ws_extra;
         return;
     }
     else if (p.act_copy) *floats = act_copy_offset(p) + (M * K + 127) / 128 * 64 + p.ws_extra;   // bf16 [M, K] (+ sums)

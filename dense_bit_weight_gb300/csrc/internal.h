@@ -108,7 +108,7 @@ int w4tc_stages(int bn);
 cudaError_t launch_w4tc(const GemmArgs &a, const Plan &p, const LaunchCtx &c);
 // Prefill on CTA pairs (umma2.cu): 256 x 256 tiles, tcgen05.mma.cta_group::2;
 // the grid is twice the number of pairs.
-int umma_pair_grid(int64_t M, int64_t N, int sm_count);
+void plan_pair(int64_t M, int64_t N, int64_t K, int sm_count, Plan *p);
 cudaError_t launch_umma_pair(const GemmArgs &a, const Plan &p, const LaunchCtx &c);
 // W4A16 with many tokens: weights dequantised to bf16 into the workspace
 // (act_copy, N * K bf16), then the pair GEMM.
@@ -126,6 +126,8 @@ bool make_map_bf16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int
 // Bytes [rows, width] (fp8 / packed fp4 codes): boxes of 128 bytes x box_rows
 // rows, 128-byte swizzle.
 bool make_map_u8(CUtensorMap *m, const void *ptr, int64_t rows, int64_t width, int box_rows);
+// C [rows, cols] bf16 for TMA stores of 32 x 32 boxes (64-byte swizzle).
+bool make_map_c32(CUtensorMap *m, void *C, int64_t rows, int64_t cols, int64_t ld);
 // Packed 4-bit weights [rows, K/8] (uint32): boxes of 16 words (128 k) x
 // box_rows rows, 64-byte swizzle.
 bool make_map_words16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int box_rows);

@@ -134,12 +134,22 @@ extern "C" int gemm_bf16_noalloc(const void *A, const void *B, void *C, int64_t 
         // the counters must start at zero; an earlier call that timed out may have left some set
         if (cudaMemsetAsync(s->counters, 0, (size_t)tiles * sizeof(int), st) != cudaSuccess) return GEMM_ERR_CUDA;
     }
+    if (p.variant == GEMM_VARIANT_PAIR && p.mode == 1) {
+        // CTA pairs: both CTAs of a sharing pair keep two 128 x 256 partials
+        const int64_t per_pair = 4 * (int64_t)kUmmaBM * p.bn;
+        const int64_t max_pairs = kScratchFloats / per_pair;
+        if (p.sk_grid > max_pairs) p.sk_grid = (int)max_pairs;
+        if (p.whole == 0) p.grid = 2 * p.sk_grid;   // stream-K throughout: only the sharing pairs run
+        const int64_t counters = 2 * ((M + 255) / 256) * ((N + p.bn - 1) / p.bn);
+        if (counters > kScratchCounters) return GEMM_ERR_SHAPE;
+        if (cudaMemsetAsync(s->counters, 0, (size_t)counters * sizeof(int), st) != cudaSuccess) return GEMM_ERR_CUDA;
+    }
     GemmArgs a{A, B, nullptr, nullptr, C, M, N, K, lda, ldb, ldc, 0};
     cudaError_t e;
     switch (p.variant) {
     case GEMM_VARIANT_ZERO: e = launch_zero_fill(a, c); break;
     case GEMM_VARIANT_GEMV: e = launch_gemv_bf16(a, p, c); break;
-    case GEMM_VARIANT_PAIR: e = launch_umma_pair(a, p, c); break;   // no scratch
+    case GEMM_VARIANT_PAIR: e = launch_umma_pair(a, p, c); break;
     default: e = launch_umma_bf16(a, p, c); break;
     }
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;

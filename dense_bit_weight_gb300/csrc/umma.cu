@@ -1093,6 +1093,22 @@ cudaError_t launch_t(const CUtensorMap &mx, const CUtensorMap &my, const CUtenso
 
 }  // namespace
 
+// C [rows, cols] bf16 (row pitch ld elements) for TMA stores of 32 x 32
+// boxes with the 64-byte swizzle; elements beyond the extents are not written.
+bool make_map_c32(CUtensorMap *m, void *C, int64_t rows, int64_t cols, int64_t ld)
+{
+    if ((reinterpret_cast<uintptr_t>(C) & 15) || (ld * 2) % 16) return false;
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 bool make_map_bf16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int64_t ld, int box_rows)
 {
     return make_map(m, ptr, rows, K, ld, box_rows);

@@ -12,7 +12,7 @@
 // 128 x 256 tile fed by 32 KB of operands per 64-k stage instead of the
 // 48 KB a single-CTA 128 x 256 tile needs.
 //
-// Roles (192 threads per CTA, one CTA per SM, persistent over pair tiles):
+// Roles (320 threads per CTA, one CTA per SM, persistent over pair tiles):
 //   warp 0      producer, in both CTAs: per stage the CTA's 128 rows of A and
 //               its 128 rows of B (TMA, 128-byte swizzle), both copies
 //               signalling the LEADER's full barrier (the .cta_group::2 form);
@@ -21,11 +21,17 @@
 //               issues four MMAs (K = 16) per stage and commits the stage's
 //               release and the accumulator's completion to the barriers of
 //               both CTAs (multicast)
-//   warps 2-5   epilogue, in both CTAs: the CTA's 128 accumulator rows ->
-//               bf16 -> C; each warp then releases the accumulator on the
-//               leader's barrier (eight arrivals: four local, four remote)
+//   warps 2-9   epilogue, in both CTAs: two warps per quarter of the CTA's
+//               128 accumulator rows (a warp reads only its quarter of the
+//               tensor memory lanes), each taking 128 of the 256 columns ->
+//               bf16 -> C through TMA stores; each warp then releases the
+//               accumulator on the leader's barrier (sixteen arrivals)
 // Two accumulators of 256 columns let the epilogue of one tile overlap the
-// MMAs of the next.  Every wait is bounded (waits.cuh); a cluster barrier
+// MMAs of the next.  Schedule (sched.cuh, the pairs as its CTAs): whole tiles
+// round-robin, or stream-K ranges of (tile, k-block) units when whole tiles
+// would leave the last wave of pairs mostly idle; a split tile's partials are
+// kept per CTA half (each CTA its 128 rows) and summed in k order by the last
+// contributor.  Every wait is bounded (waits.cuh); a cluster barrier
 // before exit keeps either CTA from leaving while its partner may still
 // signal its barriers or read its shared memory.
 #include <cuda.h>
@@ -50,11 +56,17 @@ constexpr int STAGES = 6;
 constexpr int A_BYTES = BMC * BK * 2;    // 16 KB
 constexpr int B_BYTES = BNC * BK * 2;    // 16 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int BAR_OFF = STAGES * STAGE_BYTES;
-constexpr int NBARS = 2 * STAGES + 4 + 1;
+constexpr int kEpiWarps = 8;                       // warps 2-9
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int EPI_OFF = STAGES * STAGE_BYTES;      // the epilogue warps' staging boxes for C
+constexpr int EPI_BOX_BYTES = 32 * 64;             // 32 rows x 32 bf16 columns
+constexpr int EPI_WARP_BYTES = 2 * EPI_BOX_BYTES;  // two boxes per warp (double buffered)
+constexpr int BAR_OFF = EPI_OFF + kEpiWarps * EPI_WARP_BYTES;
+constexpr int FIX_SLOTS = STAGES;                  // staged fixup: 16 KB slots per column half
+constexpr int FIX_SLOT_BYTES = STAGES * STAGE_BYTES / (2 * FIX_SLOTS);
+constexpr int NBARS = 2 * STAGES + 4 + 1 + 3 + 2 * FIX_SLOTS;
 constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
 constexpr int SMEM = MISC_OFF + 16 + 1024;
-constexpr int kEpiThreads = 128;
 
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols)
 {
@@ -123,9 +135,190 @@ __device__ __forceinline__ void arrive_remote(uint32_t bar_cluster)
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 
-__global__ void __launch_bounds__(192, 1)
-k_umma_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, uint16_t *__restrict__ C,
-            int M, int N, int64_t ldc, const __grid_constant__ Sched sched, int *__restrict__ d_error)
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+
+// bf16 store of 32 columns of this warp's 32 accumulator rows (row r0 + lane
+// held by each lane): the lanes write a 32 x 32 box into one of the warp's two
+// staging boxes in shared memory and lane 0 hands it to the TMA engine, which
+// writes the rows of C (clipping rows >= M and columns >= N), while the warp
+// goes on with the next box.  The box uses the 64-byte swizzle of the C map:
+// the 16-byte chunk j of row x sits at chunk j ^ ((x / 2) % 4), so the lanes'
+// writes spread over all banks.  Before a box is refilled, the store issued
+// from it two boxes earlier has finished reading it.
+__device__ __forceinline__ void store_box(const CUtensorMap *tmC, int M, int N, int r0, int q0, const float (&f)[32],
+                                          uint32_t wbuf, int &sel, int lane)
+{
+    if (r0 >= M || q0 >= N) return;   // the box lies wholly outside C
+    const uint32_t box = wbuf + (uint32_t)(sel * EPI_BOX_BYTES);
+    if (lane == 0) bulk_wait_read1();
+    __syncwarp();
+    const uint32_t sw = (uint32_t)((lane >> 1) & 3);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint4 w;
+        w.x = pack_bf16x2_rn(f[8 * j], f[8 * j + 1]);
+        w.y = pack_bf16x2_rn(f[8 * j + 2], f[8 * j + 3]);
+        w.z = pack_bf16x2_rn(f[8 * j + 4], f[8 * j + 5]);
+        w.w = pack_bf16x2_rn(f[8 * j + 6], f[8 * j + 7]);
+        ptx::sts128(box + (uint32_t)(lane * 64) + (((uint32_t)j ^ sw) << 4), w);
+    }
+    ptx::fence_proxy_async_smem();   // the box is read by the TMA engine
+    __syncwarp();
+    if (lane == 0) {
+        ptx::tma_store_2d(tmC, box, q0, r0);
+        ptx::bulk_commit_group();
+    }
+    sel ^= 1;
+}
+
+// Stream-K fixup with plain loads (a split tile that is not this CTA's final
+// segment, so the operand ring is busy): this warp's 128 columns, 32 at a
+// time, the partials of the contributors in increasing order; the same sums,
+// in the same order, as staged_fixup.  emit(c0, f) takes 32 columns.
+template <typename Emit>
+__device__ __forceinline__ void direct_fixup(const Sched &sched, const float *__restrict__ ws, int t, int row,
+                                             int col0, Emit &emit)
+{
+    const int c_first = cta_of_unit(sched, (long long)t * sched.nk);
+    const int c_last = cta_of_unit(sched, (long long)(t + 1) * sched.nk - 1);
+    const float4 *wsv = reinterpret_cast<const float4 *>(ws);
+#pragma unroll 1
+    for (int cb = col0 / 4; cb < (col0 + BN / 2) / 4; cb += 8) {
+        float4 a4[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+        for (int cta = c_first; cta <= c_last; ++cta) {
+            const int slot = (int)(range_begin(sched, cta) / sched.nk) == t ? 0 : 1;
+            const float4 *p = wsv + (int64_t)(cta * 2 + slot) * (BMC * BN / 4) + (int64_t)cb * BMC + row;
+            float4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = __ldcg(p + j * BMC);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                a4[j].x += v[j].x;
+                a4[j].y += v[j].y;
+                a4[j].z += v[j].z;
+                a4[j].w += v[j].w;
+            }
+        }
+        float f[32];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            f[4 * u] = a4[u].x;
+            f[4 * u + 1] = a4[u].y;
+            f[4 * u + 2] = a4[u].z;
+            f[4 * u + 3] = a4[u].w;
+        }
+        emit(cb * 4, f);
+    }
+}
+
+// Stream-K fixup of tile t by its last contributor, when the tile is this
+// CTA's final segment: every MMA of the pair has then completed and no copy
+// is in flight, so the operand ring stages the partials.  Each column half
+// (four warps) has FIX_SLOTS slots of 16 KB and its own barriers; its chunk i
+// (32 columns x 128 rows of contributor c_first + i % nc, column batch
+// i / nc of the half) arrives by one bulk copy into slot i % FIX_SLOTS, all
+// slots in flight at once, where plain loads would keep only a few KB per
+// warp in flight and wait out the L2 latency many times.  Sums run over the
+// contributors in increasing order, the same arithmetic as direct_fixup, so
+// the bits do not depend on which path ran.  emit(c0, f) takes 32 columns.
+// Returns false on a timeout or abort, after waiting (bounded) for the copies
+// still in flight.
+template <typename Emit>
+__device__ __noinline__ bool staged_fixup(const Sched &sched, const float *__restrict__ ws, int t, int row, int half,
+                                          bool issuer, const uint8_t *ring, uint32_t ring_s, uint32_t stg0,
+                                          uint32_t hbar, uint32_t &hphase, volatile uint32_t *abort_flag,
+                                          int *d_error, Emit &emit)
+{
+    constexpr int CHUNK_F4 = 8 * BMC;                   // 8 float4 columns of 128 rows
+    constexpr uint32_t CHUNK_BYTES = CHUNK_F4 * 16;     // 16 KB, one slot
+    static_assert(CHUNK_BYTES == (uint32_t)FIX_SLOT_BYTES, "a partial chunk fills one slot");
+    const int c_first = cta_of_unit(sched, (long long)t * sched.nk);
+    const int c_last = cta_of_unit(sched, (long long)(t + 1) * sched.nk - 1);
+    const int nc = c_last - c_first + 1;
+    constexpr int BATCHES = BN / 2 / 32;                // column batches of a half
+    const int chunks = BATCHES * nc;
+    const float4 *wsv = reinterpret_cast<const float4 *>(ws);
+    auto issue = [&](int i) {
+        const int cta = c_first + i % nc;
+        const int slot = (int)(range_begin(sched, cta) / sched.nk) == t ? 0 : 1;
+        const int cb = half * (BN / 8) + (i / nc) * 8;   // first float4 column of the batch
+        const float4 *src = wsv + (int64_t)(cta * 2 + slot) * (BMC * BN / 4) + (int64_t)cb * BMC;
+        const uint32_t bar = stg0 + 8u * (i % FIX_SLOTS);
+        ptx::mbar_arrive_expect_tx(bar, CHUNK_BYTES);
+        bulk_load(ring_s + (uint32_t)((i % FIX_SLOTS) * FIX_SLOT_BYTES), src, CHUNK_BYTES, bar);
+    };
+    int issued = 0;
+    if (issuer) {
+        // the partials were written by other threads' plain stores (released
+        // through the tile counter); order them before the bulk copies read them
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        for (; issued < chunks && issued < FIX_SLOTS; ++issued) issue(issued);
+    }
+    bool ok = true;
+    int i = 0;
+    float4 a4[8];
+    for (; i < chunks; ++i) {
+        const int b = i % FIX_SLOTS;
+        if (i % nc == 0) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) a4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (!wait_bar_warp(stg0 + 8u * b, (uint32_t)(i / FIX_SLOTS) & 1u, abort_flag, d_error)) {
+            ok = false;
+            break;
+        }
+        const float4 *buf = reinterpret_cast<const float4 *>(ring + b * FIX_SLOT_BYTES);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float4 v = buf[j * BMC + row];
+            a4[j].x += v.x;
+            a4[j].y += v.y;
+            a4[j].z += v.z;
+            a4[j].w += v.w;
+        }
+        if (i + FIX_SLOTS < chunks) {
+            // every warp of this half has read slot b: refill it
+            if (!group_sync_warp(hbar, hphase, abort_flag, d_error)) {
+                ok = false;
+                ++i;
+                break;
+            }
+            if (issuer) issue(issued++);
+        }
+        if (i % nc == nc - 1) {
+            float f[32];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                f[4 * u] = a4[u].x;
+                f[4 * u + 1] = a4[u].y;
+                f[4 * u + 2] = a4[u].z;
+                f[4 * u + 3] = a4[u].w;
+            }
+            emit(half * (BN / 2) + (i / nc) * 32, f);
+        }
+    }
+    if (!ok && issuer) {
+        // copies issued beyond the last one waited for are still landing
+        for (int k = i; k < issued; ++k) wait_bar_drain(stg0 + 8u * (k % FIX_SLOTS), (uint32_t)(k / FIX_SLOTS) & 1u);
+    }
+    return ok;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+k_umma_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+            const __grid_constant__ CUtensorMap tmC, int M, int N, const __grid_constant__ Sched sched,
+            float *__restrict__ ws,
+            int *__restrict__ counters, int *__restrict__ d_error)
 {
     constexpr uint32_t IDESC = ptx::idesc_bf16_f32(2 * BMC, BN);
     extern __shared__ uint8_t pair_raw[];
@@ -137,7 +330,10 @@ k_umma_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     auto TFULL = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
     auto TEMPTY = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
     const uint32_t DONE = bar0 + 8u * (2 * STAGES + 4);
-    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + MISC_OFF);   // [0] tmem, [1] abort
+    const uint32_t FIXB = bar0 + 8u * (2 * STAGES + 5);   // this CTA's epilogue warps (stream-K counter)
+    const uint32_t HALFB = bar0 + 8u * (2 * STAGES + 6);  // [2]: the four warps of a column half
+    const uint32_t STG0 = bar0 + 8u * (2 * STAGES + 8);   // [2][FIX_SLOTS]: partials staged for the fixup
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + MISC_OFF);   // [0] tmem, [1] abort, [2] last flag
     volatile uint32_t *abort_flag = misc + 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = ptx::cluster_ctarank();
@@ -151,10 +347,14 @@ k_umma_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(TFULL(a), 1);
-            ptx::mbar_init(TEMPTY(a), 2 * kEpiThreads / 32);   // (used in the leader) both CTAs' epilogue warps
+            ptx::mbar_init(TEMPTY(a), 2 * kEpiWarps);   // (used in the leader) both CTAs' epilogue warps
         }
         ptx::mbar_init(DONE, 1);
+        ptx::mbar_init(FIXB, kEpiWarps);
+        for (int h = 0; h < 2; ++h) ptx::mbar_init(HALFB + 8u * h, kEpiWarps / 2);
+        for (int b = 0; b < 2 * FIX_SLOTS; ++b) ptx::mbar_init(STG0 + 8u * b, 1);
         misc[1] = 0;
+        misc[2] = 0;
         ptx::fence_mbar_init();
     }
     if (warp == 1) {
@@ -164,6 +364,7 @@ k_umma_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&tmA);
         ptx::prefetch_tmap(&tmB);
+        ptx::prefetch_tmap(&tmC);
     }
     ptx::tc_fence_before();
     // both CTAs' barriers are initialised before any copy or commit signals them
@@ -184,10 +385,12 @@ k_umma_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             int stage = 0, issued = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int t = pair; ok && t < sched.tiles; t += npairs) {
+            SegIter it(sched, pair, sched.tiles);
+            Segment seg;
+            while (ok && it.next(sched, seg)) {
                 int tm, tn;
-                tile_coords(sched, t, tm, tn);
-                for (int kb = 0; kb < sched.nk; ++kb) {
+                tile_coords(sched, seg.tile, tm, tn);
+                for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
                     if (!wait_bar(EMPTY(stage), phase ^ 1u, abort_flag, d_error)) {
                         ok = false;
                         break;
@@ -214,11 +417,13 @@ k_umma_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            for (int t = pair; ok && t < sched.tiles; t += npairs) {
+            SegIter it(sched, pair, sched.tiles);
+            Segment seg;
+            while (ok && it.next(sched, seg)) {
                 if (!wait_bar_warp(TEMPTY(acc), acc_phase ^ 1u, abort_flag, d_error)) break;
                 ptx::tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(acc * BN);
-                for (int kb = 0; kb < sched.nk; ++kb) {
+                for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
                     if (!wait_bar_warp(FULL(stage), phase, abort_flag, d_error)) {
                         ok = false;
                         break;
@@ -228,7 +433,7 @@ k_umma_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     const uint64_t ad = ptx::sdesc_kmajor_sw128(st), bd = ptx::sdesc_kmajor_sw128(st + A_BYTES);
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)
-                        mma_pair_warp(d, ad + 2u * k, bd + 2u * k, IDESC, (kb > 0 || k > 0) ? 1u : 0u);
+                        mma_pair_warp(d, ad + 2u * k, bd + 2u * k, IDESC, (kb > seg.kb0 || k > 0) ? 1u : 0u);
                     commit_pair_warp(EMPTY(stage));
                     if (++stage == STAGES) {
                         stage = 0;
@@ -247,30 +452,53 @@ k_umma_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         }
     } else {
         // ------------------------------------------------------------ epilogue (both CTAs)
-        const int q4 = warp & 3;
+        const int q4 = warp & 3;                 // tensor memory lane quarter this warp may read
         const int row = q4 * 32 + lane;
+        const int half = (warp - 2) >> 2;        // columns [128 half, 128 half + 128)
+        const int col0 = half * (BN / 2);
         ptx::pdl_wait();
         const uint32_t temp_leader0 = ptx::map_cluster(TEMPTY(0), 0u);
         const uint32_t temp_leader1 = ptx::map_cluster(TEMPTY(1), 0u);
         int acc = 0;
-        uint32_t acc_phase = 0;
-        for (int t = pair; t < sched.tiles; t += npairs) {
+        uint32_t acc_phase = 0, fphase = 0, hphase = 0;
+        const int etid = threadIdx.x - 64;
+        const uint32_t wbuf = sbase + (uint32_t)(EPI_OFF + (warp - 2) * EPI_WARP_BYTES);
+        int sel = 0;   // this warp's staging box for the next C store
+        // stream-K: each CTA keeps its own half-tile partials and counters
+        // (rank r's region), and the pairs act as the schedule's CTAs
+        float *wsr = ws + (size_t)rank * ((size_t)sched.sk_grid * 2 * BMC * BN);
+        int *cnt = counters + (size_t)rank * sched.tiles;
+        SegIter it(sched, pair, sched.tiles);
+        Segment seg;
+        while (it.next(sched, seg)) {
             if (!wait_bar_warp(TFULL(acc), acc_phase, abort_flag, d_error)) break;
             ptx::tc_fence_after();
             int tm, tn;
-            tile_coords(sched, t, tm, tn);
-            const int r = tm * (2 * BMC) + (int)rank * BMC + row;
+            tile_coords(sched, seg.tile, tm, tn);
+            const int r0 = tm * (2 * BMC) + (int)rank * BMC + q4 * 32, qb = tn * BN;
             const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(acc * BN);
+            const bool whole = seg.kb0 == 0 && seg.kb1 == sched.nk;
+            float4 *part = reinterpret_cast<float4 *>(wsr) + (int64_t)(pair * 2 + seg.slot) * (BMC * BN / 4);
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 16) {
-                uint32_t v[16];
+            for (int c = col0; c < col0 + BN / 2; c += 32) {
+                uint32_t v[16], v2[16];
                 __syncwarp();
                 ptx::tmem_ld16(taddr + (uint32_t)c, v);
+                ptx::tmem_ld16(taddr + (uint32_t)(c + 16), v2);
                 ptx::tmem_wait_ld();
-                float f[16];
+                float f[32];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(v[j]);
-                store_chunk<false>(C, ldc, M, N, r, tn * BN + c, f);
+                for (int j = 0; j < 16; ++j) {
+                    f[j] = __uint_as_float(v[j]);
+                    f[16 + j] = __uint_as_float(v2[j]);
+                }
+                if (whole) {
+                    store_box(&tmC, M, N, r0, qb + c, f, wbuf, sel, lane);
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        __stcg(part + (c / 4 + u) * BMC + row, make_float4(f[4 * u], f[4 * u + 1], f[4 * u + 2], f[4 * u + 3]));
+                }
             }
             ptx::tc_fence_before();
             __syncwarp();
@@ -279,9 +507,39 @@ k_umma_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 acc = 0;
                 acc_phase ^= 1u;
             }
+            if (whole) continue;
+            // the last contributor (pair) of this half tile sums the partials in k order
+            const int t = seg.tile;
+            const int c_first = cta_of_unit(sched, (long long)t * sched.nk);
+            const int c_last = cta_of_unit(sched, (long long)(t + 1) * sched.nk - 1);
+            __threadfence();
+            if (!group_sync_warp(FIXB, fphase, abort_flag, d_error)) break;
+            if (etid == 0) {
+                const int old = atomicAdd(cnt + t, 1);
+                const bool last = old == c_last - c_first;
+                if (last) cnt[t] = 0;
+                misc[2] = last ? 1u : 0u;
+            }
+            if (!group_sync_warp(FIXB, fphase, abort_flag, d_error)) break;
+            if (!misc[2]) continue;
+            __threadfence();
+            auto emit32 = [&](int c0, const float(&f)[32]) { store_box(&tmC, M, N, r0, qb + c0, f, wbuf, sel, lane); };
+            SegIter peek = it;
+            Segment after;
+            if (peek.next(sched, after)) {
+                direct_fixup(sched, wsr, t, row, col0, emit32);
+            } else if (!staged_fixup(sched, wsr, t, row, half, (warp & 3) == 2 && lane == 0,
+                                     smem + half * (FIX_SLOTS * FIX_SLOT_BYTES),
+                                     sbase + (uint32_t)(half * (FIX_SLOTS * FIX_SLOT_BYTES)),
+                                     STG0 + 8u * (uint32_t)(half * FIX_SLOTS), HALFB + 8u * (uint32_t)half, hphase,
+                                     abort_flag, d_error, emit32)) {
+                break;
+            }
         }
     }
 
+    // the epilogue warps' C stores have read their staging boxes
+    if (warp >= 2 && lane == 0) ptx::bulk_wait_group_read0();
     // no CTA leaves while its partner may still signal its barriers, read its
     // shared memory or write its tensor memory
     __syncwarp();
@@ -331,7 +589,7 @@ __global__ void __launch_bounds__(256) k_w4_dequant(const uint4 *__restrict__ bq
 }  // namespace
 
 // W4A16 at prefill sizes: dequantise the weights once into the workspace
-// (bf16 [N, K]), then the pair GEMM on them.
+// (bf16 [N, K], after the stream-K partials), then the pair GEMM on them.
 cudaError_t launch_w4_pair(const GemmArgs &a, const Plan &p, const LaunchCtx &c)
 {
     if (!c.act_copy) return cudaErrorInvalidValue;
@@ -360,29 +618,68 @@ cudaError_t launch_w4_pair(const GemmArgs &a, const Plan &p, const LaunchCtx &c)
     return launch_umma_pair(b, p, c);
 }
 
-// Pair tiles for the prefill shapes: 256 x 256 tiles in a grouped raster,
-// whole tiles round-robin over the pairs (two CTAs per pair, at most one pair
-// per two SMs).
-int umma_pair_grid(int64_t M, int64_t N, int sm_count)
+// Pair plan (tiles of 256 x 256, the pairs are the schedule's CTAs, at most
+// one pair per two SMs):
+//   - a last wave holding a quarter to half of the pairs, on a long K: the
+//     full waves run whole tiles and each leftover tile is split along K among
+//     S = 2 or 3 pairs (stream-K over those), so the last wave ends after 1/S
+//     of a tile.  The split pays only when the time it saves, (1 - 1/S) of a
+//     tile's k-blocks, exceeds the cost of the fixup (partials written and
+//     summed, about 15 us, as long as 48 k-blocks at the MMA rate), measured
+//     on GB300: 4096 x 4096 x 12288 +5-10%, 768 x 8192 x 8192 +5-20%, while
+//     1024 x 6144 x 4096, 4096 x 4096 x 4096 and 512 x 14336 x 4096 (K = 4096,
+//     64 k-blocks) ran 5-10% slower split than as whole tiles;
+//   - tiles for at least half the pairs: whole tiles round-robin;
+//   - fewer: stream-K over every pair.
+// Sets mode, grid (CTAs, two per pair), whole, sk_grid (pairs) and split.
+void plan_pair(int64_t M, int64_t N, int64_t K, int sm_count, Plan *p)
 {
+    constexpr int64_t kFixupKBlocks = 48;
     const int64_t tiles = ((M + 255) / 256) * ((N + BN - 1) / BN);
-    return (int)std::min<int64_t>(tiles, sm_count / 2) * 2;
+    const int64_t nk = (K + BK - 1) / BK;
+    const int64_t pairs = std::max(1, sm_count / 2);
+    const int64_t rem = tiles % pairs;
+    const int64_t S = rem ? std::min<int64_t>({3, pairs / rem, nk}) : 1;
+    p->whole = 0;
+    p->sk_grid = 0;
+    if (tiles > pairs && rem * 4 > pairs && rem * 2 <= pairs && S >= 2 && (S - 1) * nk > kFixupKBlocks * S) {
+        p->mode = 1;
+        p->grid = (int)(2 * pairs);
+        p->whole = (int)(tiles - rem);
+        p->sk_grid = (int)(rem * S);
+        p->split = (int)S;
+    } else if (2 * tiles >= pairs || tiles * nk < 2 * pairs) {
+        p->mode = 0;
+        p->grid = (int)(2 * std::min(tiles, pairs));
+        p->split = 1;
+    } else {
+        p->mode = 1;
+        p->grid = (int)(2 * pairs);
+        p->sk_grid = (int)pairs;
+        const int64_t per_pair = tiles * nk / pairs;   // >= 2
+        p->split = (int)std::min<int64_t>(pairs, (nk + per_pair - 1) / per_pair + 1);
+    }
 }
 
 cudaError_t launch_umma_pair(const GemmArgs &a, const Plan &p, const LaunchCtx &c)
 {
-    CUtensorMap ma, mb;
-    if (!make_map_bf16(&ma, a.A, a.M, a.K, a.lda, BMC) || !make_map_bf16(&mb, a.B, a.N, a.K, a.ldb, BNC))
+    CUtensorMap ma, mb, mc;
+    if (!make_map_bf16(&ma, a.A, a.M, a.K, a.lda, BMC) || !make_map_bf16(&mb, a.B, a.N, a.K, a.ldb, BNC) ||
+        !make_map_c32(&mc, a.C, a.M, a.N, a.ldc))
         return cudaErrorInvalidValue;
     Sched s{};
-    s.mode = 0;
+    s.mode = p.mode;
     s.tiles_r = (int)((a.M + 255) / 256);
     s.tiles_q = (int)((a.N + BN - 1) / BN);
     s.tiles = s.tiles_r * s.tiles_q;
     s.nk = (int)((a.K + BK - 1) / BK);
-    s.grid = p.grid / 2;   // pairs
+    s.grid = p.grid / 2;   // the schedule's CTAs are the pairs
     s.group_r = std::min(s.tiles_r, 8);
+    s.whole = s.mode == 1 ? p.whole : 0;
+    s.sk_grid = s.mode == 1 ? std::min(p.sk_grid, s.grid) : 0;
+    s.units = (long long)(s.tiles - s.whole) * s.nk;
     s.stall = g_debug_stall;
+    if (s.mode == 1 && (!c.workspace || !c.counters)) return cudaErrorInvalidValue;
     static std::once_flag once[64];
     static cudaError_t attr_err[64];
     int dev = 0;
@@ -393,7 +690,7 @@ cudaError_t launch_umma_pair(const GemmArgs &a, const Plan &p, const LaunchCtx &
     if (attr_err[dev & 63] != cudaSuccess) return attr_err[dev & 63];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid, 1, 1);
-    cfg.blockDim = dim3(192, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = SMEM;
     cfg.stream = c.stream;
     cudaLaunchAttribute at[2];
@@ -405,7 +702,7 @@ cudaError_t launch_umma_pair(const GemmArgs &a, const Plan &p, const LaunchCtx &
     at[1].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, k_umma_pair, ma, mb, (uint16_t *)a.C, (int)a.M, (int)a.N, a.ldc, s, c.d_error);
+    return cudaLaunchKernelEx(&cfg, k_umma_pair, ma, mb, mc, (int)a.M, (int)a.N, s, c.workspace, c.counters, c.d_error);
 }
 
 }  // namespace dbw

@@ -222,6 +222,30 @@ def test_prefill_on_cta_pairs():
     assert g.gemm_bf16_plan(8, 64, 64, "pair", num_sms=sms)["grid"] == 2
 
 
+def test_pair_schedules():
+    # whole pair tiles round-robin when they fill at least half the pairs;
+    # a last wave of a quarter to half the pairs: full waves whole, each
+    # leftover tile split along K among up to three pairs; fewer tiles:
+    # stream-K over every pair
+    from dense_bit_weight_gb300 import gemm as g
+    sms = 152
+    plan = lambda M, N, K: g.gemm_bf16_plan(M, N, K, "pair", num_sms=sms)
+    assert (plan(1024, 4096, 4096)["split"], plan(1024, 4096, 4096)["grid"]) == (1, 128)   # 64 tiles
+    # a leftover quarter to half wave is split along K only on a long K
+    # (the fixup costs about 48 k-blocks)
+    assert (plan(1024, 6144, 4096)["split"], plan(1024, 6144, 4096)["grid"]) == (1, 152)   # 96: 76 + 20, 64 k-blocks
+    assert (plan(768, 8192, 8192)["split"], plan(768, 8192, 8192)["grid"]) == (3, 152)     # 96, 128 k-blocks
+    assert plan(4096, 4096, 4096)["split"] == 1                                            # 256: 228 + 28
+    assert plan(4096, 4096, 12288)["split"] == 2                                           # 192 k-blocks
+    assert plan(4096, 24576, 4096)["split"] == 1                                           # 1536: 1520 + 16
+    assert plan(4096, 6144, 4096)["split"] == 1                                            # 384: 380 + 4
+    p = plan(512, 4096, 12288)                                                             # 32 tiles
+    assert p["grid"] == sms and p["split"] >= 2
+    p = plan(700, 1000, 1000)                                                              # 12 tiles x 16 k-blocks
+    assert p["grid"] == sms and p["split"] >= 2
+    assert plan(129, 4104, 8)["split"] == 1                                                # 17 units: too few to share
+
+
 def test_wide_tiles_for_one_token_tile():
     # M <= 128 and a weight count that fills one wave of 176-256-row tiles:
     # the prefill kernel, weights read once each; otherwise the skinny split-K

@@ -85,6 +85,56 @@ def test_wide_single_token_tile(g, M, N, K, bn, kind):
     (assert_exact if kind == "int" else assert_close)(host_bits(C), ref, what=f"wide {bn} {M}x{N}x{K}")
 
 
+# CTA pairs (256 x 256 tiles) under stream-K: a handful of tiles over every
+# pair (each tile split among two to seven pairs, ragged M, N and K).
+PAIR_STREAM_K = [(300, 1200, 4096), (700, 1000, 1000), (512, 4096, 1024)]
+
+
+@pytest.mark.parametrize("M,N,K", PAIR_STREAM_K)
+@pytest.mark.parametrize("kind", ["normal", "int"])
+def test_pair_stream_k(g, M, N, K, kind):
+    p = g.gemm_bf16_plan(M, N, K, "pair")
+    if p["grid"] != 152:
+        pytest.skip(f"plan on this device: {p}")
+    assert p["split"] > 1
+    A, B = bf16_inputs(M, N, K, seed=M + 3 * K, kind=kind)
+    dA, dB = dev_bf16(A), dev_bf16(B)
+    C = host_bits(g.gemm_bf16(dA, dB, variant="pair"))
+    ref = oracle.gemm_bf16(A, B)
+    (assert_exact if kind == "int" else assert_close)(C, ref, what=f"pair stream-K {M}x{N}x{K}")
+    # the fixup sums in a fixed order: a second call gives the same bits
+    assert np.array_equal(host_bits(g.gemm_bf16(dA, dB, variant="pair")), C)
+
+
+@pytest.mark.parametrize("kind", ["normal", "int"])
+def test_pair_full_waves_then_split_leftovers(g, kind):
+    # 96 pair tiles on 76 pairs: one wave of whole tiles, then the 20 leftover
+    # tiles (columns 4864-6143 in the grouped raster) split three ways along
+    # K = 4800 (75 k-blocks, a ragged last block).  Checked on every column of
+    # sampled rows and on every row of sampled columns, half of them in the
+    # leftover tiles.
+    M, N, K = 1024, 6144, 4800
+    p = g.gemm_bf16_plan(M, N, K)
+    if p["grid"] != 152:
+        pytest.skip(f"plan on this device: {p}")
+    assert p["variant"] == 9 and p["split"] == 3
+    A, B = bf16_inputs(M, N, K, seed=21, kind=kind)
+    dA, dB = dev_bf16(A), dev_bf16(B)
+    C = host_bits(g.gemm_bf16(dA, dB))
+    rows = sample_rows(M, 4, seed=5)
+    cols = np.concatenate([sample_rows(4864, 2, seed=6), 4864 + sample_rows(N - 4864, 2, seed=7)])
+    ref_r = oracle.gemm_bf16(A[rows], B)
+    ref_c = oracle.gemm_bf16(A, B[cols])
+    if kind == "int":
+        assert_exact(C[rows], ref_r, what="rows")
+        assert_exact(C[:, cols], ref_c, what="cols")
+    else:
+        rms = float(np.sqrt(np.mean(np.concatenate([ref_r.ravel(), ref_c.ravel()]) ** 2)))
+        assert_close(C[rows], ref_r, rms, what="rows")
+        assert_close(C[:, cols], ref_c, rms, what="cols")
+    assert np.array_equal(host_bits(g.gemm_bf16(dA, dB)), C)
+
+
 def test_leading_dimensions_and_views(g):
     import torch
     M, N, K = 37, 200, 96
