@@ -161,7 +161,7 @@ int run(const GemmArgs &a, const Plan &p, cudaStream_t st, bool w4, int mx_fmt =
         break;
     case GEMM_VARIANT_FRAGMENT:
         if (!w4) return GEMM_ERR_VARIANT;
-        e = launch_w4_frag(a, p, c);
+        e = p.mode == 1 ? launch_w4_gemv(a, p, c) : launch_w4_frag(a, p, c);
         break;
     case GEMM_VARIANT_GROUPWISE:
         if (!w4) return GEMM_ERR_VARIANT;
@@ -415,9 +415,16 @@ void plan_grouped(int64_t G, int64_t M, int64_t N, int64_t K, int sm_count, Plan
 
 // W4A16 routing (AUTO), from GB300 timings over the four decode shapes
 // (N, K) in {(7168, 5120), (5120, 5120), (34816, 5120), (5120, 17408)}:
-//   M <= 8       TMA-fed fragment kernel (w4frag.cu): 31.7 / 11.4 / 10.8 /
-//                30.8 us at M = 1 against 39.5 / 12.6 / 12.2 / 28.2 for the
-//                register-fragment kernel and 43 / 18 / 15 / 30 for tcgen05
+//   M <= 16, at most three CTAs per SM (two per 32-row tile)
+//                fragment kernel with K split over clusters of two CTAs
+//                (w4gemv.cu, mode 1): M = 1: 9.4 / 8.8 / - / 22.5 us, M = 8:
+//                10.0 / 9.2 / - / 23.5, M = 16: 13.3 / 12.4 / - / 29.3, against
+//                11.1 / 11.0 / - / 30.3 (M = 1) for the fragment kernel with a
+//                pre-pass and 17.2 / 14.9 / - / 30.0 (M = 16) for tcgen05
+//   M <= 8, more tiles
+//                fragment kernel with a pre-pass (w4frag.cu, mode 0), its
+//                warps resident at once: 31.7 us on 34816 x 5120 against 36.9
+//                for the clusters running in waves
 //   9 and up     tcgen05 kernel with in-kernel dequantisation into TMEM
 //                (stages of 256 k, tokens in tiles of up to 128): cluster
 //                split-K (mode 2) when the tiles fit one wave, stream-K
@@ -443,7 +450,10 @@ bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int
         const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
         const int64_t pairs_n = std::max<int64_t>(1, sm_count / 2);
         const int64_t waves = (pair_tiles + pairs_n - 1) / pairs_n;
+        const bool gemv_fits = 2 * ((N + kW4GemvRows - 1) / kW4GemvRows) <= 3 * (int64_t)sm_count &&
+                               K / group <= kW4GemvMaxGroups;
         variant = M >= 1024 && 4 * pair_tiles >= 3 * waves * pairs_n ? GEMM_VARIANT_PAIR
+                  : M <= 16 && gemv_fits                                ? GEMM_VARIANT_FRAGMENT
                   : M <= 8                                              ? GEMM_VARIANT_FRAGMENT
                                                                         : GEMM_VARIANT_SKINNY;
     }
@@ -501,11 +511,25 @@ bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int
     if (variant == GEMM_VARIANT_FRAGMENT) {
         if (M > 16) return false;
         p->variant = GEMM_VARIANT_FRAGMENT;
-        p->kernels = 2;                      // activation copy and group sums, then the GEMM
-        p->act_copy = 1;
         p->tile_m = M <= 8 ? 8 : 16;         // tokens of the MMAs (N side)
-        p->split = w4_frag_split(N, K, sm_count, p->tile_m);   // warps per tile
+        const int64_t tiles = (N + kW4GemvRows - 1) / kW4GemvRows;
+        if (2 * tiles <= 3 * (int64_t)sm_count && K / group <= kW4GemvMaxGroups) {
+            // mode 1 (w4gemv.cu): a cluster of two CTAs per 32-row tile, all
+            // resident at once; one kernel, no workspace
+            p->mode = 1;
+            p->kernels = 1;
+            p->tile_n = kW4GemvRows;
+            p->grid = w4_gemv_grid(N);
+            p->split = (int)std::min<int64_t>(2 * kW4GemvWarps, (K + 127) / 128);   // warps sharing a tile's K
+            return true;
+        }
+        // mode 0 (w4frag.cu): the activation pre-pass, then 32-row tiles
+        // shared by 1, 2 or 4 warps of a CTA
+        p->mode = 0;
+        p->kernels = 2;
+        p->act_copy = 1;
         p->tile_n = kW4FragRows;
+        p->split = w4_frag_split(N, K, sm_count, p->tile_m);   // warps per tile
         p->grid = w4_frag_grid(N, p->split);
         p->ws_extra = w4_frag_workspace_floats(M, p->tile_m, K, group);   // activation copy and group sums
         return true;
@@ -641,8 +665,8 @@ void workspace_need(const Plan &p, int64_t M, int64_t N, int64_t K, int64_t *flo
         *counters = ((M + p.tile_m - 1) / p.tile_m) * ((N + p.tile_n - 1) / p.tile_n);
         if (p.variant == GEMM_VARIANT_PAIR) *counters *= 2;   // one per CTA half of a tile
     }
-    if (p.variant == GEMM_VARIANT_FRAGMENT) {
-        *floats = p.ws_extra;
+    if (p.variant == GEMM_VARIANT_FRAGMENT) {   // mode 0: activation copy and group sums; mode 1: none
+        if (p.mode == 0) *floats = p.ws_extra;
         return;
     }
     if (p.variant == GEMM_VARIANT_BLOCK_SCALED) {   // rearranged scale chunks after the partials

@@ -95,6 +95,14 @@ int w4_register_grid(int64_t N);
 constexpr int kW4FragRows = 32;
 constexpr int kW4FragWarps = 4;
 cudaError_t launch_w4_frag(const GemmArgs &a, const Plan &p, const LaunchCtx &c);
+// W4A16 for up to 16 tokens (w4gemv.cu): a cluster of two CTAs of
+// kW4GemvWarps warps per tile of kW4GemvRows weight rows, the warps splitting
+// K; one kernel, no workspace.
+constexpr int kW4GemvRows = 32;
+constexpr int kW4GemvWarps = 4;
+constexpr int kW4GemvMaxGroups = 192;   // K / group: the tile's scale and zero rows are staged whole
+cudaError_t launch_w4_gemv(const GemmArgs &a, const Plan &p, const LaunchCtx &c);
+int w4_gemv_grid(int64_t N);
 int w4_frag_split(int64_t N, int64_t K, int sm_count, int tile_m);
 int w4_frag_grid(int64_t N, int P);
 int64_t w4_frag_workspace_floats(int64_t M, int64_t TP, int64_t K, int64_t group);

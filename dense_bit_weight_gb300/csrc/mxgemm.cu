@@ -59,7 +59,6 @@ constexpr int kEpiThreads = 128;
 
 template <int FMT>   // 0: E4M3 x E4M3, 1: packed E2M1 x E2M1
 struct MxKind {
-    static constexpr int KMMA = FMT == 0 ? 32 : 64;            // k per MMA
     static constexpr int KSTAGE = FMT == 0 ? 128 : 256;        // k per stage (128 bytes per row)
     static constexpr int CHUNKS = KSTAGE / 128;                // 4-block scale chunks per stage
     static constexpr uint32_t ATYPE = FMT == 0 ? 0u : 1u;      // E4M3 (mxf8f6f4) / E2M1 (mxf4)

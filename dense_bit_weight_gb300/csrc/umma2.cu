@@ -338,7 +338,7 @@ k_umma_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = ptx::cluster_ctarank();
     const bool leader = rank == 0;
-    const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
+    const int pair = (int)(blockIdx.x >> 1);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {

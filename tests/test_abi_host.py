@@ -129,15 +129,27 @@ def test_plans_are_host_only_and_cover_the_workloads(g):
         assert (p["variant"], p["kernels"], p["tile_m"]) == (9, 2, 256) and p["grid"] <= sms
     assert g.gemm_w4a16_plan(4096, 5120, 17408, 128, num_sms=sms)["variant"] == 9     # 320 pair tiles: 0.84
     assert g.gemm_w4a16_plan(1024, 5120, 17408, 128, num_sms=sms)["variant"] == 2     # 80 pair tiles: 0.53
-    # the fragment kernel stages scales per stage: any number of groups plans
-    assert g.gemm_w4a16_plan(1, 4096, 32 * 545, 32, num_sms=sms)["variant"] == 6
+    # the one-kernel fragment plan stages a tile's scale rows whole (up to
+    # 192 groups); beyond, the pre-pass fragment kernel (scales per stage)
+    assert g.gemm_w4a16_plan(1, 4096, 32 * 192, 32, num_sms=sms)["kernels"] == 1
+    p = g.gemm_w4a16_plan(1, 4096, 32 * 545, 32, num_sms=sms)
+    assert (p["variant"], p["kernels"]) == (6, 2)
+    assert g.gemm_w4a16_plan(16, 4096, 32 * 545, 32, num_sms=sms)["variant"] == 2
     # beyond the staged-scale limit (K / group > 544 groups) the register kernel does not plan
     with pytest.raises(g.GemmError):
         g.gemm_w4a16_plan(1, 4096, 32 * 545, 32, "register", num_sms=sms)
-    # warps per 32-row tile: enough to fill the device, never more than the 256-k stages
-    assert g.gemm_w4a16_plan(1, 34816, 5120, 128, num_sms=sms)["split"] == 2
-    assert g.gemm_w4a16_plan(1, 5120, 5120, 128, num_sms=sms)["split"] == 4
-    assert g.gemm_w4a16_plan(1, 5120, 256, 128, num_sms=sms)["split"] == 1
+    # up to three CTAs per SM: a cluster of two CTAs per 32-row tile, its
+    # eight warps sharing the 128-k chunks of K (one kernel); more tiles: the
+    # activation pre-pass, then 32-row tiles shared by 1, 2 or 4 warps
+    p = g.gemm_w4a16_plan(1, 7168, 5120, 128, num_sms=sms)      # 224 tiles
+    assert (p["variant"], p["kernels"], p["grid"], p["split"], p["tile_n"]) == (6, 1, 448, 8, 32)
+    p = g.gemm_w4a16_plan(16, 5120, 17408, 128, num_sms=sms)    # M = 16 too
+    assert (p["variant"], p["kernels"], p["grid"], p["tile_m"]) == (6, 1, 320, 16)
+    p = g.gemm_w4a16_plan(1, 5120, 256, 128, num_sms=sms)       # two chunks: two warps
+    assert (p["grid"], p["split"]) == (320, 2)
+    p = g.gemm_w4a16_plan(1, 34816, 5120, 128, num_sms=sms)     # 1088 tiles: pre-pass kernel
+    assert (p["variant"], p["kernels"], p["split"]) == (6, 2, 2)
+    assert g.gemm_w4a16_plan(16, 34816, 5120, 128, num_sms=sms)["variant"] == 2
     with pytest.raises(g.GemmError):
         g.gemm_bf16_plan(4, 4, 4, num_sms=sms)       # K % 8
     with pytest.raises(g.GemmError):
