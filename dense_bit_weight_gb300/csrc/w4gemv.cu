@@ -63,8 +63,8 @@ constexpr int kRing = kWarps * kSlots * kSlot;   // 40 KB
 constexpr int kMaxGroups = kW4GemvMaxGroups;     // scale and zero rows staged whole
 constexpr int kSzOff = kRing;                    // scales [32][G] bf16, zeros [32][G] u8
 constexpr int kBarOff = kSzOff + kRows * kMaxGroups * 3;
-constexpr int kRedOff = kBarOff + kWarps * kSlots * 8;   // the partner CTA's sum, two tiles of [32][16] fp32
-constexpr int kPartOff = kRedOff + 2 * kRows * 16 * 4;  // the warps' sums [warp][32][16] fp32
+constexpr int kRedOff = kBarOff + kWarps * kSlots * 8;   // the partner CTA's sum [32][16] fp32
+constexpr int kPartOff = kRedOff + kRows * 16 * 4;      // the warps' sums [warp][32][16] fp32
 constexpr int kSzBar = kPartOff + kWarps * kRows * 16 * 4;
 constexpr int kFlagOff = kSzBar + 8;
 constexpr int kSmem = kFlagOff + 8 + 1024;       // + alignment slack
@@ -146,44 +146,36 @@ k_w4_gemv(const __grid_constant__ CUtensorMap tmQ, const uint16_t *__restrict__ 
     const uint32_t sbase = ptx::smem_addr(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
-    // a cluster of two CTAs per tile, each taking half of K; the clusters
-    // walk the tiles tile0, tile0 + nclusters, ...
+    // a cluster of two CTAs per tile, each taking half of K
     const uint32_t rank = ptx::cluster_ctarank();
-    const int tile0 = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
-    const int tiles = (N + kRows - 1) / kRows;
+    const int tile = blockIdx.x >> 1, n0 = tile * kRows;
     const int G = K / GROUP;
     const int nk = (K + 127) >> 7;                                    // 128-k chunks
     const int wk = (int)rank * kWarps + warp;                         // this warp among the tile's eight
-    const int c0 = wk * nk / (2 * kWarps), nu = (wk + 1) * nk / (2 * kWarps) - c0;   // its chunks of every tile
-    const int ntile = tile0 < tiles ? (tiles - 1 - tile0) / nclusters + 1 : 0;   // tiles of this cluster
-    const int nseq = ntile * nu;                                      // this warp's chunks over all its tiles
+    const int c0 = wk * nk / (2 * kWarps), nu = (wk + 1) * nk / (2 * kWarps) - c0;   // its chunks
     const uint32_t ring = sbase + (uint32_t)(warp * kSlots * kSlot);
     const uint32_t bar0 = sbase + (uint32_t)(kBarOff + warp * kSlots * 8);
     const uint32_t szbar = sbase + (uint32_t)kSzBar;
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + kFlagOff);
-    // the current tile's scales [32][G] (bf16) and zeros [32][G] (u8), rows beyond N zero
+    // the tile's scales [32][G] (bf16) and zeros [32][G] (u8), rows beyond N zero
     const uint16_t *sS = reinterpret_cast<const uint16_t *>(smem + kSzOff);
     const uint8_t *sZ = smem + kSzOff + kRows * G * 2;
     const uint64_t policy = ptx::policy_evict_first();
-    auto tile_of = [&](int i) { return tile0 + i * nclusters; };
-    auto vrows_of = [&](int tile) { return min(kRows, N - tile * kRows); };
+    const int vr = min(kRows, N - n0);   // rows of the tile within N
     // the scale and zero rows of a tile are contiguous: two bulk copies when
     // their sizes are whole 16-byte units, else plain loads
-    auto bulk_ok = [&](int tile) { return (vrows_of(tile) * G) % 16 == 0; };
+    const bool bulk = (vr * G) % 16 == 0;
 
-    // chunk q of this warp's sequence (tile q / nu, chunk c0 + q % nu) -> slot q % kSlots (lane 0 only)
+    // chunk c0 + q of this warp -> slot q % kSlots (lane 0 only)
     auto issue = [&](int q) {
-        const int tile = tile_of(q / nu), ch = c0 + q % nu;
         const uint32_t bar = bar0 + 8u * (uint32_t)(q % kSlots);
         ptx::mbar_arrive_expect_tx(bar, (uint32_t)kSlot);
-        ptx::tma_load_2d(ring + (uint32_t)((q % kSlots) * kSlot), &tmQ, bar, ch * 16, tile * kRows, policy);
+        ptx::tma_load_2d(ring + (uint32_t)((q % kSlots) * kSlot), &tmQ, bar, (c0 + q) * 16, n0, policy);
     };
     // the tile's scale and zero rows into shared memory (thread 0 issues the
     // copies; every thread takes part in the plain loads)
-    auto load_sz = [&](int tile) {
-        const int vr = vrows_of(tile), n0 = tile * kRows;
-        const bool bulk = bulk_ok(tile);
-        if (bulk && threadIdx.x == 0 && !stall && !*abort_flag) {
+    auto load_sz = [&]() {
+        if (bulk && threadIdx.x == 0 && !stall) {
             ptx::mbar_arrive_expect_tx(szbar, (uint32_t)(vr * G * 3));
             bulk_load(sbase + (uint32_t)kSzOff, scales + (int64_t)n0 * G, (uint32_t)(vr * G * 2), szbar);
             bulk_load(sbase + (uint32_t)(kSzOff + kRows * G * 2), zeros + (int64_t)n0 * G, (uint32_t)(vr * G), szbar);
@@ -196,34 +188,30 @@ k_w4_gemv(const __grid_constant__ CUtensorMap tmQ, const uint16_t *__restrict__ 
             wZ[i] = v ? zeros[(int64_t)n0 * G + i] : (uint8_t)0;
         }
     };
-    auto prefetch_sz = [&](int tile) {
-        if (bulk_ok(tile)) {
-            const int vr = vrows_of(tile), n0 = tile * kRows;
-            bulk_prefetch_l2(scales + (int64_t)n0 * G, (uint32_t)(vr * G * 2));
-            bulk_prefetch_l2(zeros + (int64_t)n0 * G, (uint32_t)(vr * G));
-        }
-    };
 
-    // Before the grid dependency wait only L2 prefetches of this CTA's first
+    // Before the grid dependency wait only L2 prefetches of this CTA's
     // weights and scale rows are issued (L2 is the coherence point, so
     // nothing stale is consumed); the copies into shared memory follow it.
     if (threadIdx.x == 0) {
         *abort_flag = 0u;
         ptx::mbar_init(szbar, 1);
-        if (ntile > 0) prefetch_sz(tile_of(0));
+        if (bulk) {
+            bulk_prefetch_l2(scales + (int64_t)n0 * G, (uint32_t)(vr * G * 2));
+            bulk_prefetch_l2(zeros + (int64_t)n0 * G, (uint32_t)(vr * G));
+        }
     }
     if (lane == 0) {
         for (int s = 0; s < kSlots; ++s) ptx::mbar_init(bar0 + 8u * (uint32_t)s, 1);
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tmQ);
-        for (int q = 0; q < nu && q < nseq; ++q) ptx::tma_prefetch_l2_2d(&tmQ, (c0 + q) * 16, tile_of(0) * kRows);
+        for (int q = 0; q < nu; ++q) ptx::tma_prefetch_l2_2d(&tmQ, (c0 + q) * 16, n0);
     }
     __syncthreads();   // barriers and the abort flag initialised
     ptx::pdl_wait();   // the activations (and C) may belong to the previous kernel
     ptx::pdl_launch_dependents();
     int issued = 0;
     if (lane == 0 && !stall)
-        for (; issued < kSlots && issued < nseq; ++issued) issue(issued);
+        for (; issued < kSlots && issued < nu; ++issued) issue(issued);
 
     // lanes of absent tokens (8u + g >= M) read token M - 1's row: their MMA
     // columns are never stored
@@ -237,7 +225,7 @@ k_w4_gemv(const __grid_constant__ CUtensorMap tmQ, const uint16_t *__restrict__ 
             for (int i = 0; i < WPT; ++i) o.a[u][i] = ld_ro_v4(arow[u] + gi * GROUP + 8 * i);
     };
 
-    const int gbeg = c0 * GU, gend = min(G, (c0 + nu) * GU);   // this warp's groups of every tile
+    const int gbeg = c0 * GU, gend = min(G, (c0 + nu) * GU);   // this warp's groups
     float acc[2][NT][4];
     int q = 0;   // chunks of the sequence consumed
     // group gi of the current tile with its activations in `cur`, fetching
@@ -245,7 +233,7 @@ k_w4_gemv(const __grid_constant__ CUtensorMap tmQ, const uint16_t *__restrict__ 
     auto step = [&](int gi, const GroupAct<NT, WPT> &cur, GroupAct<NT, WPT> &nxt) {
         const int h = gi % GU;
         const uint32_t slot = ring + (uint32_t)((q % kSlots) * kSlot);
-        load_act(gi + 1 < gend ? gi + 1 : gbeg, nxt);   // (the first group again: the next tile's)
+        if (gi + 1 < gend) load_act(gi + 1, nxt);
         if (h == 0 && !wait_bar_warp(bar0 + 8u * (uint32_t)(q % kSlots), (uint32_t)(q / kSlots) & 1u, abort_flag,
                                      d_error))
             return;
@@ -322,7 +310,7 @@ k_w4_gemv(const __grid_constant__ CUtensorMap tmQ, const uint16_t *__restrict__ 
             // every lane's reads of the slot have completed (their values were
             // used above): hand it back to the copy engine for chunk q + slots
             __syncwarp();
-            if (lane == 0 && !stall && issued < nseq && !*abort_flag) {
+            if (lane == 0 && !stall && issued < nu && !*abort_flag) {
                 ptx::fence_proxy_async_smem();
                 issue(issued++);
             }
@@ -332,74 +320,64 @@ k_w4_gemv(const __grid_constant__ CUtensorMap tmQ, const uint16_t *__restrict__ 
 
     GroupAct<NT, WPT> A0, A1;
     if (gbeg < gend) load_act(gbeg, A0);
-    uint32_t szphase = 0;   // phases of the scale-row barrier completed
+    load_sz();
+    __syncthreads();   // the plain-loaded scale rows
+    if (bulk && !stall) {
+        // (a copy issued before an abort still lands before the CTA leaves)
+        if (!wait_bar(szbar, 0u, abort_flag, d_error) && threadIdx.x == 0) wait_bar_drain(szbar, 0u);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int b = 0; b < 2; ++b)
+#pragma unroll
+        for (int u = 0; u < NT; ++u)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[b][u][e] = 0.f;
+    // the warp's groups, two per pass (activations alternate between A0 and A1)
+#pragma unroll 1
+    for (int gi = gbeg; gi < gend && !*abort_flag; gi += 2) {
+        step(gi, A0, A1);
+        if (gi + 1 < gend) step(gi + 1, A1, A0);
+    }
+    // the eight warps' sums of the tile [row][token]: each CTA adds its four
+    // in warp order, the second CTA hands its sum to the first through
+    // distributed shared memory, and the first adds the two (deterministic)
+    // and stores
     float *part = reinterpret_cast<float *>(smem + kPartOff);   // [warp][row][token]
-#pragma unroll 1
-    for (int it = 0; it < ntile; ++it) {
-        const int tile = tile_of(it), n0 = tile * kRows;
-        load_sz(tile);
-        __syncthreads();   // the plain-loaded scale rows
-        if (threadIdx.x == 0 && it + 1 < ntile) prefetch_sz(tile_of(it + 1));
-        if (bulk_ok(tile) && !stall && !*abort_flag) {
-            // (a copy issued before an abort still lands before it is reused)
-            if (!wait_bar(szbar, szphase, abort_flag, d_error) && threadIdx.x == 0) wait_bar_drain(szbar, szphase);
-            szphase ^= 1u;
+    float *mine = part + warp * (kRows * TP);
+#pragma unroll
+    for (int b = 0; b < 2; ++b)
+#pragma unroll
+        for (int u = 0; u < NT; ++u)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                mine[(16 * b + g + 8 * (e >> 1)) * TP + 8 * u + 2 * t + (e & 1)] = acc[b][u][e];
+    __syncthreads();
+    float *red = reinterpret_cast<float *>(smem + kRedOff);   // the partner's sum (in the first CTA)
+    float v[(kRows * TP + kWarps * 32 - 1) / (kWarps * 32)];
+#pragma unroll
+    for (int r = 0; r < (int)(sizeof(v) / sizeof(float)); ++r) {
+        const int i = threadIdx.x + r * kWarps * 32;
+        v[r] = 0.f;
+        if (i < kRows * TP) {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) v[r] += part[w * (kRows * TP) + i];
+            if (rank == 1) {
+                const uint32_t dst = ptx::map_cluster(ptx::smem_addr(red + i), 0u);
+                asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst), "f"(v[r]) : "memory");
+            }
         }
-        __syncwarp();
-#pragma unroll
-        for (int b = 0; b < 2; ++b)
-#pragma unroll
-            for (int u = 0; u < NT; ++u)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[b][u][e] = 0.f;
-        // the warp's groups, two per pass (activations alternate between A0 and A1)
-#pragma unroll 1
-        for (int gi = gbeg; gi < gend && !*abort_flag; gi += 2) {
-            step(gi, A0, A1);
-            if (gi + 1 < gend) step(gi + 1, A1, A0);
-            else A0 = A1;   // (an odd count: the next tile's first group is in A1)
-        }
-        // the eight warps' sums of the tile [row][token]: each CTA adds its
-        // four in warp order, the second CTA hands its sum to the first
-        // through distributed shared memory (double buffered by tile), and the
-        // first adds the two (deterministic) and stores
-        float *mine = part + warp * (kRows * TP);
-#pragma unroll
-        for (int b = 0; b < 2; ++b)
-#pragma unroll
-            for (int u = 0; u < NT; ++u)
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    mine[(16 * b + g + 8 * (e >> 1)) * TP + 8 * u + 2 * t + (e & 1)] = acc[b][u][e];
-        __syncthreads();
-        float *red = reinterpret_cast<float *>(smem + kRedOff) + (it & 1) * (kRows * 16);   // the partner's sum
-        float v[(kRows * TP + kWarps * 32 - 1) / (kWarps * 32)];
+    }
+    ptx::cluster_arrive_release();
+    ptx::cluster_wait();
+    if (rank == 0 && !*abort_flag) {
 #pragma unroll
         for (int r = 0; r < (int)(sizeof(v) / sizeof(float)); ++r) {
             const int i = threadIdx.x + r * kWarps * 32;
-            v[r] = 0.f;
-            if (i < kRows * TP) {
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w) v[r] += part[w * (kRows * TP) + i];
-                if (rank == 1) {
-                    const uint32_t dst = ptx::map_cluster(ptx::smem_addr(red + i), 0u);
-                    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst), "f"(v[r]) : "memory");
-                }
-            }
+            const int row = i / TP, tok = i % TP;
+            if (i < kRows * TP && tok < M && n0 + row < N)
+                C[(int64_t)tok * N + n0 + row] = f32_to_bf16_rn(v[r] + red[i]);
         }
-        ptx::cluster_arrive_release();
-        ptx::cluster_wait();
-        if (rank == 0 && !*abort_flag) {
-#pragma unroll
-            for (int r = 0; r < (int)(sizeof(v) / sizeof(float)); ++r) {
-                const int i = threadIdx.x + r * kWarps * 32;
-                const int row = i / TP, tok = i % TP;
-                if (i < kRows * TP && tok < M && n0 + row < N)
-                    C[(int64_t)tok * N + n0 + row] = f32_to_bf16_rn(v[r] + red[i]);
-            }
-        }
-        // (the next tile's partial sums reuse `part`: every thread has read it
-        // before the cluster barrier above)
     }
     if (*abort_flag && lane == 0 && !stall) {
         // chunks issued but not consumed land before the ring is released
