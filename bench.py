@@ -69,23 +69,28 @@ WORKLOAD = ("decode projections, Qwen3-8B-like dims: bf16 A[M,4096], M in {1,8,3
 
 
 # DRAM bytes (read + write) per launch of each decode GEMM, from one ncu pass
-# (profiles/decode_step_dram_traffic.md) over the kernel sources with this
-# SHA-256; reported only while the sources are unchanged.
-TRAFFIC_SOURCES_SHA256 = "cfc7aa04407f07fceb86e81a54c43183fb51ed37eee3d408b24510a70a075d39"
-TRAFFIC_BYTES = {(1, 4096, 4096): 33.57e6, (1, 6144, 4096): 50.35e6, (1, 24576, 4096): 201.46e6,
-                 (8, 4096, 4096): 33.70e6, (8, 6144, 4096): 50.48e6, (8, 24576, 4096): 201.59e6,
-                 (32, 4096, 4096): 33.90e6, (32, 6144, 4096): 50.68e6, (32, 24576, 4096): 201.81e6,
-                 (128, 4096, 4096): 34.69e6, (128, 6144, 4096): 51.47e6, (128, 24576, 4096): 202.66e6}
+# per shape (profiles/decode_step_dram_traffic.md) over the sources of the
+# decode step's kernels and their planner (DECODE_KERNEL_SOURCES) with this
+# SHA-256; reported only while those sources are unchanged.
+TRAFFIC_SOURCES_SHA256 = "338ac4319e8e8f4d0a0636941924f251d8bf30192bd0df1dc5a669fb79c68821"
+TRAFFIC_BYTES = {(1, 4096, 4096): 33.57e6, (1, 6144, 4096): 50.35e6, (1, 24576, 4096): 204.28e6,
+                 (8, 4096, 4096): 33.71e6, (8, 6144, 4096): 50.48e6, (8, 24576, 4096): 204.27e6,
+                 (32, 4096, 4096): 33.91e6, (32, 6144, 4096): 50.68e6, (32, 24576, 4096): 204.49e6,
+                 (128, 4096, 4096): 34.70e6, (128, 6144, 4096): 51.48e6, (128, 24576, 4096): 205.27e6}
+
+
+DECODE_KERNEL_SOURCES = ["api.cu", "common.cuh", "gemv.cu", "internal.h", "ptx.cuh", "sched.cuh", "umma.cu",
+                         "waits.cuh"]
 
 
 def kernel_sources_sha256():
     import hashlib
     csrc = os.path.join(ROOT, "dense_bit_weight_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(f.encode())
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in DECODE_KERNEL_SOURCES:
+        h.update(f.encode())
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "dbw_gemm.h"), "rb").read())
     return h.hexdigest()
 
 

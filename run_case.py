@@ -1,11 +1,13 @@
 """Run one GEMM shape repeatedly on the GPU (for profiling and quick timing).
 
     python run_case.py --M 1 --N 24576 --K 4096 \
-        [--kind bf16|w4a16|silu_mul|grouped] [--variant auto|gemv|skinny|prefill]
+        [--kind bf16|w4a16|silu_mul|grouped|mxfp8|mxfp4] [--variant auto|gemv|skinny|prefill]
         [--groups G] [--reps 4] [--copies 0]
 
 --kind silu_mul runs the fused gate/up projection (C [M,N], weights 2N rows);
---kind grouped runs the grouped GEMM with M tokens split evenly over G experts.
+--kind grouped runs the grouped GEMM with M tokens split evenly over G experts;
+--kind mxfp8 / mxfp4 the block-scaled GEMM on random E4M3 / packed E2M1 codes
+with random E8M0 scales (one per 32 along K).
 
 Weights are drawn on the device with torch's seeded generator; `--copies`
 weight copies (0 = enough to exceed three L2 sizes) are used round robin so
@@ -25,7 +27,7 @@ def main(argv=None):
     ap.add_argument("--M", type=int, required=True)
     ap.add_argument("--N", type=int, required=True)
     ap.add_argument("--K", type=int, required=True)
-    ap.add_argument("--kind", choices=["bf16", "w4a16", "silu_mul", "grouped"], default="bf16")
+    ap.add_argument("--kind", choices=["bf16", "w4a16", "silu_mul", "grouped", "mxfp8", "mxfp4"], default="bf16")
     ap.add_argument("--groups", type=int, default=8)
     ap.add_argument("--variant", default="auto")
     ap.add_argument("--group", type=int, default=128)
@@ -42,7 +44,7 @@ def main(argv=None):
     gen.manual_seed(0)
     M, N, K = a.M, a.N, a.K
     NB = 2 * N if a.kind == "silu_mul" else a.groups * N if a.kind == "grouped" else N   # weight rows
-    wbytes = NB * K * 2 if a.kind != "w4a16" else N * K // 2
+    wbytes = (N * K // 2 if a.kind in ("w4a16", "mxfp4") else N * K if a.kind == "mxfp8" else NB * K * 2)
     copies = a.copies or max(1, min(16, math.ceil(3 * 130e6 / wbytes)))
     A = torch.randn((M, K), generator=gen, device=dev).to(torch.bfloat16)
     C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
@@ -59,6 +61,18 @@ def main(argv=None):
         plan = {"variant_name": "prefill (grouped)", "groups": a.groups}
         fn = lambda i: g.gemm_bf16_grouped(A, Bs[i % copies], ends, C=C)
         work = {"GB": 2 * (M * K + NB * K + M * N) / 1e9, "TFLOP": 2 * M * N * K / 1e12}
+    elif a.kind in ("mxfp8", "mxfp4"):
+        fmt = "e4m3" if a.kind == "mxfp8" else "e2m1"
+        kb = K if fmt == "e4m3" else K // 2   # bytes per row
+        rnd = lambda r, c: torch.randint(0, 256, (r, c), generator=gen, device=dev, dtype=torch.uint8)
+        codes = lambda r, c: (rnd(r, c) & 0x77) if fmt == "e4m3" else rnd(r, c)   # E4M3: no NaN codes
+        scales = lambda r: torch.randint(124, 131, (r, K // 32), generator=gen, device=dev, dtype=torch.uint8)
+        A = codes(M, kb)
+        SA = scales(M)
+        Bs = [(codes(N, kb), scales(N)) for _ in range(copies)]
+        plan = g.gemm_mx_plan(M, N, K, fmt)
+        fn = lambda i: g.gemm_mx(A, SA, Bs[i % copies][0], Bs[i % copies][1], fmt, C)
+        work = {"GB": ((M + N) * kb + (M + N) * K // 32 + 2 * M * N) / 1e9, "TFLOP": 2 * M * N * K / 1e12}
     elif a.kind == "bf16":
         Bs = [(torch.randn((N, K), generator=gen, device=dev) * K ** -0.5).to(torch.bfloat16)
               for _ in range(copies)]
