@@ -172,7 +172,7 @@ int run(const GemmArgs &a, const Plan &p, cudaStream_t st, bool w4, int mx_fmt =
         e = launch_mx(a, p, c, mx_fmt);
         break;
     case GEMM_VARIANT_PAIR:
-        if (mx_fmt >= 0 || a.epi != GEMM_EPI_NONE || a.gends) return GEMM_ERR_VARIANT;
+        if (mx_fmt >= 0 || a.gends || (w4 && a.epi != GEMM_EPI_NONE)) return GEMM_ERR_VARIANT;
         e = w4 ? launch_w4_pair(a, p, c) : launch_umma_pair(a, p, c);
         break;
     case GEMM_VARIANT_SKINNY:
@@ -351,7 +351,7 @@ bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan 
         // 128 x 256 tiles (every shape faster); below that the single-CTA
         // kernel's stream-K spreads the work over every SM
         const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
-        variant = !fused && M > 128 && 4 * pair_tiles >= sm_count           ? GEMM_VARIANT_PAIR
+        variant = M > 128 && 4 * pair_tiles >= sm_count                     ? GEMM_VARIANT_PAIR
                   : M > 128 || wide_bn(M, N, sm_count, pairs)               ? GEMM_VARIANT_PREFILL
                   : M <= 4                                                  ? GEMM_VARIANT_GEMV
                                                                             : GEMM_VARIANT_SKINNY;
@@ -379,7 +379,7 @@ bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan 
         return true;
     }
     case GEMM_VARIANT_PAIR: {
-        if (pairs || fused) return false;   // plain C = A B^T only
+        (void)fused;   // every epilogue runs on the pair kernel (N: weight rows, 2N for (gate, up) pairs)
         p->variant = GEMM_VARIANT_PAIR;
         p->kernels = 1;
         p->bn = 256;

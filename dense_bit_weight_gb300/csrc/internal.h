@@ -134,8 +134,14 @@ bool make_map_bf16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int
 // Bytes [rows, width] (fp8 / packed fp4 codes): boxes of 128 bytes x box_rows
 // rows, 128-byte swizzle.
 bool make_map_u8(CUtensorMap *m, const void *ptr, int64_t rows, int64_t width, int box_rows);
-// C [rows, cols] bf16 for TMA stores of 32 x 32 boxes (64-byte swizzle).
+// C [rows, cols] bf16 for TMA stores of 32 x 32 boxes (64-byte swizzle) or of
+// 32 rows x 16 columns (32-byte swizzle).
 bool make_map_c32(CUtensorMap *m, void *C, int64_t rows, int64_t cols, int64_t ld);
+bool make_map_c16(CUtensorMap *m, void *C, int64_t rows, int64_t cols, int64_t ld);
+// A fused gate/up weight [2N, K] (gate rows, then up rows) as the 3-D view
+// [N][2][K]: boxes of 64 k x 2 x box_pairs put gate and up row j next to each
+// other in shared memory (128-byte swizzle).
+bool make_map_pairs(CUtensorMap *m, const void *ptr, int64_t N, int64_t K, int64_t ld, int box_pairs);
 // Packed 4-bit weights [rows, K/8] (uint32): boxes of 16 words (128 k) x
 // box_rows rows, 64-byte swizzle.
 bool make_map_words16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int box_rows);

@@ -1007,23 +1007,6 @@ bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int64_t 
     return r == CUDA_SUCCESS;
 }
 
-// Fused gate/up weights [2N, K] bf16 (gate rows 0..N-1, up rows N..2N-1) as
-// the 3-D view [N][2][K]: a box of 64 k x 2 x box_pairs puts the gate and up
-// rows of output column j next to each other (rows 2j, 2j + 1 of the tile),
-// 128-byte swizzle as make_map.
-bool make_map_pairs(CUtensorMap *m, const void *ptr, int64_t N, int64_t K, int64_t ld, int box_pairs)
-{
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)K, 2, (cuuint64_t)N};
-    cuuint64_t strides[2] = {(cuuint64_t)(N * ld * 2), (cuuint64_t)ld * 2};
-    cuuint32_t box[3] = {(cuuint32_t)BK, 2, (cuuint32_t)box_pairs};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
 
 // C of the skinny kernels ([Q tokens][R columns] bf16, row pitch ldc) for the
 // cluster split-K's TMA store: a box of BM / S columns x bn tokens, no swizzle.
@@ -1092,6 +1075,40 @@ cudaError_t launch_t(const CUtensorMap &mx, const CUtensorMap &my, const CUtenso
 }
 
 }  // namespace
+
+// Fused gate/up weights [2N, K] bf16 (gate rows 0..N-1, up rows N..2N-1) as
+// the 3-D view [N][2][K]: a box of 64 k x 2 x box_pairs puts the gate and up
+// rows of output column j next to each other (rows 2j, 2j + 1 of the tile),
+// 128-byte swizzle as make_map.
+bool make_map_pairs(CUtensorMap *m, const void *ptr, int64_t N, int64_t K, int64_t ld, int box_pairs)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)K, 2, (cuuint64_t)N};
+    cuuint64_t strides[2] = {(cuuint64_t)(N * ld * 2), (cuuint64_t)ld * 2};
+    cuuint32_t box[3] = {(cuuint32_t)BK, 2, (cuuint32_t)box_pairs};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// C [rows, cols] bf16 for TMA stores of 32 rows x 16 columns with the
+// 32-byte swizzle; elements beyond the extents are not written.
+bool make_map_c16(CUtensorMap *m, void *C, int64_t rows, int64_t cols, int64_t ld)
+{
+    if ((reinterpret_cast<uintptr_t>(C) & 15) || (ld * 2) % 16) return false;
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint32_t box[2] = {16, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
 
 // C [rows, cols] bf16 (row pitch ld elements) for TMA stores of 32 x 32
 // boxes with the 64-byte swizzle; elements beyond the extents are not written.

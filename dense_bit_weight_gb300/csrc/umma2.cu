@@ -120,6 +120,18 @@ __device__ __forceinline__ void tma_load_pair(uint32_t dst, const CUtensorMap *m
         : "memory");
 }
 
+// 3-D tile load (the (gate, up) row-pair view of a fused gate/up weight) into
+// this CTA's shared memory, completion counted on the leader's barrier.
+__device__ __forceinline__ void tma_load_pair_3d(uint32_t dst, const CUtensorMap *m, uint32_t bar_cluster, int32_t c0,
+                                                 int32_t c1, int32_t c2, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+        : "memory");
+}
+
 // Arrive on this CTA's barrier once the MMAs issued so far have completed.
 __device__ __forceinline__ void commit_local_warp(uint32_t bar)
 {
@@ -144,30 +156,32 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
 
 __device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 
-// bf16 store of 32 columns of this warp's 32 accumulator rows (row r0 + lane
-// held by each lane): the lanes write a 32 x 32 box into one of the warp's two
-// staging boxes in shared memory and lane 0 hands it to the TMA engine, which
-// writes the rows of C (clipping rows >= M and columns >= N), while the warp
-// goes on with the next box.  The box uses the 64-byte swizzle of the C map:
-// the 16-byte chunk j of row x sits at chunk j ^ ((x / 2) % 4), so the lanes'
-// writes spread over all banks.  Before a box is refilled, the store issued
-// from it two boxes earlier has finished reading it.
-__device__ __forceinline__ void store_box(const CUtensorMap *tmC, int M, int N, int r0, int q0, const float (&f)[32],
+// bf16 store of W (32 or 16) columns of this warp's 32 accumulator rows
+// (row r0 + lane held by each lane): the lanes write a 32 x W box into one of
+// the warp's two staging boxes in shared memory and lane 0 hands it to the
+// TMA engine, which writes the rows of C (clipping rows >= M and columns >=
+// N), while the warp goes on with the next box.  The box uses the swizzle of
+// its C map (64-byte rows: chunk j of row x at j ^ ((x / 2) % 4); 32-byte rows:
+// j ^ ((x / 4) % 2)), so the lanes' writes spread over all banks.  Before a box
+// is refilled, the store issued from it two boxes earlier has finished reading it.
+template <int W>
+__device__ __forceinline__ void store_box(const CUtensorMap *tmC, int M, int N, int r0, int q0, const float (&f)[W],
                                           uint32_t wbuf, int &sel, int lane)
 {
+    static_assert(W == 32 || W == 16, "boxes of 32 or 16 columns");
     if (r0 >= M || q0 >= N) return;   // the box lies wholly outside C
     const uint32_t box = wbuf + (uint32_t)(sel * EPI_BOX_BYTES);
     if (lane == 0) bulk_wait_read1();
     __syncwarp();
-    const uint32_t sw = (uint32_t)((lane >> 1) & 3);
+    const uint32_t sw = W == 32 ? (uint32_t)((lane >> 1) & 3) : (uint32_t)((lane >> 2) & 1);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < W / 8; ++j) {
         uint4 w;
         w.x = pack_bf16x2_rn(f[8 * j], f[8 * j + 1]);
         w.y = pack_bf16x2_rn(f[8 * j + 2], f[8 * j + 3]);
         w.z = pack_bf16x2_rn(f[8 * j + 4], f[8 * j + 5]);
         w.w = pack_bf16x2_rn(f[8 * j + 6], f[8 * j + 7]);
-        ptx::sts128(box + (uint32_t)(lane * 64) + (((uint32_t)j ^ sw) << 4), w);
+        ptx::sts128(box + (uint32_t)(lane * (2 * W)) + (((uint32_t)j ^ sw) << 4), w);
     }
     ptx::fence_proxy_async_smem();   // the box is read by the TMA engine
     __syncwarp();
@@ -176,6 +190,46 @@ __device__ __forceinline__ void store_box(const CUtensorMap *tmC, int M, int N, 
         ptx::bulk_commit_group();
     }
     sel ^= 1;
+}
+
+// The epilogue of 32 accumulator columns (c0 .. c0 + 31 of the tile, whose
+// first output column is qb): plain or bias (+ activation) results go out as
+// a 32-column box; with (gate, up) row pairs the columns alternate gate and
+// up, and silu(gate) * up gives 16 output columns (qb + c0 / 2 ...).
+template <bool PAIRS>
+__device__ __forceinline__ void emit_cols(const CUtensorMap *tmC, const Sched &sched, int M, int N, int r0, int qb,
+                                          int c0, float (&f)[32], uint32_t wbuf, int &sel, int lane)
+{
+    if constexpr (PAIRS) {
+        float o[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) o[j] = silu_mul(f[2 * j], f[2 * j + 1]);
+        store_box<16>(tmC, M, N, r0, qb + c0 / 2, o, wbuf, sel, lane);
+    } else {
+        if (epi_has_bias(sched.epi)) {
+            const int q0 = qb + c0;
+            const uint16_t *bp = sched.bias + q0;
+            if (q0 + 32 <= N && (reinterpret_cast<uintptr_t>(bp) & 15) == 0) {   // four 16-byte loads
+#pragma unroll
+                for (int j8 = 0; j8 < 4; ++j8) {
+                    const uint4 w = ld_ro_v4(bp + 8 * j8);
+                    const uint32_t h[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        f[8 * j8 + 2 * e] = bias_act(f[8 * j8 + 2 * e], bf16lo(h[e]), sched.epi);
+                        f[8 * j8 + 2 * e + 1] = bias_act(f[8 * j8 + 2 * e + 1], bf16hi(h[e]), sched.epi);
+                    }
+                }
+            } else {   // (a bias only 2-byte aligned, or the columns past N)
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float b = q0 + j < N ? bf16lo((uint32_t)__ldg(bp + j)) : 0.f;
+                    f[j] = bias_act(f[j], b, sched.epi);
+                }
+            }
+        }
+        store_box<32>(tmC, M, N, r0, qb + c0, f, wbuf, sel, lane);
+    }
 }
 
 // Stream-K fixup with plain loads (a split tile that is not this CTA's final
@@ -314,6 +368,7 @@ __device__ __noinline__ bool staged_fixup(const Sched &sched, const float *__res
     return ok;
 }
 
+template <bool PAIRS>
 __global__ void __launch_bounds__(kThreads, 1)
 k_umma_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
             const __grid_constant__ CUtensorMap tmC, int M, int N, const __grid_constant__ Sched sched,
@@ -400,7 +455,11 @@ k_umma_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                         if (leader) ptx::mbar_arrive_expect_tx(FULL(stage), 2u * STAGE_BYTES);
                         const uint32_t st = sbase + (uint32_t)(stage * STAGE_BYTES);
                         tma_load_pair(st, &tmA, full, kb * BK, tm * (2 * BMC) + (int)rank * BMC, pol_a);
-                        tma_load_pair(st + A_BYTES, &tmB, full, kb * BK, tn * BN + (int)rank * BNC, pol_b);
+                        if (PAIRS)   // (gate, up) row pairs: 64 pairs per CTA
+                            tma_load_pair_3d(st + A_BYTES, &tmB, full, kb * BK, 0, tn * (BN / 2) + (int)rank * (BNC / 2),
+                                             pol_b);
+                        else
+                            tma_load_pair(st + A_BYTES, &tmB, full, kb * BK, tn * BN + (int)rank * BNC, pol_b);
                         ++issued;
                     }
                     if (++stage == STAGES) {
@@ -475,7 +534,8 @@ k_umma_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             ptx::tc_fence_after();
             int tm, tn;
             tile_coords(sched, seg.tile, tm, tn);
-            const int r0 = tm * (2 * BMC) + (int)rank * BMC + q4 * 32, qb = tn * BN;
+            // qb: the tile's first output column (a tile of row pairs has BN / 2)
+            const int r0 = tm * (2 * BMC) + (int)rank * BMC + q4 * 32, qb = tn * (PAIRS ? BN / 2 : BN);
             const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(acc * BN);
             const bool whole = seg.kb0 == 0 && seg.kb1 == sched.nk;
             float4 *part = reinterpret_cast<float4 *>(wsr) + (int64_t)(pair * 2 + seg.slot) * (BMC * BN / 4);
@@ -493,7 +553,7 @@ k_umma_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     f[16 + j] = __uint_as_float(v2[j]);
                 }
                 if (whole) {
-                    store_box(&tmC, M, N, r0, qb + c, f, wbuf, sel, lane);
+                    emit_cols<PAIRS>(&tmC, sched, M, N, r0, qb, c, f, wbuf, sel, lane);
                 } else {
 #pragma unroll
                     for (int u = 0; u < 8; ++u)
@@ -523,7 +583,12 @@ k_umma_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             if (!group_sync_warp(FIXB, fphase, abort_flag, d_error)) break;
             if (!misc[2]) continue;
             __threadfence();
-            auto emit32 = [&](int c0, const float(&f)[32]) { store_box(&tmC, M, N, r0, qb + c0, f, wbuf, sel, lane); };
+            auto emit32 = [&](int c0, const float(&f)[32]) {
+                float g[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) g[j] = f[j];
+                emit_cols<PAIRS>(&tmC, sched, M, N, r0, qb, c0, g, wbuf, sel, lane);
+            };
             SegIter peek = it;
             Segment after;
             if (peek.next(sched, after)) {
@@ -663,14 +728,19 @@ void plan_pair(int64_t M, int64_t N, int64_t K, int sm_count, Plan *p)
 
 cudaError_t launch_umma_pair(const GemmArgs &a, const Plan &p, const LaunchCtx &c)
 {
+    // with the SiLU-mul epilogue B holds 2N rows (gate, then up) and a tile
+    // covers 128 output columns through the (gate, up) row-pair view
+    const bool pairs = a.epi == GEMM_EPI_SILU_MUL;
     CUtensorMap ma, mb, mc;
-    if (!make_map_bf16(&ma, a.A, a.M, a.K, a.lda, BMC) || !make_map_bf16(&mb, a.B, a.N, a.K, a.ldb, BNC) ||
-        !make_map_c32(&mc, a.C, a.M, a.N, a.ldc))
+    if (!make_map_bf16(&ma, a.A, a.M, a.K, a.lda, BMC) ||
+        !(pairs ? make_map_pairs(&mb, a.B, a.N, a.K, a.ldb, BNC / 2) : make_map_bf16(&mb, a.B, a.N, a.K, a.ldb, BNC)) ||
+        !(pairs ? make_map_c16(&mc, a.C, a.M, a.N, a.ldc) : make_map_c32(&mc, a.C, a.M, a.N, a.ldc)))
         return cudaErrorInvalidValue;
+    if (epi_has_bias(a.epi) && !a.bias) return cudaErrorInvalidValue;
     Sched s{};
     s.mode = p.mode;
     s.tiles_r = (int)((a.M + 255) / 256);
-    s.tiles_q = (int)((a.N + BN - 1) / BN);
+    s.tiles_q = (int)((a.N + (pairs ? BN / 2 : BN) - 1) / (pairs ? BN / 2 : BN));
     s.tiles = s.tiles_r * s.tiles_q;
     s.nk = (int)((a.K + BK - 1) / BK);
     s.grid = p.grid / 2;   // the schedule's CTAs are the pairs
@@ -679,15 +749,19 @@ cudaError_t launch_umma_pair(const GemmArgs &a, const Plan &p, const LaunchCtx &
     s.sk_grid = s.mode == 1 ? std::min(p.sk_grid, s.grid) : 0;
     s.units = (long long)(s.tiles - s.whole) * s.nk;
     s.stall = g_debug_stall;
+    s.epi = a.epi;
+    s.pairs = pairs ? 1 : 0;
+    s.bias = (const uint16_t *)a.bias;
     if (s.mode == 1 && (!c.workspace || !c.counters)) return cudaErrorInvalidValue;
-    static std::once_flag once[64];
-    static cudaError_t attr_err[64];
+    auto kern = pairs ? k_umma_pair<true> : k_umma_pair<false>;
+    static std::once_flag once[2][64];
+    static cudaError_t attr_err[2][64];
     int dev = 0;
     cudaGetDevice(&dev);
-    std::call_once(once[dev & 63], [&] {
-        attr_err[dev & 63] = cudaFuncSetAttribute(k_umma_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    std::call_once(once[pairs][dev & 63], [&] {
+        attr_err[pairs][dev & 63] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     });
-    if (attr_err[dev & 63] != cudaSuccess) return attr_err[dev & 63];
+    if (attr_err[pairs][dev & 63] != cudaSuccess) return attr_err[pairs][dev & 63];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -702,7 +776,7 @@ cudaError_t launch_umma_pair(const GemmArgs &a, const Plan &p, const LaunchCtx &
     at[1].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, k_umma_pair, ma, mb, mc, (int)a.M, (int)a.N, s, c.workspace, c.counters, c.d_error);
+    return cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, (int)a.M, (int)a.N, s, c.workspace, c.counters, c.d_error);
 }
 
 }  // namespace dbw

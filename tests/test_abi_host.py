@@ -199,13 +199,17 @@ def test_fused_epilogue_argument_errors():
         assert g.gemm_bf16_fused_ptr(p, p, 0, p, 8, 8, 8, 8, 8, 8, epi) == 11
     assert g.gemm_bf16_fused_ptr(p, p, 0, p, 8, 8, 8, 8, 8, 8, -1) == 11
     assert g.gemm_status_string(11) != g.gemm_status_string(99)
-    # every fused epilogue stays on the single-CTA kernels (the pair kernel stores the plain product)
-    for epi in ("bias", "bias_relu", "bias_silu", "bias_gelu"):
-        assert g.gemm_bf16_fused_plan(4096, 8192, 8192, epi, num_sms=152)["variant"] == 3
-    # the SiLU-mul plans are plans on the 2N weight rows, on single-CTA kernels
+    # every fused epilogue runs on CTA pairs at prefill sizes too (256 weight
+    # rows per pair tile: 128 output columns for the (gate, up) row pairs)
+    for epi in ("bias", "silu_mul", "bias_relu", "bias_silu", "bias_gelu"):
+        p = g.gemm_bf16_fused_plan(4096, 8192, 8192, epi, num_sms=152)
+        assert (p["variant"], p["tile_m"], p["tile_n"]) == (9, 256, 256)
+    # the SiLU-mul plans are plans on the 2N weight rows: single-CTA kernels up
+    # to 128 tokens, CTA pairs beyond
     sms = 152
-    for M in (1, 8, 128, 4096):
+    for M in (1, 8, 128):
         assert g.gemm_bf16_fused_plan(M, 12288, 4096, "silu_mul", num_sms=sms)["variant"] in (1, 2, 3)
+    assert g.gemm_bf16_fused_plan(4096, 12288, 4096, "silu_mul", num_sms=sms)["variant"] == 9
 
 
 def test_prefill_last_wave_split():
@@ -229,8 +233,8 @@ def test_prefill_on_cta_pairs():
     assert g.gemm_bf16_plan(4096, 24576, 4096, num_sms=sms)["grid"] == sms
     assert g.gemm_bf16_plan(512, 4096, 12288, num_sms=sms)["variant"] == 3    # 32 pair tiles: stream-K instead
     assert g.gemm_bf16_plan(300, 1200, 4096, num_sms=sms)["variant"] == 3
-    # fused epilogues stay on the single-CTA kernel; the pair kernel can be forced
-    assert g.gemm_bf16_fused_plan(4096, 12288, 4096, "silu_mul", num_sms=sms)["variant"] == 3
+    # fused epilogues take the pair kernel too; it can be forced
+    assert g.gemm_bf16_fused_plan(4096, 12288, 4096, "silu_mul", num_sms=sms)["variant"] == 9
     assert g.gemm_bf16_plan(8, 64, 64, "pair", num_sms=sms)["grid"] == 2
 
 

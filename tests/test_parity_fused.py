@@ -2,7 +2,8 @@
 
 Small and ragged shapes are compared element by element for every kernel
 family and split path (GEMV; skinny tcgen05 with whole tiles, cluster split-K
-and stream-K; prefill tcgen05 with whole tiles and stream-K).  The decode and
+and stream-K; prefill tcgen05 with whole tiles and stream-K; CTA pairs with
+whole tiles and stream-K).  The decode and
 prefill gate/up projections run at full size: every element of C up to
 M = 1024, sampled rows and columns at M = 4096.  Integer-valued inputs with a bias are exact; everything else
 must satisfy |out - ref| <= 1e-2*|ref| + 1e-2*rms(ref).
@@ -39,7 +40,7 @@ SMALL = [(1, 8, 16), (3, 72, 264), (4, 1000, 136),               # GEMV
          (128, 200, 4096), (8, 20480, 512),                      # skinny, split 8 / stream-K (320 tiles)
          (129, 264, 72), (300, 1200, 4096), (1000, 136, 136),    # prefill, stream-K
          (2048, 2048, 1024)]                                     # prefill, whole tiles
-VARIANTS = ["gemv", "skinny", "prefill"]
+VARIANTS = ["gemv", "skinny", "prefill", "pair"]
 
 
 def runnable(g, M, NB, K, variant):
@@ -109,7 +110,7 @@ def test_silu_mul(g, M, N, K, variant):
     assert_close(host_bits(C), oracle.gemm_bf16_silu_mul(A, B), what=f"silu_mul {variant} {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("variant,M", [("skinny", 16), ("skinny", 64), ("prefill", 512)])
+@pytest.mark.parametrize("variant,M", [("skinny", 16), ("skinny", 64), ("prefill", 512), ("pair", 512)])
 def test_silu_mul_splits_keep_pairs(g, variant, M):
     # shapes whose plan splits K: the gate and up rows of a column must be reduced together
     N, K = 64, 8192
@@ -137,6 +138,19 @@ def test_wide_single_token_tile(g, epilogue):
         C = g.gemm_bf16_fused(dev_bf16(A), dev_bf16(B), epilogue="silu_mul")
         ref = oracle.gemm_bf16_silu_mul(A, B)
     assert_close(host_bits(C), ref, what=f"wide {epilogue}")
+
+
+@pytest.mark.parametrize("variant", ["prefill", "pair"])
+def test_bias_two_byte_aligned(g, variant):
+    # a bias view starting 2 bytes past a 16-byte boundary (the header asks
+    # only for 2-byte alignment): the kernels fall back to element loads
+    M, N, K = 512, 1024, 256
+    A, B = bf16_inputs(M, N, K, seed=13)
+    big = synth.bf16_normal((N + 8,), 1.0, 13, synth.STREAM_B)
+    dbias = dev_bf16(big)[1:1 + N]
+    C = g.gemm_bf16_fused(dev_bf16(A), dev_bf16(B), dbias, epilogue="bias_relu", variant=variant)
+    ref = oracle.gemm_bf16_bias_act(A, B, big[1:1 + N], "relu")
+    assert_close(host_bits(C), ref, what=f"unaligned bias {variant}")
 
 
 def test_strided_operands_and_padding(g):
