@@ -172,7 +172,7 @@ int run(const GemmArgs &a, const Plan &p, cudaStream_t st, bool w4, int mx_fmt =
         e = launch_mx(a, p, c, mx_fmt);
         break;
     case GEMM_VARIANT_PAIR:
-        if (mx_fmt >= 0 || a.gends || (w4 && a.epi != GEMM_EPI_NONE)) return GEMM_ERR_VARIANT;
+        if (mx_fmt >= 0 || (w4 && (a.epi != GEMM_EPI_NONE || a.gends))) return GEMM_ERR_VARIANT;
         e = w4 ? launch_w4_pair(a, p, c) : launch_umma_pair(a, p, c);
         break;
     case GEMM_VARIANT_SKINNY:
@@ -411,6 +411,15 @@ void plan_grouped(int64_t G, int64_t M, int64_t N, int64_t K, int sm_count, Plan
     p->grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, sm_count));
     p->group_r = 1;
     (void)K;
+    if (G <= kPairMaxExperts && M >= 256 * G) {
+        // experts of at least 256 tokens on average: CTA pairs with 256-row
+        // m-tiles (an expert's last, partial one stores its rows directly)
+        const int64_t pt = ((M + 255) / 256 + G) * ((N + 255) / 256);
+        p->variant = GEMM_VARIANT_PAIR;
+        p->tile_m = 256;
+        p->stages = 6;
+        p->grid = (int)(2 * std::max<int64_t>(1, std::min<int64_t>(pt, sm_count / 2)));
+    }
 }
 
 // W4A16 routing (AUTO), from GB300 timings over the four decode shapes

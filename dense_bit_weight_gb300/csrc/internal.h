@@ -35,8 +35,10 @@ struct GemmArgs {
     const void *sfb = nullptr;
 };
 
-// Grouped GEMM: experts the prefill kernel's shared-memory table holds.
+// Grouped GEMM: experts the prefill kernel's shared-memory table holds, and
+// the (smaller) number the pair kernel's holds.
 constexpr int kMaxExperts = 1024;
+constexpr int kPairMaxExperts = 192;
 
 // Host-side plan (pure function of the sizes and the SM count).
 struct Plan {

@@ -66,7 +66,9 @@ constexpr int FIX_SLOTS = STAGES;                  // staged fixup: 16 KB slots 
 constexpr int FIX_SLOT_BYTES = STAGES * STAGE_BYTES / (2 * FIX_SLOTS);
 constexpr int NBARS = 2 * STAGES + 4 + 1 + 3 + 2 * FIX_SLOTS;
 constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
-constexpr int SMEM = MISC_OFF + 16 + 1024;
+constexpr int GRP_OFF = MISC_OFF + 16;             // grouped GEMM: expert row ends, m-tile prefix
+constexpr int GRP_BYTES = 4 * (2 * kPairMaxExperts + 1);
+constexpr int SMEM = GRP_OFF + GRP_BYTES + 1024;
 
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols)
 {
@@ -196,10 +198,35 @@ __device__ __forceinline__ void store_box(const CUtensorMap *tmC, int M, int N, 
 // first output column is qb): plain or bias (+ activation) results go out as
 // a 32-column box; with (gate, up) row pairs the columns alternate gate and
 // up, and silu(gate) * up gives 16 output columns (qb + c0 / 2 ...).
-template <bool PAIRS>
+template <bool PAIRS, bool GRP>
 __device__ __forceinline__ void emit_cols(const CUtensorMap *tmC, const Sched &sched, int M, int N, int r0, int qb,
-                                          int c0, float (&f)[32], uint32_t wbuf, int &sel, int lane)
+                                          int c0, float (&f)[32], uint32_t wbuf, int &sel, int lane, int rlim,
+                                          uint16_t *__restrict__ Cg, int64_t ldc)
 {
+    if constexpr (GRP) {
+        // an expert's last rows: the box would cross into the next expert's
+        // rows of C, so this lane stores its own row (below rlim) directly
+        if (r0 + 32 > rlim) {
+            const int r = r0 + lane, q0 = qb + c0;
+            if (r < rlim && q0 < N) {
+                uint16_t *dst = Cg + (int64_t)r * ldc + q0;
+                if (q0 + 32 <= N) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint4 w;
+                        w.x = pack_bf16x2_rn(f[8 * j], f[8 * j + 1]);
+                        w.y = pack_bf16x2_rn(f[8 * j + 2], f[8 * j + 3]);
+                        w.z = pack_bf16x2_rn(f[8 * j + 4], f[8 * j + 5]);
+                        w.w = pack_bf16x2_rn(f[8 * j + 6], f[8 * j + 7]);
+                        reinterpret_cast<uint4 *>(dst)[j] = w;
+                    }
+                } else {
+                    for (int j = 0; j < 32 && q0 + j < N; ++j) dst[j] = f32_to_bf16_rn(f[j]);
+                }
+            }
+            return;
+        }
+    }
     if constexpr (PAIRS) {
         float o[16];
 #pragma unroll
@@ -368,10 +395,11 @@ __device__ __noinline__ bool staged_fixup(const Sched &sched, const float *__res
     return ok;
 }
 
-template <bool PAIRS>
+template <bool PAIRS, bool GRP>
 __global__ void __launch_bounds__(kThreads, 1)
 k_umma_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-            const __grid_constant__ CUtensorMap tmC, int M, int N, const __grid_constant__ Sched sched,
+            const __grid_constant__ CUtensorMap tmC, uint16_t *__restrict__ Cg, int64_t ldc, int M, int N,
+            const __grid_constant__ Sched sched,
             float *__restrict__ ws,
             int *__restrict__ counters, int *__restrict__ d_error)
 {
@@ -429,6 +457,86 @@ k_umma_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = misc[0];
+
+    // Grouped GEMM: expert g owns the token rows [end[g-1], end[g]) of A and C
+    // and multiplies them by its weight rows g*gN .. g*gN + gN - 1 of B.  The
+    // row ends come from the previous kernel (a router), so every thread waits
+    // for them; warp 0 of each CTA clamps them into a non-decreasing sequence
+    // within [0, M] and writes the exclusive prefix of the experts' 256-row
+    // m-tile counts; expert g then owns the pair tiles from gpre[g] * tiles_q,
+    // m-tile fastest, and an expert with no rows owns none.
+    int *gend = reinterpret_cast<int *>(smem + GRP_OFF);
+    int *gpre = gend + kPairMaxExperts;
+    int ntiles = sched.tiles;
+    if constexpr (GRP) {
+        ptx::pdl_wait();
+        if (warp == 0) {
+            const int G = sched.groups;
+            const int per = (G + 31) / 32;   // consecutive experts per lane
+            const int g0 = min(G, lane * per), g1 = min(G, g0 + per);
+            int run = 0;                     // prefix max of the raw ends within this lane's run
+            for (int g = g0; g < g1; ++g) run = max(run, __ldg(sched.gends + g));
+            int before = run;                // inclusive max-scan over lanes, then shifted to exclusive
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, before, o);
+                if (lane >= o) before = max(before, v);
+            }
+            before = __shfl_up_sync(0xffffffffu, before, 1);
+            if (lane == 0) before = 0;
+            int prev = min(before, M), mt = 0;
+            run = before;
+            for (int g = g0; g < g1; ++g) {
+                run = max(run, __ldg(sched.gends + g));
+                const int e = min(run, M);
+                gend[g] = e;
+                mt += (e - prev + 2 * BMC - 1) / (2 * BMC);
+                prev = e;
+            }
+            int base = mt;                   // exclusive sum-scan of the m-tile counts
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, base, o);
+                if (lane >= o) base += v;
+            }
+            if (lane == 31) gpre[G] = base;
+            base -= mt;
+            prev = min(before, M);
+            for (int g = g0; g < g1; ++g) {
+                gpre[g] = base;
+                base += (gend[g] - (g == g0 ? prev : gend[g - 1]) + 2 * BMC - 1) / (2 * BMC);
+            }
+        }
+        __syncthreads();
+        ntiles = gpre[sched.groups] * sched.tiles_q;
+    }
+    // pair tile t -> A rows from xrow (this CTA's half at xrow + 128 rank), B
+    // rows from yrow, C rows below rlim, the first output column qb
+    auto geo = [&](int t, int &xrow, int &yrow, int &rlim, int &qb) {
+        if constexpr (GRP) {
+            const int mt = t / sched.tiles_q;   // expert g owns tiles [gpre[g], gpre[g + 1]) * tiles_q
+            int lo = 0, hi = sched.groups;      // the expert: largest lo < G with gpre[lo] <= mt
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (gpre[mid] <= mt) lo = mid;
+                else hi = mid;
+            }
+            // within the expert, m-tiles vary fastest: the pairs that read one
+            // weight tile run side by side, so it comes from DRAM once
+            const int nm = gpre[lo + 1] - gpre[lo];
+            const int local = t - gpre[lo] * sched.tiles_q;
+            const int tqe = local / nm, mte = local - tqe * nm;
+            xrow = (lo > 0 ? gend[lo - 1] : 0) + mte * (2 * BMC);
+            rlim = gend[lo];
+            yrow = lo * sched.gN + tqe * BN;
+            qb = tqe * BN;
+        } else {
+            int tm, tn;
+            tile_coords(sched, t, tm, tn);
+            xrow = tm * (2 * BMC);
+            yrow = tn * BN;
+            rlim = M;
+            qb = tn * (PAIRS ? BN / 2 : BN);   // a tile of (gate, up) row pairs has BN / 2 output columns
+        }
+    };
     ptx::pdl_launch_dependents();
 
     if (warp == 0) {
@@ -440,11 +548,12 @@ k_umma_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             int stage = 0, issued = 0;
             uint32_t phase = 0;
             bool ok = true;
-            SegIter it(sched, pair, sched.tiles);
+            SegIter it(sched, pair, ntiles);
             Segment seg;
             while (ok && it.next(sched, seg)) {
-                int tm, tn;
-                tile_coords(sched, seg.tile, tm, tn);
+                int xrow, yrow, rlim, qb;
+                geo(seg.tile, xrow, yrow, rlim, qb);
+                (void)rlim;
                 for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
                     if (!wait_bar(EMPTY(stage), phase ^ 1u, abort_flag, d_error)) {
                         ok = false;
@@ -454,12 +563,12 @@ k_umma_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                         const uint32_t full = ptx::map_cluster(FULL(stage), 0u);   // the leader's barrier
                         if (leader) ptx::mbar_arrive_expect_tx(FULL(stage), 2u * STAGE_BYTES);
                         const uint32_t st = sbase + (uint32_t)(stage * STAGE_BYTES);
-                        tma_load_pair(st, &tmA, full, kb * BK, tm * (2 * BMC) + (int)rank * BMC, pol_a);
+                        tma_load_pair(st, &tmA, full, kb * BK, xrow + (int)rank * BMC, pol_a);
                         if (PAIRS)   // (gate, up) row pairs: 64 pairs per CTA
-                            tma_load_pair_3d(st + A_BYTES, &tmB, full, kb * BK, 0, tn * (BN / 2) + (int)rank * (BNC / 2),
+                            tma_load_pair_3d(st + A_BYTES, &tmB, full, kb * BK, 0, yrow / 2 + (int)rank * (BNC / 2),
                                              pol_b);
                         else
-                            tma_load_pair(st + A_BYTES, &tmB, full, kb * BK, tn * BN + (int)rank * BNC, pol_b);
+                            tma_load_pair(st + A_BYTES, &tmB, full, kb * BK, yrow + (int)rank * BNC, pol_b);
                         ++issued;
                     }
                     if (++stage == STAGES) {
@@ -476,7 +585,7 @@ k_umma_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            SegIter it(sched, pair, sched.tiles);
+            SegIter it(sched, pair, ntiles);
             Segment seg;
             while (ok && it.next(sched, seg)) {
                 if (!wait_bar_warp(TEMPTY(acc), acc_phase ^ 1u, abort_flag, d_error)) break;
@@ -527,15 +636,14 @@ k_umma_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         // (rank r's region), and the pairs act as the schedule's CTAs
         float *wsr = ws + (size_t)rank * ((size_t)sched.sk_grid * 2 * BMC * BN);
         int *cnt = counters + (size_t)rank * sched.tiles;
-        SegIter it(sched, pair, sched.tiles);
+        SegIter it(sched, pair, ntiles);
         Segment seg;
         while (it.next(sched, seg)) {
             if (!wait_bar_warp(TFULL(acc), acc_phase, abort_flag, d_error)) break;
             ptx::tc_fence_after();
-            int tm, tn;
-            tile_coords(sched, seg.tile, tm, tn);
-            // qb: the tile's first output column (a tile of row pairs has BN / 2)
-            const int r0 = tm * (2 * BMC) + (int)rank * BMC + q4 * 32, qb = tn * (PAIRS ? BN / 2 : BN);
+            int xrow, yrow, rlim, qb;
+            geo(seg.tile, xrow, yrow, rlim, qb);
+            const int r0 = xrow + (int)rank * BMC + q4 * 32;
             const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(acc * BN);
             const bool whole = seg.kb0 == 0 && seg.kb1 == sched.nk;
             float4 *part = reinterpret_cast<float4 *>(wsr) + (int64_t)(pair * 2 + seg.slot) * (BMC * BN / 4);
@@ -553,7 +661,7 @@ k_umma_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     f[16 + j] = __uint_as_float(v2[j]);
                 }
                 if (whole) {
-                    emit_cols<PAIRS>(&tmC, sched, M, N, r0, qb, c, f, wbuf, sel, lane);
+                    emit_cols<PAIRS, GRP>(&tmC, sched, M, N, r0, qb, c, f, wbuf, sel, lane, rlim, Cg, ldc);
                 } else {
 #pragma unroll
                     for (int u = 0; u < 8; ++u)
@@ -587,7 +695,7 @@ k_umma_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 float g[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) g[j] = f[j];
-                emit_cols<PAIRS>(&tmC, sched, M, N, r0, qb, c0, g, wbuf, sel, lane);
+                emit_cols<PAIRS, GRP>(&tmC, sched, M, N, r0, qb, c0, g, wbuf, sel, lane, rlim, Cg, ldc);
             };
             SegIter peek = it;
             Segment after;
@@ -731,9 +839,12 @@ cudaError_t launch_umma_pair(const GemmArgs &a, const Plan &p, const LaunchCtx &
     // with the SiLU-mul epilogue B holds 2N rows (gate, then up) and a tile
     // covers 128 output columns through the (gate, up) row-pair view
     const bool pairs = a.epi == GEMM_EPI_SILU_MUL;
+    const bool grp = a.gends != nullptr;   // grouped: B stacks the experts' weights [groups * N, K]
+    if (grp && (pairs || a.groups < 1 || a.groups > kPairMaxExperts || p.mode != 0)) return cudaErrorInvalidValue;
     CUtensorMap ma, mb, mc;
     if (!make_map_bf16(&ma, a.A, a.M, a.K, a.lda, BMC) ||
-        !(pairs ? make_map_pairs(&mb, a.B, a.N, a.K, a.ldb, BNC / 2) : make_map_bf16(&mb, a.B, a.N, a.K, a.ldb, BNC)) ||
+        !(pairs ? make_map_pairs(&mb, a.B, a.N, a.K, a.ldb, BNC / 2)
+                : make_map_bf16(&mb, a.B, grp ? a.groups * a.N : a.N, a.K, a.ldb, BNC)) ||
         !(pairs ? make_map_c16(&mc, a.C, a.M, a.N, a.ldc) : make_map_c32(&mc, a.C, a.M, a.N, a.ldc)))
         return cudaErrorInvalidValue;
     if (epi_has_bias(a.epi) && !a.bias) return cudaErrorInvalidValue;
@@ -741,7 +852,9 @@ cudaError_t launch_umma_pair(const GemmArgs &a, const Plan &p, const LaunchCtx &
     s.mode = p.mode;
     s.tiles_r = (int)((a.M + 255) / 256);
     s.tiles_q = (int)((a.N + (pairs ? BN / 2 : BN) - 1) / (pairs ? BN / 2 : BN));
-    s.tiles = s.tiles_r * s.tiles_q;
+    // grouped: at most one partial m-tile per expert beyond the M / 256 full
+    // ones (the tiles are found on the device)
+    s.tiles = (grp ? s.tiles_r + (int)a.groups : s.tiles_r) * s.tiles_q;
     s.nk = (int)((a.K + BK - 1) / BK);
     s.grid = p.grid / 2;   // the schedule's CTAs are the pairs
     s.group_r = std::min(s.tiles_r, 8);
@@ -752,16 +865,20 @@ cudaError_t launch_umma_pair(const GemmArgs &a, const Plan &p, const LaunchCtx &
     s.epi = a.epi;
     s.pairs = pairs ? 1 : 0;
     s.bias = (const uint16_t *)a.bias;
+    s.gends = a.gends;
+    s.groups = (int)a.groups;
+    s.gN = (int)a.N;
     if (s.mode == 1 && (!c.workspace || !c.counters)) return cudaErrorInvalidValue;
-    auto kern = pairs ? k_umma_pair<true> : k_umma_pair<false>;
-    static std::once_flag once[2][64];
-    static cudaError_t attr_err[2][64];
+    auto kern = pairs ? k_umma_pair<true, false> : grp ? k_umma_pair<false, true> : k_umma_pair<false, false>;
+    const int ki = pairs ? 1 : grp ? 2 : 0;
+    static std::once_flag once[3][64];
+    static cudaError_t attr_err[3][64];
     int dev = 0;
     cudaGetDevice(&dev);
-    std::call_once(once[pairs][dev & 63], [&] {
-        attr_err[pairs][dev & 63] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    std::call_once(once[ki][dev & 63], [&] {
+        attr_err[ki][dev & 63] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     });
-    if (attr_err[pairs][dev & 63] != cudaSuccess) return attr_err[pairs][dev & 63];
+    if (attr_err[ki][dev & 63] != cudaSuccess) return attr_err[ki][dev & 63];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -776,7 +893,8 @@ cudaError_t launch_umma_pair(const GemmArgs &a, const Plan &p, const LaunchCtx &
     at[1].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, (int)a.M, (int)a.N, s, c.workspace, c.counters, c.d_error);
+    return cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, (uint16_t *)a.C, a.ldc, (int)a.M, (int)a.N, s, c.workspace,
+                              c.counters, c.d_error);
 }
 
 }  // namespace dbw

@@ -51,6 +51,8 @@ CASES = [  # (expert token counts, N, K, spare rows past the last expert)
     ([0, 0, 0, 1000], 264, 1024, 3),                # all tokens on one expert
     ([3] * 64, 256, 128, 0),                        # many small experts (decode-like)
     ([130], 4104, 72, 0),                           # one expert = the plain GEMM, ragged N
+    ([700, 0, 300, 513], 264, 520, 7),              # CTA pairs (>= 256 tokens per expert on average):
+                                                    # partial m-tiles, an empty expert, ragged N and K
     # the bench's loads, full size
     ([512] * 8, 4096, 4096, 0),
     ([1024, 0, 512, 37, 0, 800, 256, 1, 600, 0, 300, 64, 200, 150, 100, 52], 4096, 4096, 0),
