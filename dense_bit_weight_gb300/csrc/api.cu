@@ -301,6 +301,14 @@ static void plan_umma(int64_t M, int64_t N, int64_t K, bool swap, int bn, int sm
         const int64_t units = tiles * nk;
         p->mode = 1;
         p->grid = (int)std::min<int64_t>(G, units);
+        if (!swap && tiles_r > 1 && p->grid >= 2 * tiles_r) {
+            // token tiles in lockstep: tile-rows in order (group_r = 1) and a
+            // grid that is a multiple of them, so CTA c and CTA c + grid / tiles_r
+            // cover the same (weight tile, k) units of neighbouring token tiles
+            // at the same time and each weight stage comes from HBM once
+            p->grid = p->grid / (int)tiles_r * (int)tiles_r;
+            p->group_r = 1;
+        }
         const int64_t per_cta = units / p->grid;   // >= 1
         p->split = (int)std::min<int64_t>(p->grid, (nk + per_cta - 1) / per_cta + 1);
         if (p->split < 1) p->split = 1;

@@ -815,6 +815,7 @@ void plan_pair(int64_t M, int64_t N, int64_t K, int sm_count, Plan *p)
     const int64_t S = rem ? std::min<int64_t>({3, pairs / rem, nk}) : 1;
     p->whole = 0;
     p->sk_grid = 0;
+    p->group_r = 0;
     if (tiles > pairs && rem * 4 > pairs && rem * 2 <= pairs && S >= 2 && (S - 1) * nk > kFixupKBlocks * S) {
         p->mode = 1;
         p->grid = (int)(2 * pairs);
@@ -826,11 +827,17 @@ void plan_pair(int64_t M, int64_t N, int64_t K, int sm_count, Plan *p)
         p->grid = (int)(2 * std::min(tiles, pairs));
         p->split = 1;
     } else {
+        // token tiles in lockstep (as in the single-CTA planner): tile-rows in
+        // order and a multiple of them sharing the units
+        const int64_t tiles_r = (M + 255) / 256;
+        const bool lock = tiles_r > 1 && pairs >= 2 * tiles_r;
+        const int64_t sk = lock ? pairs / tiles_r * tiles_r : pairs;
         p->mode = 1;
-        p->grid = (int)(2 * pairs);
-        p->sk_grid = (int)pairs;
-        const int64_t per_pair = tiles * nk / pairs;   // >= 2
-        p->split = (int)std::min<int64_t>(pairs, (nk + per_pair - 1) / per_pair + 1);
+        p->grid = (int)(2 * sk);
+        p->sk_grid = (int)sk;
+        p->group_r = lock ? 1 : 0;
+        const int64_t per_pair = tiles * nk / sk;   // >= 2
+        p->split = (int)std::min<int64_t>(sk, (nk + per_pair - 1) / per_pair + 1);
     }
 }
 
@@ -857,7 +864,7 @@ cudaError_t launch_umma_pair(const GemmArgs &a, const Plan &p, const LaunchCtx &
     s.tiles = (grp ? s.tiles_r + (int)a.groups : s.tiles_r) * s.tiles_q;
     s.nk = (int)((a.K + BK - 1) / BK);
     s.grid = p.grid / 2;   // the schedule's CTAs are the pairs
-    s.group_r = std::min(s.tiles_r, 8);
+    s.group_r = p.mode == 1 && p.group_r > 0 ? p.group_r : std::min(s.tiles_r, 8);
     s.whole = s.mode == 1 ? p.whole : 0;
     s.sk_grid = s.mode == 1 ? std::min(p.sk_grid, s.grid) : 0;
     s.units = (long long)(s.tiles - s.whole) * s.nk;

@@ -242,7 +242,8 @@ def test_pair_schedules():
     # whole pair tiles round-robin when they fill at least half the pairs;
     # a last wave of a quarter to half the pairs: full waves whole, each
     # leftover tile split along K among up to three pairs; fewer tiles:
-    # stream-K over every pair
+    # stream-K over the largest multiple of the token tile-rows that fits the
+    # pairs (the tile-rows then run in lockstep)
     from dense_bit_weight_gb300 import gemm as g
     sms = 152
     plan = lambda M, N, K: g.gemm_bf16_plan(M, N, K, "pair", num_sms=sms)
@@ -258,8 +259,22 @@ def test_pair_schedules():
     p = plan(512, 4096, 12288)                                                             # 32 tiles
     assert p["grid"] == sms and p["split"] >= 2
     p = plan(700, 1000, 1000)                                                              # 12 tiles x 16 k-blocks
-    assert p["grid"] == sms and p["split"] >= 2
+    assert p["grid"] == 2 * (76 // 3 * 3) and p["split"] >= 2                              # 3 tile-rows: 75 pairs
+    assert plan(300, 4096, 12288)["grid"] == 2 * 76                                        # 2 tile-rows
+    assert plan(256, 4096, 12288)["grid"] == 2 * 76                                        # one tile-row
     assert plan(129, 4104, 8)["split"] == 1                                                # 17 units: too few to share
+
+
+def test_single_cta_stream_k_grid_is_a_multiple_of_the_token_tiles():
+    # single-CTA prefill under stream-K: the grid is the largest multiple of
+    # the 128-row token tiles within the SMs
+    from dense_bit_weight_gb300 import gemm as g
+    sms = 152
+    plan = lambda M, N, K: g.gemm_bf16_plan(M, N, K, "prefill", num_sms=sms)
+    assert plan(512, 4096, 12288)["grid"] == 152                                           # 4 tile-rows
+    assert plan(384, 4096, 12288)["grid"] == 150                                           # 3 tile-rows
+    assert plan(640, 2048, 12288)["grid"] == 150                                           # 5 tile-rows x 8
+    assert plan(128, 4096, 12288)["grid"] == 152                                           # 1 tile-row
 
 
 def test_wide_tiles_for_one_token_tile():
