@@ -79,8 +79,8 @@ TRAFFIC_BYTES = {(1, 4096, 4096): 33.57e6, (1, 6144, 4096): 50.35e6, (1, 24576, 
                  (128, 4096, 4096): 34.70e6, (128, 6144, 4096): 51.48e6, (128, 24576, 4096): 205.27e6}
 
 
-DECODE_KERNEL_SOURCES = ["api.cu", "common.cuh", "gemv.cu", "internal.h", "ptx.cuh", "sched.cuh", "umma.cu",
-                         "waits.cuh"]
+DECODE_KERNEL_SOURCES = ["api.cu", "common.cuh", "gemv.cu", "gemvband.cu", "internal.h", "ptx.cuh", "sched.cuh",
+                         "umma.cu", "waits.cuh"]
 
 
 def kernel_sources_sha256():

@@ -155,6 +155,10 @@ int run(const GemmArgs &a, const Plan &p, cudaStream_t st, bool w4, int mx_fmt =
     switch (p.variant) {
     case GEMM_VARIANT_ZERO: e = launch_zero_fill(a, c); break;
     case GEMM_VARIANT_GEMV: e = w4 ? launch_gemv_w4a16(a, p, c) : launch_gemv_bf16(a, p, c); break;
+    case GEMM_VARIANT_BAND:
+        if (w4 || mx_fmt >= 0 || a.gends) return GEMM_ERR_VARIANT;
+        e = launch_gemv_band(a, p, c);
+        break;
     case GEMM_VARIANT_REGISTER:
         if (!w4) return GEMM_ERR_VARIANT;
         e = launch_w4_register(a, p, c);
@@ -341,6 +345,25 @@ static int wide_bn(int64_t M, int64_t N, int sm_count, bool pairs)
     return 0;
 }
 
+// Whether the band kernel (gemvband.cu) serves a decode shape under AUTO.
+// Measured on GB300, graph-timed with the weights from HBM (us, band against
+// the route it replaces): 6144 x 4096: M = 1 11.0 / 13.1 (GEMV), M = 4
+// 11.0 / 26.5 (GEMV), M = 8 11.0 / 12.5 (skinny); 7168 x 4096: 11.3 / 14.0,
+// 11.3 / 27.2, 11.2 / 13.2; 4096 x 4096 (27-row bands): M = 1 8.6 / 8.2,
+// M = 4 8.6 / 14.9, M = 8 8.6 / 9.5; 4096 x 12288: M = 1 20.5 / 19.6,
+// M = 4 20.5 / 38.8, M = 8 20.6 / 18.8; at M = 16 and 32 the skinny kernel
+// leads (its tensor-core MMAs; the band kernel's warp-level ones grow with
+// the tokens).  So: 2 to 4 tokens whenever a band fits; 1 and 5-8 tokens with
+// K up to 8192, and at 1 token only bands of at least 32 rows.
+static bool band_first(int64_t M, int64_t N, int64_t K, int sm_count, bool pairs)
+{
+    if (pairs || M > 8 || N < 1) return false;
+    const int64_t rows = (N + std::min<int64_t>(sm_count, N) - 1) / std::min<int64_t>(sm_count, N);
+    if (rows > kBandMaxRows) return false;
+    if (M >= 2 && M <= 4) return true;
+    return K <= 8192 && (M > 1 || rows >= 32);
+}
+
 bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan *p, bool query, bool pairs,
                bool fused)
 {
@@ -361,6 +384,7 @@ bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan 
         const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
         variant = M > 128 && 4 * pair_tiles >= sm_count                     ? GEMM_VARIANT_PAIR
                   : M > 128 || wide_bn(M, N, sm_count, pairs)               ? GEMM_VARIANT_PREFILL
+                  : band_first(M, N, K, sm_count, pairs)                    ? GEMM_VARIANT_BAND
                   : M <= 4                                                  ? GEMM_VARIANT_GEMV
                                                                             : GEMM_VARIANT_SKINNY;
     }
@@ -386,6 +410,9 @@ bool plan_bf16(int64_t M, int64_t N, int64_t K, int variant, int sm_count, Plan 
         plan_umma(M, N, K, false, bn ? bn : 256, sm_count, query, p, pairs);
         return true;
     }
+    case GEMM_VARIANT_BAND:
+        // the (gate, up) pairs of the SiLU-mul epilogue are not served here
+        return !pairs && plan_band(M, N, K, sm_count, p);
     case GEMM_VARIANT_PAIR: {
         (void)fused;   // every epilogue runs on the pair kernel (N: weight rows, 2N for (gate, up) pairs)
         p->variant = GEMM_VARIANT_PAIR;

@@ -116,6 +116,15 @@ cudaError_t launch_w4_prep(const GemmArgs &a, const LaunchCtx &c, uint16_t *Ap, 
 // (16, 32 or 64), 128-k stages, stream-K over (weight tile, stage) units.
 int w4tc_stages(int bn);
 cudaError_t launch_w4tc(const GemmArgs &a, const Plan &p, const LaunchCtx &c);
+// bf16 decode for up to kBandMaxTokens tokens (gemvband.cu): CTA c streams
+// weight rows [c N / grid, (c + 1) N / grid) (at most kBandMaxRows) through
+// bulk copies into warp-level MMAs; no workspace.  plan_band is false when
+// the shape does not fit (then another variant serves it).  Plan.bn holds
+// the k per stage.
+constexpr int kBandMaxRows = 64;
+constexpr int kBandMaxTokens = 32;
+bool plan_band(int64_t M, int64_t N, int64_t K, int sm_count, Plan *p);
+cudaError_t launch_gemv_band(const GemmArgs &a, const Plan &p, const LaunchCtx &c);
 // Prefill on CTA pairs (umma2.cu): 256 x 256 tiles, tcgen05.mma.cta_group::2;
 // the grid is twice the number of pairs.
 void plan_pair(int64_t M, int64_t N, int64_t K, int sm_count, Plan *p);
@@ -136,6 +145,9 @@ bool make_map_bf16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int
 // Bytes [rows, width] (fp8 / packed fp4 codes): boxes of 128 bytes x box_rows
 // rows, 128-byte swizzle.
 bool make_map_u8(CUtensorMap *m, const void *ptr, int64_t rows, int64_t width, int box_rows);
+// bf16 [rows, K], K a multiple of 64, as [K / 64][rows][64]: boxes of
+// box_kb 64-k blocks x box_rows rows (box_kb make_map_bf16 boxes in one copy).
+bool make_map_kblocks(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int64_t ld, int box_rows, int box_kb);
 // C [rows, cols] bf16 for TMA stores of 32 x 32 boxes (64-byte swizzle) or of
 // 32 rows x 16 columns (32-byte swizzle).
 bool make_map_c32(CUtensorMap *m, void *C, int64_t rows, int64_t cols, int64_t ld);

@@ -149,6 +149,7 @@ extern "C" int gemm_bf16_noalloc(const void *A, const void *B, void *C, int64_t 
     switch (p.variant) {
     case GEMM_VARIANT_ZERO: e = launch_zero_fill(a, c); break;
     case GEMM_VARIANT_GEMV: e = launch_gemv_bf16(a, p, c); break;
+    case GEMM_VARIANT_BAND: e = launch_gemv_band(a, p, c); break;
     case GEMM_VARIANT_PAIR: e = launch_umma_pair(a, p, c); break;
     default: e = launch_umma_bf16(a, p, c); break;
     }

@@ -1094,6 +1094,25 @@ bool make_map_pairs(CUtensorMap *m, const void *ptr, int64_t N, int64_t K, int64
     return r == CUDA_SUCCESS;
 }
 
+// bf16 [rows, K] (K a multiple of 64, leading dimension ld) as the 3-D view
+// [K / 64][rows][64]: one box of box_kb 64-k blocks x box_rows rows lands as
+// box_kb consecutive [box_rows][64] tiles (128-byte swizzle), the layout of
+// box_kb separate 2-D boxes of make_map_bf16, in one copy.
+bool make_map_kblocks(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int64_t ld, int box_rows, int box_kb)
+{
+    if (K % BK) return false;
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)BK, (cuuint64_t)rows, (cuuint64_t)(K / BK)};
+    cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)BK * 2};
+    cuuint32_t box[3] = {(cuuint32_t)BK, (cuuint32_t)box_rows, (cuuint32_t)box_kb};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // C [rows, cols] bf16 for TMA stores of 32 rows x 16 columns with the
 // 32-byte swizzle; elements beyond the extents are not written.
 bool make_map_c16(CUtensorMap *m, void *C, int64_t rows, int64_t cols, int64_t ld)

@@ -22,7 +22,7 @@ STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_NULL", 2: "GEMM_ERR_SHAPE", 3: "GEMM_ERR_LD
           7: "GEMM_ERR_DEVICE_TIMEOUT", 8: "GEMM_ERR_ARCH", 9: "GEMM_ERR_ALIAS",
           10: "GEMM_ERR_VARIANT", 11: "GEMM_ERR_EPILOGUE"}
 VARIANT = {"auto": 0, "gemv": 1, "skinny": 2, "prefill": 3, "zero": 4, "register": 5, "fragment": 6,
-           "groupwise": 7, "block_scaled": 8, "pair": 9}
+           "groupwise": 7, "block_scaled": 8, "pair": 9, "band": 10}
 VARIANT_NAME = {v: k for k, v in VARIANT.items()}
 
 EXPORTS = ["gemm_bf16", "gemm_w4a16", "gemm_bf16_ex", "gemm_w4a16_ex", "gemm_bf16_plan",

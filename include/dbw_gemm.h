@@ -72,8 +72,11 @@ typedef enum {
                                  /* one tcgen05 accumulator per quantisation       */
                                  /* group, scale and zero applied per group        */
     GEMM_VARIANT_BLOCK_SCALED = 8, /* MX: block-scaled tcgen05 MMAs (gemm_mxfp*)   */
-    GEMM_VARIANT_PAIR = 9        /* bf16 prefill on CTA pairs: 256 x 256 tiles,    */
-                                 /* tcgen05.mma.cta_group::2 (plain epilogue only) */
+    GEMM_VARIANT_PAIR = 9,       /* bf16 prefill on CTA pairs: 256 x 256 tiles,    */
+                                 /* tcgen05.mma.cta_group::2                       */
+    GEMM_VARIANT_BAND = 10       /* bf16 decode, M <= 32: each SM streams a band   */
+                                 /* of at most 64 weight rows by bulk copies into  */
+                                 /* warp-level MMAs (no K split, no workspace)     */
 } gemm_variant;
 
 typedef struct {

@@ -105,7 +105,7 @@ def test_plans_are_host_only_and_cover_the_workloads(g):
     for M in (1, 8, 32, 128):
         for N, K in ((6144, 4096), (4096, 4096), (24576, 4096)):
             p = g.gemm_bf16_plan(M, N, K, num_sms=sms)
-            assert p["variant"] in (1, 2, 3) and p["kernels"] >= 1 and p["grid"] >= 1
+            assert p["variant"] in (1, 2, 3, 10) and p["kernels"] >= 1 and p["grid"] >= 1
     for M in (1024, 4096, 16384):
         p = g.gemm_bf16_plan(M, 8192, 8192, num_sms=sms)
         assert p["variant"] == 9 and p["tile_m"] == p["tile_n"] == 256
@@ -238,6 +238,29 @@ def test_prefill_on_cta_pairs():
     assert g.gemm_bf16_plan(8, 64, 64, "pair", num_sms=sms)["grid"] == 2
 
 
+def test_band_plans():
+    # the band kernel: one band of at most 64 weight rows per SM, tokens in
+    # MMA tiles of 8 (at most 32); a ring of eight stages (two per MMA warp),
+    # or one slot per stage when K spans at most four
+    from dense_bit_weight_gb300 import gemm as g
+    sms = 152
+    plan = lambda M, N, K: g.gemm_bf16_plan(M, N, K, "band", num_sms=sms)
+    p = plan(1, 6144, 4096)
+    assert (p["variant"], p["grid"], p["tile_m"], p["tile_n"], p["stages"]) == (10, 152, 8, 41, 8)
+    p = plan(32, 9728, 520)                                    # 64-row bands, 32 tokens, nine 64-k stages
+    assert (p["grid"], p["tile_m"], p["tile_n"], p["stages"]) == (152, 32, 64, 8)
+    assert plan(1, 4096, 256)["stages"] == 1                   # K in one stage: one slot
+    assert plan(9, 64, 2056)["grid"] == 64                     # one row per CTA
+    assert plan(16, 4096, 12288)["tile_m"] == 16
+    for M, N in ((33, 4096), (1, 9729)):                       # too many tokens / a band of 65 rows
+        with pytest.raises(g.GemmError):
+            plan(M, N, 4096)
+    # the bias epilogues run on it; the SiLU-mul (gate, up) pairs do not
+    assert g.gemm_bf16_fused_plan(8, 4096, 4096, "bias_gelu", "band", num_sms=sms)["variant"] == 10
+    with pytest.raises(g.GemmError):
+        g.gemm_bf16_fused_plan(8, 4096, 4096, "silu_mul", "band", num_sms=sms)
+
+
 def test_pair_schedules():
     # whole pair tiles round-robin when they fill at least half the pairs;
     # a last wave of a quarter to half the pairs: full waves whole, each
@@ -290,7 +313,11 @@ def test_wide_tiles_for_one_token_tile():
     assert g.gemm_bf16_plan(128, 16384, 4096, num_sms=sms)["variant"] == 2      # 176 rows: 94 tiles, too few
     assert g.gemm_bf16_plan(128, 4096, 4096, num_sms=sms)["variant"] == 2
     assert g.gemm_bf16_plan(129, 24576, 4096, num_sms=sms)["tile_n"] == 256     # two token tiles
-    assert g.gemm_bf16_plan(4, 4096, 4096, num_sms=sms)["variant"] == 1         # GEMV below 5 rows
+    assert g.gemm_bf16_plan(4, 4096, 4096, num_sms=sms)["variant"] == 10        # band kernel at 2-4 tokens
+    assert g.gemm_bf16_plan(1, 4096, 4096, num_sms=sms)["variant"] == 1         # GEMV: 1 token, 27-row bands
+    assert g.gemm_bf16_plan(1, 6144, 4096, num_sms=sms)["variant"] == 10        # band: 41-row bands
+    assert g.gemm_bf16_plan(8, 4096, 12288, num_sms=sms)["variant"] == 2        # skinny beyond K = 8192
+    assert g.gemm_bf16_plan(16, 6144, 4096, num_sms=sms)["variant"] == 2        # skinny from 9 tokens
     # forced variants keep their kernels; the fused gate/up pairs take the same tiles
     assert g.gemm_bf16_plan(128, 24576, 4096, "skinny", num_sms=sms)["variant"] == 2
     assert g.gemm_bf16_plan(128, 2 * 12288, 4096, num_sms=sms)["tile_n"] == 176
@@ -324,8 +351,10 @@ def test_planner_invariants_over_shapes():
             N = rnd.randrange(8, 40000, 8)
             K = rnd.randrange(8, 16384, 8)
             p = g.gemm_bf16_plan(M, N, K, num_sms=sms)
-            assert p["variant"] in (1, 2, 3, 9), p
+            assert p["variant"] in (1, 2, 3, 9, 10), p
             assert p["grid"] >= 1 and p["split"] >= 1
+            if p["variant"] == 10:   # band: one band of at most 64 rows per CTA, at most 8 tokens
+                assert M <= 8 and p["grid"] == min(N, sms) and p["tile_n"] <= 64 and p["split"] == 1, (M, N, K, p)
             if p["variant"] in (2, 3):
                 assert p["grid"] <= 2 * sms, (M, N, K, p)
             if p["variant"] == 9:

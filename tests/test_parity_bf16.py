@@ -18,7 +18,7 @@ from gpu_helpers import assert_close, assert_exact, bf16_inputs, dev_bf16, host_
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = ["gemv", "skinny", "prefill", "pair"]
+VARIANTS = ["gemv", "skinny", "prefill", "pair", "band"]
 
 
 @pytest.fixture(scope="module")
@@ -133,6 +133,27 @@ def test_pair_full_waves_then_split_leftovers(g, kind):
         assert_close(C[rows], ref_r, rms, what="rows")
         assert_close(C[:, cols], ref_c, rms, what="cols")
     assert np.array_equal(host_bits(g.gemm_bf16(dA, dB)), C)
+
+
+# The band kernel (bf16 decode, M <= 32): K tails of half an MMA step
+# (K % 16 == 8) in the first and in a later chunk, bands of exactly 64 rows,
+# bands shorter than one MMA tile, 1-32 tokens, and the decode shapes at full
+# size with every element compared.
+BAND = [(1, 152, 8), (5, 1000, 3080), (32, 9728, 520), (17, 304, 4104), (9, 64, 2056), (31, 7000, 1024),
+        (1, 6144, 4096), (8, 4096, 4096), (32, 6144, 4096), (16, 4096, 12288)]
+
+
+@pytest.mark.parametrize("M,N,K", BAND)
+@pytest.mark.parametrize("kind", ["normal", "int"])
+def test_band(g, M, N, K, kind):
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    p = g.gemm_bf16_plan(M, N, K, "band")
+    assert p["variant"] == 10 and p["grid"] == min(N, sms)
+    A, B = bf16_inputs(M, N, K, seed=M * 7 + N + K, kind=kind)
+    C = host_bits(g.gemm_bf16(dev_bf16(A), dev_bf16(B), variant="band"))
+    ref = oracle.gemm_bf16(A, B)
+    (assert_exact if kind == "int" else assert_close)(C, ref, what=f"band {M}x{N}x{K}")
 
 
 def test_leading_dimensions_and_views(g):

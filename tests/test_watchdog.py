@@ -15,7 +15,7 @@ from gpu_helpers import assert_close, bf16_inputs, dev_bf16, host_bits
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("variant,M", [("skinny", 16), ("prefill", 256), ("pair", 512)])
+@pytest.mark.parametrize("variant,M", [("skinny", 16), ("prefill", 256), ("pair", 512), ("band", 8)])
 def test_forced_timeout_is_reported_and_recoverable(variant, M):
     import torch
     from dense_bit_weight_gb300 import gemm as g
