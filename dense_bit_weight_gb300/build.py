@@ -23,7 +23,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libdbw_gemm.so")
-SOURCES = ["api.cu", "gemv.cu", "gemvband.cu", "umma.cu", "umma2.cu", "w4mma.cu", "w4frag.cu", "w4gemv.cu", "w4tc.cu", "mxgemm.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "gemv.cu", "gemvband.cu", "w4band.cu", "umma.cu", "umma2.cu", "w4mma.cu", "w4frag.cu", "w4gemv.cu", "w4tc.cu", "mxgemm.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-Xptxas", "-v", "--expt-relaxed-constexpr", f"-I{INCLUDE}"]

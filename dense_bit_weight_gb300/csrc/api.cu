@@ -156,8 +156,8 @@ int run(const GemmArgs &a, const Plan &p, cudaStream_t st, bool w4, int mx_fmt =
     case GEMM_VARIANT_ZERO: e = launch_zero_fill(a, c); break;
     case GEMM_VARIANT_GEMV: e = w4 ? launch_gemv_w4a16(a, p, c) : launch_gemv_bf16(a, p, c); break;
     case GEMM_VARIANT_BAND:
-        if (w4 || mx_fmt >= 0 || a.gends) return GEMM_ERR_VARIANT;
-        e = launch_gemv_band(a, p, c);
+        if (mx_fmt >= 0 || a.gends) return GEMM_ERR_VARIANT;
+        e = w4 ? launch_w4_band(a, p, c) : launch_gemv_band(a, p, c);
         break;
     case GEMM_VARIANT_REGISTER:
         if (!w4) return GEMM_ERR_VARIANT;
@@ -501,6 +501,7 @@ bool plan_w4a16(int64_t M, int64_t N, int64_t K, int64_t group, int variant, int
                   : M <= 8                                              ? GEMM_VARIANT_FRAGMENT
                                                                         : GEMM_VARIANT_SKINNY;
     }
+    if (variant == GEMM_VARIANT_BAND) return plan_w4_band(M, N, K, group, sm_count, p);
     if (variant == GEMM_VARIANT_PAIR) {
         p->variant = GEMM_VARIANT_PAIR;
         p->kernels = 2;                      // dequantisation, then the pair GEMM

@@ -170,6 +170,18 @@ int umma_w4_stages(int bn);
 cudaError_t launch_umma_w4a16(const GemmArgs &a, const Plan &p, const LaunchCtx &c);
 // TMA map of packed 4-bit weights [rows, K/8] (uint32): 32-word x box_rows boxes, 128-byte swizzle.
 bool make_map_words(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int box_rows);
+// The same weights (K a multiple of 256) as [K / 256][rows][32 words]: box_kb
+// make_map_words boxes in one copy.
+bool make_map_words_kblocks(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int box_rows, int box_kb);
+// W4A16 decode for up to kW4BandMaxTokens tokens on bands of weight rows
+// (w4band.cu): CTA c streams rows [c N / grid, (c + 1) N / grid) (at most
+// kW4BandMaxRows) over all of K, K / group at most kW4BandMaxGroups; no
+// workspace.  Plan.bn holds the k per stage.
+constexpr int kW4BandMaxRows = 64;
+constexpr int kW4BandMaxTokens = 8;
+constexpr int kW4BandMaxGroups = 192;
+bool plan_w4_band(int64_t M, int64_t N, int64_t K, int64_t group, int sm_count, Plan *p);
+cudaError_t launch_w4_band(const GemmArgs &a, const Plan &p, const LaunchCtx &c);
 extern int g_debug_stall;   // test hook: producers issue no copies (forces the watchdog)
 
 }  // namespace dbw

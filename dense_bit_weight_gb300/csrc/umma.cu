@@ -1199,6 +1199,24 @@ bool make_map_words(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, in
     return r == CUDA_SUCCESS;
 }
 
+// Packed 4-bit weights [rows, K/8] (uint32), K a multiple of 256, as the 3-D
+// view [K / 256][rows][32 words]: a box of box_kb 256-k blocks x box_rows rows
+// lands as box_kb consecutive make_map_words boxes (128-byte swizzle).
+bool make_map_words_kblocks(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int box_rows, int box_kb)
+{
+    if (K % 256) return false;
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {32, (cuuint64_t)rows, (cuuint64_t)(K / 256)};
+    cuuint64_t strides[2] = {(cuuint64_t)(K / 8) * 4, 128};
+    cuuint32_t box[3] = {32, (cuuint32_t)box_rows, (cuuint32_t)box_kb};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Pipeline depth per tile width.  Skinny (decode) kernels come in a deep form
 // (one CTA per SM, about 190 KB of shared memory) used when the grid fits in
 // one wave, and a shallow form (two CTAs per SM, about 100 KB each) for grids

@@ -17,7 +17,7 @@ from gpu_helpers import assert_close, assert_exact, dev_bf16, dev_raw, host_bits
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = ["gemv", "skinny", "prefill", "register", "fragment", "groupwise", "pair"]
+VARIANTS = ["gemv", "skinny", "prefill", "register", "fragment", "groupwise", "pair", "band"]
 
 
 @pytest.fixture(scope="module")
@@ -72,6 +72,24 @@ def test_small_shapes(g, M, N, K, group, variant, kind):
     C = run(g, A, Bq, S, Z, group, variant)
     ref = oracle.gemm_w4a16(A, Bq, S, Z, group)
     (assert_exact if kind == "int" else assert_close)(C, ref, what=f"{variant} {M}x{N}x{K}/{group}")
+
+
+# The band kernel (M <= 8): the whole band requested at once (four stages)
+# and the eight-slot ring (long K), K not a multiple of 256 (one 2-D copy per
+# box, the last one half past K), fewer than four boxes, 64-row bands, the
+# three group sizes.
+W4_BAND = [(1, 7168, 5120, 128), (8, 5120, 17408, 128), (8, 5120, 5120, 64), (5, 1000, 2080, 32),
+           (1, 152, 128, 128), (3, 9728, 1024, 128), (7, 4104, 3072, 32)]
+
+
+@pytest.mark.parametrize("M,N,K,group", W4_BAND)
+@pytest.mark.parametrize("kind", ["normal", "int"])
+def test_band(g, M, N, K, group, kind):
+    assert g.gemm_w4a16_plan(M, N, K, group, "band")["variant"] == 10
+    A, Bq, S, Z = operands(M, N, K, group, seed=3 * M + N, kind=kind)
+    C = run(g, A, Bq, S, Z, group, "band")
+    ref = oracle.gemm_w4a16(A, Bq, S, Z, group)
+    (assert_exact if kind == "int" else assert_close)(C, ref, what=f"band {M}x{N}x{K}/{group}")
 
 
 def test_deterministic(g):

@@ -38,12 +38,12 @@ def test_forced_timeout_is_reported_and_recoverable(variant, M):
     assert g.gemm_last_device_error() == 0
 
 
-@pytest.mark.parametrize("variant", ["skinny", "fragment", "groupwise"])
+@pytest.mark.parametrize("variant", ["skinny", "fragment", "groupwise", "band"])
 def test_forced_timeout_w4a16(variant):
     import torch
     from dense_bit_weight_gb300 import gemm as g, synth
     from gpu_helpers import dev_raw
-    M, N, K, group = 16, 512, 1024, 128
+    M, N, K, group = (8 if variant == "band" else 16), 512, 1024, 128
     A = synth.bf16_normal((M, K), 1.0, 3, synth.STREAM_A)
     Bq, S, Z = synth.w4a16_operands(N, K, group, 3)
     args = (dev_bf16(A), dev_raw(Bq), dev_bf16(S), dev_raw(Z), group)
