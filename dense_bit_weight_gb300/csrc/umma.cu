@@ -36,7 +36,12 @@
 //           whichever contributor arrives last: every contributor stores its
 //           fp32 partial in the workspace, bumps the tile's counter, and the
 //           last one adds all partials in increasing-k order (deterministic,
-//           no float atomics) and resets the counter to zero.
+//           no float atomics) and resets the counter to zero.  Prefill
+//           stream-K orders the tiles token-tile-row by row (raster groups of
+//           one row) on a grid that is a multiple of the tile-rows: CTA c and
+//           CTA c + G / rows then cover the same (weight tile, k-block) units
+//           of neighbouring token tiles at the same time, and each weight
+//           stage is read from HBM once.
 //   mode 2  cluster split-K (decode): the S CTAs that split one tile's K
 //           form a thread-block cluster, and CTA o owns row block o of the
 //           tile.  Each CTA reads its fp32 partial from TMEM and sends every
