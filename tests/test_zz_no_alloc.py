@@ -7,7 +7,7 @@ allocating.  The test calls it through the C ABI twice in a row on each shape
 and checks both results against the fp64 oracle (bit for bit on integer
 inputs, |out - ref| <= 1e-2*|ref| + 1e-2*rms(ref) on N(0,1) inputs) and
 against the allocating entry point gemm_bf16 within the same tolerance.
-Shapes cover the GEMV path, cluster split-K (skinny), the skinny kernel's
+Shapes cover the GEMV path, the band kernel, cluster split-K (skinny), the skinny kernel's
 stream-K schedule with more CTAs than the fixed partials allow, prefill on
 CTA pairs, and stream-K prefill that must run on fewer CTAs.
 
@@ -24,11 +24,11 @@ from gpu_helpers import assert_close, assert_exact, bf16_inputs, dev_bf16, host_
 
 pytestmark = pytest.mark.gpu
 
-# (M, N, K): GEMV, cluster split-K, skinny stream-K over 320 weight tiles of 128
-# columns (its 152 partial writers need more than the fixed 16 MiB: 128 share
-# the units), prefill on CTA pairs (no scratch), stream-K prefill on 15 tiles
-# (64 CTAs), and 4096^3 on CTA pairs.
-SHAPES = [(1, 4096, 4096), (16, 4096, 4096), (128, 40960, 512), (1024, 4096, 4096),
+# (M, N, K): GEMV, the band kernel (no scratch), cluster split-K, skinny
+# stream-K over 320 weight tiles of 128 columns (its 152 partial writers need
+# more than the fixed 16 MiB: 128 share the units), prefill on CTA pairs (no
+# scratch), stream-K prefill on 15 tiles (64 CTAs), and 4096^3 on CTA pairs.
+SHAPES = [(1, 4096, 4096), (8, 6144, 4096), (16, 4096, 4096), (128, 40960, 512), (1024, 4096, 4096),
           (300, 1200, 2056), (4096, 4096, 4096)]
 
 
