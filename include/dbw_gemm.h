@@ -74,9 +74,10 @@ typedef enum {
     GEMM_VARIANT_BLOCK_SCALED = 8, /* MX: block-scaled tcgen05 MMAs (gemm_mxfp*)   */
     GEMM_VARIANT_PAIR = 9,       /* bf16 prefill on CTA pairs: 256 x 256 tiles,    */
                                  /* tcgen05.mma.cta_group::2                       */
-    GEMM_VARIANT_BAND = 10       /* bf16 decode, M <= 32: each SM streams a band   */
-                                 /* of at most 64 weight rows by bulk copies into  */
-                                 /* warp-level MMAs (no K split, no workspace)     */
+    GEMM_VARIANT_BAND = 10       /* decode on bands of weight rows: each SM takes  */
+                                 /* at most 64 rows over all of K, TMA copies into */
+                                 /* warp-level MMAs (no K split, no workspace);    */
+                                 /* bf16 M <= 32, W4A16 M <= 8                     */
 } gemm_variant;
 
 typedef struct {
