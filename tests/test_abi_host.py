@@ -261,6 +261,21 @@ def test_band_plans():
         g.gemm_bf16_fused_plan(8, 4096, 4096, "silu_mul", "band", num_sms=sms)
 
 
+def test_w4a16_band_plans():
+    # the W4A16 band kernel (forced only): up to 8 tokens, bands of at most 64
+    # rows, at most 192 quantisation groups per row; a band that fits shared
+    # memory whole goes in four stages, a longer one through eight slots
+    from dense_bit_weight_gb300 import gemm as g
+    plan = lambda M, N, K, grp: g.gemm_w4a16_plan(M, N, K, grp, "band", num_sms=152)
+    p = plan(1, 7168, 5120, 128)
+    assert (p["variant"], p["grid"], p["tile_m"], p["tile_n"], p["stages"]) == (10, 152, 8, 48, 4)
+    assert plan(8, 5120, 17408, 128)["stages"] == 8
+    for args in ((9, 7168, 5120, 128), (1, 34816, 5120, 128), (1, 5120, 17408, 32)):
+        with pytest.raises(g.GemmError):
+            plan(*args)
+    assert g.gemm_w4a16_plan(1, 7168, 5120, 128, num_sms=152)["variant_name"] == "fragment"   # not routed
+
+
 def test_pair_schedules():
     # whole pair tiles round-robin when they fill at least half the pairs;
     # a last wave of a quarter to half the pairs: full waves whole, each
