@@ -177,7 +177,7 @@ bool make_map_words_kblocks(CUtensorMap *m, const void *ptr, int64_t rows, int64
 // (w4band.cu): CTA c streams rows [c N / grid, (c + 1) N / grid) (at most
 // kW4BandMaxRows) over all of K, K / group at most kW4BandMaxGroups; no
 // workspace.  Plan.bn holds the k per stage.
-constexpr int kW4BandMaxRows = 64;
+constexpr int kW4BandMaxRows = 48;
 constexpr int kW4BandMaxTokens = 8;
 constexpr int kW4BandMaxGroups = 192;
 bool plan_w4_band(int64_t M, int64_t N, int64_t K, int64_t group, int sm_count, Plan *p);

@@ -20,16 +20,17 @@
 // one 3-D copy when K is a multiple of 256 (the rows past the band belong to
 // the neighbouring band, which asks for them at the same time; their sums are
 // dropped).  A band that fits the shared-memory budget whole is requested at
-// once in four stages, one per pair of MMA warps; a longer one streams through
-// eight slots, two owned by each pair (the previous use of a slot is always
-// the same pair's previous stage, so no parity wait can see a phase two steps
-// away); the two MMA warps of a pair take alternate quantisation groups of
+// once in four stages, one per set of MMA warps; a longer one streams through
+// eight slots, two owned by each set (the previous use of a slot is always
+// the same set's previous stage, so no parity wait can see a phase two steps
+// away); the three MMA warps of a set take every third quantisation group of
 // their stages.  The band's scale and zero rows (contiguous in memory) are staged in
 // shared memory once, after the grid dependency wait; before it the copy
 // warp only asks L2 for the first stages.  The activations come straight from
 // A (16 bytes per lane and packed word, through L1), permuted in registers to
-// the nibble-pair order.  The eight MMA warps' sums meet once in shared
-// memory, added in warp order (deterministic).
+// the nibble-pair order.  The twelve MMA warps (three per SM sub-partition,
+// at most 128 registers a thread) keep their own sums; they meet once in
+// shared memory, added in warp order (deterministic).
 //
 // Fragment mapping (lane: g = lane / 4, t = lane % 4), as in w4gemv.cu: a
 // group has 4 WPT words per row (WPT = group / 32); lane t holds words
@@ -51,8 +52,9 @@
 namespace dbw {
 namespace {
 
-constexpr int kMmaWarps = 8;                      // two per stage: a pair takes every fourth stage
-constexpr int kPairs = kMmaWarps / 2;
+constexpr int kMmaWarps = 12;                     // three per stage: a set takes every fourth stage
+constexpr int kPairs = 4;                         // consumer sets
+constexpr int kPer = kMmaWarps / kPairs;          // warps per set
 constexpr int kThreads = (kMmaWarps + 1) * 32;   // + the copy warp
 constexpr int kMaxTiles = kW4BandMaxRows / 16;    // 16-row MMA tiles per band
 constexpr int kMaxStages = 8;
@@ -151,7 +153,7 @@ k_w4_band(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
     if (threadIdx.x == 0) {
         for (int s = 0; s < geo.stages; ++s) {
             ptx::mbar_init(FULL(s), 1);
-            ptx::mbar_init(EMPTY(s), 2);   // the pair of MMA warps that consumes it
+            ptx::mbar_init(EMPTY(s), kPer);   // the set of MMA warps that consumes it
         }
         ptx::mbar_init(SZB, kMmaWarps);
         ptx::mbar_init(REDB, kMmaWarps);
@@ -231,7 +233,7 @@ k_w4_band(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[i][u][e] = 0.f;
     constexpr uint32_t ONES = 0x3F803F80u;
-    constexpr int NCH = NT == 1 ? 2 : 1;   // D_g chains per token tile
+    constexpr int NCH = 1;   // D_g chains per token tile (the tiles give independent chains)
 
     // a group's activation words (16 bytes per token tile and packed word)
     auto load_act = [&](int gi, uint4 (&av)[NT][WPT]) {
@@ -312,10 +314,10 @@ k_w4_band(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
         }
     };
 
-    // the warp's groups in order: every other group (from `half`) of the
+    // the warp's groups in order: every third group (from `half`) of the
     // stages pair, pair + 4, ...; each group's activations are loaded while the
     // previous group is multiplied
-    const int pair = warp & 3, half = warp >> 2;
+    const int pair = warp & 3, half = warp >> 2;   // set, member
     uint4 cur[NT][WPT], nxt[NT][WPT];
     if (pair < nch && pair * geo.nkb * GU + half < G) load_act(pair * geo.nkb * GU + half, cur);
 #pragma unroll 1
@@ -330,8 +332,8 @@ k_w4_band(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
         const int gn = ch + kPairs < nch && (ch + kPairs) * geo.nkb * GU + half < G
                            ? (ch + kPairs) * geo.nkb * GU + half : -1;                    // the next stage's first
 #pragma unroll 1
-        for (int gi = g0 + half; gi < g1; gi += 2) {
-            const int next = gi + 2 < g1 ? gi + 2 : gn;
+        for (int gi = g0 + half; gi < g1; gi += kPer) {
+            const int next = gi + kPer < g1 ? gi + kPer : gn;
             if (next >= 0) load_act(next, nxt);
             group(st + (uint32_t)((gi - g0) / GU) * wbox, (gi - g0) % GU, gi, cur);
 #pragma unroll
@@ -342,7 +344,7 @@ k_w4_band(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
         arrive_warp(EMPTY(s));
     }
 
-    // the eight warps' sums of each output meet in shared memory
+    // the twelve warps' sums of each output meet in shared memory
     constexpr int RC = 8 * NT;
     if (ok) {
         float *mine = red + warp * (16 * kMaxTiles * RC);

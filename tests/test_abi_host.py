@@ -262,7 +262,7 @@ def test_band_plans():
 
 
 def test_w4a16_band_plans():
-    # the W4A16 band kernel (forced only): up to 8 tokens, bands of at most 64
+    # the W4A16 band kernel (forced only): up to 8 tokens, bands of at most 48
     # rows, at most 192 quantisation groups per row; a band that fits shared
     # memory whole goes in four stages, a longer one through eight slots
     from dense_bit_weight_gb300 import gemm as g
@@ -270,7 +270,7 @@ def test_w4a16_band_plans():
     p = plan(1, 7168, 5120, 128)
     assert (p["variant"], p["grid"], p["tile_m"], p["tile_n"], p["stages"]) == (10, 152, 8, 48, 4)
     assert plan(8, 5120, 17408, 128)["stages"] == 8
-    for args in ((9, 7168, 5120, 128), (1, 34816, 5120, 128), (1, 5120, 17408, 32)):
+    for args in ((9, 7168, 5120, 128), (1, 7304, 5120, 128), (1, 5120, 17408, 32)):
         with pytest.raises(g.GemmError):
             plan(*args)
     assert g.gemm_w4a16_plan(1, 7168, 5120, 128, num_sms=152)["variant_name"] == "fragment"   # not routed

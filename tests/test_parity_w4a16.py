@@ -76,10 +76,10 @@ def test_small_shapes(g, M, N, K, group, variant, kind):
 
 # The band kernel (M <= 8): the whole band requested at once (four stages)
 # and the eight-slot ring (long K), K not a multiple of 256 (one 2-D copy per
-# box, the last one half past K), fewer than four boxes, 64-row bands, the
+# box, the last one half past K), fewer than four boxes, 48-row bands, the
 # three group sizes.
 W4_BAND = [(1, 7168, 5120, 128), (8, 5120, 17408, 128), (8, 5120, 5120, 64), (5, 1000, 2080, 32),
-           (1, 152, 128, 128), (3, 9728, 1024, 128), (7, 4104, 3072, 32)]
+           (1, 152, 128, 128), (3, 7296, 1024, 128), (7, 4104, 3072, 32)]
 
 
 @pytest.mark.parametrize("M,N,K,group", W4_BAND)
