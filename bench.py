@@ -72,7 +72,7 @@ WORKLOAD = ("decode projections, Qwen3-8B-like dims: bf16 A[M,4096], M in {1,8,3
 # per shape (profiles/decode_step_dram_traffic.md) over the sources of the
 # decode step's kernels and their planner (DECODE_KERNEL_SOURCES) with this
 # SHA-256; reported only while those sources are unchanged.
-TRAFFIC_SOURCES_SHA256 = "1a1bc5b258e72005588bb7d023051c8cde8d4b52e6965e869901f3105e081ea4"
+TRAFFIC_SOURCES_SHA256 = "66104083d2303030a902e631ecd228c56aee28307a799c6879a0ec29ee519724"
 TRAFFIC_BYTES = {(1, 4096, 4096): 33.57e6, (1, 6144, 4096): 50.38e6, (1, 24576, 4096): 204.19e6,
                  (8, 4096, 4096): 33.66e6, (8, 6144, 4096): 50.43e6, (8, 24576, 4096): 204.27e6,
                  (32, 4096, 4096): 33.91e6, (32, 6144, 4096): 50.69e6, (32, 24576, 4096): 204.42e6,
