@@ -156,6 +156,22 @@ def test_band(g, M, N, K, kind):
     (assert_exact if kind == "int" else assert_close)(C, ref, what=f"band {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,K", [(5, 4096), (8, 200)])   # 3-D k-block copies / 2-D boxes (K % 64 != 0)
+def test_band_leading_dimensions(g, M, K):
+    # the band kernel on strided views: lda = K + 16, ldb = K + 64, ldc = N + 24
+    import torch
+    N = 3000
+    A, B = bf16_inputs(M, N, K + 64, seed=11)
+    At = dev_bf16(A)[:, 16:16 + K]
+    Bt = dev_bf16(B)[:, 64:64 + K]
+    Cbig = torch.zeros((M, N + 24), dtype=torch.bfloat16, device="cuda")
+    C = Cbig[:, :N]
+    g.gemm_bf16(At, Bt, C, variant="band")
+    ref = oracle.gemm_bf16(np.ascontiguousarray(A[:, 16:16 + K]), np.ascontiguousarray(B[:, 64:64 + K]))
+    assert_close(host_bits(C), ref, what=f"band strided {M}x{N}x{K}")
+    assert not host_bits(Cbig[:, N:]).any()     # nothing written past N
+
+
 def test_leading_dimensions_and_views(g):
     import torch
     M, N, K = 37, 200, 96
