@@ -43,6 +43,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "frag.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "sched.cuh"
@@ -114,13 +115,6 @@ __device__ __forceinline__ void sf_copy_warp(uint32_t taddr, uint32_t saddr)
         "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
         "l"(desc)
         : "memory");
-}
-
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-                 : "memory");
 }
 
 // Shared memory: a ring of STAGES data stages (A tile, then B tile; 1024-byte

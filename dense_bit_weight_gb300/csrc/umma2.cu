@@ -40,6 +40,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "frag.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "sched.cuh"
@@ -147,13 +148,6 @@ __device__ __forceinline__ void commit_local_warp(uint32_t bar)
 __device__ __forceinline__ void arrive_remote(uint32_t bar_cluster)
 {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
-}
-
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-                 : "memory");
 }
 
 __device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }

@@ -45,6 +45,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "frag.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "waits.cuh"
@@ -78,20 +79,6 @@ int w4band_nt(int64_t M) { return M <= 8 ? 1 : 2; }   // (M <= kW4BandMaxTokens 
 int w4band_smem(const W4BandGeo &g, int nt)
 {
     return g.stages * g.stage_bytes + g.sz_bytes + red_bytes(nt) + kBarBytes + 1024;   // + alignment slack
-}
-
-__device__ __forceinline__ uint32_t pair128(uint32_t x, int p)
-{
-    return ((x >> (4 * p)) & 0x000F000Fu) | 0x43004300u;
-}
-
-__device__ __forceinline__ void mma_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                        uint32_t b0, uint32_t b1)
-{
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // Words i = 0..WPT-1 of lane t in group h of a box row r (128-byte rows,

@@ -42,6 +42,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "frag.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "waits.cuh"
@@ -56,21 +57,6 @@ constexpr int kThreads = kW4FragWarps * 32;
 // Weight row (within eight) of MMA row n.
 __device__ __forceinline__ int col_row(int n) { return (n >> 1) | ((n & 1) << 2); }
 
-// bf16x2 (128 + q_p, 128 + q_{p+4}) from nibble pair p of a packed word.
-__device__ __forceinline__ uint32_t pair128(uint32_t x, int p)
-{
-    return ((x >> (4 * p)) & 0x000F000Fu) | 0x43004300u;
-}
-
-// d (+)= A B for one 16 x 8 x 16 bf16 MMA.
-__device__ __forceinline__ void mma_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                        uint32_t b0, uint32_t b1)
-{
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
 __device__ __forceinline__ void mma_first(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                           uint32_t b0, uint32_t b1)
 {

@@ -48,6 +48,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "frag.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "waits.cuh"
@@ -68,21 +69,6 @@ constexpr int kPartOff = kRedOff + kRows * 16 * 4;      // the warps' sums [warp
 constexpr int kSzBar = kPartOff + kWarps * kRows * 16 * 4;
 constexpr int kFlagOff = kSzBar + 8;
 constexpr int kSmem = kFlagOff + 8 + 1024;       // + alignment slack
-
-// bf16x2 (128 + q_p, 128 + q_{p+4}) from nibble pair p of a packed word.
-__device__ __forceinline__ uint32_t pair128(uint32_t x, int p)
-{
-    return ((x >> (4 * p)) & 0x000F000Fu) | 0x43004300u;
-}
-
-__device__ __forceinline__ void mma_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                        uint32_t b0, uint32_t b1)
-{
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
 
 // Words i of rows r and r + 8 of group h for lane t, from a slot (64-byte
 // rows, 16-byte piece c of row r at piece c ^ ((r / 2) % 4)).
@@ -118,19 +104,6 @@ template <int NT, int WPT>
 struct GroupAct {
     uint4 a[NT][WPT];
 };
-
-__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-                 : "memory");
-}
 
 template <int NT, int WPT>
 __global__ void __launch_bounds__(kWarps * 32, 3)

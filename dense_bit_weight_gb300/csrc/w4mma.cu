@@ -35,6 +35,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "frag.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -81,12 +82,6 @@ __global__ void __launch_bounds__(256) k_w4_prep(const uint16_t *__restrict__ A,
         dst[4 * (b % wpt) + b / wpt] = o;
     }
     S[(int64_t)gi * Mp + m] = sum;
-}
-
-// bf16x2 (128 + q_p, 128 + q_{p+4}) from nibble pair p of a packed word
-__device__ __forceinline__ uint32_t pair128(uint32_t x, int p)
-{
-    return ((x >> (4 * p)) & 0x000F000Fu) | 0x43004300u;
 }
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
